@@ -1,0 +1,318 @@
+// CPU oracle for the grouped-expert MoE FFN layer.
+//
+// TEST INFRASTRUCTURE ONLY. This file is the slow, obviously correct reference that the
+// CUDA path is checked against. Only the tests, the smoke check and the benchmark's
+// CPU-baseline leg may load it; the library never does. It shares no code, header,
+// table or constant with the CUDA sources.
+//
+// It computes the layer by its plain definition, one token at a time:
+//
+//   route:    per token, the top_k largest fp32 logits (ties toward the lowest expert id;
+//             slots ordered by logit descending, then id ascending) and a softmax over the
+//             selected logits, so the k weights sum to 1 ("top-k softmax routing").
+//   quant:    per token s = amax|x| / 127 (fp32), q = round-half-even(x / s), |q| <= 127.
+//   expert:   acc_g[i] = sum_h q_x[h] * Wg[e,i,h]  (int32, exact), likewise acc_u;
+//             g = (float(acc_g) * s_x) * s_g[e,i], u likewise;
+//             h = g / (1 + exp(-g)) * u  ("SiLU(gate) * up"), fp32;
+//             requant h per (token, expert) row with the same rule as the activations;
+//             acc_d[o] = sum_i q_h[i] * Wd[e,o,i] (int32); d = (float(acc_d) * s_h) * s_d[e,o].
+//   combine:  y[t,o] = sum_j w[t,j] * d_j[o] + d_shared[o]   (shared expert weight 1, no gate),
+//             summed in slot order in double precision.
+//
+// The source pages describe this layer without printing formulas: a concatenated-expert
+// gate/up GEMM with N = TOP_K x 2 x IM_EXP followed by one GLU region over all experts
+// (page "Qwen3.6-35B-A3B Linux v1.0.4: ~2.7s fixed per-request TTFT ...", section "The fix
+// (concatenated-expert dispatch)"), and batched decode that deduplicates experts across rows
+// and uses an int8 dot (page "[job] Strix Halo: multi-session serving ... #145", section
+// "Status", item "Next"). The precise arithmetic above is the layer definition the library
+// implements: W8A8 with per-output-channel weight scales, per-token activation scales,
+// fp32 scales and an fp32 output.
+//
+// Built with -O2 -ffp-contract=off and no fast-math, so every fp32 operation is a single
+// IEEE-rounded operation in the order written.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+extern "C" {
+
+typedef struct {
+  int E, k, H, I, Is;                 // Is = 0: no shared expert
+  const int8_t* w_gate;               // [E, I, H]
+  const int8_t* w_up;                 // [E, I, H]
+  const int8_t* w_down;               // [E, H, I]
+  const float* s_gate;                // [E, I]
+  const float* s_up;                  // [E, I]
+  const float* s_down;                // [E, H]
+  const int8_t* sh_gate;              // [Is, H]
+  const int8_t* sh_up;                // [Is, H]
+  const int8_t* sh_down;              // [H, Is]
+  const float* sh_s_gate;             // [Is]
+  const float* sh_s_up;               // [Is]
+  const float* sh_s_down;             // [H]
+} oracle_layer;
+
+// Optional intermediates, all indexed by (token, slot); slot j < k is routed slot j,
+// slot k is the shared expert. Imax = max(I, Is). Any pointer may be NULL.
+typedef struct {
+  int8_t* qx;      // [T, H]
+  float* sx;       // [T]
+  int32_t* acc_gu; // [T, S, 2, Imax]  gate accumulators then up accumulators
+  int8_t* hq;      // [T, S, Imax]
+  float* sh;       // [T, S]
+  int32_t* acc_d;  // [T, S, H]
+} oracle_taps;
+
+}  // extern "C"
+
+namespace {
+
+float bf16_to_float(uint16_t b) {
+  uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+// Per-row symmetric int8 quantisation: s = amax / 127, q = rne(v / s), clamp +-127.
+void quantize_row(const float* v, int n, int8_t* q, float* s_out) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) amax = std::max(amax, std::fabs(v[i]));
+  const float s = amax / 127.0f;
+  for (int i = 0; i < n; ++i) {
+    if (s == 0.0f) {
+      q[i] = 0;
+      continue;
+    }
+    float r = std::nearbyint(v[i] / s);  // default rounding mode: to nearest, ties to even
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    q[i] = static_cast<int8_t>(r);
+  }
+  *s_out = s;
+}
+
+// One expert applied to one quantised token row. Weight rows are row-major with the
+// reduction dimension contiguous. Writes d[H] (fp32) and, optionally, intermediates.
+void expert_ffn(const int8_t* qx, float sx, int H, int I,
+                const int8_t* Wg, const int8_t* Wu, const int8_t* Wd,
+                const float* sg, const float* su, const float* sd,
+                float* d, int32_t* acc_gu_tap, int8_t* hq_tap, float* sh_tap,
+                int32_t* acc_d_tap, int Imax) {
+  std::vector<float> h(I);
+  for (int i = 0; i < I; ++i) {
+    int32_t ag = 0, au = 0;
+    for (int c = 0; c < H; ++c) {
+      ag += static_cast<int32_t>(qx[c]) * static_cast<int32_t>(Wg[(size_t)i * H + c]);
+      au += static_cast<int32_t>(qx[c]) * static_cast<int32_t>(Wu[(size_t)i * H + c]);
+    }
+    if (acc_gu_tap) {
+      acc_gu_tap[i] = ag;
+      acc_gu_tap[Imax + i] = au;
+    }
+    const float g = (static_cast<float>(ag) * sx) * sg[i];
+    const float u = (static_cast<float>(au) * sx) * su[i];
+    const float silu = g / (1.0f + std::exp(-g));
+    h[i] = silu * u;
+  }
+  std::vector<int8_t> hq(I);
+  float sh = 0.0f;
+  quantize_row(h.data(), I, hq.data(), &sh);
+  if (hq_tap) std::memcpy(hq_tap, hq.data(), I);
+  if (sh_tap) *sh_tap = sh;
+  for (int o = 0; o < H; ++o) {
+    int32_t ad = 0;
+    for (int i = 0; i < I; ++i)
+      ad += static_cast<int32_t>(hq[i]) * static_cast<int32_t>(Wd[(size_t)o * I + i]);
+    if (acc_d_tap) acc_d_tap[o] = ad;
+    d[o] = (static_cast<float>(ad) * sh) * sd[o];
+  }
+}
+
+int check_layer(const oracle_layer* L) {
+  if (!L || L->E <= 0 || L->k <= 0 || L->k > L->E || L->H <= 0 || L->I <= 0 || L->Is < 0)
+    return -1;
+  return 0;
+}
+
+template <class F>
+void parallel_tokens(int T, int nthreads, F f) {
+  if (nthreads <= 1 || T <= 1) {
+    for (int t = 0; t < T; ++t) f(t);
+    return;
+  }
+  nthreads = std::min(nthreads, T);
+  std::vector<std::thread> th;
+  th.reserve(nthreads);
+  for (int w = 0; w < nthreads; ++w) {
+    th.emplace_back([=]() {
+      for (int t = w; t < T; t += nthreads) f(t);
+    });
+  }
+  for (auto& x : th) x.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+// Top-k routing of fp32 logits [T, E] -> idx int32 [T, k], w fp32 [T, k].
+// Selection compares logits (strictly greater wins, so ties go to the lowest id);
+// the weights are a softmax over the k selected logits, computed in double.
+int oracle_route(const float* logits, int T, int E, int k, int32_t* idx, float* w) {
+  if (T < 0 || E <= 0 || k <= 0 || k > E) return -1;
+  std::vector<char> taken(E);
+  std::vector<double> ex(k);
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (size_t)t * E;
+    for (int e = 0; e < E; ++e) {
+      if (!std::isfinite(l[e])) return -2;
+      taken[e] = 0;
+    }
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e)
+        if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;
+      taken[best] = 1;
+      idx[(size_t)t * k + j] = best;
+    }
+    const double m = l[idx[(size_t)t * k]];
+    double z = 0.0;
+    for (int j = 0; j < k; ++j) {
+      ex[j] = std::exp(static_cast<double>(l[idx[(size_t)t * k + j]]) - m);
+      z += ex[j];
+    }
+    for (int j = 0; j < k; ++j) w[(size_t)t * k + j] = static_cast<float>(ex[j] / z);
+  }
+  return 0;
+}
+
+// Per-token activation quantisation of bf16 x [T, H] -> q int8 [T, H], s fp32 [T].
+int oracle_quant_rows(const uint16_t* x, int T, int H, int8_t* q, float* s) {
+  std::vector<float> v(H);
+  for (int t = 0; t < T; ++t) {
+    for (int c = 0; c < H; ++c) v[c] = bf16_to_float(x[(size_t)t * H + c]);
+    quantize_row(v.data(), H, q + (size_t)t * H, s + t);
+  }
+  return 0;
+}
+
+// Token-by-expert permutation. counts[e] = number of (t, j) with idx[t,j] = e;
+// offsets = exclusive prefix sum (E + 1 entries); perm lists the flat slot t*k + j of every
+// assignment, grouped by expert in id order and, inside an expert, by (t, j) ascending.
+int oracle_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
+                   int32_t* offsets, int32_t* perm) {
+  const long R = (long)T * k;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (long r = 0; r < R; ++r) {
+    if (idx[r] < 0 || idx[r] >= E) return -1;
+    counts[idx[r]]++;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  long pos = 0;
+  for (int e = 0; e < E; ++e)
+    for (long r = 0; r < R; ++r)
+      if (idx[r] == e) perm[pos++] = (int32_t)r;
+  return 0;
+}
+
+// The whole layer, token by token (see the file header). y is double [T, H].
+int oracle_forward(const oracle_layer* L, const uint16_t* x, int T, const int32_t* idx,
+                   const float* w, double* y, const oracle_taps* taps, int nthreads) {
+  if (check_layer(L)) return -1;
+  const int H = L->H, I = L->I, Is = L->Is, k = L->k, E = L->E;
+  const int S = k + (Is > 0 ? 1 : 0);
+  const int Imax = std::max(I, Is);
+  for (long r = 0; r < (long)T * k; ++r)
+    if (idx[r] < 0 || idx[r] >= E) return -2;
+  parallel_tokens(T, nthreads, [&](int t) {
+    std::vector<float> xf(H), d(H);
+    std::vector<int8_t> qx(H);
+    for (int c = 0; c < H; ++c) xf[c] = bf16_to_float(x[(size_t)t * H + c]);
+    float sx = 0.0f;
+    quantize_row(xf.data(), H, qx.data(), &sx);
+    if (taps && taps->qx) std::memcpy(taps->qx + (size_t)t * H, qx.data(), H);
+    if (taps && taps->sx) taps->sx[t] = sx;
+    double* yt = y + (size_t)t * H;
+    for (int o = 0; o < H; ++o) yt[o] = 0.0;
+    for (int s = 0; s < S; ++s) {
+      const bool shared = (s == k);
+      const int e = shared ? -1 : idx[(size_t)t * k + s];
+      const int Ie = shared ? Is : I;
+      const size_t slot = (size_t)t * S + s;
+      int32_t* agu = (taps && taps->acc_gu) ? taps->acc_gu + slot * 2 * Imax : nullptr;
+      int8_t* hq = (taps && taps->hq) ? taps->hq + slot * Imax : nullptr;
+      float* sh = (taps && taps->sh) ? taps->sh + slot : nullptr;
+      int32_t* ad = (taps && taps->acc_d) ? taps->acc_d + slot * H : nullptr;
+      if (shared) {
+        expert_ffn(qx.data(), sx, H, Is, L->sh_gate, L->sh_up, L->sh_down, L->sh_s_gate,
+                   L->sh_s_up, L->sh_s_down, d.data(), agu, hq, sh, ad, Imax);
+      } else {
+        expert_ffn(qx.data(), sx, H, I, L->w_gate + (size_t)e * I * H,
+                   L->w_up + (size_t)e * I * H, L->w_down + (size_t)e * H * I,
+                   L->s_gate + (size_t)e * I, L->s_up + (size_t)e * I,
+                   L->s_down + (size_t)e * H, d.data(), agu, hq, sh, ad, Imax);
+      }
+      const double wt = shared ? 1.0 : static_cast<double>(w[(size_t)t * k + s]);
+      for (int o = 0; o < H; ++o) yt[o] += wt * static_cast<double>(d[o]);
+      (void)Ie;
+    }
+  });
+  return 0;
+}
+
+// Brute force: every routed expert applied to every token, each weighted by its routing
+// weight (0 when the token did not select it), summed in expert-id order, plus the shared
+// expert. Equal to oracle_forward up to the order of the double additions.
+int oracle_dense(const oracle_layer* L, const uint16_t* x, int T, const int32_t* idx,
+                 const float* w, double* y, int nthreads) {
+  if (check_layer(L)) return -1;
+  const int H = L->H, I = L->I, Is = L->Is, k = L->k, E = L->E;
+  parallel_tokens(T, nthreads, [&](int t) {
+    std::vector<float> xf(H), d(H);
+    std::vector<int8_t> qx(H);
+    for (int c = 0; c < H; ++c) xf[c] = bf16_to_float(x[(size_t)t * H + c]);
+    float sx = 0.0f;
+    quantize_row(xf.data(), H, qx.data(), &sx);
+    std::vector<double> mask(E, 0.0);
+    for (int j = 0; j < k; ++j) mask[idx[(size_t)t * k + j]] += w[(size_t)t * k + j];
+    double* yt = y + (size_t)t * H;
+    for (int o = 0; o < H; ++o) yt[o] = 0.0;
+    for (int e = 0; e < E; ++e) {
+      expert_ffn(qx.data(), sx, H, I, L->w_gate + (size_t)e * I * H,
+                 L->w_up + (size_t)e * I * H, L->w_down + (size_t)e * H * I,
+                 L->s_gate + (size_t)e * I, L->s_up + (size_t)e * I, L->s_down + (size_t)e * H,
+                 d.data(), nullptr, nullptr, nullptr, nullptr, I);
+      for (int o = 0; o < H; ++o) yt[o] += mask[e] * static_cast<double>(d[o]);
+    }
+    if (Is > 0) {
+      expert_ffn(qx.data(), sx, H, Is, L->sh_gate, L->sh_up, L->sh_down, L->sh_s_gate,
+                 L->sh_s_up, L->sh_s_down, d.data(), nullptr, nullptr, nullptr, nullptr, Is);
+      for (int o = 0; o < H; ++o) yt[o] += static_cast<double>(d[o]);
+    }
+  });
+  return 0;
+}
+
+// Router projection of the stacked-prefill workload: logits[t,e] = sum_h x[t,h] * Wr[h,e],
+// x bf16 [T, H], Wr fp32 [H, E], summed in double (h ascending). Output double [T, E].
+int oracle_router_logits(const uint16_t* x, const float* Wr, int T, int H, int E,
+                         double* logits, int nthreads) {
+  parallel_tokens(T, nthreads, [&](int t) {
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int h = 0; h < H; ++h)
+        acc += static_cast<double>(bf16_to_float(x[(size_t)t * H + h])) *
+               static_cast<double>(Wr[(size_t)h * E + e]);
+      logits[(size_t)t * E + e] = acc;
+    }
+  });
+  return 0;
+}
+
+}  // extern "C"

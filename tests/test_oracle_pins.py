@@ -1,0 +1,352 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Every test here runs on the CPU. Each one checks the oracle against a hand-worked example,
+a closed form, an invariant, a brute-force search or a library routine on a special case,
+so that a dropped term, a wrong sign or index, or a transposed operand in the oracle fails
+at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits(x):
+    return torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def layer_from_arrays(E, k, H, I, Is, **arrs):
+    W = {}
+    for key, v in arrs.items():
+        dt = np.float32 if key.startswith("s_") or key.startswith("sh_s_") else np.int8
+        W[key] = np.ascontiguousarray(np.array(v, dtype=dt))
+    return oracle.Layer(W, E, k, H, I, Is), W
+
+
+# ---------------------------------------------------------------- routing
+
+def test_route_golden_ties():
+    cases = json.load(open(os.path.join(GOLD, "route_ties.json")))["cases"]
+    for c in cases:
+        lg = np.array([c["logits"]], np.float32)
+        idx, w = oracle.route(lg, c["k"])
+        assert idx[0].tolist() == c["idx"], c
+        sel = lg[0, idx[0]].astype(np.float64)
+        closed = np.exp(sel - sel.max()) / np.exp(sel - sel.max()).sum()
+        np.testing.assert_allclose(w[0], closed, rtol=0, atol=1e-7)
+        if "w" in c:
+            np.testing.assert_array_equal(w[0], np.array(c["w"], np.float32))
+
+
+def test_route_all_equal_is_uniform():
+    for E, k in [(8, 2), (128, 8), (5, 5), (3, 1)]:
+        idx, w = oracle.route(np.full((4, E), 0.3, np.float32), k)
+        assert (idx == np.arange(k)).all()
+        assert (w == np.float32(1.0 / k)).all()
+
+
+def test_route_k_equals_E_is_library_softmax():
+    rng = np.random.default_rng(0)
+    lg = rng.standard_normal((32, 16)).astype(np.float32)
+    idx, w = oracle.route(lg, 16)
+    order = np.argsort(-lg, axis=1, kind="stable")
+    assert (idx == order).all()
+    sm = torch.softmax(torch.from_numpy(lg).double(), dim=1).numpy()
+    np.testing.assert_allclose(w, np.take_along_axis(sm, idx, 1), rtol=0, atol=1e-7)
+
+
+def test_route_bruteforce_subsets():
+    rng = np.random.default_rng(1)
+    for trial in range(200):
+        E = int(rng.integers(1, 7))
+        k = int(rng.integers(1, E + 1))
+        lg = rng.integers(-2, 3, size=(1, E)).astype(np.float32)  # many ties
+        idx, w = oracle.route(lg, k)
+        best = None
+        for sub in itertools.combinations(range(E), k):
+            s = float(lg[0, list(sub)].sum())
+            if best is None or s > best[0]:        # combinations() is lexicographic: first wins ties
+                best = (s, sub)
+        assert tuple(sorted(idx[0].tolist())) == best[1]
+        # slot order: logit descending, then id ascending
+        keys = [(-lg[0, e], e) for e in idx[0]]
+        assert keys == sorted(keys)
+
+
+def test_route_library_topk_and_sum():
+    rng = np.random.default_rng(2)
+    lg = (rng.standard_normal((200, 64)) * 3).astype(np.float32)
+    idx, w = oracle.route(lg, 8)
+    tv, ti = torch.topk(torch.from_numpy(lg), 8, dim=1)
+    assert (idx == ti.numpy()).all()          # distinct continuous draws: no ties
+    assert np.abs(w.astype(np.float64).sum(1) - 1).max() <= 1e-6
+    assert (np.diff(w, axis=1) <= 0).all()
+
+
+# ---------------------------------------------------------------- activation quant
+
+def test_quant_round_half_even_ties():
+    # amax = 127 makes s = 1 exactly, so q = rne(x): the .5 cases land on even integers.
+    row = [127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, 126.5, -0.5, 0.25, 0.0, -127.0]
+    exp = [127, 2, 4, -2, -4, 0, 2, 126, 0, 0, 0, -127]
+    x = bf16_bits([row])
+    q, s = oracle.quant_rows(x)
+    assert s[0] == np.float32(1.0)
+    assert q[0].tolist() == exp
+
+
+def test_quant_zero_row_and_extremes():
+    rng = np.random.default_rng(3)
+    xf = rng.standard_normal((20, 300)).astype(np.float32) * 3
+    xf[5] = 0
+    x = bf16_bits(xf)
+    q, s = oracle.quant_rows(x)
+    assert s[5] == 0 and (q[5] == 0).all()
+    xr = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).float()
+    for t in range(20):
+        if t == 5:
+            continue
+        am = int(np.argmax(np.abs(xr[t].numpy())))
+        assert abs(int(q[t, am])) == 127 and np.sign(q[t, am]) == np.sign(xr[t, am].item())
+        assert np.abs(q[t]).max() <= 127
+    # library: torch.round is round-half-even on the IEEE fp32 quotient
+    sl = (xr.abs().amax(1) / 127.0)
+    ql = torch.round(xr / torch.where(sl > 0, sl, torch.ones_like(sl))[:, None]).clamp(-127, 127)
+    ql[5] = 0
+    assert (torch.from_numpy(q.astype(np.float32)) == ql).all()
+    assert (torch.from_numpy(s) == sl).all()
+
+
+# ---------------------------------------------------------------- permutation
+
+def test_permute_is_stable_sort_and_bijection():
+    rng = np.random.default_rng(4)
+    for T, E, k in [(16, 8, 2), (37, 128, 8), (1, 4, 4), (300, 256, 8)]:
+        lg = rng.standard_normal((T, E)).astype(np.float32)
+        idx, _ = oracle.route(lg, k)
+        counts, offsets, perm = oracle.permute(idx, E)
+        assert (counts == np.bincount(idx.ravel(), minlength=E)).all()
+        assert counts.sum() == T * k and offsets[-1] == T * k
+        assert (np.diff(offsets) >= 0).all()
+        assert sorted(perm.tolist()) == list(range(T * k))
+        assert (perm == np.argsort(idx.ravel(), kind="stable")).all()
+        for e in range(E):
+            seg = perm[offsets[e]:offsets[e + 1]]
+            assert (idx.ravel()[seg] == e).all()
+
+
+# ---------------------------------------------------------------- integer GEMMs
+
+def _tiny_layer(seed, T=5, H=64, E=4, k=2, I=32, Is=16):
+    d = synth.small_layer(T, H, E, k, I, Is, seed)
+    L = oracle.Layer(d["weights"], E, k, H, I, Is)
+    idx, w = oracle.route(d["logits"], k)
+    return d, L, idx, w
+
+
+def test_gemm_accumulators_match_library_matmul():
+    d, L, idx, w = _tiny_layer(5)
+    W = {k_: v.numpy() for k_, v in d["weights"].items()}
+    y, tp = oracle.forward(L, d["x"], idx, w, taps=True)
+    qx = tp["qx"].astype(np.int64)
+    T, S = tp["sh"].shape
+    for t in range(T):
+        for s in range(S):
+            if s < L.k:
+                e = idx[t, s]
+                wg, wu, wd, I = W["w_gate"][e], W["w_up"][e], W["w_down"][e], L.I
+            else:
+                wg, wu, wd, I = W["sh_gate"], W["sh_up"], W["sh_down"], L.Is
+            ag = wg.astype(np.int64) @ qx[t]
+            au = wu.astype(np.int64) @ qx[t]
+            assert (tp["acc_gu"][t, s, 0, :I] == ag).all()
+            assert (tp["acc_gu"][t, s, 1, :I] == au).all()
+            ad = wd.astype(np.int64) @ tp["hq"][t, s, :I].astype(np.int64)
+            assert (tp["acc_d"][t, s] == ad).all()
+
+
+@pytest.mark.parametrize("val", [127, -127])
+def test_gemm_extremes_closed_form(val):
+    # x constant -> q_x = 127 everywhere; weights all `val` -> acc = 127 * val * H.
+    H, I, E, k = 128, 16, 2, 1
+    lay, _ = layer_from_arrays(
+        E, k, H, I, 0,
+        w_gate=np.full((E, I, H), val), w_up=np.full((E, I, H), val),
+        w_down=np.full((E, H, I), val), s_gate=np.full((E, I), 0.001),
+        s_up=np.full((E, I), 0.001), s_down=np.full((E, H), 0.001))
+    x = bf16_bits(np.full((1, H), 0.5))
+    idx = np.array([[1]], np.int32)
+    w = np.array([[1.0]], np.float32)
+    y, tp = oracle.forward(lay, x, idx, w, taps=True)
+    assert (tp["qx"] == 127).all()
+    assert (tp["acc_gu"][0, 0] == 127 * val * H).all()
+    # every h is equal -> q_h = +-127 (sign of h), acc_d = 127 * sign * val * I
+    hs = int(np.sign(tp["hq"][0, 0, 0]))
+    assert (tp["hq"][0, 0] == 127 * hs).all()
+    assert (tp["acc_d"][0, 0] == 127 * hs * val * I).all()
+
+
+# ---------------------------------------------------------------- whole layer
+
+def test_golden_hand_layer():
+    G = json.load(open(os.path.join(GOLD, "hand_layer.json")))
+    lay, W = layer_from_arrays(2, 1, 4, 2, 0, w_gate=G["w_gate"], w_up=G["w_up"],
+                               w_down=G["w_down"], s_gate=G["s_gate"], s_up=G["s_up"],
+                               s_down=G["s_down"])
+    x = bf16_bits([G["x"]])
+    idx, w = oracle.route(np.array([G["logits"]], np.float32), G["top_k"])
+    ex = G["expect"]
+    assert idx[0].tolist() == ex["idx"] and w[0].tolist() == ex["w"]
+    y, tp = oracle.forward(lay, x, idx, w, taps=True)
+    assert tp["qx"][0].tolist() == ex["q_x"]
+    assert tp["acc_gu"][0, 0, 0].tolist() == ex["acc_gate"]
+    assert tp["acc_gu"][0, 0, 1].tolist() == ex["acc_up"]
+    assert tp["hq"][0, 0].tolist() == ex["q_h"]
+    assert tp["acc_d"][0, 0].tolist() == ex["acc_down"]
+    # closed form in double
+    sx = 1.0 / 127
+    g = [32 * sx * 0.01, -95 * sx * 0.02]
+    u = [64 * sx * 0.5, 127 * sx * 0.25]
+    h = [gi / (1 + math.exp(-gi)) * ui for gi, ui in zip(g, u)]
+    s_h = abs(h[1]) / 127
+    yc = [a * s_h * sd for a, sd in zip(ex["acc_down"], G["s_down"][1])]
+    np.testing.assert_allclose(y[0], yc, rtol=2e-6, atol=0)
+
+
+@pytest.mark.parametrize("shape", [(16, 256, 8, 2, 128, 0), (7, 64, 6, 3, 32, 48), (3, 32, 4, 4, 16, 16)])
+def test_dense_equals_sparse(shape):
+    T, H, E, k, I, Is = shape
+    d = synth.small_layer(T, H, E, k, I, Is, seed=11, zipf_s=1.1)
+    L = oracle.Layer(d["weights"], E, k, H, I, Is)
+    idx, w = oracle.route(d["logits"], k)
+    ys = oracle.forward(L, d["x"], idx, w)
+    yd = oracle.dense(L, d["x"], idx, w)
+    np.testing.assert_allclose(ys, yd, rtol=1e-12, atol=1e-15 * np.abs(ys).max())
+
+
+def _unquantised_reference(d, idx, w, E, k, H, I, Is):
+    """The same layer with no activation quantisation (fp64 library matmuls on x and the
+    dequantised weights); the oracle differs from it only by int8 activation error."""
+    W = d["weights"]
+    x = d["x"].double()
+
+    def deq(q, s):
+        return q.double() * s.double()[..., None]
+
+    y = torch.zeros_like(x)
+    for t in range(x.shape[0]):
+        for j in range(k):
+            e = int(idx[t, j])
+            g = deq(W["w_gate"][e], W["s_gate"][e]) @ x[t]
+            u = deq(W["w_up"][e], W["s_up"][e]) @ x[t]
+            h = torch.nn.functional.silu(g) * u
+            y[t] += float(w[t, j]) * (deq(W["w_down"][e], W["s_down"][e]) @ h)
+        if Is:
+            g = deq(W["sh_gate"], W["sh_s_gate"]) @ x[t]
+            u = deq(W["sh_up"], W["sh_s_up"]) @ x[t]
+            h = torch.nn.functional.silu(g) * u
+            y[t] += deq(W["sh_down"], W["sh_s_down"]) @ h
+    return y.numpy()
+
+
+@pytest.mark.parametrize("shape", [(16, 256, 8, 2, 128, 0), (9, 128, 6, 3, 64, 96)])
+def test_close_to_unquantised_layer(shape):
+    T, H, E, k, I, Is = shape
+    d = synth.small_layer(T, H, E, k, I, Is, seed=12)
+    L = oracle.Layer(d["weights"], E, k, H, I, Is)
+    idx, w = oracle.route(d["logits"], k)
+    y = oracle.forward(L, d["x"], idx, w)
+    yr = _unquantised_reference(d, idx, w, E, k, H, I, Is)
+    rel = np.sqrt(((y - yr) ** 2).mean() / (yr ** 2).mean())
+    assert rel < 3e-2, rel       # int8 activation + int8 h quantisation error only
+    # a wrong slot weight or scale index would be far off; check per-token too
+    per_tok = np.sqrt(((y - yr) ** 2).mean(1) / (yr ** 2).mean(1))
+    assert per_tok.max() < 0.1
+
+
+def test_single_expert_is_dense_swiglu_ffn():
+    # E=1, k=1, no shared expert: the layer is one W8A8 SwiGLU FFN; its integer GEMMs are
+    # library int64 matmuls and its activation is torch's SiLU.
+    T, H, I = 6, 64, 48
+    d = synth.small_layer(T, H, 1, 1, I, 0, seed=13)
+    L = oracle.Layer(d["weights"], 1, 1, H, I, 0)
+    idx, w = oracle.route(d["logits"], 1)
+    assert (idx == 0).all() and (w == 1).all()
+    y, tp = oracle.forward(L, d["x"], idx, w, taps=True)
+    W = d["weights"]
+    qx = torch.from_numpy(tp["qx"]).long()
+    sx = torch.from_numpy(tp["sx"])
+    ag = qx @ W["w_gate"][0].long().T
+    au = qx @ W["w_up"][0].long().T
+    g = (ag.float() * sx[:, None]) * W["s_gate"][0][None]
+    u = (au.float() * sx[:, None]) * W["s_up"][0][None]
+    h = torch.nn.functional.silu(g) * u
+    hq = torch.from_numpy(tp["hq"][:, 0, :I]).long()
+    sh = torch.from_numpy(tp["sh"][:, 0])
+    # torch's SiLU may differ from g/(1+exp(-g)) in the last ulp: q_h may move by 1 at a tie
+    assert (hq.float() - torch.round(h / sh[:, None])).abs().max() <= 1
+    assert torch.allclose(sh, h.abs().amax(1) / 127, rtol=1e-6, atol=0)
+    ad = hq @ W["w_down"][0].long().T
+    assert (torch.from_numpy(tp["acc_d"][:, 0]).long() == ad).all()
+    yl = (ad.float() * sh[:, None]) * W["s_down"][0][None]
+    np.testing.assert_allclose(y, yl.double().numpy(), rtol=1e-6, atol=1e-9)
+
+
+def test_token_permutation_equivariance():
+    d = synth.small_layer(12, 64, 6, 2, 32, 16, seed=14)
+    L = oracle.Layer(d["weights"], 6, 2, 64, 32, 16)
+    idx, w = oracle.route(d["logits"], 2)
+    y = oracle.forward(L, d["x"], idx, w)
+    p = np.random.default_rng(0).permutation(12)
+    yp = oracle.forward(L, d["x"][p], idx[p], w[p])
+    np.testing.assert_array_equal(yp, y[p])
+
+
+def test_shared_expert_alone():
+    # Routed experts with zero weights contribute nothing; the shared one is a plain FFN
+    # with weight 1 that matches the unquantised shared FFN up to int8 error.
+    T, H, E, k, I, Is = 8, 128, 4, 2, 32, 64
+    d = synth.small_layer(T, H, E, k, I, Is, seed=15)
+    W = d["weights"]
+    for key in ("w_gate", "w_up", "w_down"):
+        W[key].zero_()
+    for key in ("s_gate", "s_up", "s_down"):
+        W[key].zero_()
+    L = oracle.Layer(W, E, k, H, I, Is)
+    idx, w = oracle.route(d["logits"], k)
+    y = oracle.forward(L, d["x"], idx, w)
+    yr = _unquantised_reference(d, idx, w, E, k, H, I, Is)
+    rel = np.sqrt(((y - yr) ** 2).mean() / (yr ** 2).mean())
+    assert rel < 3e-2
+
+
+def test_router_logits_library_matmul():
+    d = synth.make_layer(synth.Workload("p", synth.LayerShape(5, 96, 12, 2, 16, 0), 0,
+                                        router="projection"))
+    lg = oracle.router_logits(d["x"], d["w_router"])
+    ref = d["x"].double() @ d["w_router"].double()
+    np.testing.assert_allclose(lg, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_workload_properties():
+    # Zipf skew readings: the decode rows share experts; the stress routing puts > 40% of
+    # assignments on the top 4 experts and leaves some experts empty.
+    dec = synth.WORKLOADS["decode"]
+    lg = synth.make_logits(dec.shape.T, dec.shape.E, dec.seed, dec.zipf_s)
+    idx, _ = oracle.route(lg, dec.shape.k)
+    assert len(np.unique(idx)) < idx.size
+    st = synth.WORKLOADS["stress"]
+    lg = synth.make_logits(st.shape.T, st.shape.E, st.seed, st.zipf_s)
+    idx, _ = oracle.route(lg, st.shape.k)
+    c = np.bincount(idx.ravel(), minlength=st.shape.E)
+    assert np.sort(c)[::-1][:4].sum() > 0.4 * idx.size
+    assert (c == 0).any()
