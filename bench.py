@@ -1,0 +1,425 @@
+"""Benchmark of the grouped-expert MoE FFN layer on one GB300 (one JSON line on stdout).
+
+Default workload: the 40-layer stacked prefill at T=2600 (35B-A3B-shaped layers, H=2048,
+E=128, top_k=8, I=512, shared expert I=512, distinct seeded weights per layer, router logits
+= x @ W_r per layer, residual x <- bf16(x + y)). One step = the whole stack over one batch.
+`value` = MoE-layer tokens per second (T x 40 per step). The same run also measures batched
+decode at C=8 rows through the same 40 layers' weights (microseconds per layer and the HBM
+roofline over the unique experts' bytes).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the layer has no
+exchange step); rank 0 prints the line with the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer tokens/s (prefill) & µs/layer decode C=8; % int8/HBM roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.item()
+
+
+# ---------------------------------------------------------------- clocks
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        try:
+            self.idx = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        except Exception:
+            self.idx = "0"
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def build_stack(moe, wl, n_layers, dev):
+    sh = wl.shape
+    plan = moe.moe_plan(sh.E, sh.k, sh.H, sh.I, sh.Is, sh.T)
+    layers = []
+    for l in range(n_layers):
+        seed = synth.layer_seed(wl, l)
+        W = synth.make_weights(sh, seed, device=dev)
+        wr = synth.make_router_weight(sh.H, sh.E, seed, device=dev)
+        packed = moe.moe_pack_weights(plan, W)
+        layers.append((W, wr, packed))
+    torch.cuda.synchronize()
+    return plan, layers
+
+
+def oracle_sample_rate(W_dev, wl, n_tokens, nthreads):
+    """Oracle (as it stands) on n_tokens tokens of one stacked-prefill layer; returns
+    (layer-tokens per second, seconds, threads)."""
+    import oracle
+    sh = wl.shape
+    L = oracle.Layer({k: v.cpu() for k, v in W_dev.items()}, sh.E, sh.k, sh.H, sh.I, sh.Is)
+    x = synth.make_activations(sh.T, sh.H, wl.seed)[:n_tokens].contiguous()
+    wr = synth.make_router_weight(sh.H, sh.E, wl.seed)
+    t0 = time.perf_counter()
+    lg = oracle.router_logits(x, wr, nthreads=nthreads).astype(np.float32)
+    idx, w = oracle.route(lg, sh.k)
+    oracle.forward(L, x, idx, w, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt
+
+
+def run_ours(args, world, rank):
+    import grouped_expert_ffn_gb300 as moe
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda")
+    wl = synth.WORKLOADS["stack"]
+    sh = wl.shape
+    n_layers = args.layers
+    plan, layers = build_stack(moe, wl, n_layers, dev)
+    T, H, E, k = sh.T, sh.H, sh.E, sh.k
+    x0 = synth.make_activations(T, H, wl.seed, wl.outliers, dev)
+    x = torch.empty_like(x0)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        x.copy_(x0)
+        for (W, wr, packed) in layers:
+            moe.moe_router_logits(x, wr, logits)
+            moe.moe_route(plan, logits, idx, w)
+            moe.moe_forward(plan, packed, x, idx, w, y)
+            moe.moe_residual_add(x, y)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(plan) == 0
+    moe.moe_profile_enable(plan, True)
+    clocks = Clocks()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    moe.moe_profile_enable(plan, False)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
+    st, calls = moe.moe_profile_read(plan, 0)
+    stage_ms = [v / max(calls, 1) for v in st]
+    assert moe.moe_get_error(plan) == 0
+    ms_step = ms_total / args.steps
+    layer_tokens = T * n_layers
+    value = layer_tokens * world / (ms_step / 1e3)
+
+    # roofline of the dominant kernel (gate/up GEMM): 2*R*2I*H flops per launch
+    R = T * k + T
+    gu_flops = 2.0 * R * 2 * sh.I * H
+    gu_ms = stage_ms[1]
+    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    achieved_tf = gu_flops / (gu_ms / 1e3) / 1e12
+    down_flops = 2.0 * R * H * sh.I
+    layer_flops = gu_flops + down_flops
+    moe_ms = sum(stage_ms)
+
+    # ---- e2e: host (pinned) x in, host result out, inside the timed region
+    x_host = x0.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+
+    def step_e2e():
+        x.copy_(x_host, non_blocking=True)
+        for (W, wr, packed) in layers:
+            moe.moe_router_logits(x, wr, logits)
+            moe.moe_route(plan, logits, idx, w)
+            moe.moe_forward(plan, packed, x, idx, w, y)
+            moe.moe_residual_add(x, y)
+        out_host.copy_(x, non_blocking=True)
+
+    step_e2e()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    e2e_value = layer_tokens * world / (ms_e2e / 1e3)
+
+    # ---- decode: C=8 rows through the same 40 layers' weights (CUDA graph of route+forward)
+    dwl = synth.WORKLOADS["decode"]
+    xd = synth.make_activations(dwl.shape.T, H, dwl.seed, dwl.outliers, dev)
+    lgd = synth.make_logits(dwl.shape.T, E, dwl.seed, dwl.zipf_s, dev)
+    idd = torch.empty((dwl.shape.T, k), dtype=torch.int32, device=dev)
+    wd = torch.empty((dwl.shape.T, k), dtype=torch.float32, device=dev)
+    yd = torch.empty((dwl.shape.T, H), dtype=torch.float32, device=dev)
+
+    def decode_stack():
+        for (W, wr, packed) in layers:
+            moe.moe_route(plan, lgd, idd, wd)
+            moe.moe_forward(plan, packed, xd, idd, wd, yd)
+
+    decode_stack()
+    torch.cuda.synchronize()
+    counts = moe.moe_debug_tap(plan, moe.TAP_COUNTS)
+    U = int((counts > 0).sum())
+    g = torch.cuda.CUDAGraph()
+    s2 = torch.cuda.Stream()
+    s2.wait_stream(stream)
+    with torch.cuda.stream(s2):
+        with torch.cuda.graph(g, stream=s2):
+            decode_stack()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(args.steps, 5)
+    d0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    us_layer = d0.elapsed_time(d1) * 1e3 / reps / n_layers
+    # per-stage decode timing (eager, profiled)
+    moe.moe_profile_enable(plan, True)
+    for _ in range(3):
+        decode_stack()
+    torch.cuda.synchronize()
+    st, calls = moe.moe_profile_read(plan, 1)
+    moe.moe_profile_enable(plan, False)
+    dstage_us = [v * 1e3 / max(calls, 1) for v in st][:3]
+    bpe = synth.weight_bytes_per_expert(H, sh.I)
+    uniq_bytes = (U + 1) * bpe
+    hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    dec_gbs = uniq_bytes / (us_layer * 1e-6) / 1e9
+    kern_us = dstage_us[1] + dstage_us[2]
+
+    # ---- oracle CPU baseline (bounded sample, rank 0 only, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        n_tok = args.cpu_tokens
+        rate, secs = oracle_sample_rate(layers[0][0], wl, n_tok, nthreads)
+        cpu = {"value": rate, "unit": "MoE-layer tokens/s", "cores": nthreads, "kind": "oracle",
+               "sample": f"{n_tok} tokens of layer 0 of the stack (router projection + route + "
+                         f"layer), {secs:.1f} s"}
+
+    n_launch = n_layers * 9 * args.steps
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "MoE-layer tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8 (W8A8) on the fp16 tensor pipe, fp32 epilogue",
+        "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": f"stacked prefill {n_layers} layers x T={T}, H={H}, E={E}, top_k={k}, "
+                               f"I={sh.I}, shared I={sh.Is}",
+                   "global_batch": T * world, "seq_len": T, "layers": n_layers,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (each layer's weights > 129 MB)"},
+        "per_layer_us": ms_step * 1e3 / n_layers,
+        "moe_layer_us": moe_ms * 1e3,
+        "stack_prompt_tokens_per_s": T * world / (ms_step / 1e3),
+        "stage_us": {"permute_quant": stage_ms[0] * 1e3, "gate_up_gemm": stage_ms[1] * 1e3,
+                     "requant": stage_ms[2] * 1e3, "down_gemm_combine": stage_ms[3] * 1e3},
+        "roofline": {"bound": "tensor", "kernel": "grouped gate/up GEMM (tcgen05 kind::f16)",
+                     "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved_tf / peak_tf, "traffic": None,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 = bf16 rate)",
+                     "flops_per_launch": gu_flops},
+        "layer_tflops": layer_flops / (moe_ms / 1e3) / 1e12,
+        "decode": {"workload": f"C=8 rows, T=8, Zipf(1.1) routing, same 40 layers' weights",
+                   "us_per_layer": us_layer, "unique_experts": U,
+                   "unique_bytes_per_layer": uniq_bytes, "achieved_gbs": dec_gbs,
+                   "hbm_peak_gbs": hbm, "frac": dec_gbs / hbm,
+                   "stage_us": {"dedup_quant": dstage_us[0], "gate_up_stream": dstage_us[1],
+                                "down_stream_combine": dstage_us[2]},
+                   "kernel_gbs": uniq_bytes / (kern_us * 1e-6) / 1e9 if kern_us > 0 else None},
+        "e2e": {"value": e2e_value, "unit": "MoE-layer tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
+        "gpu_launches": n_launch,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    wl = synth.WORKLOADS["stack"]
+    sh = wl.shape
+    nthreads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    W = synth.make_weights(sh, synth.layer_seed(wl, 0), device="cpu")
+    L = oracle.Layer(W, sh.E, sh.k, sh.H, sh.I, sh.Is)
+    wr = synth.make_router_weight(sh.H, sh.E, wl.seed)
+    x_all = synth.make_activations(sh.T, sh.H, wl.seed)
+    n_tok = args.ref_tokens
+
+    def step(i):
+        off = (i * n_tok) % (sh.T - n_tok)
+        x = x_all[off:off + n_tok].contiguous()
+        lg = oracle.router_logits(x, wr, nthreads=nthreads).astype(np.float32)
+        idx, w = oracle.route(lg, sh.k)
+        oracle.forward(L, x, idx, w, nthreads=nthreads)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = n_tok * args.steps / dt
+    line = {"metric": METRIC, "value": value, "unit": "MoE-layer tokens/s", "impl": "reference",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8 W8A8, fp32 epilogue (scalar C++)",
+            "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": f"stacked prefill layer, T={sh.T} sampled {n_tok} tokens per step, "
+                                   f"H={sh.H}, E={sh.E}, top_k={sh.k}, I={sh.I}, shared I={sh.Is}",
+                       "global_batch": n_tok, "seq_len": sh.T, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "MoE-layer tokens/s", "cores": nthreads,
+                             "kind": "oracle", "sample": f"{n_tok} tokens of one layer per step"},
+            "e2e": {"value": value, "unit": "MoE-layer tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=40)
+    ap.add_argument("--cpu-tokens", type=int, default=2600,
+                    help="tokens of layer 0 the oracle baseline runs (our arm)")
+    ap.add_argument("--ref-tokens", type=int, default=512,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        run_reference(args, world, rank)
+        return
+    world, rank = dist_init(args.gpus)
+    run_ours(args, world, rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

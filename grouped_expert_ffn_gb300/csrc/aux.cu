@@ -1,0 +1,165 @@
+// Weight packing for the tensor-core path, and the two steps around the layer in a stacked
+// prefill (router projection and the bf16 residual update).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// Gate/up rows interleaved in blocks of BN rows: packed rows [b*BN, b*BN + BN/2) are gate
+// channels [b*BN/2, (b+1)*BN/2), the next BN/2 rows the up channels of the same range, so one
+// BN-row weight tile yields SiLU(gate)*up for BN/2 channels. int8 values widened to fp16
+// (exact). 8 elements per thread.
+__global__ void pack_gu_kernel(const int8_t* __restrict__ gate, const int8_t* __restrict__ up,
+                               int n_mats, int I, int H, int BN, __half* __restrict__ out) {
+  const size_t n8 = (size_t)n_mats * 2 * I * H / 8;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8;
+       v += (size_t)gridDim.x * blockDim.x) {
+    const size_t el = v * 8;
+    const int h = (int)(el % H);
+    const size_t prow = el / H;  // packed row over all matrices
+    const int m = (int)(prow / (2 * I));
+    const int p = (int)(prow % (2 * I));
+    const int b = p / BN, r = p % BN, half = BN / 2;
+    const int ch = b * half + (r % half);
+    const int8_t* src = (r < half ? gate : up) + ((size_t)m * I + ch) * H + h;
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);
+    const int8_t* q = reinterpret_cast<const int8_t*>(&raw);
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h2 = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
+      ow[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(out + el) = o;
+  }
+}
+
+__global__ void widen_kernel(const int8_t* __restrict__ src, size_t n, __half* __restrict__ out) {
+  const size_t n8 = n / 8;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8;
+       v += (size_t)gridDim.x * blockDim.x) {
+    const uint2 raw = reinterpret_cast<const uint2*>(src)[v];
+    const int8_t* q = reinterpret_cast<const int8_t*>(&raw);
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h2 = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
+      ow[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    reinterpret_cast<uint4*>(out)[v] = o;
+  }
+}
+
+cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H, int BN,
+                           __half* out, cudaStream_t s) {
+  pack_gu_kernel<<<1216, 256, 0, s>>>(gate, up, n_mats, I, H, BN, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_widen(const int8_t* src, size_t n, __half* out, cudaStream_t s) {
+  widen_kernel<<<1216, 256, 0, s>>>(src, n, out);
+  return cudaGetLastError();
+}
+
+// logits[T, E] = float(x[T, H]) @ wr[H, E] in fp32. 64x64 output tile per block, 16-deep K
+// slices through shared memory, 4x4 outputs per thread.
+__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
+                                                            const float* __restrict__ wr, int T,
+                                                            int H, int E, float* __restrict__ out) {
+  __shared__ float As[16][64 + 4];
+  __shared__ __align__(16) float Bs[16][64];
+  const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
+  const int tid = threadIdx.x;
+  const int ty = tid / 16, tx = tid % 16;
+  float acc[4][4] = {};
+  const int la_row = tid / 4, la_k = (tid % 4) * 4;   // A: 64 rows x 16 k, 4 per thread
+  const int lb_k = tid / 16, lb_c = (tid % 16) * 4;   // B: 16 k x 64 cols, 4 per thread
+  for (int k0 = 0; k0 < H; k0 += 16) {
+    {
+      const int t = t0 + la_row;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t < T) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(x + (size_t)t * H + k0 + la_k);
+        v[0] = bf16_bits_to_float((uint16_t)(raw.x & 0xffffu));
+        v[1] = bf16_bits_to_float((uint16_t)(raw.x >> 16));
+        v[2] = bf16_bits_to_float((uint16_t)(raw.y & 0xffffu));
+        v[3] = bf16_bits_to_float((uint16_t)(raw.y >> 16));
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) As[la_k + i][la_row] = v[i];
+    }
+    {
+      const int c = e0 + lb_c;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c + 3 < E) {
+        v = *reinterpret_cast<const float4*>(wr + (size_t)(k0 + lb_k) * E + c);
+      } else {
+        float* pv = reinterpret_cast<float*>(&v);
+        for (int i = 0; i < 4; ++i)
+          if (c + i < E) pv[i] = wr[(size_t)(k0 + lb_k) * E + c + i];
+      }
+      *reinterpret_cast<float4*>(&Bs[lb_k][lb_c]) = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = e0 + tx * 4 + j;
+      if (c < E) out[(size_t)t * E + c] = acc[i][j];
+    }
+  }
+}
+
+cudaError_t launch_router_logits(const uint16_t* x, const float* wr, int T, int H, int E,
+                                 float* out, cudaStream_t s) {
+  const dim3 grid((E + 63) / 64, (T + 63) / 64);
+  router_logits_kernel<<<grid, 256, 0, s>>>(x, wr, T, H, E, out);
+  return cudaGetLastError();
+}
+
+__global__ void residual_kernel(uint16_t* __restrict__ x, const float* __restrict__ y, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n / 4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 yv = reinterpret_cast<const float4*>(y)[i];
+    uint2 xv = reinterpret_cast<uint2*>(x)[i];
+    const float f[4] = {bf16_bits_to_float((uint16_t)(xv.x & 0xffffu)) + yv.x,
+                        bf16_bits_to_float((uint16_t)(xv.x >> 16)) + yv.y,
+                        bf16_bits_to_float((uint16_t)(xv.y & 0xffffu)) + yv.z,
+                        bf16_bits_to_float((uint16_t)(xv.y >> 16)) + yv.w};
+    uint16_t b[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(f[j]);
+      b[j] = *reinterpret_cast<const uint16_t*>(&h);
+    }
+    xv.x = (uint32_t)b[0] | ((uint32_t)b[1] << 16);
+    xv.y = (uint32_t)b[2] | ((uint32_t)b[3] << 16);
+    reinterpret_cast<uint2*>(x)[i] = xv;
+  }
+}
+
+cudaError_t launch_residual(uint16_t* x, const float* y, size_t n, cudaStream_t s) {
+  residual_kernel<<<1216, 256, 0, s>>>(x, y, n);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

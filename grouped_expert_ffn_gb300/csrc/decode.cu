@@ -1,0 +1,292 @@
+// Batched decode (T <= 8 rows): experts deduplicated across rows, each unique expert's int8
+// weights streamed from HBM exactly once and applied to every row that routed to it, with an
+// int8 dot (dp4a) into exact int32 accumulators. This is the kernel the page "[job] Strix
+// Halo: multi-session serving ... #145" names as the C>1 limiter (section "Status", items
+// "Batched decode doesn't scale" and "Next": expert dedup across rows plus int8 dot).
+//
+//  decode_prep_kernel  one block: per-token int8 quant, the unique-expert list (with the
+//                      shared expert as group 0), the canonical row order, y zeroed.
+//  decode_gu_kernel    (16 channels of one unique expert) per block: streams 16 gate and 16
+//                      up rows, dp4a against the expert's <= 8 quantised token rows held in
+//                      shared memory; fused SiLU(gate)*up.
+//  decode_down_kernel  (64 output channels of one unique expert) per block: requantises the
+//                      expert's h rows into shared memory, streams 64 down rows, dp4a, and
+//                      adds w * d into y.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+__device__ __forceinline__ int4 ld_stream(const void* p) {
+  int4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ int dot16(int4 a, int4 b, int c) {
+  c = __dp4a(a.x, b.x, c);
+  c = __dp4a(a.y, b.y, c);
+  c = __dp4a(a.z, b.z, c);
+  return __dp4a(a.w, b.w, c);
+}
+
+// v[i] summed over the warp; afterwards lane L holds the total of index L in v[0].
+__device__ __forceinline__ void transpose_reduce32(int (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const int send = up ? v[i] : v[i + o];
+      const int keep = up ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+}
+
+__global__ void decode_prep_kernel(DecodeArgs a) {
+  __shared__ int s_cnt[256];
+  __shared__ int s_off[257];
+  __shared__ int s_idx[kDecodeMaxRows * 8];
+  const int T = a.T, k = a.k, E = a.E, H = a.H;
+  const int T_sh = a.has_shared ? T : 0;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int r = tid; r < T * k; r += blockDim.x) {
+    int e = a.idx[r];
+    if (e < 0 || e >= E) {
+      set_error(a.err, kErrDevice);
+      e = 0;
+    }
+    s_idx[r] = e;
+  }
+  __syncthreads();
+  for (int r = tid; r < T * k; r += blockDim.x) {
+    atomicAdd(&s_cnt[s_idx[r]], 1);
+    const int t = r / k;
+    for (int q = t * k; q < r; ++q)
+      if (s_idx[q] == s_idx[r]) set_error(a.err, kErrDevice);  // expert repeated in a token
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int off = 0, n = 0;
+    if (a.has_shared) a.groups[n++] = make_int4(E, 0, T, 0);
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = off;
+      a.offsets[e] = off;
+      a.counts[e] = s_cnt[e];
+      // a group never has more rows than tokens (<= 8); more means repeated experts (flagged)
+      if (s_cnt[e] > 0) a.groups[n++] = make_int4(e, T_sh + off, min(s_cnt[e], T), 0);
+      off += s_cnt[e];
+    }
+    s_off[E] = off;
+    a.offsets[E] = off;
+    *a.n_groups = n;
+  }
+  __syncthreads();
+  for (int r = tid; r < T * k; r += blockDim.x) {
+    const int t = r / k, e = s_idx[r];
+    int rank = 0;
+    for (int q = 0; q < t * k; ++q) rank += (s_idx[q] == e);
+    const int pos = min(s_off[e] + rank, T * k - 1);
+    a.perm[pos] = r;
+    const int row = T_sh + pos;
+    a.row_token[row] = t;
+    a.row_w[row] = a.w[r];
+  }
+  if (a.has_shared && tid < T) {
+    a.row_token[tid] = tid;
+    a.row_w[tid] = 1.0f;
+  }
+  // per-token quantisation, warp t handles token t
+  const int warp = tid / 32, lane = tid % 32;
+  if (warp < T) {
+    const uint16_t* xr = a.x + (size_t)warp * H;
+    float amax = 0.0f;
+    for (int c = lane * 8; c < H; c += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax = fmaxf(amax, fabsf(bf16_bits_to_float((uint16_t)(u[i] & 0xffffu))));
+        amax = fmaxf(amax, fabsf(bf16_bits_to_float((uint16_t)(u[i] >> 16))));
+      }
+    }
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+    for (int c = lane * 8; c < H; c += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+      uint2 qv;
+      uint8_t* qb = reinterpret_cast<uint8_t*>(&qv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = bf16_bits_to_float((uint16_t)(u[i] & 0xffffu));
+        const float hi = bf16_bits_to_float((uint16_t)(u[i] >> 16));
+        qb[2 * i] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(lo, s) : 0);
+        qb[2 * i + 1] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(hi, s) : 0);
+      }
+      *reinterpret_cast<uint2*>(a.qtok + (size_t)warp * H + c) = qv;
+    }
+    if (lane == 0) a.stok[warp] = s;
+  }
+  float4* y4 = reinterpret_cast<float4*>(a.y);
+  for (int i = tid; i < T * H / 4; i += blockDim.x) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+constexpr int kGuChannelsPerBlock = 16;  // 8 warps x 2 channels
+constexpr int kDownRowsPerBlock = 64;    // 8 warps x 8 output rows
+
+__global__ void __launch_bounds__(256) decode_gu_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) int8_t xs[];  // [8][H]
+  const int g = blockIdx.y;
+  if (g >= *a.n_groups) return;
+  const int4 grp = a.groups[g];
+  const bool shared = grp.x == a.E;
+  const int Ig = shared ? a.Is : a.I;
+  const int c0 = blockIdx.x * kGuChannelsPerBlock;
+  if (c0 >= Ig) return;
+  const int H = a.H, nr = grp.z, row0 = grp.y;
+  const int8_t* Wg = shared ? a.sh_gate : a.w_gate + (size_t)grp.x * a.I * H;
+  const int8_t* Wu = shared ? a.sh_up : a.w_up + (size_t)grp.x * a.I * H;
+  const float* sg = shared ? a.sh_s_gate : a.s_gate + (size_t)grp.x * a.I;
+  const float* su = shared ? a.sh_s_up : a.s_up + (size_t)grp.x * a.I;
+  for (int i = threadIdx.x; i < nr * H / 16; i += blockDim.x) {
+    const int n = i / (H / 16), u = i % (H / 16);
+    const int tok = a.row_token[row0 + n];
+    reinterpret_cast<int4*>(xs + (size_t)n * H)[u] =
+        reinterpret_cast<const int4*>(a.qtok + (size_t)tok * H)[u];
+  }
+  __syncthreads();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int c = c0 + 2 * warp;
+  const int8_t* rows[4] = {Wg + (size_t)c * H, Wu + (size_t)c * H, Wg + (size_t)(c + 1) * H,
+                           Wu + (size_t)(c + 1) * H};
+  int acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0;
+#pragma unroll 4
+  for (int u = lane; u < H / 16; u += 32) {
+    int4 wv[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) wv[r] = ld_stream(rows[r] + (size_t)u * 16);
+#pragma unroll
+    for (int n = 0; n < kDecodeMaxRows; ++n) {
+      if (n < nr) {
+        const int4 xv = *reinterpret_cast<const int4*>(xs + (size_t)n * H + u * 16);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r * 8 + n] = dot16(wv[r], xv, acc[r * 8 + n]);
+      }
+    }
+  }
+  transpose_reduce32(acc, lane);
+  const int mine = acc[0];
+  const int other = __shfl_down_sync(0xffffffffu, mine, 8);
+  const int r = lane >> 3, n = lane & 7;
+  if ((r & 1) == 0 && n < nr) {
+    const int ch = c + (r >> 1);
+    const int row = row0 + n;
+    const float sx = a.stok[a.row_token[row]];
+    a.h32[(size_t)row * a.Imax + ch] = silu_mul(dequant(mine, sx, sg[ch]), dequant(other, sx, su[ch]));
+    if (a.tap_gu) {
+      a.tap_gu[(size_t)row * 2 * a.Imax + ch] = mine;
+      a.tap_gu[(size_t)row * 2 * a.Imax + a.Imax + ch] = other;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) int8_t hs[];  // [8][Imax]
+  __shared__ float shs[kDecodeMaxRows];
+  const int g = blockIdx.y;
+  if (g >= *a.n_groups) return;
+  const int4 grp = a.groups[g];
+  const bool shared = grp.x == a.E;
+  const int Ig = shared ? a.Is : a.I;
+  const int H = a.H, nr = grp.z, row0 = grp.y, Imax = a.Imax;
+  const int o0 = blockIdx.x * kDownRowsPerBlock;
+  const int8_t* Wd = shared ? a.sh_down : a.w_down + (size_t)grp.x * H * a.I;
+  const float* sd = shared ? a.sh_s_down : a.s_down + (size_t)grp.x * H;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // requantise this expert's h rows (warp n handles row n)
+  if (warp < nr) {
+    const int row = row0 + warp;
+    const float* h = a.h32 + (size_t)row * Imax;
+    float amax = 0.0f;
+    for (int i = lane; i < Ig; i += 32) amax = fmaxf(amax, fabsf(h[i]));
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+    for (int i = lane; i < Ig; i += 32) {
+      const int q = s > 0.0f ? quant_code(h[i], s) : 0;
+      hs[(size_t)warp * Imax + i] = (int8_t)q;
+      if (a.tap_d && blockIdx.x == 0) a.hq[(size_t)row * Imax + i] = __int2half_rn(q);
+    }
+    if (lane == 0) {
+      shs[warp] = s;
+      if (a.tap_d && blockIdx.x == 0) a.sh[row] = s;
+    }
+  }
+  __syncthreads();
+  const int ob = o0 + warp * 8;
+  int acc[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) acc[i] = 0;
+#pragma unroll 1
+  for (int u = lane; u < Ig / 16; u += 32) {
+    int4 wv[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) wv[r] = ld_stream(Wd + (size_t)(ob + r) * Ig + (size_t)u * 16);
+#pragma unroll
+    for (int n = 0; n < kDecodeMaxRows; ++n) {
+      if (n < nr) {
+        const int4 xv = *reinterpret_cast<const int4*>(hs + (size_t)n * Imax + u * 16);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) acc[r * 8 + n] = dot16(wv[r], xv, acc[r * 8 + n]);
+      }
+    }
+  }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    int v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = acc[half * 32 + i];
+    transpose_reduce32(v, lane);
+    const int r = half * 4 + (lane >> 3), n = lane & 7;
+    if (n < nr) {
+      const int o = ob + r;
+      const int row = row0 + n;
+      const float d = dequant(v[0], shs[n], sd[o]);
+      atomicAdd(a.y + (size_t)a.row_token[row] * H + o, __fmul_rn(a.row_w[row], d));
+      if (a.tap_d) a.tap_d[(size_t)row * H + o] = v[0];
+    }
+  }
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) {
+  if (ev) cudaEventRecord(ev[0], s);
+  decode_prep_kernel<<<1, 256, 0, s>>>(a);
+  if (ev) cudaEventRecord(ev[1], s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int gmax = min(a.E, a.T * a.k) + (a.has_shared ? 1 : 0);
+  const dim3 ggu((a.Imax + kGuChannelsPerBlock - 1) / kGuChannelsPerBlock, gmax);
+  decode_gu_kernel<<<ggu, 256, kDecodeMaxRows * a.H, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (ev) cudaEventRecord(ev[2], s);
+  const dim3 gd(a.H / kDownRowsPerBlock, gmax);
+  decode_down_kernel<<<gd, 256, kDecodeMaxRows * a.Imax, s>>>(a);
+  if (ev) cudaEventRecord(ev[3], s);
+  return cudaGetLastError();
+}
+
+cudaError_t decode_set_attributes(int H, int Imax) {
+  cudaError_t e = cudaFuncSetAttribute(decode_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kDecodeMaxRows * H);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kDecodeMaxRows * Imax);
+}
+
+}  // namespace moe

@@ -1,0 +1,129 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kBM = 128;        // tensor-core tile rows (token rows)
+constexpr int kBK = 64;         // K elements per pipeline stage (128 bytes of fp16)
+constexpr int kChunkK = 1024;   // K elements summed in one fp32 TMEM accumulator
+constexpr int kTokPerBlk = 64;  // tokens per histogram block (one 64-bit mask per expert)
+constexpr int kDecodeMaxRows = 8;
+
+// One unit of grouped-GEMM work: rows [row0, row0 + rows) of group `group` (expert id, or E
+// for the shared expert) against weight rows [n0, n0 + BN).
+// Stored as int4 {group, row0, rows, n0}.
+
+struct GemmArgs {
+  const int4* items;
+  const int* n_items;
+  int E;
+  int K_r, K_s;          // reduction length of routed / shared groups
+  int I, Is, Imax, H;
+  // gate/up epilogue
+  const float* sx;       // per row activation scale
+  const float* s_g;      // [E, I]
+  const float* s_u;      // [E, I]
+  const float* sh_s_g;   // [Is]
+  const float* sh_s_u;   // [Is]
+  float* h32;            // [R, Imax]
+  // down epilogue
+  const float* s_h;      // per row
+  const float* s_d;      // [E, H]
+  const float* sh_s_d;   // [H]
+  const int* row_token;  // per row
+  const float* row_w;    // per row
+  float* y;              // [T, H]
+  // taps (NULL = off)
+  int32_t* tap;
+  int* err;
+};
+
+cudaError_t launch_grouped_gemm(bool gate_up, int BN, const GemmArgs& a, const CUtensorMap& tmA,
+                                const CUtensorMap& tmB, const CUtensorMap& tmBs, int grid,
+                                cudaStream_t s);
+cudaError_t gemm_set_attributes();
+
+cudaError_t launch_requant(const float* h32, int R, int T_sh, int I, int Is, int Imax,
+                           __half* hq, float* sh, cudaStream_t s);
+
+// routing / permutation
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                         int* err, cudaStream_t s);
+
+struct PrepArgs {
+  const int32_t* idx;
+  const float* w;
+  const uint16_t* x;
+  int T, k, E, H, I, Is, has_shared, bn_gu, bn_d;
+  unsigned long long* bmask;  // [nblk, E]
+  int* bhist;                 // [nblk, E]
+  int* counts;                // [E]
+  int* offsets;               // [E + 1]
+  int* perm;                  // [T*k]
+  int4* items_gu;
+  int4* items_d;
+  int* n_items;               // [2]
+  __half* xq;                 // [R, H]
+  float* sx;                  // [R]
+  int* row_token;             // [R]
+  float* row_w;               // [R]
+  float* y;                   // [T, H] zeroed
+  int8_t* qtok;               // [T, H] or NULL
+  float* stok;                // [T]   or NULL
+  int* err;
+};
+cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+  const int32_t* idx;
+  const float* w;
+  const uint16_t* x;
+  int T, k, E, H, I, Is, Imax, has_shared;
+  const int8_t* w_gate;
+  const int8_t* w_up;
+  const int8_t* w_down;
+  const float* s_gate;
+  const float* s_up;
+  const float* s_down;
+  const int8_t* sh_gate;
+  const int8_t* sh_up;
+  const int8_t* sh_down;
+  const float* sh_s_gate;
+  const float* sh_s_up;
+  const float* sh_s_down;
+  int* counts;
+  int* offsets;
+  int* perm;
+  int4* groups;      // [E + 1] {group, row0, nrows, 0}
+  int* n_groups;
+  int* row_token;
+  float* row_w;
+  int8_t* qtok;      // [T, H]
+  float* stok;       // [T]
+  float* h32;        // [R, Imax]
+  __half* hq;        // [R, Imax] (tap only)
+  float* sh;         // [R]       (tap only)
+  float* y;
+  int32_t* tap_gu;   // NULL = off
+  int32_t* tap_d;
+  int* err;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev);
+cudaError_t decode_set_attributes(int H, int Imax);
+
+// weight packing and the stacked-prefill helpers
+cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H, int BN,
+                           __half* out, cudaStream_t s);
+cudaError_t launch_widen(const int8_t* src, size_t n, __half* out, cudaStream_t s);
+cudaError_t launch_router_logits(const uint16_t* x, const float* wr, int T, int H, int E,
+                                 float* out, cudaStream_t s);
+cudaError_t launch_residual(uint16_t* x, const float* y, size_t n, cudaStream_t s);
+
+}  // namespace moe

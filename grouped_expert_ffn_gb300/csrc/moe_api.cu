@@ -1,0 +1,640 @@
+// The C ABI (include/moe.h): argument checks, plan workspace, weight packing, TMA tensor
+// maps, and the per-call launch sequence of the decode and prefill paths.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+using namespace moe;
+
+struct moe_plan_s {
+  int E = 0, k = 0, H = 0, I = 0, Is = 0, max_tokens = 0, Imax = 0, has_shared = 0;
+  int device = 0, num_sms = 0;
+  int bn_gu = 0, bn_d = 0;
+  size_t R_max = 0;
+  int max_items_gu = 0, max_items_d = 0;
+  // workspace (device)
+  __half* xq = nullptr;
+  float* sx = nullptr;
+  int* row_token = nullptr;
+  float* row_w = nullptr;
+  float* h32 = nullptr;
+  __half* hq = nullptr;
+  float* sh = nullptr;
+  int* counts = nullptr;
+  int* offsets = nullptr;
+  int* perm = nullptr;
+  unsigned long long* bmask = nullptr;
+  int* bhist = nullptr;
+  int4* items_gu = nullptr;
+  int4* items_d = nullptr;
+  int* n_items = nullptr;
+  int8_t* qtok = nullptr;
+  float* stok = nullptr;
+  int4* groups = nullptr;
+  int* n_groups = nullptr;
+  int* err = nullptr;
+  // taps
+  int debug = 0;
+  int32_t* tap_gu = nullptr;
+  int32_t* tap_d = nullptr;
+  int last_T = 0;
+  // per-stage timing
+  int profile = 0;
+  struct ProfRec {
+    int path;
+    cudaEvent_t ev[5];
+  };
+  std::vector<ProfRec> prof_pending;
+  std::vector<cudaEvent_t> ev_pool;
+  CUtensorMap tmA_gu, tmA_d;
+  std::vector<void*> allocs;
+};
+
+struct moe_packed_s {
+  moe_plan_s* plan = nullptr;
+  moe_weights w;
+  __half* gu16 = nullptr;
+  __half* d16 = nullptr;
+  __half* shgu16 = nullptr;
+  __half* shd16 = nullptr;
+  CUtensorMap tmB_gu, tmBs_gu, tmB_d, tmBs_d;
+};
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// fp16 tensor of `rank` dims (innermost first), box {64, box_rows[, 1]}, 128-byte swizzle.
+bool encode_f16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                const uint64_t* strides_bytes, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[3], st[2];
+  cuuint32_t box[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) d[i] = dims[i];
+  for (int i = 0; i < rank - 1; ++i) st[i] = strides_bytes[i];
+  box[0] = kBK;
+  box[1] = box_rows;
+  box[2] = 1;
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(base), d, st, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <class T>
+moe_status dalloc(moe_plan_s* p, T** out, size_t count) {
+  void* ptr = nullptr;
+  if (count == 0) count = 1;
+  if (cudaMalloc(&ptr, count * sizeof(T)) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_OOM;
+  }
+  p->allocs.push_back(ptr);
+  *out = static_cast<T*>(ptr);
+  return MOE_OK;
+}
+
+void free_plan(moe_plan_s* p) {
+  for (auto& r : p->prof_pending)
+    for (cudaEvent_t e : r.ev) p->ev_pool.push_back(e);
+  for (cudaEvent_t e : p->ev_pool) cudaEventDestroy(e);
+  for (void* a : p->allocs) cudaFree(a);
+  if (p->tap_gu) cudaFree(p->tap_gu);
+  if (p->tap_d) cudaFree(p->tap_d);
+  delete p;
+}
+
+int pick_bn(int cap, bool (*ok)(int, const moe_plan_s*), const moe_plan_s* p) {
+  for (int bn = 256; bn >= 64; bn >>= 1)
+    if (bn <= cap && ok(bn, p)) return bn;
+  return 0;
+}
+bool ok_gu(int bn, const moe_plan_s* p) {
+  return p->I % (bn / 2) == 0 && (p->Is == 0 || p->Is % (bn / 2) == 0);
+}
+bool ok_d(int bn, const moe_plan_s* p) { return p->H % bn == 0; }
+
+moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  if (e == cudaErrorMemoryAllocation) return MOE_ERR_OOM;
+  return MOE_ERR_CUDA;
+}
+
+// Five timing events for one forward, from the plan's pool (NULL when profiling is off).
+cudaEvent_t* prof_events(moe_plan_s* p, int path) {
+  if (!p->profile) return nullptr;
+  moe_plan_s::ProfRec r;
+  r.path = path;
+  for (int i = 0; i < 5; ++i) {
+    if (p->ev_pool.empty()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      p->ev_pool.push_back(e);
+    }
+    r.ev[i] = p->ev_pool.back();
+    p->ev_pool.pop_back();
+  }
+  p->prof_pending.push_back(r);
+  return p->prof_pending.back().ev;
+}
+
+size_t tap_bytes(const moe_plan_s* p, int which, int T) {
+  const size_t R = (size_t)T * p->k + (p->has_shared ? T : 0);
+  switch (which) {
+    case MOE_TAP_COUNTS: return (size_t)p->E * 4;
+    case MOE_TAP_OFFSETS: return (size_t)(p->E + 1) * 4;
+    case MOE_TAP_PERM: return (size_t)T * p->k * 4;
+    case MOE_TAP_QX: return (size_t)T * p->H;
+    case MOE_TAP_SX: return (size_t)T * 4;
+    case MOE_TAP_ACC_GU: return R * 2 * p->Imax * 4;
+    case MOE_TAP_HQ: return R * p->Imax;
+    case MOE_TAP_SH: return R * 4;
+    case MOE_TAP_ACC_D: return R * p->H * 4;
+    default: return 0;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_OOM: return "out of device memory";
+    case MOE_ERR_CAPACITY: return "more tokens than the plan's max_tokens";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE: return "device-side range check failed";
+    case MOE_ERR_NO_DEVICE: return "no sm_103 CUDA device";
+    default: return "unknown status";
+  }
+}
+
+moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens,
+                    moe_plan_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (E < 1 || top_k < 1 || top_k > E || H < 1 || I < 1 || I_shared < 0 || max_tokens < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (E > 256 || top_k > 8 || H % 64 || I % 64 || I_shared % 64 || H > 8192 || I > 4096 ||
+      I_shared > 4096 || max_tokens > (1 << 20))
+    return MOE_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_NO_DEVICE;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
+    cudaGetLastError();
+    return MOE_ERR_NO_DEVICE;
+  }
+  moe_plan_s* p = new (std::nothrow) moe_plan_s();
+  if (!p) return MOE_ERR_OOM;
+  p->E = E;
+  p->k = top_k;
+  p->H = H;
+  p->I = I;
+  p->Is = I_shared;
+  p->has_shared = I_shared > 0;
+  p->Imax = std::max(I, I_shared);
+  p->max_tokens = max_tokens;
+  p->device = dev;
+  p->num_sms = prop.multiProcessorCount;
+  const int nch_gu = (H + kChunkK - 1) / kChunkK;
+  const int nch_d = (p->Imax + kChunkK - 1) / kChunkK;
+  p->bn_gu = pick_bn(512 / nch_gu, ok_gu, p);
+  p->bn_d = pick_bn(512 / nch_d, ok_d, p);
+  if (!p->bn_gu || !p->bn_d) {
+    delete p;
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const size_t T = max_tokens;
+  p->R_max = T * top_k + (p->has_shared ? T : 0);
+  const size_t nblk = (T + kTokPerBlk - 1) / kTokPerBlk;
+  const size_t mtiles = (T * top_k + (size_t)(kBM - 1) * E) / kBM + (p->has_shared ? (T + kBM - 1) / kBM : 0) + 1;
+  p->max_items_gu = (int)(mtiles * (2 * p->Imax / p->bn_gu));
+  p->max_items_d = (int)(mtiles * (H / p->bn_d));
+  moe_status st = MOE_OK;
+#define ALLOC(ptr, n)                                  \
+  if ((st = dalloc(p, &p->ptr, (n))) != MOE_OK) {      \
+    free_plan(p);                                      \
+    return st;                                         \
+  }
+  ALLOC(xq, p->R_max * H);
+  ALLOC(sx, p->R_max);
+  ALLOC(row_token, p->R_max);
+  ALLOC(row_w, p->R_max);
+  ALLOC(h32, p->R_max * p->Imax);
+  ALLOC(hq, p->R_max * p->Imax);
+  ALLOC(sh, p->R_max);
+  ALLOC(counts, (size_t)E);
+  ALLOC(offsets, (size_t)E + 1);
+  ALLOC(perm, T * top_k);
+  ALLOC(bmask, nblk * E);
+  ALLOC(bhist, nblk * E);
+  ALLOC(items_gu, (size_t)p->max_items_gu);
+  ALLOC(items_d, (size_t)p->max_items_d);
+  ALLOC(n_items, 2);
+  ALLOC(qtok, T * H);
+  ALLOC(stok, T);
+  ALLOC(groups, (size_t)E + 1);
+  ALLOC(n_groups, 1);
+  ALLOC(err, 1);
+#undef ALLOC
+  if (cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess ||
+      cudaMemset(p->hq, 0, p->R_max * p->Imax * sizeof(__half)) != cudaSuccess) {
+    free_plan(p);
+    return MOE_ERR_CUDA;
+  }
+  // A operands of the two GEMMs: fp16 rows of the plan's row order.
+  {
+    const uint64_t dims[2] = {(uint64_t)H, (uint64_t)p->R_max};
+    const uint64_t st2[1] = {(uint64_t)H * 2};
+    if (!encode_f16(&p->tmA_gu, p->xq, 2, dims, st2, kBM)) {
+      free_plan(p);
+      return MOE_ERR_CUDA;
+    }
+    const uint64_t dims_d[2] = {(uint64_t)p->Imax, (uint64_t)p->R_max};
+    const uint64_t st_d[1] = {(uint64_t)p->Imax * 2};
+    if (!encode_f16(&p->tmA_d, p->hq, 2, dims_d, st_d, kBM)) {
+      free_plan(p);
+      return MOE_ERR_CUDA;
+    }
+  }
+  cudaError_t e = gemm_set_attributes();
+  if (e == cudaSuccess) e = decode_set_attributes(H, p->Imax);
+  if (e != cudaSuccess) {
+    free_plan(p);
+    return MOE_ERR_CUDA;
+  }
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status moe_plan_destroy(moe_plan_t plan) {
+  if (!plan) return MOE_ERR_INVALID_ARG;
+  free_plan(plan);
+  return MOE_OK;
+}
+
+moe_status moe_pack_weights(moe_plan_t p, const moe_weights* w, void* stream, moe_packed_t* out) {
+  if (!p || !w || !out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  const void* need[] = {w->w_gate, w->w_up, w->w_down, w->s_gate, w->s_up, w->s_down};
+  for (const void* q : need)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (p->has_shared) {
+    const void* nsh[] = {w->sh_gate, w->sh_up, w->sh_down, w->sh_s_gate, w->sh_s_up, w->sh_s_down};
+    for (const void* q : nsh)
+      if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  moe_packed_s* pk = new (std::nothrow) moe_packed_s();
+  if (!pk) return MOE_ERR_OOM;
+  pk->plan = p;
+  pk->w = *w;
+  const size_t E = p->E, H = p->H, I = p->I, Is = p->Is;
+  auto fail = [&](moe_status st) {
+    if (pk->gu16) cudaFree(pk->gu16);
+    if (pk->d16) cudaFree(pk->d16);
+    if (pk->shgu16) cudaFree(pk->shgu16);
+    if (pk->shd16) cudaFree(pk->shd16);
+    cudaGetLastError();
+    delete pk;
+    return st;
+  };
+  if (cudaMalloc(&pk->gu16, E * 2 * I * H * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
+  if (cudaMalloc(&pk->d16, E * H * I * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
+  if (p->has_shared) {
+    if (cudaMalloc(&pk->shgu16, 2 * Is * H * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
+    if (cudaMalloc(&pk->shd16, H * Is * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
+  }
+  cudaError_t e = launch_pack_gu(w->w_gate, w->w_up, (int)E, (int)I, (int)H, p->bn_gu, pk->gu16, s);
+  if (e == cudaSuccess) e = launch_widen(w->w_down, E * H * I, pk->d16, s);
+  if (e == cudaSuccess && p->has_shared) {
+    e = launch_pack_gu(w->sh_gate, w->sh_up, 1, (int)Is, (int)H, p->bn_gu, pk->shgu16, s);
+    if (e == cudaSuccess) e = launch_widen(w->sh_down, H * Is, pk->shd16, s);
+  }
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA);
+  bool ok = true;
+  {
+    const uint64_t dims[3] = {H, 2 * I, E};
+    const uint64_t st[2] = {H * 2, 2 * I * H * 2};
+    ok = ok && encode_f16(&pk->tmB_gu, pk->gu16, 3, dims, st, p->bn_gu);
+    const uint64_t dd[3] = {I, H, E};
+    const uint64_t sd[2] = {I * 2, H * I * 2};
+    ok = ok && encode_f16(&pk->tmB_d, pk->d16, 3, dd, sd, p->bn_d);
+    if (p->has_shared) {
+      const uint64_t ds[2] = {H, 2 * Is};
+      const uint64_t ss[1] = {H * 2};
+      ok = ok && encode_f16(&pk->tmBs_gu, pk->shgu16, 2, ds, ss, p->bn_gu);
+      const uint64_t dsd[2] = {Is, H};
+      const uint64_t ssd[1] = {Is * 2};
+      ok = ok && encode_f16(&pk->tmBs_d, pk->shd16, 2, dsd, ssd, p->bn_d);
+    } else {
+      pk->tmBs_gu = pk->tmB_gu;  // never read: no shared group exists
+      pk->tmBs_d = pk->tmB_d;
+    }
+  }
+  if (!ok) return fail(MOE_ERR_CUDA);
+  *out = pk;
+  return MOE_OK;
+}
+
+moe_status moe_packed_destroy(moe_packed_t pk) {
+  if (!pk) return MOE_ERR_INVALID_ARG;
+  if (pk->gu16) cudaFree(pk->gu16);
+  if (pk->d16) cudaFree(pk->d16);
+  if (pk->shgu16) cudaFree(pk->shgu16);
+  if (pk->shd16) cudaFree(pk->shd16);
+  delete pk;
+  return MOE_OK;
+}
+
+moe_status moe_route(moe_plan_t p, const float* logits, int T, int32_t* idx, float* w,
+                     void* stream) {
+  if (!p || !logits || !idx || !w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(idx) || !aligned16(w)) return MOE_ERR_INVALID_ARG;
+  if (T < 1) return MOE_ERR_INVALID_ARG;
+  if (T > p->max_tokens) return MOE_ERR_CAPACITY;
+  return cuda_status(launch_route(logits, T, p->E, p->k, idx, w, p->err,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
+                       const int32_t* idx, const float* w, float* y, void* stream) {
+  if (!p || !pk || !x || !idx || !w || !y || pk->plan != p) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(idx) || !aligned16(w) || !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  if (T < 1) return MOE_ERR_INVALID_ARG;
+  if (T > p->max_tokens) return MOE_ERR_CAPACITY;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int T_sh = p->has_shared ? T : 0;
+  const int R = T * p->k + T_sh;
+  p->last_T = T;
+  cudaError_t e;
+  if (T <= kDecodeMaxRows) {
+    DecodeArgs a;
+    a.idx = idx;
+    a.w = w;
+    a.x = x;
+    a.T = T;
+    a.k = p->k;
+    a.E = p->E;
+    a.H = p->H;
+    a.I = p->I;
+    a.Is = p->Is;
+    a.Imax = p->Imax;
+    a.has_shared = p->has_shared;
+    a.w_gate = pk->w.w_gate;
+    a.w_up = pk->w.w_up;
+    a.w_down = pk->w.w_down;
+    a.s_gate = pk->w.s_gate;
+    a.s_up = pk->w.s_up;
+    a.s_down = pk->w.s_down;
+    a.sh_gate = pk->w.sh_gate;
+    a.sh_up = pk->w.sh_up;
+    a.sh_down = pk->w.sh_down;
+    a.sh_s_gate = pk->w.sh_s_gate;
+    a.sh_s_up = pk->w.sh_s_up;
+    a.sh_s_down = pk->w.sh_s_down;
+    a.counts = p->counts;
+    a.offsets = p->offsets;
+    a.perm = p->perm;
+    a.groups = p->groups;
+    a.n_groups = p->n_groups;
+    a.row_token = p->row_token;
+    a.row_w = p->row_w;
+    a.qtok = p->qtok;
+    a.stok = p->stok;
+    a.h32 = p->h32;
+    a.hq = p->hq;
+    a.sh = p->sh;
+    a.y = y;
+    a.tap_gu = p->debug ? p->tap_gu : nullptr;
+    a.tap_d = p->debug ? p->tap_d : nullptr;
+    a.err = p->err;
+    e = launch_decode(a, s, prof_events(p, 1));
+    return cuda_status(e);
+  }
+  PrepArgs pa;
+  pa.idx = idx;
+  pa.w = w;
+  pa.x = x;
+  pa.T = T;
+  pa.k = p->k;
+  pa.E = p->E;
+  pa.H = p->H;
+  pa.I = p->I;
+  pa.Is = p->Is;
+  pa.has_shared = p->has_shared;
+  pa.bn_gu = p->bn_gu;
+  pa.bn_d = p->bn_d;
+  pa.bmask = p->bmask;
+  pa.bhist = p->bhist;
+  pa.counts = p->counts;
+  pa.offsets = p->offsets;
+  pa.perm = p->perm;
+  pa.items_gu = p->items_gu;
+  pa.items_d = p->items_d;
+  pa.n_items = p->n_items;
+  pa.xq = p->xq;
+  pa.sx = p->sx;
+  pa.row_token = p->row_token;
+  pa.row_w = p->row_w;
+  pa.y = y;
+  pa.qtok = p->debug ? p->qtok : nullptr;
+  pa.stok = p->debug ? p->stok : nullptr;
+  pa.err = p->err;
+  cudaEvent_t* ev = prof_events(p, 0);
+  if (ev) cudaEventRecord(ev[0], s);
+  if ((e = launch_prefill_prep(pa, s)) != cudaSuccess) return cuda_status(e);
+  if (ev) cudaEventRecord(ev[1], s);
+
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.E = p->E;
+  g.I = p->I;
+  g.Is = p->Is;
+  g.Imax = p->Imax;
+  g.H = p->H;
+  g.sx = p->sx;
+  g.s_g = pk->w.s_gate;
+  g.s_u = pk->w.s_up;
+  g.sh_s_g = pk->w.sh_s_gate;
+  g.sh_s_u = pk->w.sh_s_up;
+  g.h32 = p->h32;
+  g.s_h = p->sh;
+  g.s_d = pk->w.s_down;
+  g.sh_s_d = pk->w.sh_s_down;
+  g.row_token = p->row_token;
+  g.row_w = p->row_w;
+  g.y = y;
+  g.err = p->err;
+  const int grid = p->num_sms;
+  // gate/up: K = H for every group
+  g.items = p->items_gu;
+  g.n_items = p->n_items;
+  g.K_r = p->H;
+  g.K_s = p->H;
+  g.tap = p->debug ? p->tap_gu : nullptr;
+  if ((e = launch_grouped_gemm(true, p->bn_gu, g, p->tmA_gu, pk->tmB_gu, pk->tmBs_gu, grid, s)) !=
+      cudaSuccess)
+    return cuda_status(e);
+  if (ev) cudaEventRecord(ev[2], s);
+  if ((e = launch_requant(p->h32, R, T_sh, p->I, p->Is, p->Imax, p->hq, p->sh, s)) != cudaSuccess)
+    return cuda_status(e);
+  if (ev) cudaEventRecord(ev[3], s);
+  // down: K = I (routed) or I_shared (shared)
+  g.items = p->items_d;
+  g.n_items = p->n_items + 1;
+  g.K_r = p->I;
+  g.K_s = p->has_shared ? p->Is : p->I;
+  g.tap = p->debug ? p->tap_d : nullptr;
+  e = launch_grouped_gemm(false, p->bn_d, g, p->tmA_d, pk->tmB_d, pk->tmBs_d, grid, s);
+  if (ev) cudaEventRecord(ev[4], s);
+  return cuda_status(e);
+}
+
+moe_status moe_profile_enable(moe_plan_t p, int on) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  p->profile = on ? 1 : 0;
+  return MOE_OK;
+}
+
+moe_status moe_profile_read(moe_plan_t p, int path, float* ms_out, int* calls) {
+  if (!p || !ms_out || !calls || (path != 0 && path != 1)) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i) ms_out[i] = 0.0f;
+  *calls = 0;
+  std::vector<moe_plan_s::ProfRec> keep;
+  moe_status st = MOE_OK;
+  for (auto& r : p->prof_pending) {
+    if (r.path != path) {
+      keep.push_back(r);
+      continue;
+    }
+    const int nst = path == 0 ? 4 : 3;
+    if (cudaEventSynchronize(r.ev[nst]) != cudaSuccess) st = MOE_ERR_CUDA;
+    for (int i = 0; i < nst && st == MOE_OK; ++i) {
+      float ms = 0.0f;
+      if (cudaEventElapsedTime(&ms, r.ev[i], r.ev[i + 1]) != cudaSuccess) st = MOE_ERR_CUDA;
+      ms_out[i] += ms;
+    }
+    *calls += 1;
+    for (cudaEvent_t e : r.ev) p->ev_pool.push_back(e);
+  }
+  p->prof_pending.swap(keep);
+  return st;
+}
+
+moe_status moe_get_error(moe_plan_t p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return static_cast<moe_status>(v);
+}
+
+moe_status moe_clear_error(moe_plan_t p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaMemset(p->err, 0, sizeof(int)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_debug_enable(moe_plan_t p, int on) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (on && !p->tap_gu) {
+    if (cudaMalloc(&p->tap_gu, p->R_max * 2 * p->Imax * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&p->tap_d, p->R_max * p->H * sizeof(int32_t)) != cudaSuccess) {
+      cudaGetLastError();
+      if (p->tap_gu) cudaFree(p->tap_gu);
+      p->tap_gu = nullptr;
+      return MOE_ERR_OOM;
+    }
+  }
+  p->debug = on ? 1 : 0;
+  return MOE_OK;
+}
+
+size_t moe_debug_tap_bytes(moe_plan_t p, int which) {
+  if (!p) return 0;
+  return tap_bytes(p, which, p->last_T);
+}
+
+moe_status moe_debug_tap(moe_plan_t p, int which, void* dst, size_t bytes) {
+  if (!p || !dst || p->last_T < 1) return MOE_ERR_INVALID_ARG;
+  const size_t need = tap_bytes(p, which, p->last_T);
+  if (need == 0 || bytes != need) return MOE_ERR_INVALID_ARG;
+  if ((which == MOE_TAP_ACC_GU || which == MOE_TAP_ACC_D) && !p->tap_gu)
+    return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  const void* src = nullptr;
+  switch (which) {
+    case MOE_TAP_COUNTS: src = p->counts; break;
+    case MOE_TAP_OFFSETS: src = p->offsets; break;
+    case MOE_TAP_PERM: src = p->perm; break;
+    case MOE_TAP_QX: src = p->qtok; break;
+    case MOE_TAP_SX: src = p->stok; break;
+    case MOE_TAP_ACC_GU: src = p->tap_gu; break;
+    case MOE_TAP_SH: src = p->sh; break;
+    case MOE_TAP_ACC_D: src = p->tap_d; break;
+    case MOE_TAP_HQ: {
+      const size_t n = need;
+      std::vector<__half> tmp(n);
+      if (cudaMemcpy(tmp.data(), p->hq, n * sizeof(__half), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      int8_t* d = static_cast<int8_t*>(dst);
+      for (size_t i = 0; i < n; ++i) d[i] = static_cast<int8_t>(__half2float(tmp[i]));
+      return MOE_OK;
+    }
+    default: return MOE_ERR_INVALID_ARG;
+  }
+  return cudaMemcpy(dst, src, need, cudaMemcpyDeviceToHost) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_router_logits(const uint16_t* x, const float* w_router, int T, int H, int E,
+                             float* logits, void* stream) {
+  if (!x || !w_router || !logits || T < 1 || H < 16 || E < 1 || H % 16) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router_logits(x, w_router, T, H, E, logits,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_residual_add(uint16_t* x, const float* y, int T, int H, void* stream) {
+  if (!x || !y || T < 1 || H < 4 || H % 4) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_residual(x, y, (size_t)T * H, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,287 @@
+// Routing and the token-by-expert permutation of the prefill path.
+//
+//  route_kernel      warp per token: top-k of the fp32 logits (ties to the lowest expert id),
+//                    softmax over the selected logits.
+//  hist_kernel       per block of 64 tokens, one 64-bit token mask per expert (which of the
+//                    block's tokens chose it); its popcount is the block's histogram.
+//  scan_kernel       one block: per-expert counts, exclusive prefixes over blocks and over
+//                    experts, and the grouped-GEMM work lists (expert-tile queue).
+//  scatter_kernel    block per token: per-token int8 quantisation of x, written as fp16
+//                    integers into every row the token occupies (one per routed slot plus the
+//                    shared expert's row) with 16-byte stores; row metadata; y zeroed.
+// Row order: the shared expert's rows [0, T) first (row t = token t), then the routed
+// assignments grouped by expert id and, inside an expert, by token. This is the order a
+// stable sort of the flattened idx by expert id gives.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kMaxEPerLane = 8;  // E <= 256
+
+__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int k,
+                             int32_t* __restrict__ idx, float* __restrict__ w, int* err) {
+  const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (t >= T) return;
+  const float* l = logits + (size_t)t * E;
+  float v[kMaxEPerLane];
+  bool taken[kMaxEPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxEPerLane; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = e < E ? l[e] : 0.0f;
+    taken[i] = e >= E;
+  }
+  float sel_v[8];
+  int sel_e[8];
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    // lane-local best among untaken: highest value, then lowest id
+    float bv = 0.0f;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxEPerLane; ++i) {
+      const int e = i * 32 + lane;
+      if (!taken[i] && (be == 0x7fffffff || v[i] > bv)) {
+        bv = v[i];
+        be = e;
+      }
+    }
+    // warp argmax on (value desc, id asc); lanes with nothing left carry id = INT_MAX
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      const bool better = (oe != 0x7fffffff) &&
+                          (be == 0x7fffffff || ov > bv || (ov == bv && oe < be));
+      if (better) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    sel_v[j] = bv;
+    sel_e[j] = be;
+    if ((be & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < kMaxEPerLane; ++i)
+        if (i == (be >> 5)) taken[i] = true;
+    }
+  }
+  if (lane == 0) {
+    const float m = sel_v[0];
+    float ex[8];
+    float z = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      ex[j] = expf(sel_v[j] - m);
+      z += ex[j];
+    }
+    for (int j = 0; j < k; ++j) {
+      idx[(size_t)t * k + j] = sel_e[j];
+      w[(size_t)t * k + j] = ex[j] / z;
+    }
+  }
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                         int* err, cudaStream_t s) {
+  const int warps = 8;
+  route_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(logits, T, E, k, idx, w, err);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------
+__global__ void hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
+                            unsigned long long* __restrict__ bmask, int* __restrict__ bhist,
+                            int* err) {
+  extern __shared__ unsigned long long mask[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0ull;
+  __syncthreads();
+  const int t0 = blockIdx.x * kTokPerBlk;
+  const int n = min(kTokPerBlk, T - t0) * k;
+  for (int r = threadIdx.x; r < n; r += blockDim.x) {
+    const int e = idx[(size_t)t0 * k + r];
+    if (e < 0 || e >= E) {
+      set_error(err, kErrDevice);
+      continue;
+    }
+    const unsigned long long bit = 1ull << (r / k);
+    const unsigned long long old = atomicOr(&mask[e], bit);
+    if (old & bit) set_error(err, kErrDevice);  // an expert repeated within a token
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    bmask[(size_t)blockIdx.x * E + e] = mask[e];
+    bhist[(size_t)blockIdx.x * E + e] = __popcll(mask[e]);
+  }
+}
+
+// One block of 1024 threads. Turns bhist into exclusive per-expert prefixes over blocks,
+// writes counts/offsets and the two work lists (gate/up and down), ordered by group, then
+// weight tile, then row tile so that consecutive items reuse one weight tile from L2.
+__global__ void scan_kernel(PrepArgs a, int nblk) {
+  __shared__ int s_cnt[257];
+  __shared__ int s_off[258];
+  __shared__ int s_base_gu[258];
+  __shared__ int s_base_d[258];
+  const int E = a.E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      const int v = a.bhist[(size_t)b * E + e];
+      a.bhist[(size_t)b * E + e] = run;
+      run += v;
+    }
+    s_cnt[e] = run;
+    a.counts[e] = run;
+  }
+  __syncthreads();
+  const int T_sh = a.has_shared ? a.T : 0;
+  const int ng = E + (a.has_shared ? 1 : 0);
+  if (threadIdx.x == 0) {
+    int off = 0;
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = off;
+      a.offsets[e] = off;
+      off += s_cnt[e];
+    }
+    s_off[E] = off;
+    a.offsets[E] = off;
+    // group g: g < has_shared -> shared; else expert g - has_shared
+    int bg = 0, bd = 0;
+    for (int g = 0; g < ng; ++g) {
+      const bool sh = a.has_shared && g == 0;
+      const int cnt = sh ? a.T : s_cnt[g - a.has_shared];
+      const int mt = (cnt + kBM - 1) / kBM;
+      const int ntg = (2 * (sh ? a.Is : a.I)) / a.bn_gu;
+      const int ntd = a.H / a.bn_d;
+      s_base_gu[g] = bg;
+      s_base_d[g] = bd;
+      bg += mt * ntg;
+      bd += mt * ntd;
+    }
+    s_base_gu[ng] = bg;
+    s_base_d[ng] = bd;
+    a.n_items[0] = bg;
+    a.n_items[1] = bd;
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < ng; g += blockDim.x) {
+    const bool sh = a.has_shared && g == 0;
+    const int gid = sh ? E : g - a.has_shared;
+    const int cnt = sh ? a.T : s_cnt[gid];
+    const int row0 = sh ? 0 : T_sh + s_off[gid];
+    const int mt = (cnt + kBM - 1) / kBM;
+    const int ntg = (2 * (sh ? a.Is : a.I)) / a.bn_gu;
+    const int ntd = a.H / a.bn_d;
+    int p = s_base_gu[g];
+    for (int n = 0; n < ntg; ++n)
+      for (int m = 0; m < mt; ++m)
+        a.items_gu[p++] = make_int4(gid, row0 + m * kBM, min(kBM, cnt - m * kBM), n * a.bn_gu);
+    p = s_base_d[g];
+    for (int n = 0; n < ntd; ++n)
+      for (int m = 0; m < mt; ++m)
+        a.items_d[p++] = make_int4(gid, row0 + m * kBM, min(kBM, cnt - m * kBM), n * a.bn_d);
+  }
+}
+
+// Block per token: quantise x[t] once, write its fp16 integer codes to each of its rows.
+__global__ void scatter_kernel(PrepArgs a) {
+  const int t = blockIdx.x;
+  const int H = a.H, k = a.k, E = a.E;
+  const int T_sh = a.has_shared ? a.T : 0;
+  __shared__ int s_rows[9];
+  __shared__ float s_red[32];
+  if (threadIdx.x < k) {
+    const int j = threadIdx.x;
+    int e = a.idx[(size_t)t * k + j];
+    if (e < 0 || e >= E) e = 0;  // flagged by hist_kernel; keep the index in range
+    const int b = t / kTokPerBlk, tl = t % kTokPerBlk;
+    const unsigned long long m = a.bmask[(size_t)b * E + e];
+    const int rank = __popcll(m & ((1ull << tl) - 1ull));
+    int pos = a.offsets[e] + a.bhist[(size_t)b * E + e] + rank;
+    if (pos < 0 || pos >= a.T * k) {
+      set_error(a.err, kErrDevice);
+      pos = 0;
+    }
+    a.perm[pos] = t * k + j;
+    const int row = T_sh + pos;
+    s_rows[j] = row;
+    a.row_token[row] = t;
+    a.row_w[row] = a.w[(size_t)t * k + j];
+  } else if (threadIdx.x == k && a.has_shared) {
+    s_rows[k] = t;
+    a.row_token[t] = t;
+    a.row_w[t] = 1.0f;
+  }
+  // amax over the row (8 bf16 per thread per pass)
+  const uint16_t* xr = a.x + (size_t)t * H;
+  float amax = 0.0f;
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_float((uint16_t)(u[i] & 0xffffu))));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_float((uint16_t)(u[i] >> 16))));
+    }
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x / 32] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < blockDim.x / 32 ? s_red[threadIdx.x] : 0.0f;
+    v = warp_max(v);
+    if (threadIdx.x == 0) s_red[0] = v;
+  }
+  __syncthreads();
+  const float s = __fdiv_rn(s_red[0], 127.0f);
+  const int nrows = k + (a.has_shared ? 1 : 0);
+  if (threadIdx.x < nrows) a.sx[s_rows[threadIdx.x]] = s;
+  if (threadIdx.x == 0 && a.stok) a.stok[t] = s;
+  float* yr = a.y + (size_t)t * H;
+  for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    int q[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = bf16_bits_to_float((uint16_t)(u[i] & 0xffffu));
+      const float hi = bf16_bits_to_float((uint16_t)(u[i] >> 16));
+      q[2 * i] = s > 0.0f ? quant_code(lo, s) : 0;
+      q[2 * i + 1] = s > 0.0f ? quant_code(hi, s) : 0;
+    }
+    uint4 hv;
+    uint32_t* hw = reinterpret_cast<uint32_t*>(&hv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h2 = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
+      hw[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    for (int r = 0; r < nrows; ++r)
+      *reinterpret_cast<uint4*>(a.xq + (size_t)s_rows[r] * H + c) = hv;
+    if (a.qtok) {
+      uint2 qv;
+      uint8_t* qb = reinterpret_cast<uint8_t*>(&qv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) qb[i] = (uint8_t)(int8_t)q[i];
+      *reinterpret_cast<uint2*>(a.qtok + (size_t)t * H + c) = qv;
+    }
+    *reinterpret_cast<float4*>(yr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(yr + c + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s) {
+  const int nblk = (a.T + kTokPerBlk - 1) / kTokPerBlk;
+  hist_kernel<<<nblk, 256, a.E * sizeof(unsigned long long), s>>>(a.idx, a.T, a.k, a.E, a.bmask,
+                                                                  a.bhist, a.err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  scan_kernel<<<1, 1024, 0, s>>>(a, nblk);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  scatter_kernel<<<a.T, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,176 @@
+/*
+ * moe.h - C ABI of the grouped-expert MoE FFN library for GB300 (sm_103a).
+ *
+ * The layer: per token, top-k softmax routing over E experts; every routed expert and the
+ * always-on shared expert apply a W8A8 SwiGLU FFN (int8 gate/up GEMM, SiLU(gate)*up,
+ * requantisation, int8 down GEMM); the expert outputs are combined with the routing weights
+ * (shared expert weight 1). All routed experts are computed as ONE grouped computation
+ * instead of one launch per expert: the remedy the page "Qwen3.6-35B-A3B Linux v1.0.4:
+ * ~2.7s fixed per-request TTFT = ~4,900 serialized per-expert NPU execs ..." proposes in
+ * section "The fix (concatenated-expert dispatch)" (one run per operator per layer-block,
+ * N = TOP_K x 2 x IM_EXP). Batched decode (T <= 8 rows) deduplicates experts across rows
+ * and streams each unique expert's int8 weights once with an int8 dot, as the page
+ * "[job] Strix Halo: multi-session serving ... #145", section "Status", item "Next" asks.
+ *
+ * Conventions (every entry point):
+ *  - Data pointers are DEVICE pointers unless a comment says host. Tensors are row-major
+ *    and contiguous; every data pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Calls that
+ *    take a stream are asynchronous on it and never synchronise the host, except where
+ *    stated.
+ *  - Errors: argument and shape errors are detected on the host and returned before any
+ *    work is queued. Device-side failures (a bounded wait that ran out, an index out of
+ *    range) set a sticky error word in the plan, read by moe_get_error. No entry point
+ *    aborts, throws, or falls back to a CPU path.
+ *  - Numerics: integer results (routing indices, permutation, int32 accumulators) are
+ *    exact; floating point is fp32.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, T out of range        */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape the kernels do not support (see moe_plan)          */
+  MOE_ERR_OOM = 3,          /* device allocation failed                                 */
+  MOE_ERR_CAPACITY = 4,     /* T larger than the plan's max_tokens                      */
+  MOE_ERR_CUDA = 5,         /* a CUDA runtime call failed                               */
+  MOE_ERR_TIMEOUT = 6,      /* a device-side bounded wait ran out (sticky)              */
+  MOE_ERR_DEVICE = 7,       /* a device-side range check failed (sticky)                */
+  MOE_ERR_NO_DEVICE = 8     /* no CUDA device, or not an sm_103 GPU                     */
+} moe_status;
+
+typedef struct moe_plan_s* moe_plan_t;      /* shapes + workspace, one per layer shape   */
+typedef struct moe_packed_s* moe_packed_t;  /* one layer's weights, repacked for the GPU */
+
+/* One layer's quantised weights (device pointers, caller-owned).
+ * Routed experts: w_gate, w_up int8 [E, I, H]; w_down int8 [E, H, I];
+ *                 s_gate, s_up fp32 [E, I]; s_down fp32 [E, H] (per output channel).
+ * Shared expert (only when the plan has I_shared > 0, else all NULL):
+ *                 sh_gate, sh_up int8 [I_shared, H]; sh_down int8 [H, I_shared];
+ *                 sh_s_gate, sh_s_up fp32 [I_shared]; sh_s_down fp32 [H].
+ * Dequantised weight = int8 value * scale of its output channel. */
+typedef struct {
+  const int8_t* w_gate;
+  const int8_t* w_up;
+  const int8_t* w_down;
+  const float* s_gate;
+  const float* s_up;
+  const float* s_down;
+  const int8_t* sh_gate;
+  const int8_t* sh_up;
+  const int8_t* sh_down;
+  const float* sh_s_gate;
+  const float* sh_s_up;
+  const float* sh_s_down;
+} moe_weights;
+
+/* Create a plan for one layer shape and allocate its workspace for up to max_tokens
+ * tokens per call (the only allocation on the forward path's behalf).
+ *   E: routed experts (1..256); top_k: 1..min(E, 8); H: hidden size; I: routed expert
+ *   intermediate size; I_shared: shared expert intermediate size, 0 = no shared expert.
+ * Supported shapes: H and I (and I_shared when > 0) multiples of 64; H <= 8192;
+ *   I, I_shared <= 4096. Otherwise MOE_ERR_UNSUPPORTED.
+ * Uses the current CUDA device. *out receives the handle; release with moe_plan_destroy. */
+MOE_API moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens,
+                    moe_plan_t* out);
+
+/* Free the plan and its workspace. Work queued on it must have completed. */
+MOE_API moe_status moe_plan_destroy(moe_plan_t plan);
+
+/* Register one layer's weights with the plan's shapes. Allocates and fills (on `stream`)
+ * the device copy the tensor-core path reads (gate/up rows interleaved in N-tile blocks, the
+ * int8 values widened to fp16, which represents every int8 exactly); the decode path reads
+ * the caller's int8 arrays and scales directly, so they must stay alive and unchanged while
+ * the packed handle is in use. Release with moe_packed_destroy. */
+MOE_API moe_status moe_pack_weights(moe_plan_t plan, const moe_weights* w, void* stream,
+                            moe_packed_t* out);
+MOE_API moe_status moe_packed_destroy(moe_packed_t packed);
+
+/* Top-k softmax routing (warp per token).
+ *   logits fp32 [T, E] -> idx int32 [T, top_k], w fp32 [T, top_k].
+ * Selection compares the fp32 logits; ties go to the lowest expert id; slots are ordered by
+ * logit descending, then id ascending. w is a softmax over the selected logits, so each
+ * row sums to 1 (within 1e-6). Logits must be finite. 1 <= T <= max_tokens. */
+MOE_API moe_status moe_route(moe_plan_t plan, const float* logits, int T, int32_t* idx, float* w,
+                     void* stream);
+
+/* The MoE layer: y fp32 [T, H] = sum_j w[t,j] * expert_{idx[t,j]}(x[t]) + shared(x[t]).
+ *   x bf16 [T, H] (raw bf16 bits); idx, w as produced by moe_route (any valid top-k
+ *   routing: idx[t,*] distinct, in [0, E)); y is overwritten.
+ * T <= 8 runs the deduplicated weight-streaming decode kernels; larger T runs the grouped
+ * tensor-core GEMMs. Both give identical integer accumulators. Allocates nothing, never
+ * synchronises, and may be captured in a CUDA graph. The workspace is per plan: calls on
+ * one plan must not overlap in time (use one plan per concurrent stream). */
+MOE_API moe_status moe_forward(moe_plan_t plan, moe_packed_t packed, const uint16_t* x, int T,
+                       const int32_t* idx, const float* w, float* y, void* stream);
+
+/* Sticky device-side error word of the plan (synchronises the device). MOE_OK if none. */
+MOE_API moe_status moe_get_error(moe_plan_t plan);
+/* Clear the sticky error word (synchronises the device). */
+MOE_API moe_status moe_clear_error(moe_plan_t plan);
+
+/* Short static description of a status code. */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* ---- test taps: copies of intermediate results of the last moe_forward ----------------
+ * moe_debug_enable(plan, 1) allocates tap buffers and makes later forwards also write the
+ * int32 accumulators (it is the one call besides moe_plan/moe_pack_weights that allocates).
+ * Rows are in the plan's row order: rows [0, T) are the shared expert's (row t = token t),
+ * when I_shared > 0; then the routed assignments, grouped by expert id and, inside an
+ * expert, by (token, slot) ascending. moe_debug_tap copies one tap to HOST memory
+ * `dst_host` (synchronises the device); `bytes` must equal the tap's size for the last
+ * forward's T, as given by moe_debug_tap_bytes. */
+typedef enum {
+  MOE_TAP_COUNTS = 0,   /* int32 [E]              tokens per routed expert               */
+  MOE_TAP_OFFSETS = 1,  /* int32 [E + 1]          exclusive prefix of COUNTS             */
+  MOE_TAP_PERM = 2,     /* int32 [T*top_k]        flat slot t*top_k+j of each routed row */
+  MOE_TAP_QX = 3,       /* int8  [T, H]           quantised activations                  */
+  MOE_TAP_SX = 4,       /* fp32  [T]              activation scales                      */
+  MOE_TAP_ACC_GU = 5,   /* int32 [R, 2*Imax]      gate accumulators, then up accumulators */
+  MOE_TAP_HQ = 6,       /* int8  [R, Imax]        requantised SiLU(gate)*up               */
+  MOE_TAP_SH = 7,       /* fp32  [R]              scales of HQ                            */
+  MOE_TAP_ACC_D = 8     /* int32 [R, H]           down accumulators                       */
+} moe_tap;              /* R = T*top_k + (I_shared > 0 ? T : 0); Imax = max(I, I_shared)   */
+
+MOE_API moe_status moe_debug_enable(moe_plan_t plan, int on);
+MOE_API size_t moe_debug_tap_bytes(moe_plan_t plan, int which);
+MOE_API moe_status moe_debug_tap(moe_plan_t plan, int which, void* dst_host, size_t bytes);
+
+/* ---- per-stage device timing (benchmark instrument) ----------------------------------
+ * When enabled, every moe_forward also records CUDA events around its kernels on the call's
+ * stream (no extra synchronisation). moe_profile_read synchronises on those events and
+ * writes, for the chosen path (0 = prefill, 1 = decode), the summed device milliseconds of
+ * each stage over all forwards since the previous read into ms_out[4] and their number into
+ * *calls, then starts a new accumulation. Stages: prefill {permute+quant, gate/up GEMM,
+ * requant, down GEMM + combine}; decode {dedup+quant, gate/up stream, down stream +
+ * combine, 0}. Not for use inside CUDA graph capture. */
+MOE_API moe_status moe_profile_enable(moe_plan_t plan, int on);
+MOE_API moe_status moe_profile_read(moe_plan_t plan, int path, float* ms_out, int* calls);
+
+/* ---- the two steps around the layer in a stacked prefill -------------------------------
+ * Router projection: logits fp32 [T, E] = float(x bf16 [T, H]) @ w_router fp32 [H, E],
+ * fp32 accumulation. Residual: x[t,h] <- bf16_round_nearest_even(float(x[t,h]) + y[t,h]),
+ * x bf16 [T, H] updated in place, y fp32 [T, H]. Neither needs a plan. */
+MOE_API moe_status moe_router_logits(const uint16_t* x, const float* w_router, int T, int H, int E,
+                             float* logits, void* stream);
+MOE_API moe_status moe_residual_add(uint16_t* x, const float* y, int T, int H, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,112 @@
+"""Shared test helpers: run one layer through the C ABI and compare it with the oracle.
+
+Inputs come from synth (seeded); expected values come only from the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+import grouped_expert_ffn_gb300 as moe
+
+# Output tolerance of the layer (fp32 output against the oracle's double combine).
+Y_MAX_REL = 1e-2      # max |dy| <= Y_MAX_REL * max |y_ref|
+Y_RMSE_REL = 5e-3     # rms(dy) <= Y_RMSE_REL * rms(y_ref)
+W_ABS = 1e-6          # routing weights
+HQ_MISMATCH_FRAC = 1e-3
+
+
+def weights_to(W: dict, device) -> dict:
+    return {k: v.to(device).contiguous() for k, v in W.items()}
+
+
+def oracle_layer(W: dict, sh: synth.LayerShape) -> oracle.Layer:
+    return oracle.Layer({k: v.cpu() for k, v in W.items()}, sh.E, sh.k, sh.H, sh.I, sh.Is)
+
+
+def y_errors(y, y_ref):
+    y = np.asarray(y, np.float64)
+    d = y - y_ref
+    mx = np.abs(d).max() / max(np.abs(y_ref).max(), 1e-30)
+    rm = np.sqrt((d ** 2).mean()) / max(np.sqrt((y_ref ** 2).mean()), 1e-30)
+    return mx, rm
+
+
+def row_map(perm: np.ndarray, T: int, k: int, has_shared: bool):
+    """row[t, slot] in the library's row order (slot k = shared expert)."""
+    T_sh = T if has_shared else 0
+    rows = np.full((T, k + 1), -1, np.int64)
+    if has_shared:
+        rows[:, k] = np.arange(T)
+    p = np.arange(T * k)
+    rows[perm // k, perm % k] = T_sh + p
+    return rows
+
+
+def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L: oracle.Layer,
+                sample=None, layer: moe.MoELayer | None = None, plan_tokens=None):
+    """Full parity of one layer call. Returns a dict of statistics."""
+    dev = torch.device("cuda")
+    T, k, E, H = sh.T, sh.k, sh.E, sh.H
+    own = layer is None
+    if own:
+        layer = moe.MoELayer(E, k, H, sh.I, sh.Is, plan_tokens or T, W_dev)
+    try:
+        x = x_cpu.to(dev)
+        lg = logits_cpu.to(dev)
+        idx_g, w_g = layer.route(lg)
+        idx_o, w_o = oracle.route(logits_cpu, k)
+        idx_g_h = idx_g.cpu().numpy()
+        assert (idx_g_h == idx_o).all(), "routing indices differ"
+        assert np.abs(w_g.cpu().numpy() - w_o).max() <= W_ABS
+        moe.moe_debug_enable(layer.plan, True)
+        y = layer.forward(x, idx_g, w_g)
+        torch.cuda.synchronize()
+        assert moe.moe_get_error(layer.plan) == 0
+        tap = {n: moe.moe_debug_tap(layer.plan, i) for n, i in (
+            ("counts", moe.TAP_COUNTS), ("offsets", moe.TAP_OFFSETS), ("perm", moe.TAP_PERM),
+            ("qx", moe.TAP_QX), ("sx", moe.TAP_SX), ("acc_gu", moe.TAP_ACC_GU), ("hq", moe.TAP_HQ),
+            ("sh", moe.TAP_SH), ("acc_d", moe.TAP_ACC_D))}
+        counts, offsets, perm = oracle.permute(idx_o, E)
+        assert (tap["counts"] == counts).all()
+        assert (tap["offsets"] == offsets).all()
+        assert (tap["perm"] == perm).all()
+        q_o, s_o = oracle.quant_rows(x_cpu)
+        assert (tap["qx"].reshape(T, H) == q_o).all()
+        assert (tap["sx"] == s_o).all()
+
+        toks = np.arange(T) if sample is None else np.asarray(sample)
+        y_o, tp = oracle.forward(L, x_cpu[torch.from_numpy(toks)], idx_o[toks], w_o[toks], taps=True)
+        has_sh = sh.Is > 0
+        Imax = max(sh.I, sh.Is)
+        R = T * k + (T if has_sh else 0)
+        rows = row_map(perm, T, k, has_sh)
+        acc_gu = tap["acc_gu"].reshape(R, 2, Imax)
+        hq = tap["hq"].reshape(R, Imax)
+        shs = tap["sh"]
+        acc_d = tap["acc_d"].reshape(R, H)
+        n_hq_diff = 0
+        n_hq = 0
+        n_rows_d = 0
+        for i, t in enumerate(toks):
+            for s in range(k + (1 if has_sh else 0)):
+                Ig = sh.Is if s == k else sh.I
+                r = rows[t, s]
+                assert (acc_gu[r, :, :Ig] == tp["acc_gu"][i, s, :, :Ig]).all(), (t, s)
+                dq = np.abs(hq[r, :Ig].astype(np.int32) - tp["hq"][i, s, :Ig].astype(np.int32))
+                assert dq.max() <= 1, (t, s)
+                n_hq_diff += int((dq != 0).sum())
+                n_hq += Ig
+                if dq.max() == 0 and shs[r] == tp["sh"][i, s]:
+                    assert (acc_d[r] == tp["acc_d"][i, s]).all(), (t, s)
+                    n_rows_d += 1
+        assert n_hq_diff <= HQ_MISMATCH_FRAC * n_hq, (n_hq_diff, n_hq)
+        yg = y.cpu().numpy().astype(np.float64)[toks]
+        mx, rm = y_errors(yg, y_o)
+        assert mx <= Y_MAX_REL and rm <= Y_RMSE_REL, (mx, rm)
+        return dict(max_rel=mx, rmse_rel=rm, hq_diff=n_hq_diff, hq_total=n_hq,
+                    rows_down_exact=n_rows_d, y=y, idx=idx_g, w=w_g, tap=tap)
+    finally:
+        if own:
+            layer.close()
