@@ -1,8 +1,9 @@
 """Benchmark of the grouped-expert MoE FFN layer on one GB300 (one JSON line on stdout).
 
 Default workload: the 40-layer stacked prefill at T=2600 (35B-A3B-shaped layers, H=2048,
-E=128, top_k=8, I=512, shared expert I=512, distinct seeded weights per layer, router logits
-= x @ W_r per layer, residual x <- bf16(x + y)). One step = the whole stack over one batch.
+E=128, top_k=8, I=512, shared expert I=512, distinct seeded weights per layer; per layer the
+input is RMS-normalised (parameter-free pre-norm), router logits = x_in @ W_r, and the
+residual x <- bf16(x + y)). One step = the whole stack over one batch.
 `value` = MoE-layer tokens per second (T x 40 per step). The same run also measures batched
 decode at C=8 rows through the same 40 layers' weights (microseconds per layer and the HBM
 roofline over the unique experts' bytes).
@@ -154,6 +155,7 @@ def oracle_sample_rate(W_dev, wl, n_tokens, nthreads):
     x = synth.make_activations(sh.T, sh.H, wl.seed)[:n_tokens].contiguous()
     wr = synth.make_router_weight(sh.H, sh.E, wl.seed)
     t0 = time.perf_counter()
+    _, x = oracle.rmsnorm_residual(x)
     lg = oracle.router_logits(x, wr, nthreads=nthreads).astype(np.float32)
     idx, w = oracle.route(lg, sh.k)
     oracle.forward(L, x, idx, w, nthreads=nthreads)
@@ -161,93 +163,11 @@ def oracle_sample_rate(W_dev, wl, n_tokens, nthreads):
     return n_tokens / dt, dt
 
 
-def run_ours(args, world, rank):
-    import grouped_expert_ffn_gb300 as moe
-    peaks, peak_src = load_peaks()
+def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
+    """Batched decode, C=8 rows, through the same layers' weights (CUDA graph of
+    route + forward per layer); microseconds per layer and the HBM roofline."""
     dev = torch.device("cuda")
-    wl = synth.WORKLOADS["stack"]
-    sh = wl.shape
-    n_layers = args.layers
-    plan, layers = build_stack(moe, wl, n_layers, dev)
-    T, H, E, k = sh.T, sh.H, sh.E, sh.k
-    x0 = synth.make_activations(T, H, wl.seed, wl.outliers, dev)
-    x = torch.empty_like(x0)
-    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
-    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-    w = torch.empty((T, k), dtype=torch.float32, device=dev)
-    y = torch.empty((T, H), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step():
-        x.copy_(x0)
-        for (W, wr, packed) in layers:
-            moe.moe_router_logits(x, wr, logits)
-            moe.moe_route(plan, logits, idx, w)
-            moe.moe_forward(plan, packed, x, idx, w, y)
-            moe.moe_residual_add(x, y)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert moe.moe_get_error(plan) == 0
-    moe.moe_profile_enable(plan, True)
-    clocks = Clocks()
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    moe.moe_profile_enable(plan, False)
-    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
-    st, calls = moe.moe_profile_read(plan, 0)
-    stage_ms = [v / max(calls, 1) for v in st]
-    assert moe.moe_get_error(plan) == 0
-    ms_step = ms_total / args.steps
-    layer_tokens = T * n_layers
-    value = layer_tokens * world / (ms_step / 1e3)
-
-    # roofline of the dominant kernel (gate/up GEMM): 2*R*2I*H flops per launch
-    R = T * k + T
-    gu_flops = 2.0 * R * 2 * sh.I * H
-    gu_ms = stage_ms[1]
-    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
-    achieved_tf = gu_flops / (gu_ms / 1e3) / 1e12
-    down_flops = 2.0 * R * H * sh.I
-    layer_flops = gu_flops + down_flops
-    moe_ms = sum(stage_ms)
-
-    # ---- e2e: host (pinned) x in, host result out, inside the timed region
-    x_host = x0.cpu().pin_memory()
-    out_host = torch.empty_like(x_host).pin_memory()
-
-    def step_e2e():
-        x.copy_(x_host, non_blocking=True)
-        for (W, wr, packed) in layers:
-            moe.moe_router_logits(x, wr, logits)
-            moe.moe_route(plan, logits, idx, w)
-            moe.moe_forward(plan, packed, x, idx, w, y)
-            moe.moe_residual_add(x, y)
-        out_host.copy_(x, non_blocking=True)
-
-    step_e2e()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step_e2e()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
-    e2e_value = layer_tokens * world / (ms_e2e / 1e3)
-
-    # ---- decode: C=8 rows through the same 40 layers' weights (CUDA graph of route+forward)
+    n_layers = len(layers)
     dwl = synth.WORKLOADS["decode"]
     xd = synth.make_activations(dwl.shape.T, H, dwl.seed, dwl.outliers, dev)
     lgd = synth.make_logits(dwl.shape.T, E, dwl.seed, dwl.zipf_s, dev)
@@ -275,11 +195,13 @@ def run_ours(args, world, rank):
         g.replay()
     torch.cuda.synchronize()
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = max(args.steps, 5)
+    reps = max(steps, 20)
+    torch.cuda.nvtx.range_push("timed_decode")
     d0.record(stream)
     for _ in range(reps):
         g.replay()
     d1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     us_layer = d0.elapsed_time(d1) * 1e3 / reps / n_layers
     # per-stage decode timing (eager, profiled)
@@ -290,11 +212,120 @@ def run_ours(args, world, rank):
     st, calls = moe.moe_profile_read(plan, 1)
     moe.moe_profile_enable(plan, False)
     dstage_us = [v * 1e3 / max(calls, 1) for v in st][:3]
-    bpe = synth.weight_bytes_per_expert(H, sh.I)
+    bpe = synth.weight_bytes_per_expert(H, I)
     uniq_bytes = (U + 1) * bpe
     hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
     dec_gbs = uniq_bytes / (us_layer * 1e-6) / 1e9
     kern_us = dstage_us[1] + dstage_us[2]
+
+    return {"workload": "C=8 rows, T=8, Zipf(1.1) routing, outliers, through the stack's 40 layers' weights",
+            "us_per_layer": us_layer, "unique_experts": U,
+            "unique_bytes_per_layer": uniq_bytes, "achieved_gbs": dec_gbs,
+            "hbm_peak_gbs": hbm, "frac": dec_gbs / hbm,
+            "stage_us": {"dedup_quant": dstage_us[0], "gate_up_stream": dstage_us[1],
+                         "down_stream_combine": dstage_us[2]},
+            "kernel_gbs": uniq_bytes / (kern_us * 1e-6) / 1e9 if kern_us > 0 else None}
+
+
+def run_ours(args, world, rank):
+    import grouped_expert_ffn_gb300 as moe
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda")
+    wl = synth.WORKLOADS["stack"]
+    sh = wl.shape
+    n_layers = args.layers
+    plan, layers = build_stack(moe, wl, n_layers, dev)
+    T, H, E, k = sh.T, sh.H, sh.E, sh.k
+    x0 = synth.make_activations(T, H, wl.seed, wl.outliers, dev)
+    x = torch.empty_like(x0)
+    x_in = torch.empty_like(x0)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def stack():
+        # layer l: x_in = rmsnorm(x) -> logits = x_in @ W_r -> route -> y = moe(x_in) -> x += y
+        for l, (W, wr, packed) in enumerate(layers):
+            moe.moe_rmsnorm_residual(x, y if l else None, x_in)
+            moe.moe_router_logits(x_in, wr, logits)
+            moe.moe_route(plan, logits, idx, w)
+            moe.moe_forward(plan, packed, x_in, idx, w, y)
+        moe.moe_residual_add(x, y)
+
+    def step():
+        x.copy_(x0)
+        stack()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    err = moe.moe_get_error(plan)
+    if err:
+        raise moe.MoeError(err, "stacked prefill warm-up")
+    moe.moe_profile_enable(plan, True)
+    clocks = Clocks()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed_prefill")
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    moe.moe_profile_enable(plan, False)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
+    st, calls = moe.moe_profile_read(plan, 0)
+    stage_ms = [v / max(calls, 1) for v in st]
+    assert moe.moe_get_error(plan) == 0
+    ms_step = ms_total / args.steps
+    layer_tokens = T * n_layers
+    value = layer_tokens * world / (ms_step / 1e3)
+
+    # roofline of the dominant kernel (gate/up GEMM): 2*R*2I*H flops per launch
+    R = T * k + T
+    gu_flops = 2.0 * R * 2 * sh.I * H
+    gu_ms = stage_ms[1]
+    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    achieved_tf = gu_flops / (gu_ms / 1e3) / 1e12
+    down_flops = 2.0 * R * H * sh.I
+    layer_flops = gu_flops + down_flops
+    moe_ms = sum(stage_ms)
+
+    # ---- e2e: host (pinned) x in, host result out, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        x_host = x0.cpu().pin_memory()
+        out_host = torch.empty_like(x_host).pin_memory()
+
+        def step_e2e():
+            x.copy_(x_host, non_blocking=True)
+            stack()
+            out_host.copy_(x, non_blocking=True)
+
+        step_e2e()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step_e2e()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+        e2e_value = layer_tokens * world / (ms_e2e / 1e3)
+
+        e2e = {"value": e2e_value, "unit": "MoE-layer tokens/s",
+               "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2}
+
+    decode = None if args.no_decode else measure_decode(
+        moe, plan, layers, peaks, H, E, k, sh.I, args.steps, stream)
 
     # ---- oracle CPU baseline (bounded sample, rank 0 only, N=1 only)
     cpu = None
@@ -306,7 +337,7 @@ def run_ours(args, world, rank):
                "sample": f"{n_tok} tokens of layer 0 of the stack (router projection + route + "
                          f"layer), {secs:.1f} s"}
 
-    n_launch = n_layers * 9 * args.steps
+    n_launch = (n_layers * 9 + 1) * args.steps
     line = {
         "metric": METRIC,
         "value": value,
@@ -336,15 +367,8 @@ def run_ours(args, world, rank):
                      "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 = bf16 rate)",
                      "flops_per_launch": gu_flops},
         "layer_tflops": layer_flops / (moe_ms / 1e3) / 1e12,
-        "decode": {"workload": f"C=8 rows, T=8, Zipf(1.1) routing, same 40 layers' weights",
-                   "us_per_layer": us_layer, "unique_experts": U,
-                   "unique_bytes_per_layer": uniq_bytes, "achieved_gbs": dec_gbs,
-                   "hbm_peak_gbs": hbm, "frac": dec_gbs / hbm,
-                   "stage_us": {"dedup_quant": dstage_us[0], "gate_up_stream": dstage_us[1],
-                                "down_stream_combine": dstage_us[2]},
-                   "kernel_gbs": uniq_bytes / (kern_us * 1e-6) / 1e9 if kern_us > 0 else None},
-        "e2e": {"value": e2e_value, "unit": "MoE-layer tokens/s",
-                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
+        "decode": decode,
+        "e2e": e2e,
         "gpu_launches": n_launch,
         "clocks": clk,
         "cpu_baseline": cpu,
@@ -371,6 +395,7 @@ def run_reference(args, world, rank):
     def step(i):
         off = (i * n_tok) % (sh.T - n_tok)
         x = x_all[off:off + n_tok].contiguous()
+        _, x = oracle.rmsnorm_residual(x)
         lg = oracle.router_logits(x, wr, nthreads=nthreads).astype(np.float32)
         idx, w = oracle.route(lg, sh.k)
         oracle.forward(L, x, idx, w, nthreads=nthreads)
@@ -400,7 +425,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=40)
@@ -409,6 +434,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=512,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     args = ap.parse_args()
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

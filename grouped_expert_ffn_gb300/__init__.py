@@ -67,6 +67,7 @@ def lib() -> C.CDLL:
             "moe_profile_read": ([vp, i32, C.POINTER(C.c_float), C.POINTER(C.c_int)], i32),
             "moe_router_logits": ([vp, vp, i32, i32, i32, vp, vp], i32),
             "moe_residual_add": ([vp, vp, i32, i32, vp], i32),
+            "moe_rmsnorm_residual": ([vp, vp, vp, i32, i32, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -192,6 +193,13 @@ def moe_router_logits(x, w_router, logits, stream=None):
 def moe_residual_add(x, y, stream=None):
     T, H = x.shape
     _check(lib().moe_residual_add(_ptr(x), _ptr(y), T, H, _stream(stream)), "moe_residual_add")
+
+
+def moe_rmsnorm_residual(x, y, x_in, stream=None):
+    """x <- bf16(x + y) when y is not None, then x_in <- bf16(x / rms(x))."""
+    T, H = x.shape
+    _check(lib().moe_rmsnorm_residual(_ptr(x), _ptr(y), _ptr(x_in), T, H, _stream(stream)),
+           "moe_rmsnorm_residual")
 
 
 # ---- convenience wrapper ---------------------------------------------------------------

@@ -157,6 +157,67 @@ __global__ void residual_kernel(uint16_t* __restrict__ x, const float* __restric
   }
 }
 
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+// Block per token: optional residual update of x, then the RMS-normalised copy x_in.
+__global__ void rmsnorm_residual_kernel(uint16_t* __restrict__ x, const float* __restrict__ y,
+                                        uint16_t* __restrict__ x_in, int H) {
+  const int t = blockIdx.x;
+  uint16_t* xr = x + (size_t)t * H;
+  __shared__ float red[32];
+  float ss = 0.0f;
+  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+    uint2 xv = *reinterpret_cast<const uint2*>(xr + c);
+    float f[4] = {bf16_bits_to_float((uint16_t)(xv.x & 0xffffu)), bf16_bits_to_float((uint16_t)(xv.x >> 16)),
+                  bf16_bits_to_float((uint16_t)(xv.y & 0xffffu)), bf16_bits_to_float((uint16_t)(xv.y >> 16))};
+    if (y) {
+      const float4 yv = *reinterpret_cast<const float4*>(y + (size_t)t * H + c);
+      const float yy[4] = {yv.x, yv.y, yv.z, yv.w};
+      uint16_t b[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        b[j] = f2bf(f[j] + yy[j]);
+        f[j] = bf16_bits_to_float(b[j]);
+      }
+      xv.x = (uint32_t)b[0] | ((uint32_t)b[1] << 16);
+      xv.y = (uint32_t)b[2] | ((uint32_t)b[3] << 16);
+      *reinterpret_cast<uint2*>(xr + c) = xv;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ss = fmaf(f[j], f[j], ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float rms = __fsqrt_rn(__fadd_rn(__fdiv_rn(red[0], (float)H), 1e-6f));
+  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+    const uint2 xv = *reinterpret_cast<const uint2*>(xr + c);
+    const float f[4] = {bf16_bits_to_float((uint16_t)(xv.x & 0xffffu)), bf16_bits_to_float((uint16_t)(xv.x >> 16)),
+                        bf16_bits_to_float((uint16_t)(xv.y & 0xffffu)), bf16_bits_to_float((uint16_t)(xv.y >> 16))};
+    uint2 o;
+    o.x = (uint32_t)f2bf(__fdiv_rn(f[0], rms)) | ((uint32_t)f2bf(__fdiv_rn(f[1], rms)) << 16);
+    o.y = (uint32_t)f2bf(__fdiv_rn(f[2], rms)) | ((uint32_t)f2bf(__fdiv_rn(f[3], rms)) << 16);
+    *reinterpret_cast<uint2*>(x_in + (size_t)t * H + c) = o;
+  }
+}
+
+cudaError_t launch_rmsnorm_residual(uint16_t* x, const float* y, uint16_t* x_in, int T, int H,
+                                    cudaStream_t s) {
+  rmsnorm_residual_kernel<<<T, 256, 0, s>>>(x, y, x_in, H);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_residual(uint16_t* x, const float* y, size_t n, cudaStream_t s) {
   residual_kernel<<<1216, 256, 0, s>>>(x, y, n);
   return cudaGetLastError();

@@ -125,5 +125,7 @@ cudaError_t launch_widen(const int8_t* src, size_t n, __half* out, cudaStream_t 
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, int T, int H, int E,
                                  float* out, cudaStream_t s);
 cudaError_t launch_residual(uint16_t* x, const float* y, size_t n, cudaStream_t s);
+cudaError_t launch_rmsnorm_residual(uint16_t* x, const float* y, uint16_t* x_in, int T, int H,
+                                    cudaStream_t s);
 
 }  // namespace moe

@@ -631,6 +631,13 @@ moe_status moe_router_logits(const uint16_t* x, const float* w_router, int T, in
                                           static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_rmsnorm_residual(uint16_t* x, const float* y, uint16_t* x_in, int T, int H,
+                                void* stream) {
+  if (!x || !x_in || T < 1 || H < 4 || H % 4) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_in) || (y && !aligned16(y))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_rmsnorm_residual(x, y, x_in, T, H, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_residual_add(uint16_t* x, const float* y, int T, int H, void* stream) {
   if (!x || !y || T < 1 || H < 4 || H % 4) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;

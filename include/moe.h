@@ -165,6 +165,12 @@ MOE_API moe_status moe_profile_read(moe_plan_t plan, int path, float* ms_out, in
  * Router projection: logits fp32 [T, E] = float(x bf16 [T, H]) @ w_router fp32 [H, E],
  * fp32 accumulation. Residual: x[t,h] <- bf16_round_nearest_even(float(x[t,h]) + y[t,h]),
  * x bf16 [T, H] updated in place, y fp32 [T, H]. Neither needs a plan. */
+/* Stacked-prefill layer input: when y is not NULL, first x <- bf16_rne(float(x) + y) (the
+ * residual update, x updated in place); then x_in <- bf16_rne(float(x) / sqrt(mean_h(x^2) +
+ * 1e-6)) per token (a parameter-free RMS pre-norm of the next layer's input). x, x_in bf16
+ * [T, H]; y fp32 [T, H] or NULL. One block per token, fp32 arithmetic. */
+MOE_API moe_status moe_rmsnorm_residual(uint16_t* x, const float* y, uint16_t* x_in, int T, int H,
+                                        void* stream);
 MOE_API moe_status moe_router_logits(const uint16_t* x, const float* w_router, int T, int H, int E,
                              float* logits, void* stream);
 MOE_API moe_status moe_residual_add(uint16_t* x, const float* y, int T, int H, void* stream);

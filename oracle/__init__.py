@@ -34,7 +34,7 @@ def lib():
     if _lib is None:
         _lib = C.CDLL(build())
         for name in ("oracle_route", "oracle_quant_rows", "oracle_permute", "oracle_forward",
-                     "oracle_dense", "oracle_router_logits"):
+                     "oracle_dense", "oracle_router_logits", "oracle_rmsnorm_residual"):
             getattr(_lib, name).restype = C.c_int
     return _lib
 
@@ -156,3 +156,14 @@ def router_logits(x_bf16, w_router, nthreads: int | None = None):
     out = np.zeros((T, E), np.float64)
     lib().oracle_router_logits(_p(x), _p(wr), T, H, E, _p(out), nthreads or default_threads())
     return out
+
+
+def rmsnorm_residual(x_bf16, y=None):
+    """Stacked-prefill layer input. Returns (x after the residual update, x_in) as uint16
+    bf16 bit arrays; y (float64/float32 [T,H]) may be None."""
+    x = _np(x_bf16, np.uint16).copy()
+    T, H = x.shape
+    yy = None if y is None else np.ascontiguousarray(np.asarray(y, np.float64))
+    x_in = np.zeros_like(x)
+    lib().oracle_rmsnorm_residual(_p(x), _p(yy), _p(x_in), T, H)
+    return x, x_in

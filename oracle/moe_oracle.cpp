@@ -133,6 +133,14 @@ void expert_ffn(const int8_t* qx, float sx, int H, int I,
   }
 }
 
+// fp32 -> bf16, round to nearest even (finite inputs).
+uint16_t float_to_bf16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
 int check_layer(const oracle_layer* L) {
   if (!L || L->E <= 0 || L->k <= 0 || L->k > L->E || L->H <= 0 || L->I <= 0 || L->Is < 0)
     return -1;
@@ -296,6 +304,28 @@ int oracle_dense(const oracle_layer* L, const uint16_t* x, int T, const int32_t*
       for (int o = 0; o < H; ++o) yt[o] += static_cast<double>(d[o]);
     }
   });
+  return 0;
+}
+
+// Input of one layer of the stacked prefill. When y is given, first the residual update
+// x <- bf16(float(x) + float(y)) (fp32 add, round to nearest even); then the parameter-free RMS
+// pre-norm x_in = bf16(x / sqrt(mean(x^2) + 1e-6)), evaluated in double.
+int oracle_rmsnorm_residual(uint16_t* x, const double* y, uint16_t* x_in, int T, int H) {
+  for (int t = 0; t < T; ++t) {
+    uint16_t* xr = x + (size_t)t * H;
+    if (y) {
+      for (int h = 0; h < H; ++h)
+        xr[h] = float_to_bf16(bf16_to_float(xr[h]) + static_cast<float>(y[(size_t)t * H + h]));
+    }
+    double ss = 0.0;
+    for (int h = 0; h < H; ++h) {
+      const double v = bf16_to_float(xr[h]);
+      ss += v * v;
+    }
+    const double rms = std::sqrt(ss / H + 1e-6);
+    for (int h = 0; h < H; ++h)
+      x_in[(size_t)t * H + h] = float_to_bf16(static_cast<float>(bf16_to_float(xr[h]) / rms));
+  }
   return 0;
 }
 

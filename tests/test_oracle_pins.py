@@ -350,3 +350,40 @@ def test_workload_properties():
     c = np.bincount(idx.ravel(), minlength=st.shape.E)
     assert np.sort(c)[::-1][:4].sum() > 0.4 * idx.size
     assert (c == 0).any()
+
+
+# ---------------------------------------------------------------- stacked-prefill layer input
+
+def _bf16_to_f32(u16):
+    return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).float()
+
+
+def test_rmsnorm_constant_rows_closed_form():
+    # a row of a constant c normalises to c / sqrt(c^2 + 1e-6) -> +-1 in bf16
+    rows = np.array([[3.0] * 64, [-0.5] * 64, [1024.0] * 64], np.float32)
+    _, x_in = oracle.rmsnorm_residual(bf16_bits(rows))
+    f = _bf16_to_f32(x_in).numpy()
+    assert (f[0] == 1.0).all() and (f[1] == -1.0).all() and (f[2] == 1.0).all()
+
+
+def test_rmsnorm_matches_library_within_one_ulp():
+    rng = np.random.default_rng(8)
+    xf = (rng.standard_normal((40, 512)) * rng.uniform(0.1, 50, (40, 1))).astype(np.float32)
+    x = bf16_bits(xf)
+    _, x_in = oracle.rmsnorm_residual(x)
+    xd = _bf16_to_f32(x).double()
+    ref = torch.nn.functional.rms_norm(xd, (512,), eps=1e-6)
+    got = _bf16_to_f32(x_in).double()
+    ulp = ref.abs() * 2.0 ** -7      # bf16 spacing bound
+    assert ((got - ref).abs() <= ulp).all()
+
+
+def test_residual_is_fp32_add_rounded_to_bf16():
+    rng = np.random.default_rng(9)
+    x = bf16_bits(rng.standard_normal((7, 128)).astype(np.float32))
+    y = rng.standard_normal((7, 128)) * 3
+    x2, x_in = oracle.rmsnorm_residual(x, y)
+    ref = (_bf16_to_f32(x) + torch.from_numpy(y).float()).to(torch.bfloat16)
+    assert (torch.from_numpy(x2.view(np.int16)) == ref.view(torch.int16)).all()
+    _, x_in2 = oracle.rmsnorm_residual(x2)
+    assert (x_in == x_in2).all()
