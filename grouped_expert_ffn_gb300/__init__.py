@@ -68,6 +68,8 @@ def lib() -> C.CDLL:
             "moe_router_logits": ([vp, vp, i32, i32, i32, vp, vp], i32),
             "moe_residual_add": ([vp, vp, i32, i32, vp], i32),
             "moe_rmsnorm_residual": ([vp, vp, vp, i32, i32, vp], i32),
+            "moe_forward_decode_static": ([i32, i32, i32, i32, i32, C.POINTER(Weights), vp, i32,
+                                           vp, vp, vp, vp, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)

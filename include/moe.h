@@ -175,6 +175,34 @@ MOE_API moe_status moe_router_logits(const uint16_t* x, const float* w_router, i
                              float* logits, void* stream);
 MOE_API moe_status moe_residual_add(uint16_t* x, const float* y, int T, int H, void* stream);
 
+/* ---- allocation-free batched decode ---------------------------------------------------
+ * The source pages have no counterpart of this entry point; it exists for callers that
+ * cannot allocate device memory on their call path (a stream being captured into a CUDA
+ * graph, where allocation calls are not allowed; a plugin inside a host runtime that owns
+ * all device allocations; serving loops that cannot afford the implicit device
+ * synchronisation of cudaMalloc/cudaFree). moe_plan allocates a workspace, so such callers
+ * use this instead for decode-sized batches.
+ *
+ * Computes exactly what moe_forward computes for 1 <= T <= 8 rows (the deduplicated
+ * weight-streaming decode kernels), taking the shapes directly instead of a plan:
+ *   E, top_k, H, I, I_shared, w (caller-owned int8 weights and fp32 scales, as in
+ *   moe_weights), x bf16 [T, H], idx int32 [T, top_k], w fp32 [T, top_k] -> y fp32 [T, H].
+ *   status: optional device int32; receives the call's device-side error word (0 = ok,
+ *   MOE_ERR_DEVICE for an expert id out of range or repeated within a token).
+ * It allocates nothing: its scratch (at most 2 MiB: per-token codes, the unique-expert
+ * list, row maps, fp32 SiLU(gate)*up rows) is a file-scope __device__ array inside the
+ * library, present on every GPU that loads the library until the process exits. Limits:
+ * T <= 8 (else MOE_ERR_CAPACITY), E <= 256, top_k <= 8, H <= 8192, I and I_shared <= 4096,
+ * all multiples of 64 (else MOE_ERR_UNSUPPORTED). The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress); make that first call before any stream
+ * capture. Every call shares the one array and keeps the previous call's contents (only
+ * the error word is cleared per call): calls that overlap on the GPU - on two streams, or
+ * from two host threads - race and corrupt each other's results; serialise them. */
+MOE_API moe_status moe_forward_decode_static(int E, int top_k, int H, int I, int I_shared,
+                                             const moe_weights* w, const uint16_t* x, int T,
+                                             const int32_t* idx, const float* wts, float* y,
+                                             int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
