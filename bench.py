@@ -141,7 +141,7 @@ def build_stack(moe, wl, n_layers, dev):
         W = synth.make_weights(sh, seed, device=dev)
         wr = synth.make_router_weight(sh.H, sh.E, seed, device=dev)
         packed = moe.moe_pack_weights(plan, W)
-        layers.append((W, wr, packed))
+        layers.append((W, moe.moe_router_pack(wr), packed))
     torch.cuda.synchronize()
     return plan, layers
 
@@ -249,7 +249,7 @@ def run_ours(args, world, rank):
         # layer l: x_in = rmsnorm(x) -> logits = x_in @ W_r -> route -> y = moe(x_in) -> x += y
         for l, (W, wr, packed) in enumerate(layers):
             moe.moe_rmsnorm_residual(x, y if l else None, x_in)
-            moe.moe_router_logits(x_in, wr, logits)
+            moe.moe_router_logits_packed(x_in, wr, logits)
             moe.moe_route(plan, logits, idx, w)
             moe.moe_forward(plan, packed, x_in, idx, w, y)
         moe.moe_residual_add(x, y)

@@ -66,6 +66,8 @@ def lib() -> C.CDLL:
             "moe_profile_enable": ([vp, i32], i32),
             "moe_profile_read": ([vp, i32, C.POINTER(C.c_float), C.POINTER(C.c_int)], i32),
             "moe_router_logits": ([vp, vp, i32, i32, i32, vp, vp], i32),
+            "moe_router_pack": ([vp, i32, i32, vp, vp], i32),
+            "moe_router_logits_packed": ([vp, vp, i32, i32, i32, vp, vp], i32),
             "moe_residual_add": ([vp, vp, i32, i32, vp], i32),
             "moe_rmsnorm_residual": ([vp, vp, vp, i32, i32, vp], i32),
             "moe_forward_decode_static": ([i32, i32, i32, i32, i32, C.POINTER(Weights), vp, i32,
@@ -190,6 +192,23 @@ def moe_router_logits(x, w_router, logits, stream=None):
     E = w_router.shape[1]
     _check(lib().moe_router_logits(_ptr(x), _ptr(w_router), T, H, E, _ptr(logits),
                                    _stream(stream)), "moe_router_logits")
+
+
+def moe_router_pack(w_router, packed=None, stream=None):
+    """bf16 [E, 3H] split of the fp32 router weight [H, E] for moe_router_logits_packed."""
+    H, E = w_router.shape
+    if packed is None:
+        packed = torch.empty((E, 3 * H), dtype=torch.bfloat16, device=w_router.device)
+    _check(lib().moe_router_pack(_ptr(w_router), H, E, _ptr(packed), _stream(stream)),
+           "moe_router_pack")
+    return packed
+
+
+def moe_router_logits_packed(x, packed, logits, stream=None):
+    T, H = x.shape
+    E = packed.shape[0]
+    _check(lib().moe_router_logits_packed(_ptr(x), _ptr(packed), T, H, E, _ptr(logits),
+                                          _stream(stream)), "moe_router_logits_packed")
 
 
 def moe_residual_add(x, y, stream=None):

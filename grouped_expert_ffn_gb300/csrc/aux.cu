@@ -52,6 +52,32 @@ __global__ void widen_kernel(const int8_t* __restrict__ src, size_t n, __half* _
   }
 }
 
+// max over rows of sum(q^2) of an int8 matrix [rows, cols], into *out (atomicMax). Warp per
+// row; cols a multiple of 16.
+__global__ void row_sq_max_kernel(const int8_t* __restrict__ w, size_t rows, int cols,
+                                  int* __restrict__ out) {
+  const size_t nwarps = (size_t)gridDim.x * (blockDim.x / 32);
+  const int lane = threadIdx.x % 32;
+  for (size_t r = blockIdx.x * (size_t)(blockDim.x / 32) + threadIdx.x / 32; r < rows; r += nwarps) {
+    const int4* p = reinterpret_cast<const int4*>(w + r * cols);
+    int sq = 0;
+    for (int u = lane; u < cols / 16; u += 32) {
+      const int4 v = p[u];
+      sq = __dp4a(v.x, v.x, sq);
+      sq = __dp4a(v.y, v.y, sq);
+      sq = __dp4a(v.z, v.z, sq);
+      sq = __dp4a(v.w, v.w, sq);
+    }
+    sq = warp_sum_i(sq);
+    if (lane == 0) atomicMax(out, sq);
+  }
+}
+
+cudaError_t launch_row_sq_max(const int8_t* w, size_t rows, int cols, int* out, cudaStream_t s) {
+  row_sq_max_kernel<<<1216, 256, 0, s>>>(w, rows, cols, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H, int BN,
                            __half* out, cudaStream_t s) {
   pack_gu_kernel<<<1216, 256, 0, s>>>(gate, up, n_mats, I, H, BN, out);

@@ -9,15 +9,25 @@
 //
 // Exact integer products on an fp16 tensor pipe. sm_103a has no int8 tcgen05 MMA, so the
 // int8 operands are held as fp16 (every int8 value is an fp16 integer) and multiplied with
-// kind::f16 into fp32 TMEM accumulators. A product is at most 127^2 = 16129; a fresh
-// accumulator per 1024-element K chunk keeps every partial sum below 1024 * 16129 < 2^24,
-// where fp32 represents all integers, so each chunk sum is an exact integer. The epilogue
-// rounds each chunk to int32 and adds the chunks in integer arithmetic.
+// kind::f16 into fp32 TMEM accumulators. fp32 holds every integer below 2^24 exactly, so a
+// sum of integer products is exact as long as every partial sum stays below 2^24 in
+// magnitude, in whatever order the tensor core adds them. Two ways to guarantee that:
+//  - bound: for any subset of terms, |sum a_k b_k| <= sqrt(sum a^2) sqrt(sum b^2)
+//    (Cauchy-Schwarz). The producers of the A rows record max_row sum(q^2) and weight packing
+//    records max_row sum(q_w^2); when their product is below 2^48 one accumulator over the
+//    whole K is exact. This holds for realistic data by a wide margin.
+//  - chunks: otherwise a fresh accumulator per 1024-element K chunk bounds every partial
+//    sum by 1024 * 127^2 < 2^24; the epilogue rounds each chunk to int32 and adds the chunks
+//    in integer arithmetic.
+// The kernel picks one of the two for the whole launch at its start (every CTA reads the
+// same two words). With one accumulator per tile, TMEM holds two of them (2 x BN columns)
+// so the epilogue of one tile overlaps the MMAs of the next.
 //
-// Warp roles (192 threads, one CTA per SM):
-//   warps 0-3  epilogue: thread i owns TMEM lane i = tile row i;
-//   warp 4     TMA producer: A (token rows) and B (weight rows) tiles, 128-byte swizzle;
-//   warp 5     MMA issuer and TMEM owner.
+// Warp roles (320 threads, one CTA per SM):
+//   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. (tile rows) and half (w/4) of
+//              the tile's columns;
+//   warp 8     TMA producer: A (token rows) and B (weight rows) tiles, 128-byte swizzle;
+//   warp 9     MMA issuer and TMEM owner.
 // Every mbarrier wait is bounded; a wait that runs out sets the plan's error word and the
 // CTA drains its own copies and MMAs, frees TMEM and returns.
 #include "common.cuh"
@@ -34,16 +44,27 @@ struct GemmCfg {
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
   static_assert(STAGES >= 2, "pipeline depth");
-  static_assert((2 * STAGES + 3) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kProducerWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;
+constexpr int kGemmThreads = (kEpiWarps + 2) * 32;
 constexpr uint32_t kTmemCols = 512;
+
+// Whether one fp32 accumulator over the whole K is provably exact for this launch.
+__device__ __forceinline__ bool single_accumulator_exact(const GemmArgs& a) {
+  const unsigned long long r = (unsigned long long)(unsigned)*a.row_sq_max;
+  const unsigned long long w = (unsigned long long)(unsigned)*a.w_sq_max;
+  return r * w < (1ull << 48);
+}
 
 template <int BN>
 __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
-                                                 uint32_t tbase) {
-  const int m = threadIdx.x;  // 0..127
+                                                 uint32_t tbase, int half) {
+  const int m = (threadIdx.x / 32 % 4) * 32 + threadIdx.x % 32;  // tile row = TMEM lane
   const bool valid = m < wi.z;
   const int row = wi.y + m;
   const bool shared = wi.x == a.E;
@@ -51,8 +72,9 @@ __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int
   const float* su = shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I;
   const int cbase = (wi.w / BN) * (BN / 2);
   const float sx = valid ? a.sx[row] : 0.0f;
+  constexpr int kCols = BN / 4;  // channels per epilogue half
 #pragma unroll 1
-  for (int j0 = 0; j0 < BN / 2; j0 += 16) {
+  for (int j0 = half * kCols; j0 < (half + 1) * kCols; j0 += 16) {
     int ag[16], au[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) ag[i] = au[i] = 0;
@@ -93,8 +115,9 @@ __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int
 }
 
 template <int BN>
-__device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase) {
-  const int m = threadIdx.x;
+__device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase,
+                                              int half) {
+  const int m = (threadIdx.x / 32 % 4) * 32 + threadIdx.x % 32;
   const bool valid = m < wi.z;
   const int row = wi.y + m;
   const bool shared = wi.x == a.E;
@@ -103,8 +126,9 @@ __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nc
   const float wr = valid ? a.row_w[row] : 0.0f;
   const int tok = valid ? a.row_token[row] : 0;
   float* yrow = a.y + (size_t)tok * a.H;
+  constexpr int kCols = BN / 2;
 #pragma unroll 1
-  for (int j0 = 0; j0 < BN; j0 += 16) {
+  for (int j0 = half * kCols; j0 < (half + 1) * kCols; j0 += 16) {
     int acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0;
@@ -147,9 +171,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
   uint64_t* empty = full + Cfg::STAGES;
-  uint64_t* acc_full = empty + Cfg::STAGES;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
+  uint64_t* acc_full = empty + Cfg::STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;        // [2]
+  uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -159,17 +183,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], kEpiThreads);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmBs);
@@ -179,8 +205,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_items = *a.n_items;
+  // Accumulator layout for this launch: one accumulator over the whole K (two TMEM slots,
+  // double-buffered) when the bound proves it exact, else 1024-K chunks in one slot.
+  const bool single = single_accumulator_exact(a);
+  const int kmax = a.K_r > a.K_s ? a.K_r : a.K_s;
+  const int slot_cols = single ? BN : ((kmax + kChunkK - 1) / kChunkK) * BN;
+  const int nslots = slot_cols <= (int)kTmemCols / 2 ? 2 : 1;
+  const int kpc = single ? (1 << 30) : kChunkK / kBK;  // k-blocks per accumulator
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       int stage = 0;
@@ -223,18 +256,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      int it = 0;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++it) {
         const int4 wi = a.items[item];
         const int nkb = (wi.x == a.E ? a.K_s : a.K_r) / kBK;
-        if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, a.err)) break;
+        const int slot = it % nslots;
+        const uint32_t use = (uint32_t)(it / nslots) & 1u;
+        if (!mbar_wait(&acc_empty[slot], use ^ 1, abort_flag, a.err)) break;
         tc_fence_after();
+        const uint32_t tslot = tmem + (uint32_t)(slot * slot_cols);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) {
             ok = false;
@@ -244,8 +281,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
           const uint64_t da = smem_desc_sw128(sa);
           const uint64_t db = smem_desc_sw128(sa + Cfg::A_BYTES);
-          const int kpc = kChunkK / kBK;  // k-blocks per exact accumulator chunk
-          const uint32_t dt = tmem + (uint32_t)((kb / kpc) * BN);
+          const uint32_t dt = tslot + (uint32_t)((kb / kpc) * BN);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma_f16(dt, da + 2 * kk, db + 2 * kk, idesc, (kb % kpc != 0 || kk != 0) ? 1u : 0u);
@@ -256,8 +292,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(acc_full);
-        acc_phase ^= 1;
+        umma_commit(&acc_full[slot]);
       }
       // Every MMA this thread issued has completed once `drain` flips.
       umma_commit(drain);
@@ -266,28 +301,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 0-3) ----------------
-    uint32_t acc_phase = 0;
-    const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    // ---------------- epilogue (warps 0-7) ----------------
+    const int half = warp / 4;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+    int it = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
       const int4 wi = a.items[item];
       const int K = wi.x == a.E ? a.K_s : a.K_r;
-      const int nch = (K + kChunkK - 1) / kChunkK;
-      if (!mbar_wait(acc_full, acc_phase, abort_flag, a.err)) break;
+      const int nch = single ? 1 : (K + kChunkK - 1) / kChunkK;
+      const int slot = it % nslots;
+      const uint32_t use = (uint32_t)(it / nslots) & 1u;
+      if (!mbar_wait(&acc_full[slot], use, abort_flag, a.err)) break;
       tc_fence_after();
+      const uint32_t tbase = lane_base + (uint32_t)(slot * slot_cols);
       if (GU)
-        epilogue_gate_up<BN>(a, wi, nch, tbase);
+        epilogue_gate_up<BN>(a, wi, nch, tbase, half);
       else
-        epilogue_down<BN>(a, wi, nch, tbase);
+        epilogue_down<BN>(a, wi, nch, tbase, half);
       tc_fence_before();
-      mbar_arrive(acc_empty);
-      acc_phase ^= 1;
+      mbar_arrive(&acc_empty[slot]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -338,41 +376,56 @@ cudaError_t launch_grouped_gemm(bool gate_up, int BN, const GemmArgs& a, const C
 // Per-row requantisation of h = SiLU(gate)*up: s = amax/127, q = rne(h/s) (|q| <= 127),
 // written as fp16 integers for the down GEMM's A operand. One warp per row.
 __global__ void requant_kernel(const float* __restrict__ h32, int R, int T_sh, int I, int Is,
-                               int Imax, __half* __restrict__ hq, float* __restrict__ sh) {
+                               int Imax, __half* __restrict__ hq, float* __restrict__ sh,
+                               int* __restrict__ sq_max) {
+  __shared__ int s_sq[32];
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  if (row >= R) return;
-  const int n = row < T_sh ? Is : I;
-  const float* h = h32 + (size_t)row * Imax;
-  float amax = 0.0f;
-  for (int i = lane * 4; i < n; i += 128) {
-    const float4 v = *reinterpret_cast<const float4*>(h + i);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-  }
-  amax = warp_max(amax);
-  const float s = __fdiv_rn(amax, 127.0f);
-  __half* q = hq + (size_t)row * Imax;
-  for (int i = lane * 4; i < n; i += 128) {
-    const float4 v = *reinterpret_cast<const float4*>(h + i);
-    __half2 lo, hi;
-    if (s > 0.0f) {
-      lo = __halves2half2(__int2half_rn(quant_code(v.x, s)), __int2half_rn(quant_code(v.y, s)));
-      hi = __halves2half2(__int2half_rn(quant_code(v.z, s)), __int2half_rn(quant_code(v.w, s)));
-    } else {
-      lo = hi = __float2half2_rn(0.0f);
+  int sq = 0;
+  if (row < R) {
+    const int n = row < T_sh ? Is : I;
+    const float* h = h32 + (size_t)row * Imax;
+    float amax = 0.0f;
+    for (int i = lane * 4; i < n; i += 128) {
+      const float4 v = *reinterpret_cast<const float4*>(h + i);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
-    *reinterpret_cast<__half2*>(q + i) = lo;
-    *reinterpret_cast<__half2*>(q + i + 2) = hi;
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+    __half* q = hq + (size_t)row * Imax;
+    for (int i = lane * 4; i < n; i += 128) {
+      const float4 v = *reinterpret_cast<const float4*>(h + i);
+      int c[4] = {0, 0, 0, 0};
+      if (s > 0.0f) {
+        c[0] = quant_code(v.x, s);
+        c[1] = quant_code(v.y, s);
+        c[2] = quant_code(v.z, s);
+        c[3] = quant_code(v.w, s);
+      }
+      sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
+      *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));
+      *reinterpret_cast<__half2*>(q + i + 2) =
+          __halves2half2(__int2half_rn(c[2]), __int2half_rn(c[3]));
+    }
+    sq = warp_sum_i(sq);
+    if (lane == 0) sh[row] = s;
   }
-  if (lane == 0) sh[row] = s;
+  if (lane == 0) s_sq[threadIdx.x / 32] = sq;
+  __syncthreads();
+  // one guarded atomic per block: most blocks do not raise the running maximum
+  if (threadIdx.x == 0) {
+    int m = 0;
+    for (int i = 0; i < (int)(blockDim.x / 32); ++i) m = max(m, s_sq[i]);
+    if (m > *(volatile int*)sq_max) atomicMax(sq_max, m);
+  }
 }
 
 cudaError_t launch_requant(const float* h32, int R, int T_sh, int I, int Is, int Imax,
-                           __half* hq, float* sh, cudaStream_t s) {
+                           __half* hq, float* sh, int* sq_max, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
-  const int rows_per_blk = 8;
+  const int rows_per_blk = 16;
   requant_kernel<<<(R + rows_per_blk - 1) / rows_per_blk, 32 * rows_per_blk, 0, s>>>(
-      h32, R, T_sh, I, Is, Imax, hq, sh);
+      h32, R, T_sh, I, Is, Imax, hq, sh, sq_max);
   return cudaGetLastError();
 }
 

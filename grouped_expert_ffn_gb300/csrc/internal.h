@@ -40,6 +40,9 @@ struct GemmArgs {
   const int* row_token;  // per row
   const float* row_w;    // per row
   float* y;              // [T, H]
+  // exactness bound of one fp32 accumulator over the whole K (see gemm_tc.cu)
+  const int* row_sq_max;  // max over A rows of sum(q^2), written by the row producer
+  const int* w_sq_max;    // max over weight rows of sum(q_w^2), written at packing
   // taps (NULL = off)
   int32_t* tap;
   int* err;
@@ -51,7 +54,7 @@ cudaError_t launch_grouped_gemm(bool gate_up, int BN, const GemmArgs& a, const C
 cudaError_t gemm_set_attributes();
 
 cudaError_t launch_requant(const float* h32, int R, int T_sh, int I, int Is, int Imax,
-                           __half* hq, float* sh, cudaStream_t s);
+                           __half* hq, float* sh, int* sq_max, cudaStream_t s);
 
 // routing / permutation
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
@@ -77,6 +80,7 @@ struct PrepArgs {
   float* y;                   // [T, H] zeroed
   int8_t* qtok;               // [T, H] or NULL
   float* stok;                // [T]   or NULL
+  int* sq_max;                // [2] row sum(q^2) maxima (gate/up rows, down rows), reset here
   int* err;
 };
 cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s);
@@ -122,9 +126,13 @@ cudaError_t decode_set_attributes(int H, int Imax);
 cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H, int BN,
                            __half* out, cudaStream_t s);
 cudaError_t launch_widen(const int8_t* src, size_t n, __half* out, cudaStream_t s);
+cudaError_t launch_row_sq_max(const int8_t* w, size_t rows, int cols, int* out, cudaStream_t s);
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, int T, int H, int E,
                                  float* out, cudaStream_t s);
 cudaError_t launch_residual(uint16_t* x, const float* y, size_t n, cudaStream_t s);
+cudaError_t launch_router_pack(const float* w, int H, int E, uint16_t* packed, cudaStream_t s);
+cudaError_t launch_router_tc(int T, int H, int E, float* out, const CUtensorMap& tmA,
+                             const CUtensorMap& tmB, cudaStream_t s);
 cudaError_t launch_rmsnorm_residual(uint16_t* x, const float* y, uint16_t* x_in, int T, int H,
                                     cudaStream_t s);
 

@@ -39,6 +39,7 @@ struct moe_plan_s {
   float* stok = nullptr;
   int4* groups = nullptr;
   int* n_groups = nullptr;
+  int* sq_max = nullptr;  // [2] per-forward maxima of row sum(q^2): gate/up rows, down rows
   int* err = nullptr;
   // taps
   int debug = 0;
@@ -64,6 +65,7 @@ struct moe_packed_s {
   __half* d16 = nullptr;
   __half* shgu16 = nullptr;
   __half* shd16 = nullptr;
+  int* w_sq = nullptr;  // [2] max over weight rows of sum(q^2): gate/up rows, down rows
   CUtensorMap tmB_gu, tmBs_gu, tmB_d, tmBs_d;
 };
 
@@ -87,9 +89,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// fp16 tensor of `rank` dims (innermost first), box {64, box_rows[, 1]}, 128-byte swizzle.
-bool encode_f16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                const uint64_t* strides_bytes, uint32_t box_rows) {
+// 2-byte tensor of `rank` dims (innermost first), box {64, box_rows[, 1]}, 128-byte swizzle.
+bool encode_2byte(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank,
+                  const uint64_t* dims, const uint64_t* strides_bytes, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[3], st[2];
@@ -99,10 +101,15 @@ bool encode_f16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims
   box[0] = kBK;
   box[1] = box_rows;
   box[2] = 1;
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(base), d, st, box, es,
+  CUresult r = fn(m, dt, rank, const_cast<void*>(base), d, st, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool encode_f16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                const uint64_t* strides_bytes, uint32_t box_rows) {
+  return encode_2byte(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides_bytes, box_rows);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -269,6 +276,7 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   ALLOC(stok, T);
   ALLOC(groups, (size_t)E + 1);
   ALLOC(n_groups, 1);
+  ALLOC(sq_max, 2);
   ALLOC(err, 1);
 #undef ALLOC
   if (cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess ||
@@ -329,12 +337,14 @@ moe_status moe_pack_weights(moe_plan_t p, const moe_weights* w, void* stream, mo
     if (pk->d16) cudaFree(pk->d16);
     if (pk->shgu16) cudaFree(pk->shgu16);
     if (pk->shd16) cudaFree(pk->shd16);
+    if (pk->w_sq) cudaFree(pk->w_sq);
     cudaGetLastError();
     delete pk;
     return st;
   };
   if (cudaMalloc(&pk->gu16, E * 2 * I * H * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
   if (cudaMalloc(&pk->d16, E * H * I * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
+  if (cudaMalloc(&pk->w_sq, 2 * sizeof(int)) != cudaSuccess) return fail(MOE_ERR_OOM);
   if (p->has_shared) {
     if (cudaMalloc(&pk->shgu16, 2 * Is * H * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
     if (cudaMalloc(&pk->shd16, H * Is * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
@@ -344,6 +354,15 @@ moe_status moe_pack_weights(moe_plan_t p, const moe_weights* w, void* stream, mo
   if (e == cudaSuccess && p->has_shared) {
     e = launch_pack_gu(w->sh_gate, w->sh_up, 1, (int)Is, (int)H, p->bn_gu, pk->shgu16, s);
     if (e == cudaSuccess) e = launch_widen(w->sh_down, H * Is, pk->shd16, s);
+  }
+  if (e == cudaSuccess) e = cudaMemsetAsync(pk->w_sq, 0, 2 * sizeof(int), s);
+  if (e == cudaSuccess) e = launch_row_sq_max(w->w_gate, E * I, (int)H, pk->w_sq, s);
+  if (e == cudaSuccess) e = launch_row_sq_max(w->w_up, E * I, (int)H, pk->w_sq, s);
+  if (e == cudaSuccess) e = launch_row_sq_max(w->w_down, E * H, (int)I, pk->w_sq + 1, s);
+  if (e == cudaSuccess && p->has_shared) {
+    e = launch_row_sq_max(w->sh_gate, Is, (int)H, pk->w_sq, s);
+    if (e == cudaSuccess) e = launch_row_sq_max(w->sh_up, Is, (int)H, pk->w_sq, s);
+    if (e == cudaSuccess) e = launch_row_sq_max(w->sh_down, H, (int)Is, pk->w_sq + 1, s);
   }
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA);
   bool ok = true;
@@ -377,6 +396,7 @@ moe_status moe_packed_destroy(moe_packed_t pk) {
   if (pk->d16) cudaFree(pk->d16);
   if (pk->shgu16) cudaFree(pk->shgu16);
   if (pk->shd16) cudaFree(pk->shd16);
+  if (pk->w_sq) cudaFree(pk->w_sq);
   delete pk;
   return MOE_OK;
 }
@@ -475,6 +495,7 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   pa.y = y;
   pa.qtok = p->debug ? p->qtok : nullptr;
   pa.stok = p->debug ? p->stok : nullptr;
+  pa.sq_max = p->sq_max;
   pa.err = p->err;
   cudaEvent_t* ev = prof_events(p, 0);
   if (ev) cudaEventRecord(ev[0], s);
@@ -508,11 +529,14 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.K_r = p->H;
   g.K_s = p->H;
   g.tap = p->debug ? p->tap_gu : nullptr;
+  g.row_sq_max = p->sq_max;
+  g.w_sq_max = pk->w_sq;
   if ((e = launch_grouped_gemm(true, p->bn_gu, g, p->tmA_gu, pk->tmB_gu, pk->tmBs_gu, grid, s)) !=
       cudaSuccess)
     return cuda_status(e);
   if (ev) cudaEventRecord(ev[2], s);
-  if ((e = launch_requant(p->h32, R, T_sh, p->I, p->Is, p->Imax, p->hq, p->sh, s)) != cudaSuccess)
+  if ((e = launch_requant(p->h32, R, T_sh, p->I, p->Is, p->Imax, p->hq, p->sh, p->sq_max + 1, s)) !=
+      cudaSuccess)
     return cuda_status(e);
   if (ev) cudaEventRecord(ev[3], s);
   // down: K = I (routed) or I_shared (shared)
@@ -521,6 +545,8 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.K_r = p->I;
   g.K_s = p->has_shared ? p->Is : p->I;
   g.tap = p->debug ? p->tap_d : nullptr;
+  g.row_sq_max = p->sq_max + 1;
+  g.w_sq_max = pk->w_sq + 1;
   e = launch_grouped_gemm(false, p->bn_d, g, p->tmA_d, pk->tmB_d, pk->tmBs_d, grid, s);
   if (ev) cudaEventRecord(ev[4], s);
   return cuda_status(e);
@@ -629,6 +655,28 @@ moe_status moe_router_logits(const uint16_t* x, const float* w_router, int T, in
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_router_logits(x, w_router, T, H, E, logits,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_router_pack(const float* w_router, int H, int E, uint16_t* packed, void* stream) {
+  if (!w_router || !packed || H < 64 || E < 64 || H % 64 || E % 64) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_router) || !aligned16(packed)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router_pack(w_router, H, E, packed, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_router_logits_packed(const uint16_t* x, const uint16_t* packed, int T, int H, int E,
+                                    float* logits, void* stream) {
+  if (!x || !packed || !logits || T < 1 || H < 64 || E < 64 || H % 64 || E % 64)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(packed) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  const uint64_t da[2] = {(uint64_t)H, (uint64_t)T};
+  const uint64_t sa[1] = {(uint64_t)H * 2};
+  const uint64_t db[2] = {(uint64_t)3 * H, (uint64_t)E};
+  const uint64_t sb[1] = {(uint64_t)3 * H * 2};
+  if (!encode_2byte(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 2, da, sa, kBM) ||
+      !encode_2byte(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, packed, 2, db, sb, 64))
+    return MOE_ERR_CUDA;
+  return cuda_status(launch_router_tc(T, H, E, logits, ta, tb, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_rmsnorm_residual(uint16_t* x, const float* y, uint16_t* x_in, int T, int H,

@@ -93,8 +93,9 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
 // ---------------------------------------------------------------------------------------
 __global__ void hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
                             unsigned long long* __restrict__ bmask, int* __restrict__ bhist,
-                            int* err) {
+                            int* sq_max, int* err) {
   extern __shared__ unsigned long long mask[];
+  if (blockIdx.x == 0 && threadIdx.x < 2) sq_max[threadIdx.x] = 0;  // maxima of this forward
   for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0ull;
   __syncthreads();
   const int t0 = blockIdx.x * kTokPerBlk;
@@ -112,7 +113,7 @@ __global__ void hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     bmask[(size_t)blockIdx.x * E + e] = mask[e];
-    bhist[(size_t)blockIdx.x * E + e] = __popcll(mask[e]);
+    bhist[(size_t)e * gridDim.x + blockIdx.x] = __popcll(mask[e]);  // [E][nblk]
   }
 }
 
@@ -125,15 +126,36 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
   __shared__ int s_base_gu[258];
   __shared__ int s_base_d[258];
   const int E = a.E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nblk; ++b) {
-      const int v = a.bhist[(size_t)b * E + e];
-      a.bhist[(size_t)b * E + e] = run;
-      run += v;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
+  // exclusive prefix over blocks of each expert's histogram (row e of [E][nblk]), warp per
+  // expert, 128 blocks per pass with independent loads
+  for (int e = warp; e < E; e += nwarps) {
+    int* row = a.bhist + (size_t)e * nblk;
+    int carry = 0;
+    for (int b0 = 0; b0 < nblk; b0 += 128) {
+      int v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int b = b0 + i * 32 + lane;
+        v[i] = b < nblk ? row[b] : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        int incl = v[i];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        const int b = b0 + i * 32 + lane;
+        if (b < nblk) row[b] = carry + incl - v[i];
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
-    s_cnt[e] = run;
-    a.counts[e] = run;
+    if (lane == 0) {
+      s_cnt[e] = carry;
+      a.counts[e] = carry;
+    }
   }
   __syncthreads();
   const int T_sh = a.has_shared ? a.T : 0;
@@ -192,6 +214,7 @@ __global__ void scatter_kernel(PrepArgs a) {
   const int T_sh = a.has_shared ? a.T : 0;
   __shared__ int s_rows[9];
   __shared__ float s_red[32];
+  __shared__ int s_sq[32];
   if (threadIdx.x < k) {
     const int j = threadIdx.x;
     int e = a.idx[(size_t)t * k + j];
@@ -199,7 +222,8 @@ __global__ void scatter_kernel(PrepArgs a) {
     const int b = t / kTokPerBlk, tl = t % kTokPerBlk;
     const unsigned long long m = a.bmask[(size_t)b * E + e];
     const int rank = __popcll(m & ((1ull << tl) - 1ull));
-    int pos = a.offsets[e] + a.bhist[(size_t)b * E + e] + rank;
+    const int nblk = (a.T + kTokPerBlk - 1) / kTokPerBlk;
+    int pos = a.offsets[e] + a.bhist[(size_t)e * nblk + b] + rank;
     if (pos < 0 || pos >= a.T * k) {
       set_error(a.err, kErrDevice);
       pos = 0;
@@ -240,6 +264,7 @@ __global__ void scatter_kernel(PrepArgs a) {
   if (threadIdx.x < nrows) a.sx[s_rows[threadIdx.x]] = s;
   if (threadIdx.x == 0 && a.stok) a.stok[t] = s;
   float* yr = a.y + (size_t)t * H;
+  int sq = 0;  // sum of squared codes of this token (exactness bound of the gate/up GEMM)
   for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -250,6 +275,7 @@ __global__ void scatter_kernel(PrepArgs a) {
       const float hi = bf16_bits_to_float((uint16_t)(u[i] >> 16));
       q[2 * i] = s > 0.0f ? quant_code(lo, s) : 0;
       q[2 * i + 1] = s > 0.0f ? quant_code(hi, s) : 0;
+      sq += q[2 * i] * q[2 * i] + q[2 * i + 1] * q[2 * i + 1];
     }
     uint4 hv;
     uint32_t* hw = reinterpret_cast<uint32_t*>(&hv);
@@ -270,12 +296,20 @@ __global__ void scatter_kernel(PrepArgs a) {
     *reinterpret_cast<float4*>(yr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     *reinterpret_cast<float4*>(yr + c + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  sq = warp_sum_i(sq);
+  if ((threadIdx.x & 31) == 0) s_sq[threadIdx.x / 32] = sq;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int v = threadIdx.x < blockDim.x / 32 ? s_sq[threadIdx.x] : 0;
+    v = warp_sum_i(v);
+    if (threadIdx.x == 0 && v > *(volatile int*)a.sq_max) atomicMax(a.sq_max, v);
+  }
 }
 
 cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s) {
   const int nblk = (a.T + kTokPerBlk - 1) / kTokPerBlk;
   hist_kernel<<<nblk, 256, a.E * sizeof(unsigned long long), s>>>(a.idx, a.T, a.k, a.E, a.bmask,
-                                                                  a.bhist, a.err);
+                                                                  a.bhist, a.sq_max, a.err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   scan_kernel<<<1, 1024, 0, s>>>(a, nblk);

@@ -171,6 +171,16 @@ MOE_API moe_status moe_profile_read(moe_plan_t plan, int path, float* ms_out, in
  * [T, H]; y fp32 [T, H] or NULL. One block per token, fp32 arithmetic. */
 MOE_API moe_status moe_rmsnorm_residual(uint16_t* x, const float* y, uint16_t* x_in, int T, int H,
                                         void* stream);
+/* Router projection on the tensor cores. moe_router_pack splits w_router fp32 [H, E] into
+ * three bf16 parts hi + mid + lo (exact to 2^-26 relative) and stores them as packed bf16
+ * [E, 3H] (caller-allocated, 6*H*E bytes; a one-time step per router weight).
+ * moe_router_logits_packed computes logits fp32 [T, E] = float(x bf16 [T, H]) @ W as one bf16
+ * GEMM over the tripled reduction dimension (exact products, fp32 accumulation). H and E
+ * multiples of 64. Encodes two TMA descriptors on the host per call. */
+MOE_API moe_status moe_router_pack(const float* w_router, int H, int E, uint16_t* packed,
+                                   void* stream);
+MOE_API moe_status moe_router_logits_packed(const uint16_t* x, const uint16_t* packed, int T,
+                                            int H, int E, float* logits, void* stream);
 MOE_API moe_status moe_router_logits(const uint16_t* x, const float* w_router, int T, int H, int E,
                              float* logits, void* stream);
 MOE_API moe_status moe_residual_add(uint16_t* x, const float* y, int T, int H, void* stream);

@@ -194,3 +194,43 @@ def test_residual_add():
     moe.moe_residual_add(xd, y.cuda())
     ref = (x.float() + y).to(torch.bfloat16)
     assert torch.equal(xd.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_adversarial_rows_take_the_exact_chunked_path():
+    # Constant token rows quantise to +-127 everywhere and one gate row of expert 0 is all 127:
+    # the gate accumulator reaches 2048 * 127^2 > 2^24, beyond what one fp32 accumulator holds
+    # exactly, and the product of the row/weight sum-of-squares bounds exceeds 2^48, so the
+    # kernel must take the 1024-K chunked accumulation; the int32 results stay bit-exact.
+    sh = synth.LayerShape(T=40, H=2048, E=4, k=2, I=128, Is=128)
+    d = synth.small_layer(sh.T, sh.H, sh.E, sh.k, sh.I, sh.Is, seed=31)
+    W = d["weights"]
+    W["w_gate"][0, 0, :] = 127
+    W["w_up"][1, 3, :] = -127
+    x = d["x"].float()
+    x[:20] = 0.75                     # constant rows: every code is +127
+    x[20:30] = -2.0                   # every code is -127
+    x = x.to(torch.bfloat16)
+    lg = d["logits"].clone()
+    lg[:, 0] += 10.0                  # every token routes to expert 0
+    Wd = weights_to(W, "cuda")
+    st = check_layer(sh, x, lg, Wd, oracle_layer(W, sh))
+    gu = st["tap"]["acc_gu"]
+    assert np.abs(gu).max() == 2048 * 127 * 127
+
+
+@pytest.mark.parametrize("T", [2600, 77])
+def test_router_tensor_core_projection(T):
+    # bf16 x against the exact three-part bf16 split of the fp32 router weight: within the
+    # fp32-accumulation bound of a 3H-term dot product of the oracle's double logits.
+    H, E = 2048, 128
+    x = synth.make_activations(T, H, 5)
+    wr = synth.make_router_weight(H, E, 5)
+    packed = moe.moe_router_pack(wr.cuda())
+    lg = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    moe.moe_router_logits_packed(x.cuda(), packed, lg)
+    ref = oracle.router_logits(x, wr)
+    mag = np.abs(x.float().numpy()) @ np.abs(wr.numpy())
+    bound = (3 * H + 1) * 2.0 ** -23 * mag + 1e-6
+    err = np.abs(lg.cpu().numpy() - ref)
+    assert (err <= bound).all()
+    assert np.sqrt((err ** 2).mean()) <= 5e-5 * np.sqrt((ref ** 2).mean())
