@@ -337,7 +337,7 @@ def run_ours(args, world, rank):
                "sample": f"{n_tok} tokens of layer 0 of the stack (router projection + route + "
                          f"layer), {secs:.1f} s"}
 
-    n_launch = (n_layers * 9 + 1) * args.steps
+    n_launch = (n_layers * 10 + 1) * args.steps  # norm, router, route, 7 forward kernels; residual
     line = {
         "metric": METRIC,
         "value": value,

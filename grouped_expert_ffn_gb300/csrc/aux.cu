@@ -5,12 +5,12 @@
 
 namespace moe {
 
-// Gate/up rows interleaved in blocks of BN rows: packed rows [b*BN, b*BN + BN/2) are gate
-// channels [b*BN/2, (b+1)*BN/2), the next BN/2 rows the up channels of the same range, so one
-// BN-row weight tile yields SiLU(gate)*up for BN/2 channels. int8 values widened to fp16
-// (exact). 8 elements per thread.
+// Gate/up rows interleaved in pairs: packed row 2i is gate channel i and row 2i+1 up channel
+// i, so the tensor-core tile of 128 weight rows yields SiLU(gate)*up for 64 channels with
+// gate and up in adjacent TMEM lanes. int8 values widened to fp16 (exact). 8 elements per
+// thread.
 __global__ void pack_gu_kernel(const int8_t* __restrict__ gate, const int8_t* __restrict__ up,
-                               int n_mats, int I, int H, int BN, __half* __restrict__ out) {
+                               int n_mats, int I, int H, __half* __restrict__ out) {
   const size_t n8 = (size_t)n_mats * 2 * I * H / 8;
   for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8;
        v += (size_t)gridDim.x * blockDim.x) {
@@ -19,9 +19,8 @@ __global__ void pack_gu_kernel(const int8_t* __restrict__ gate, const int8_t* __
     const size_t prow = el / H;  // packed row over all matrices
     const int m = (int)(prow / (2 * I));
     const int p = (int)(prow % (2 * I));
-    const int b = p / BN, r = p % BN, half = BN / 2;
-    const int ch = b * half + (r % half);
-    const int8_t* src = (r < half ? gate : up) + ((size_t)m * I + ch) * H + h;
+    const int ch = p >> 1;
+    const int8_t* src = ((p & 1) ? up : gate) + ((size_t)m * I + ch) * H + h;
     const uint2 raw = *reinterpret_cast<const uint2*>(src);
     const int8_t* q = reinterpret_cast<const int8_t*>(&raw);
     uint4 o;
@@ -78,9 +77,32 @@ cudaError_t launch_row_sq_max(const int8_t* w, size_t rows, int cols, int* out, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H, int BN,
+// int8 gate/up rows interleaved in pairs (row 2i = gate channel i, row 2i+1 = up channel i),
+// 16 bytes per thread.
+__global__ void pack_gu8_kernel(const int8_t* __restrict__ gate, const int8_t* __restrict__ up,
+                                int n_mats, int I, int H, int8_t* __restrict__ out) {
+  const size_t n16 = (size_t)n_mats * 2 * I * H / 16;
+  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n16;
+       v += (size_t)gridDim.x * blockDim.x) {
+    const size_t el = v * 16;
+    const int h = (int)(el % H);
+    const size_t prow = el / H;
+    const int m = (int)(prow / (2 * I));
+    const int p = (int)(prow % (2 * I));
+    const int8_t* src = ((p & 1) ? up : gate) + ((size_t)m * I + (p >> 1)) * H + h;
+    *reinterpret_cast<int4*>(out + el) = *reinterpret_cast<const int4*>(src);
+  }
+}
+
+cudaError_t launch_pack_gu8(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,
+                            int8_t* out, cudaStream_t s) {
+  pack_gu8_kernel<<<1216, 256, 0, s>>>(gate, up, n_mats, I, H, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,
                            __half* out, cudaStream_t s) {
-  pack_gu_kernel<<<1216, 256, 0, s>>>(gate, up, n_mats, I, H, BN, out);
+  pack_gu_kernel<<<1216, 256, 0, s>>>(gate, up, n_mats, I, H, out);
   return cudaGetLastError();
 }
 

@@ -281,6 +281,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) 
   return cudaGetLastError();
 }
 
+bool decode_shape_supported(int H, int Imax) { return H <= 8192 && Imax <= 4096; }
+
 cudaError_t decode_set_attributes(int H, int Imax) {
   cudaError_t e = cudaFuncSetAttribute(decode_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kDecodeMaxRows * H);

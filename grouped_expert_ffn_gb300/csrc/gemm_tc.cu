@@ -1,11 +1,26 @@
 // Grouped W8A8 GEMMs of the prefill path on the 5th-generation tensor cores (tcgen05).
 //
-// One persistent kernel runs every (expert group, 128-row tile, BN-column tile) work item
+// One persistent kernel runs every (expert group, 128-row weight tile, token tile) work item
 // of a layer: the gate/up GEMM with a fused SiLU(gate)*up epilogue, or the down GEMM with a
 // fused router-weighted scatter-combine into y. This is the concatenated-expert computation
 // of the page "Qwen3.6-35B-A3B Linux v1.0.4: ~2.7s fixed per-request TTFT ...", section
 // "The fix (concatenated-expert dispatch)": one launch per operator and layer instead of one
-// per expert, with gate and up concatenated along N.
+// per expert, with gate and up concatenated along the weight dimension.
+//
+// Orientation: the weights are the MMA's M operand (128 rows per tile) and an expert's tokens
+// its N operand (N = the expert's row count rounded up to 16, at most the token tile TN <=
+// 256), so an expert with 162 tokens costs one 176-wide tile instead of two 128-row tiles.
+// The accumulator holds weight rows in TMEM lanes and tokens in columns. Gate and up rows are
+// interleaved in pairs (row 2i = gate channel i, row 2i+1 = up channel i), so SiLU(gate)*up
+// is formed by one lane-pair exchange.
+//
+// int8 weights stay int8 in HBM (half the bytes of fp16): TMA brings each 128 x 64 int8 weight
+// tile into shared memory (64-byte swizzle), and four converter warps widen it to the fp16
+// 128-byte-swizzled tile the MMA reads. The widening is exact: byte v+128 becomes the fp16
+// bit pattern 0x6400|(v+128) = 1024 + v + 128, and subtracting 1152 leaves v. Token rows are
+// already fp16 integers (written by the permutation step / requantisation) and go straight
+// from TMA (64-row boxes, 128-byte swizzle) to the MMA: widening them in shared memory too
+// would triple the shared-memory traffic of a k-block (measured slower).
 //
 // Exact integer products on an fp16 tensor pipe. sm_103a has no int8 tcgen05 MMA, so the
 // int8 operands are held as fp16 (every int8 value is an fp16 integer) and multiplied with
@@ -13,45 +28,59 @@
 // sum of integer products is exact as long as every partial sum stays below 2^24 in
 // magnitude, in whatever order the tensor core adds them. Two ways to guarantee that:
 //  - bound: for any subset of terms, |sum a_k b_k| <= sqrt(sum a^2) sqrt(sum b^2)
-//    (Cauchy-Schwarz). The producers of the A rows record max_row sum(q^2) and weight packing
-//    records max_row sum(q_w^2); when their product is below 2^48 one accumulator over the
-//    whole K is exact. This holds for realistic data by a wide margin.
+//    (Cauchy-Schwarz). The producers of the token rows record max_row sum(q^2) and weight
+//    packing records max_row sum(q_w^2); when their product is below 2^48 one accumulator over
+//    the whole K is exact. This holds for realistic data by a wide margin.
 //  - chunks: otherwise a fresh accumulator per 1024-element K chunk bounds every partial
 //    sum by 1024 * 127^2 < 2^24; the epilogue rounds each chunk to int32 and adds the chunks
 //    in integer arithmetic.
 // The kernel picks one of the two for the whole launch at its start (every CTA reads the
-// same two words). With one accumulator per tile, TMEM holds two of them (2 x BN columns)
+// same two words). With one accumulator per tile, TMEM holds two of them (2 x TN columns)
 // so the epilogue of one tile overlaps the MMAs of the next.
 //
-// Warp roles (320 threads, one CTA per SM):
-//   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. (tile rows) and half (w/4) of
-//              the tile's columns;
-//   warp 8     TMA producer: A (token rows) and B (weight rows) tiles, 128-byte swizzle;
-//   warp 9     MMA issuer and TMEM owner.
-// Every mbarrier wait is bounded; a wait that runs out sets the plan's error word and the
-// CTA drains its own copies and MMAs, frees TMEM and returns.
+// Warp roles (448 threads, one CTA per SM):
+//   warps 0-7   epilogue: warp w reads TMEM lanes 32*(w%4).. (weight rows) and every other
+//               16-column chunk (tokens) starting at chunk w/4;
+//   warps 8-11  converters: thread r widens weight row r of each k-block;
+//   warp 12     TMA producer: int8 weight tile and fp16 token tile;
+//   warp 13     MMA issuer and TMEM owner.
+// Pipeline: 4 load stages (int8 weights + fp16 tokens, released by the MMA's commit) and 2
+// fp16 weight buffers (released by the MMA's commit). Every mbarrier wait is bounded; a wait
+// that runs out sets the plan's error word and the CTA drains its own copies and MMAs, frees
+// TMEM and returns.
+//
+// The down epilogue writes w * dequant(acc) per (row, channel) to yd; combine_kernel sums each
+// token's k routed rows and its shared-expert row in slot order (deterministic, no atomics).
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 
-template <int BN>
-struct GemmCfg {
-  static constexpr int A_BYTES = kBM * kBK * 2;
-  static constexpr int B_BYTES = BN * kBK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
-  static_assert(STAGES >= 2, "pipeline depth");
-  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
-};
-
+#ifndef MOE_LOAD_STAGES
+#define MOE_LOAD_STAGES 4
+#endif
+constexpr int kTokBox = kTokenBox;                   // token rows per TMA box
+constexpr int kXBytesMax = kMaxTokTile * kBK * 2;    // fp16 token tile per stage (<= 32 KB)
+constexpr int kW8Bytes = kBM * kBK;                  // int8 weight tile per stage (8 KB)
+constexpr int kLoadStage = kXBytesMax + kW8Bytes;    // 40 KB
+constexpr int kLoadStages = MOE_LOAD_STAGES;
+constexpr int kW16Bytes = kBM * kBK * 2;             // fp16 weight tile (16 KB)
+constexpr int kConvBufs = 2;
 constexpr int kEpiWarps = 8;
+constexpr int kConvWarps = 4;
+constexpr int kOffConv = kLoadStages * kLoadStage;
+constexpr int kOffBar = kOffConv + kConvBufs * kW16Bytes;
+constexpr int kBarBytes = 256;
+constexpr int kGemmSmem = kOffBar + kBarBytes + 1024;
+static_assert((2 * kLoadStages + 2 * kConvBufs + 5) * 8 + 8 <= kBarBytes, "barrier area");
+static_assert(kGemmSmem <= 232448, "shared memory");
+
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kProducerWarp = kEpiWarps;
-constexpr int kMmaWarp = kEpiWarps + 1;
-constexpr int kGemmThreads = (kEpiWarps + 2) * 32;
+constexpr int kConvThreads = kConvWarps * 32;        // one thread per weight row
+constexpr int kConvWarp0 = kEpiWarps;
+constexpr int kProducerWarp = kEpiWarps + kConvWarps;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kGemmThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
 
 // Whether one fp32 accumulator over the whole K is provably exact for this launch.
@@ -61,127 +90,130 @@ __device__ __forceinline__ bool single_accumulator_exact(const GemmArgs& a) {
   return r * w < (1ull << 48);
 }
 
-template <int BN>
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 4 int8 (one word) -> 4 fp16, exactly: bytes v+128 placed under the fp16 exponent of 1024,
+// then 1152 subtracted.
+__device__ __forceinline__ uint2 widen4(uint32_t w) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+  const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), bias);
+  const __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), bias);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+
+// Gate/up epilogue. Lane pair (2i, 2i+1) of quadrant q holds gate and up of channel
+// m0/2 + 16q + i for every token column; the even lane finishes columns 0-7 of each 16-column
+// chunk and the odd lane columns 8-15.
 __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
                                                  uint32_t tbase, int half) {
-  const int m = (threadIdx.x / 32 % 4) * 32 + threadIdx.x % 32;  // tile row = TMEM lane
-  const bool valid = m < wi.z;
-  const int row = wi.y + m;
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const bool odd = lane & 1;
   const bool shared = wi.x == a.E;
-  const float* sg = shared ? a.sh_s_g : a.s_g + (size_t)wi.x * a.I;
-  const float* su = shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I;
-  const int cbase = (wi.w / BN) * (BN / 2);
-  const float sx = valid ? a.sx[row] : 0.0f;
-  constexpr int kCols = BN / 4;  // channels per epilogue half
+  const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
+  const float sgc = (shared ? a.sh_s_g : a.s_g + (size_t)wi.x * a.I)[ch];
+  const float suc = (shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I)[ch];
+  const int ncols = wi.z;
 #pragma unroll 1
-  for (int j0 = half * kCols; j0 < (half + 1) * kCols; j0 += 16) {
-    int ag[16], au[16];
+  for (int c0 = half * 16; c0 < ncols; c0 += 32) {
+    int v[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ag[i] = au[i] = 0;
+    for (int i = 0; i < 16; ++i) v[i] = 0;
 #pragma unroll 1
-    for (int c = 0; c < nch; ++c) {
-      uint32_t rg[16], ru[16];
-      tmem_ld16(tbase + c * BN + j0, rg);
-      tmem_ld16(tbase + c * BN + BN / 2 + j0, ru);
+    for (int kc = 0; kc < nch; ++kc) {
+      uint32_t r[16];
+      tmem_ld16(tbase + kc * a.TN + c0, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        ag[i] += __float2int_rn(__uint_as_float(rg[i]));
-        au[i] += __float2int_rn(__uint_as_float(ru[i]));
-      }
+      for (int i = 0; i < 16; ++i) v[i] += __float2int_rn(__uint_as_float(r[i]));
     }
-    if (valid) {
-      float hv[16];
+    int recv[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int ch = cbase + j0 + i;
-        hv[i] = silu_mul(dequant(ag[i], sx, sg[ch]), dequant(au[i], sx, su[ch]));
-      }
-      float4* dst = reinterpret_cast<float4*>(a.h32 + (size_t)row * a.Imax + cbase + j0);
+    for (int i = 0; i < 8; ++i) recv[i] = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[8 + i], 1);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        dst[q] = make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
-      if (a.tap) {
-        int4* tg = reinterpret_cast<int4*>(a.tap + (size_t)row * 2 * a.Imax + cbase + j0);
-        int4* tu = reinterpret_cast<int4*>(a.tap + (size_t)row * 2 * a.Imax + a.Imax + cbase + j0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          tg[q] = make_int4(ag[4 * q], ag[4 * q + 1], ag[4 * q + 2], ag[4 * q + 3]);
-          tu[q] = make_int4(au[4 * q], au[4 * q + 1], au[4 * q + 2], au[4 * q + 3]);
+    for (int i = 0; i < 8; ++i) {
+      const int col = c0 + (odd ? 8 : 0) + i;
+      if (col < ncols) {
+        const int g = odd ? recv[i] : v[i];
+        const int u = odd ? v[8 + i] : recv[i];
+        const int row = wi.y + col;
+        const float sx = a.sx[row];
+        a.h32[(size_t)row * a.Imax + ch] = silu_mul(dequant(g, sx, sgc), dequant(u, sx, suc));
+        if (a.tap) {
+          a.tap[(size_t)row * 2 * a.Imax + ch] = g;
+          a.tap[(size_t)row * 2 * a.Imax + a.Imax + ch] = u;
         }
       }
     }
   }
 }
 
-template <int BN>
+// Down epilogue: lane = output channel m0 + 32q + lane; for each token column the warp stores
+// w * dequant(acc) for 32 consecutive channels of that row of yd (one 128-byte store). The
+// combine kernel then sums each token's rows in slot order.
 __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase,
                                               int half) {
-  const int m = (threadIdx.x / 32 % 4) * 32 + threadIdx.x % 32;
-  const bool valid = m < wi.z;
-  const int row = wi.y + m;
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const bool shared = wi.x == a.E;
-  const float* sd = shared ? a.sh_s_d : a.s_d + (size_t)wi.x * a.H;
-  const float shr = valid ? a.s_h[row] : 0.0f;
-  const float wr = valid ? a.row_w[row] : 0.0f;
-  const int tok = valid ? a.row_token[row] : 0;
-  float* yrow = a.y + (size_t)tok * a.H;
-  constexpr int kCols = BN / 2;
+  const int o = wi.w + q * 32 + lane;
+  const float sdo = (shared ? a.sh_s_d : a.s_d + (size_t)wi.x * a.H)[o];
+  const int ncols = wi.z;
 #pragma unroll 1
-  for (int j0 = half * kCols; j0 < (half + 1) * kCols; j0 += 16) {
-    int acc[16];
+  for (int c0 = half * 16; c0 < ncols; c0 += 32) {
+    int v[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0;
+    for (int i = 0; i < 16; ++i) v[i] = 0;
 #pragma unroll 1
-    for (int c = 0; c < nch; ++c) {
+    for (int kc = 0; kc < nch; ++kc) {
       uint32_t r[16];
-      tmem_ld16(tbase + c * BN + j0, r);
+      tmem_ld16(tbase + kc * a.TN + c0, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] += __float2int_rn(__uint_as_float(r[i]));
+      for (int i = 0; i < 16; ++i) v[i] += __float2int_rn(__uint_as_float(r[i]));
     }
-    if (valid) {
-      const int o0 = wi.w + j0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int o = o0 + 4 * q;
-        red_add_v4(yrow + o, __fmul_rn(wr, dequant(acc[4 * q + 0], shr, sd[o + 0])),
-                   __fmul_rn(wr, dequant(acc[4 * q + 1], shr, sd[o + 1])),
-                   __fmul_rn(wr, dequant(acc[4 * q + 2], shr, sd[o + 2])),
-                   __fmul_rn(wr, dequant(acc[4 * q + 3], shr, sd[o + 3])));
-      }
-      if (a.tap) {
-        int4* t = reinterpret_cast<int4*>(a.tap + (size_t)row * a.H + o0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          t[q] = make_int4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    for (int i = 0; i < 16; ++i) {
+      const int col = c0 + i;
+      if (col < ncols) {
+        const int row = wi.y + col;
+        a.yd[(size_t)row * a.H + o] = __fmul_rn(a.row_w[row], dequant(v[i], a.s_h[row], sdo));
+        if (a.tap) a.tap[(size_t)row * a.H + o] = v[i];
       }
     }
   }
 }
 
-template <int BN, bool GU>
+template <bool GU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmBs) {
-  using Cfg = GemmCfg<BN>;
+    grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmX,
+                        const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmWs) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
-  uint64_t* empty = full + Cfg::STAGES;
-  uint64_t* acc_full = empty + Cfg::STAGES;  // [2]
-  uint64_t* acc_empty = acc_full + 2;        // [2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* empty = full + kLoadStages;
+  uint64_t* cfull = empty + kLoadStages;   // [kConvBufs]
+  uint64_t* cempty = cfull + kConvBufs;    // [kConvBufs]
+  uint64_t* acc_full = cempty + kConvBufs; // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Cfg::STAGES; ++s) {
+    for (int s = 0; s < kLoadStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kConvBufs; ++s) {
+      mbar_init(&cfull[s], kConvThreads);
+      mbar_init(&cempty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
@@ -196,9 +228,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_relinquish();
   }
   if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmBs);
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmWs);
   }
   tc_fence_before();
   __syncthreads();
@@ -206,10 +238,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int n_items = *a.n_items;
   // Accumulator layout for this launch: one accumulator over the whole K (two TMEM slots,
-  // double-buffered) when the bound proves it exact, else 1024-K chunks in one slot.
+  // double-buffered) when the bound proves it exact, else 1024-K chunks (the host sizes the
+  // token tile so that the chunks of one tile fit the 512 columns).
   const bool single = single_accumulator_exact(a);
   const int kmax = a.K_r > a.K_s ? a.K_r : a.K_s;
-  const int slot_cols = single ? BN : ((kmax + kChunkK - 1) / kChunkK) * BN;
+  const int slot_cols = single ? a.TN : ((kmax + kChunkK - 1) / kChunkK) * a.TN;
   const int nslots = slot_cols <= (int)kTmemCols / 2 ? 2 : 1;
   const int kpc = single ? (1 << 30) : kChunkK / kBK;  // k-blocks per accumulator
 
@@ -224,22 +257,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int4 wi = a.items[item];
         const bool shared = wi.x == a.E;
         const int nkb = (shared ? a.K_s : a.K_r) / kBK;
+        const int nbox = (wi.z + kTokBox - 1) / kTokBox;
+        const uint32_t bytes = kW8Bytes + nbox * kTokBox * kBK * 2;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-          uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
-          uint8_t* sb = sa + Cfg::A_BYTES;
-          tma_load_2d(sa, &tmA, &full[stage], kb * kBK, wi.y);
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          uint8_t* sx = smem + stage * kLoadStage;
+          uint8_t* sw = sx + kXBytesMax;
           if (shared)
-            tma_load_2d(sb, &tmBs, &full[stage], kb * kBK, wi.w);
+            tma_load_2d(sw, &tmWs, &full[stage], kb * kBK, wi.w);
           else
-            tma_load_3d(sb, &tmB, &full[stage], kb * kBK, wi.w, wi.x);
+            tma_load_3d(sw, &tmW, &full[stage], kb * kBK, wi.w, wi.x);
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(sx + b * kTokBox * kBK * 2, &tmX, &full[stage], kb * kBK, wi.y + b * kTokBox);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == Cfg::STAGES) {
+          if (++stage == kLoadStages) {
             stage = 0;
             phase ^= 1;
           }
@@ -247,7 +283,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) {
         // Let every copy this thread issued land before the CTA exits.
-        for (int s = 0; s < Cfg::STAGES; ++s) {
+        for (int s = 0; s < kLoadStages; ++s) {
           if (!(armed >> s & 1)) continue;
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(&full[s], (armed_par >> s) & 1) &&
@@ -256,39 +292,83 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
+  } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
+    // ---------------- converters: int8 -> fp16 weight rows ----------------
+    const int r = threadIdx.x - kConvWarp0 * 32;  // weight row within the tile
+    const int sw8 = (r >> 1) & 3;                 // 64-byte swizzle of the int8 row
+    const int sw16 = r & 7;                       // 128-byte swizzle of the fp16 row
+    int stage = 0, cb = 0;
+    uint32_t phase = 0, cphase = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const int4 wi = a.items[item];
+      const int nkb = (wi.x == a.E ? a.K_s : a.K_r) / kBK;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, a.err) ||
+            !mbar_wait(&cempty[cb], cphase ^ 1, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* src = smem + stage * kLoadStage + kXBytesMax + r * 64;
+        uint8_t* dst = smem + kOffConv + cb * kW16Bytes + r * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * (c ^ sw8));
+          const uint2 e0 = widen4(v.x), e1 = widen4(v.y), e2 = widen4(v.z), e3 = widen4(v.w);
+          *reinterpret_cast<uint4*>(dst + 16 * ((2 * c) ^ sw16)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
+          *reinterpret_cast<uint4*>(dst + 16 * ((2 * c + 1) ^ sw16)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&cfull[cb]);
+        if (++stage == kLoadStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++cb == kConvBufs) {
+          cb = 0;
+          cphase ^= 1;
+        }
+      }
+    }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, cb = 0;
+      uint32_t phase = 0, cphase = 0;
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++it) {
         const int4 wi = a.items[item];
         const int nkb = (wi.x == a.E ? a.K_s : a.K_r) / kBK;
+        const int n_mma = (wi.z + 15) & ~15;
+        const uint32_t idesc = idesc_f16_f32(kBM, n_mma);
         const int slot = it % nslots;
         const uint32_t use = (uint32_t)(it / nslots) & 1u;
         if (!mbar_wait(&acc_empty[slot], use ^ 1, abort_flag, a.err)) break;
         tc_fence_after();
         const uint32_t tslot = tmem + (uint32_t)(slot * slot_cols);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, a.err)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, a.err) ||
+              !mbar_wait(&cfull[cb], cphase, abort_flag, a.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-          const uint64_t da = smem_desc_sw128(sa);
-          const uint64_t db = smem_desc_sw128(sa + Cfg::A_BYTES);
-          const uint32_t dt = tslot + (uint32_t)((kb / kpc) * BN);
+          const uint64_t dw = smem_desc_sw128(smem_u32(smem + kOffConv + cb * kW16Bytes));
+          const uint64_t dx = smem_desc_sw128(smem_u32(smem + stage * kLoadStage));
+          const uint32_t dt = tslot + (uint32_t)((kb / kpc) * a.TN);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_f16(dt, da + 2 * kk, db + 2 * kk, idesc, (kb % kpc != 0 || kk != 0) ? 1u : 0u);
+            umma_f16(dt, dw + 2 * kk, dx + 2 * kk, idesc, (kb % kpc != 0 || kk != 0) ? 1u : 0u);
           umma_commit(&empty[stage]);
-          if (++stage == Cfg::STAGES) {
+          umma_commit(&cempty[cb]);
+          if (++stage == kLoadStages) {
             stage = 0;
             phase ^= 1;
+          }
+          if (++cb == kConvBufs) {
+            cb = 0;
+            cphase ^= 1;
           }
         }
         if (!ok) break;
@@ -300,7 +380,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
-  } else {
+  } else if (warp < kEpiWarps) {
     // ---------------- epilogue (warps 0-7) ----------------
     const int half = warp / 4;
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
@@ -315,9 +395,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tbase = lane_base + (uint32_t)(slot * slot_cols);
       if (GU)
-        epilogue_gate_up<BN>(a, wi, nch, tbase, half);
+        epilogue_gate_up(a, wi, nch, tbase, half);
       else
-        epilogue_down<BN>(a, wi, nch, tbase, half);
+        epilogue_down(a, wi, nch, tbase, half);
       tc_fence_before();
       mbar_arrive(&acc_empty[slot]);
     }
@@ -331,50 +411,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <int BN, bool GU>
-static cudaError_t set_attr() {
-  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, GU>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              GemmCfg<BN>::SMEM_BYTES);
-}
-
 cudaError_t gemm_set_attributes() {
-  cudaError_t e;
-  if ((e = set_attr<256, true>()) != cudaSuccess) return e;
-  if ((e = set_attr<256, false>()) != cudaSuccess) return e;
-  if ((e = set_attr<128, true>()) != cudaSuccess) return e;
-  if ((e = set_attr<128, false>()) != cudaSuccess) return e;
-  if ((e = set_attr<64, true>()) != cudaSuccess) return e;
-  return set_attr<64, false>();
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
 }
 
-template <int BN, bool GU>
-static cudaError_t launch_t(const GemmArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                            const CUtensorMap& tmBs, int grid, cudaStream_t s) {
-  grouped_gemm_kernel<BN, GU><<<grid, kGemmThreads, GemmCfg<BN>::SMEM_BYTES, s>>>(a, tmA, tmB, tmBs);
+cudaError_t launch_grouped_gemm(bool gate_up, const GemmArgs& a, const CUtensorMap& tmX,
+                                const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
+                                cudaStream_t s) {
+  if (gate_up)
+    grouped_gemm_kernel<true><<<grid, kGemmThreads, kGemmSmem, s>>>(a, tmX, tmW, tmWs);
+  else
+    grouped_gemm_kernel<false><<<grid, kGemmThreads, kGemmSmem, s>>>(a, tmX, tmW, tmWs);
   return cudaGetLastError();
 }
 
-cudaError_t launch_grouped_gemm(bool gate_up, int BN, const GemmArgs& a, const CUtensorMap& tmA,
-                                const CUtensorMap& tmB, const CUtensorMap& tmBs, int grid,
-                                cudaStream_t s) {
-  switch (BN) {
-    case 256:
-      return gate_up ? launch_t<256, true>(a, tmA, tmB, tmBs, grid, s)
-                     : launch_t<256, false>(a, tmA, tmB, tmBs, grid, s);
-    case 128:
-      return gate_up ? launch_t<128, true>(a, tmA, tmB, tmBs, grid, s)
-                     : launch_t<128, false>(a, tmA, tmB, tmBs, grid, s);
-    case 64:
-      return gate_up ? launch_t<64, true>(a, tmA, tmB, tmBs, grid, s)
-                     : launch_t<64, false>(a, tmA, tmB, tmBs, grid, s);
-    default:
-      return cudaErrorInvalidValue;
+// y[t] = sum over slots j of yd[row(t, j)] + yd[t] (shared expert row), in slot order. Block per
+// token, 8 consecutive channels per thread and pass.
+__global__ void combine_kernel(const float* __restrict__ yd, const int* __restrict__ slot_row,
+                               int T, int k, int H, int has_shared, float* __restrict__ y) {
+  const int t = blockIdx.x;
+  __shared__ int rows[9];
+  if (threadIdx.x < k) rows[threadIdx.x] = slot_row[(size_t)t * k + threadIdx.x];
+  if (threadIdx.x == k) rows[k] = has_shared ? t : -1;
+  __syncthreads();
+  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j <= k; ++j) {
+      const int r = rows[j];
+      if (r < 0) continue;
+      const float4 v = *reinterpret_cast<const float4*>(yd + (size_t)r * H + c);
+      acc.x = __fadd_rn(acc.x, v.x);
+      acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z);
+      acc.w = __fadd_rn(acc.w, v.w);
+    }
+    *reinterpret_cast<float4*>(y + (size_t)t * H + c) = acc;
   }
 }
 
+cudaError_t launch_combine(const float* yd, const int* slot_row, int T, int k, int H,
+                           int has_shared, float* y, cudaStream_t s) {
+  combine_kernel<<<T, 256, 0, s>>>(yd, slot_row, T, k, H, has_shared, y);
+  return cudaGetLastError();
+}
+
 // Per-row requantisation of h = SiLU(gate)*up: s = amax/127, q = rne(h/s) (|q| <= 127),
-// written as fp16 integers for the down GEMM's A operand. One warp per row.
+// written as fp16 integers for the down GEMM's token operand. One warp per row.
 __global__ void requant_kernel(const float* __restrict__ h32, int R, int T_sh, int I, int Is,
                                int Imax, __half* __restrict__ hq, float* __restrict__ sh,
                                int* __restrict__ sq_max) {

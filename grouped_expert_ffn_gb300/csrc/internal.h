@@ -10,20 +10,23 @@
 
 namespace moe {
 
-constexpr int kBM = 128;        // tensor-core tile rows (token rows)
+constexpr int kBM = 128;        // tensor-core tile rows (weight rows: the MMA's M)
+constexpr int kMaxTokTile = 256;  // token rows per tile (the MMA's N), at most
+constexpr int kTokenBox = 64;   // token rows per TMA box of the GEMMs' N operand
 constexpr int kBK = 64;         // K elements per pipeline stage (128 bytes of fp16)
 constexpr int kChunkK = 1024;   // K elements summed in one fp32 TMEM accumulator
 constexpr int kTokPerBlk = 64;  // tokens per histogram block (one 64-bit mask per expert)
 constexpr int kDecodeMaxRows = 8;
 
-// One unit of grouped-GEMM work: rows [row0, row0 + rows) of group `group` (expert id, or E
-// for the shared expert) against weight rows [n0, n0 + BN).
-// Stored as int4 {group, row0, rows, n0}.
+// One unit of grouped-GEMM work: token rows [row0, row0 + rows) of group `group` (expert id,
+// or E for the shared expert) against weight rows [m0, m0 + 128).
+// Stored as int4 {group, row0, rows, m0}.
 
 struct GemmArgs {
   const int4* items;
   const int* n_items;
   int E;
+  int TN;                // token tile (items have rows <= TN)
   int K_r, K_s;          // reduction length of routed / shared groups
   int I, Is, Imax, H;
   // gate/up epilogue
@@ -39,7 +42,7 @@ struct GemmArgs {
   const float* sh_s_d;   // [H]
   const int* row_token;  // per row
   const float* row_w;    // per row
-  float* y;              // [T, H]
+  float* yd;             // [R, H] weighted per-row down outputs
   // exactness bound of one fp32 accumulator over the whole K (see gemm_tc.cu)
   const int* row_sq_max;  // max over A rows of sum(q^2), written by the row producer
   const int* w_sq_max;    // max over weight rows of sum(q_w^2), written at packing
@@ -48,11 +51,13 @@ struct GemmArgs {
   int* err;
 };
 
-cudaError_t launch_grouped_gemm(bool gate_up, int BN, const GemmArgs& a, const CUtensorMap& tmA,
-                                const CUtensorMap& tmB, const CUtensorMap& tmBs, int grid,
+cudaError_t launch_grouped_gemm(bool gate_up, const GemmArgs& a, const CUtensorMap& tmX,
+                                const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
                                 cudaStream_t s);
 cudaError_t gemm_set_attributes();
 
+cudaError_t launch_combine(const float* yd, const int* slot_row, int T, int k, int H,
+                           int has_shared, float* y, cudaStream_t s);
 cudaError_t launch_requant(const float* h32, int R, int T_sh, int I, int Is, int Imax,
                            __half* hq, float* sh, int* sq_max, cudaStream_t s);
 
@@ -64,7 +69,7 @@ struct PrepArgs {
   const int32_t* idx;
   const float* w;
   const uint16_t* x;
-  int T, k, E, H, I, Is, has_shared, bn_gu, bn_d;
+  int T, k, E, H, I, Is, has_shared, tn_gu, tn_d;
   unsigned long long* bmask;  // [nblk, E]
   int* bhist;                 // [nblk, E]
   int* counts;                // [E]
@@ -73,11 +78,11 @@ struct PrepArgs {
   int4* items_gu;
   int4* items_d;
   int* n_items;               // [2]
-  __half* xq;                 // [R, H]
+  __half* xq;                 // [R, H] activation codes as fp16 integers, row order
   float* sx;                  // [R]
   int* row_token;             // [R]
   float* row_w;               // [R]
-  float* y;                   // [T, H] zeroed
+  int* slot_row;              // [T*k] row of each routed slot
   int8_t* qtok;               // [T, H] or NULL
   float* stok;                // [T]   or NULL
   int* sq_max;                // [2] row sum(q^2) maxima (gate/up rows, down rows), reset here
@@ -89,7 +94,7 @@ struct DecodeArgs {
   const int32_t* idx;
   const float* w;
   const uint16_t* x;
-  int T, k, E, H, I, Is, Imax, has_shared;
+  int T, k, E, H, I, Is, Imax, has_shared, num_sms;
   const int8_t* w_gate;
   const int8_t* w_up;
   const int8_t* w_down;
@@ -121,11 +126,14 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev);
 cudaError_t decode_set_attributes(int H, int Imax);
+bool decode_shape_supported(int H, int Imax);  // shapes the T <= 8 streaming kernels take
 
 // weight packing and the stacked-prefill helpers
-cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H, int BN,
+cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,
                            __half* out, cudaStream_t s);
 cudaError_t launch_widen(const int8_t* src, size_t n, __half* out, cudaStream_t s);
+cudaError_t launch_pack_gu8(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,
+                            int8_t* out, cudaStream_t s);
 cudaError_t launch_row_sq_max(const int8_t* w, size_t rows, int cols, int* out, cudaStream_t s);
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, int T, int H, int E,
                                  float* out, cudaStream_t s);

@@ -16,16 +16,18 @@ using namespace moe;
 struct moe_plan_s {
   int E = 0, k = 0, H = 0, I = 0, Is = 0, max_tokens = 0, Imax = 0, has_shared = 0;
   int device = 0, num_sms = 0;
-  int bn_gu = 0, bn_d = 0;
+  int tn_gu = 0, tn_d = 0;  // token tiles of the two GEMMs
   size_t R_max = 0;
   int max_items_gu = 0, max_items_d = 0;
   // workspace (device)
-  __half* xq = nullptr;
+  __half* xq = nullptr;  // [R, H] activation codes (fp16 integers) in row order
   float* sx = nullptr;
   int* row_token = nullptr;
   float* row_w = nullptr;
+  int* slot_row = nullptr;   // [max_tokens * k]
+  float* yd = nullptr;       // [R, H] weighted per-row down outputs
   float* h32 = nullptr;
-  __half* hq = nullptr;
+  __half* hq = nullptr;  // [R, Imax] codes of SiLU(gate)*up (fp16 integers)
   float* sh = nullptr;
   int* counts = nullptr;
   int* offsets = nullptr;
@@ -54,19 +56,17 @@ struct moe_plan_s {
   };
   std::vector<ProfRec> prof_pending;
   std::vector<cudaEvent_t> ev_pool;
-  CUtensorMap tmA_gu, tmA_d;
+  CUtensorMap tmX_gu, tmX_d;  // token rows of the two GEMMs (N operand)
   std::vector<void*> allocs;
 };
 
 struct moe_packed_s {
   moe_plan_s* plan = nullptr;
   moe_weights w;
-  __half* gu16 = nullptr;
-  __half* d16 = nullptr;
-  __half* shgu16 = nullptr;
-  __half* shd16 = nullptr;
+  int8_t* gu8 = nullptr;    // [E, 2I, H] gate/up rows interleaved in pairs
+  int8_t* shgu8 = nullptr;  // [2Is, H]
   int* w_sq = nullptr;  // [2] max over weight rows of sum(q^2): gate/up rows, down rows
-  CUtensorMap tmB_gu, tmBs_gu, tmB_d, tmBs_d;
+  CUtensorMap tmW_gu, tmWs_gu, tmW_d, tmWs_d;  // weights (M operand): routed, shared
 };
 
 namespace {
@@ -107,6 +107,21 @@ bool encode_2byte(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int 
   return r == CUDA_SUCCESS;
 }
 
+// int8 weight tiles: box {64 bytes, box_rows[, 1]}, 64-byte swizzle.
+bool encode_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+               const uint64_t* strides_bytes, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[3], st[2];
+  cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, 1}, es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) d[i] = dims[i];
+  for (int i = 0; i < rank - 1; ++i) st[i] = strides_bytes[i];
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), d, st, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool encode_f16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                 const uint64_t* strides_bytes, uint32_t box_rows) {
   return encode_2byte(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides_bytes, box_rows);
@@ -137,15 +152,13 @@ void free_plan(moe_plan_s* p) {
   delete p;
 }
 
-int pick_bn(int cap, bool (*ok)(int, const moe_plan_s*), const moe_plan_s* p) {
-  for (int bn = 256; bn >= 64; bn >>= 1)
-    if (bn <= cap && ok(bn, p)) return bn;
-  return 0;
+// Token tile: 256 rows, or fewer when the exact 1024-K chunks of one tile would not fit the
+// 512 TMEM columns (chunks x tile <= 512), a multiple of 32.
+int token_tile(int K) {
+  const int nch = (K + kChunkK - 1) / kChunkK;
+  int tn = (512 / nch) & ~31;
+  return tn > kMaxTokTile ? kMaxTokTile : tn;
 }
-bool ok_gu(int bn, const moe_plan_s* p) {
-  return p->I % (bn / 2) == 0 && (p->Is == 0 || p->Is % (bn / 2) == 0);
-}
-bool ok_d(int bn, const moe_plan_s* p) { return p->H % bn == 0; }
 
 moe_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MOE_OK;
@@ -212,7 +225,7 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   *out = nullptr;
   if (E < 1 || top_k < 1 || top_k > E || H < 1 || I < 1 || I_shared < 0 || max_tokens < 1)
     return MOE_ERR_INVALID_ARG;
-  if (E > 256 || top_k > 8 || H % 64 || I % 64 || I_shared % 64 || H > 8192 || I > 4096 ||
+  if (E > 256 || top_k > 8 || H % 128 || I % 64 || I_shared % 64 || H > 8192 || I > 4096 ||
       I_shared > 4096 || max_tokens > (1 << 20))
     return MOE_ERR_UNSUPPORTED;
   int dev = 0;
@@ -237,20 +250,17 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   p->max_tokens = max_tokens;
   p->device = dev;
   p->num_sms = prop.multiProcessorCount;
-  const int nch_gu = (H + kChunkK - 1) / kChunkK;
-  const int nch_d = (p->Imax + kChunkK - 1) / kChunkK;
-  p->bn_gu = pick_bn(512 / nch_gu, ok_gu, p);
-  p->bn_d = pick_bn(512 / nch_d, ok_d, p);
-  if (!p->bn_gu || !p->bn_d) {
-    delete p;
-    return MOE_ERR_UNSUPPORTED;
-  }
+  p->tn_gu = token_tile(H);
+  p->tn_d = token_tile(p->Imax);
   const size_t T = max_tokens;
   p->R_max = T * top_k + (p->has_shared ? T : 0);
   const size_t nblk = (T + kTokPerBlk - 1) / kTokPerBlk;
-  const size_t mtiles = (T * top_k + (size_t)(kBM - 1) * E) / kBM + (p->has_shared ? (T + kBM - 1) / kBM : 0) + 1;
-  p->max_items_gu = (int)(mtiles * (2 * p->Imax / p->bn_gu));
-  p->max_items_d = (int)(mtiles * (H / p->bn_d));
+  // sum over groups of ceil(rows / tile) <= (routed rows + (tile-1) E) / tile + shared tiles
+  auto tiles = [&](int tn) {
+    return (T * top_k + (size_t)(tn - 1) * E) / tn + (p->has_shared ? (T + tn - 1) / tn : 0) + 1;
+  };
+  p->max_items_gu = (int)(tiles(p->tn_gu) * (2 * p->Imax / kBM));
+  p->max_items_d = (int)(tiles(p->tn_d) * (H / kBM));
   moe_status st = MOE_OK;
 #define ALLOC(ptr, n)                                  \
   if ((st = dalloc(p, &p->ptr, (n))) != MOE_OK) {      \
@@ -261,6 +271,8 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   ALLOC(sx, p->R_max);
   ALLOC(row_token, p->R_max);
   ALLOC(row_w, p->R_max);
+  ALLOC(slot_row, T * top_k);
+  ALLOC(yd, p->R_max * H);
   ALLOC(h32, p->R_max * p->Imax);
   ALLOC(hq, p->R_max * p->Imax);
   ALLOC(sh, p->R_max);
@@ -284,17 +296,17 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
     free_plan(p);
     return MOE_ERR_CUDA;
   }
-  // A operands of the two GEMMs: fp16 rows of the plan's row order.
+  // Token-row operands of the two GEMMs (fp16 rows in the plan's row order), 64-row boxes.
   {
     const uint64_t dims[2] = {(uint64_t)H, (uint64_t)p->R_max};
     const uint64_t st2[1] = {(uint64_t)H * 2};
-    if (!encode_f16(&p->tmA_gu, p->xq, 2, dims, st2, kBM)) {
+    if (!encode_f16(&p->tmX_gu, p->xq, 2, dims, st2, kTokenBox)) {
       free_plan(p);
       return MOE_ERR_CUDA;
     }
     const uint64_t dims_d[2] = {(uint64_t)p->Imax, (uint64_t)p->R_max};
     const uint64_t st_d[1] = {(uint64_t)p->Imax * 2};
-    if (!encode_f16(&p->tmA_d, p->hq, 2, dims_d, st_d, kBM)) {
+    if (!encode_f16(&p->tmX_d, p->hq, 2, dims_d, st_d, kTokenBox)) {
       free_plan(p);
       return MOE_ERR_CUDA;
     }
@@ -333,28 +345,19 @@ moe_status moe_pack_weights(moe_plan_t p, const moe_weights* w, void* stream, mo
   pk->w = *w;
   const size_t E = p->E, H = p->H, I = p->I, Is = p->Is;
   auto fail = [&](moe_status st) {
-    if (pk->gu16) cudaFree(pk->gu16);
-    if (pk->d16) cudaFree(pk->d16);
-    if (pk->shgu16) cudaFree(pk->shgu16);
-    if (pk->shd16) cudaFree(pk->shd16);
+    if (pk->gu8) cudaFree(pk->gu8);
+    if (pk->shgu8) cudaFree(pk->shgu8);
     if (pk->w_sq) cudaFree(pk->w_sq);
     cudaGetLastError();
     delete pk;
     return st;
   };
-  if (cudaMalloc(&pk->gu16, E * 2 * I * H * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
-  if (cudaMalloc(&pk->d16, E * H * I * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
+  if (cudaMalloc(&pk->gu8, E * 2 * I * H) != cudaSuccess) return fail(MOE_ERR_OOM);
   if (cudaMalloc(&pk->w_sq, 2 * sizeof(int)) != cudaSuccess) return fail(MOE_ERR_OOM);
-  if (p->has_shared) {
-    if (cudaMalloc(&pk->shgu16, 2 * Is * H * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
-    if (cudaMalloc(&pk->shd16, H * Is * 2) != cudaSuccess) return fail(MOE_ERR_OOM);
-  }
-  cudaError_t e = launch_pack_gu(w->w_gate, w->w_up, (int)E, (int)I, (int)H, p->bn_gu, pk->gu16, s);
-  if (e == cudaSuccess) e = launch_widen(w->w_down, E * H * I, pk->d16, s);
-  if (e == cudaSuccess && p->has_shared) {
-    e = launch_pack_gu(w->sh_gate, w->sh_up, 1, (int)Is, (int)H, p->bn_gu, pk->shgu16, s);
-    if (e == cudaSuccess) e = launch_widen(w->sh_down, H * Is, pk->shd16, s);
-  }
+  if (p->has_shared && cudaMalloc(&pk->shgu8, 2 * Is * H) != cudaSuccess) return fail(MOE_ERR_OOM);
+  cudaError_t e = launch_pack_gu8(w->w_gate, w->w_up, (int)E, (int)I, (int)H, pk->gu8, s);
+  if (e == cudaSuccess && p->has_shared)
+    e = launch_pack_gu8(w->sh_gate, w->sh_up, 1, (int)Is, (int)H, pk->shgu8, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(pk->w_sq, 0, 2 * sizeof(int), s);
   if (e == cudaSuccess) e = launch_row_sq_max(w->w_gate, E * I, (int)H, pk->w_sq, s);
   if (e == cudaSuccess) e = launch_row_sq_max(w->w_up, E * I, (int)H, pk->w_sq, s);
@@ -367,22 +370,23 @@ moe_status moe_pack_weights(moe_plan_t p, const moe_weights* w, void* stream, mo
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA);
   bool ok = true;
   {
+    // weights (the MMA's M operand): int8, 128 rows x 64 bytes per tile
     const uint64_t dims[3] = {H, 2 * I, E};
-    const uint64_t st[2] = {H * 2, 2 * I * H * 2};
-    ok = ok && encode_f16(&pk->tmB_gu, pk->gu16, 3, dims, st, p->bn_gu);
+    const uint64_t st[2] = {H, 2 * I * H};
+    ok = ok && encode_u8(&pk->tmW_gu, pk->gu8, 3, dims, st, kBM);
     const uint64_t dd[3] = {I, H, E};
-    const uint64_t sd[2] = {I * 2, H * I * 2};
-    ok = ok && encode_f16(&pk->tmB_d, pk->d16, 3, dd, sd, p->bn_d);
+    const uint64_t sd[2] = {I, H * I};
+    ok = ok && encode_u8(&pk->tmW_d, w->w_down, 3, dd, sd, kBM);
     if (p->has_shared) {
       const uint64_t ds[2] = {H, 2 * Is};
-      const uint64_t ss[1] = {H * 2};
-      ok = ok && encode_f16(&pk->tmBs_gu, pk->shgu16, 2, ds, ss, p->bn_gu);
+      const uint64_t ss[1] = {H};
+      ok = ok && encode_u8(&pk->tmWs_gu, pk->shgu8, 2, ds, ss, kBM);
       const uint64_t dsd[2] = {Is, H};
-      const uint64_t ssd[1] = {Is * 2};
-      ok = ok && encode_f16(&pk->tmBs_d, pk->shd16, 2, dsd, ssd, p->bn_d);
+      const uint64_t ssd[1] = {Is};
+      ok = ok && encode_u8(&pk->tmWs_d, w->sh_down, 2, dsd, ssd, kBM);
     } else {
-      pk->tmBs_gu = pk->tmB_gu;  // never read: no shared group exists
-      pk->tmBs_d = pk->tmB_d;
+      pk->tmWs_gu = pk->tmW_gu;  // never read: no shared group exists
+      pk->tmWs_d = pk->tmW_d;
     }
   }
   if (!ok) return fail(MOE_ERR_CUDA);
@@ -392,10 +396,8 @@ moe_status moe_pack_weights(moe_plan_t p, const moe_weights* w, void* stream, mo
 
 moe_status moe_packed_destroy(moe_packed_t pk) {
   if (!pk) return MOE_ERR_INVALID_ARG;
-  if (pk->gu16) cudaFree(pk->gu16);
-  if (pk->d16) cudaFree(pk->d16);
-  if (pk->shgu16) cudaFree(pk->shgu16);
-  if (pk->shd16) cudaFree(pk->shd16);
+  if (pk->gu8) cudaFree(pk->gu8);
+  if (pk->shgu8) cudaFree(pk->shgu8);
   if (pk->w_sq) cudaFree(pk->w_sq);
   delete pk;
   return MOE_OK;
@@ -423,7 +425,7 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   const int R = T * p->k + T_sh;
   p->last_T = T;
   cudaError_t e;
-  if (T <= kDecodeMaxRows) {
+  if (T <= kDecodeMaxRows && decode_shape_supported(p->H, p->Imax)) {
     DecodeArgs a;
     a.idx = idx;
     a.w = w;
@@ -436,6 +438,7 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
     a.Is = p->Is;
     a.Imax = p->Imax;
     a.has_shared = p->has_shared;
+    a.num_sms = p->num_sms;
     a.w_gate = pk->w.w_gate;
     a.w_up = pk->w.w_up;
     a.w_down = pk->w.w_down;
@@ -478,8 +481,8 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   pa.I = p->I;
   pa.Is = p->Is;
   pa.has_shared = p->has_shared;
-  pa.bn_gu = p->bn_gu;
-  pa.bn_d = p->bn_d;
+  pa.tn_gu = p->tn_gu;
+  pa.tn_d = p->tn_d;
   pa.bmask = p->bmask;
   pa.bhist = p->bhist;
   pa.counts = p->counts;
@@ -492,7 +495,7 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   pa.sx = p->sx;
   pa.row_token = p->row_token;
   pa.row_w = p->row_w;
-  pa.y = y;
+  pa.slot_row = p->slot_row;
   pa.qtok = p->debug ? p->qtok : nullptr;
   pa.stok = p->debug ? p->stok : nullptr;
   pa.sq_max = p->sq_max;
@@ -520,7 +523,7 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.sh_s_d = pk->w.sh_s_down;
   g.row_token = p->row_token;
   g.row_w = p->row_w;
-  g.y = y;
+  g.yd = p->yd;
   g.err = p->err;
   const int grid = p->num_sms;
   // gate/up: K = H for every group
@@ -528,11 +531,11 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.n_items = p->n_items;
   g.K_r = p->H;
   g.K_s = p->H;
+  g.TN = p->tn_gu;
   g.tap = p->debug ? p->tap_gu : nullptr;
   g.row_sq_max = p->sq_max;
   g.w_sq_max = pk->w_sq;
-  if ((e = launch_grouped_gemm(true, p->bn_gu, g, p->tmA_gu, pk->tmB_gu, pk->tmBs_gu, grid, s)) !=
-      cudaSuccess)
+  if ((e = launch_grouped_gemm(true, g, p->tmX_gu, pk->tmW_gu, pk->tmWs_gu, grid, s)) != cudaSuccess)
     return cuda_status(e);
   if (ev) cudaEventRecord(ev[2], s);
   if ((e = launch_requant(p->h32, R, T_sh, p->I, p->Is, p->Imax, p->hq, p->sh, p->sq_max + 1, s)) !=
@@ -544,10 +547,12 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.n_items = p->n_items + 1;
   g.K_r = p->I;
   g.K_s = p->has_shared ? p->Is : p->I;
+  g.TN = p->tn_d;
   g.tap = p->debug ? p->tap_d : nullptr;
   g.row_sq_max = p->sq_max + 1;
   g.w_sq_max = pk->w_sq + 1;
-  e = launch_grouped_gemm(false, p->bn_d, g, p->tmA_d, pk->tmB_d, pk->tmBs_d, grid, s);
+  e = launch_grouped_gemm(false, g, p->tmX_d, pk->tmW_d, pk->tmWs_d, grid, s);
+  if (e == cudaSuccess) e = launch_combine(p->yd, p->slot_row, T, p->k, p->H, p->has_shared, y, s);
   if (ev) cudaEventRecord(ev[4], s);
   return cuda_status(e);
 }

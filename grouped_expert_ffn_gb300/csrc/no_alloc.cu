@@ -26,11 +26,12 @@ namespace {
 
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
 
 // Device address of the scratch array for the current device, looked up once per device.
 // In host code `g_decode_scratch` names a host-side stand-in, not device memory, so the
 // address must come from cudaGetSymbolAddress with that device current.
-cudaError_t scratch_for_current_device(void** out) {
+cudaError_t scratch_for_current_device(void** out, int* num_sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -40,9 +41,14 @@ cudaError_t scratch_for_current_device(void** out) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_num_sms[dev] = n;
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];
+  *num_sms = g_num_sms[dev];
   return cudaSuccess;
 }
 
@@ -66,8 +72,8 @@ extern "C" moe_status moe_forward_decode_static(int E, int top_k, int H, int I, 
   if (!wt || !x || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
   if (E < 1 || top_k < 1 || top_k > E || H < 1 || I < 1 || I_shared < 0) return MOE_ERR_INVALID_ARG;
   if (T < 1 || T > kDecodeMaxRows) return MOE_ERR_CAPACITY;
-  if (E > 256 || top_k > 8 || H % 64 || I % 64 || I_shared % 64 || H > 8192 || I > 4096 ||
-      I_shared > 4096)
+  if (E > 256 || top_k > 8 || H % 128 || I % 64 || I_shared % 64 ||
+      !decode_shape_supported(H, I > I_shared ? I : I_shared))
     return MOE_ERR_UNSUPPORTED;
   const void* need[] = {x, idx, w, y, wt->w_gate, wt->w_up, wt->w_down, wt->s_gate, wt->s_up,
                         wt->s_down};
@@ -100,14 +106,16 @@ extern "C" moe_status moe_forward_decode_static(int E, int top_k, int H, int I, 
   if (off > kScratchBytes) return MOE_ERR_CAPACITY;
 
   unsigned char* base = nullptr;
-  cudaError_t e = scratch_for_current_device(reinterpret_cast<void**>(&base));
+  int num_sms = 0;
+  cudaError_t e = scratch_for_current_device(reinterpret_cast<void**>(&base), &num_sms);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? MOE_ERR_NO_DEVICE
                                                                        : MOE_ERR_CUDA;
   }
   // The decode kernels take up to 8 rows x H (gate/up) and 8 rows x Imax (down) bytes of
-  // dynamic shared memory; raise their limit to this library's largest shapes.
+  // dynamic shared memory; raise their limit to this library's largest shapes (set per call:
+  // a plan created later may have lowered it).
   if ((e = decode_set_attributes(8192, 4096)) != cudaSuccess) return MOE_ERR_CUDA;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -128,6 +136,7 @@ extern "C" moe_status moe_forward_decode_static(int E, int top_k, int H, int I, 
   a.Is = I_shared;
   a.Imax = Imax;
   a.has_shared = has_shared;
+  a.num_sms = num_sms;
   a.w_gate = wt->w_gate;
   a.w_up = wt->w_up;
   a.w_down = wt->w_down;

@@ -6,9 +6,9 @@
 //                    block's tokens chose it); its popcount is the block's histogram.
 //  scan_kernel       one block: per-expert counts, exclusive prefixes over blocks and over
 //                    experts, and the grouped-GEMM work lists (expert-tile queue).
-//  scatter_kernel    block per token: per-token int8 quantisation of x, written as fp16
-//                    integers into every row the token occupies (one per routed slot plus the
-//                    shared expert's row) with 16-byte stores; row metadata; y zeroed.
+//  scatter_kernel    block per token: per-token int8 quantisation of x, the codes written as
+//                    fp16 integers into every row the token occupies (one per routed slot plus
+//                    the shared expert's row) with 16-byte stores; row metadata.
 // Row order: the shared expert's rows [0, T) first (row t = token t), then the routed
 // assignments grouped by expert id and, inside an expert, by token. This is the order a
 // stable sort of the flattened idx by expert id gives.
@@ -21,6 +21,8 @@ constexpr int kMaxEPerLane = 8;  // E <= 256
 
 __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int k,
                              int32_t* __restrict__ idx, float* __restrict__ w, int* err) {
+  // a dependent decode launch may start now; it waits for this grid before reading idx / w
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (t >= T) return;
@@ -118,8 +120,9 @@ __global__ void hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E
 }
 
 // One block of 1024 threads. Turns bhist into exclusive per-expert prefixes over blocks,
-// writes counts/offsets and the two work lists (gate/up and down), ordered by group, then
-// weight tile, then row tile so that consecutive items reuse one weight tile from L2.
+// writes counts/offsets and the two work lists (gate/up and down): per group, every
+// (128-row weight tile, token tile of at most TN rows) pair, ordered by group, then weight
+// tile, then token tile, so consecutive items of a large group reuse one weight tile from L2.
 __global__ void scan_kernel(PrepArgs a, int nblk) {
   __shared__ int s_cnt[257];
   __shared__ int s_off[258];
@@ -174,13 +177,12 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
     for (int g = 0; g < ng; ++g) {
       const bool sh = a.has_shared && g == 0;
       const int cnt = sh ? a.T : s_cnt[g - a.has_shared];
-      const int mt = (cnt + kBM - 1) / kBM;
-      const int ntg = (2 * (sh ? a.Is : a.I)) / a.bn_gu;
-      const int ntd = a.H / a.bn_d;
+      const int wtg = (2 * (sh ? a.Is : a.I)) / kBM;  // gate/up weight tiles
+      const int wtd = a.H / kBM;                       // down weight tiles
       s_base_gu[g] = bg;
       s_base_d[g] = bd;
-      bg += mt * ntg;
-      bd += mt * ntd;
+      bg += wtg * ((cnt + a.tn_gu - 1) / a.tn_gu);
+      bd += wtd * ((cnt + a.tn_d - 1) / a.tn_d);
     }
     s_base_gu[ng] = bg;
     s_base_d[ng] = bd;
@@ -193,21 +195,22 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
     const int gid = sh ? E : g - a.has_shared;
     const int cnt = sh ? a.T : s_cnt[gid];
     const int row0 = sh ? 0 : T_sh + s_off[gid];
-    const int mt = (cnt + kBM - 1) / kBM;
-    const int ntg = (2 * (sh ? a.Is : a.I)) / a.bn_gu;
-    const int ntd = a.H / a.bn_d;
+    const int wtg = (2 * (sh ? a.Is : a.I)) / kBM;
+    const int wtd = a.H / kBM;
+    const int ttg = (cnt + a.tn_gu - 1) / a.tn_gu;
+    const int ttd = (cnt + a.tn_d - 1) / a.tn_d;
     int p = s_base_gu[g];
-    for (int n = 0; n < ntg; ++n)
-      for (int m = 0; m < mt; ++m)
-        a.items_gu[p++] = make_int4(gid, row0 + m * kBM, min(kBM, cnt - m * kBM), n * a.bn_gu);
+    for (int w = 0; w < wtg; ++w)
+      for (int t = 0; t < ttg; ++t)
+        a.items_gu[p++] = make_int4(gid, row0 + t * a.tn_gu, min(a.tn_gu, cnt - t * a.tn_gu), w * kBM);
     p = s_base_d[g];
-    for (int n = 0; n < ntd; ++n)
-      for (int m = 0; m < mt; ++m)
-        a.items_d[p++] = make_int4(gid, row0 + m * kBM, min(kBM, cnt - m * kBM), n * a.bn_d);
+    for (int w = 0; w < wtd; ++w)
+      for (int t = 0; t < ttd; ++t)
+        a.items_d[p++] = make_int4(gid, row0 + t * a.tn_d, min(a.tn_d, cnt - t * a.tn_d), w * kBM);
   }
 }
 
-// Block per token: quantise x[t] once, write its fp16 integer codes to each of its rows.
+// Block per token: quantise x[t] once, write its codes (fp16 integers) to each of its rows.
 __global__ void scatter_kernel(PrepArgs a) {
   const int t = blockIdx.x;
   const int H = a.H, k = a.k, E = a.E;
@@ -231,6 +234,7 @@ __global__ void scatter_kernel(PrepArgs a) {
     a.perm[pos] = t * k + j;
     const int row = T_sh + pos;
     s_rows[j] = row;
+    a.slot_row[(size_t)t * k + j] = row;
     a.row_token[row] = t;
     a.row_w[row] = a.w[(size_t)t * k + j];
   } else if (threadIdx.x == k && a.has_shared) {
@@ -263,7 +267,6 @@ __global__ void scatter_kernel(PrepArgs a) {
   const int nrows = k + (a.has_shared ? 1 : 0);
   if (threadIdx.x < nrows) a.sx[s_rows[threadIdx.x]] = s;
   if (threadIdx.x == 0 && a.stok) a.stok[t] = s;
-  float* yr = a.y + (size_t)t * H;
   int sq = 0;  // sum of squared codes of this token (exactness bound of the gate/up GEMM)
   for (int c = threadIdx.x * 8; c < H; c += blockDim.x * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
@@ -293,8 +296,6 @@ __global__ void scatter_kernel(PrepArgs a) {
       for (int i = 0; i < 8; ++i) qb[i] = (uint8_t)(int8_t)q[i];
       *reinterpret_cast<uint2*>(a.qtok + (size_t)t * H + c) = qv;
     }
-    *reinterpret_cast<float4*>(yr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4*>(yr + c + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   sq = warp_sum_i(sq);
   if ((threadIdx.x & 31) == 0) s_sq[threadIdx.x / 32] = sq;

@@ -82,7 +82,7 @@ typedef struct {
  * tokens per call (the only allocation on the forward path's behalf).
  *   E: routed experts (1..256); top_k: 1..min(E, 8); H: hidden size; I: routed expert
  *   intermediate size; I_shared: shared expert intermediate size, 0 = no shared expert.
- * Supported shapes: H and I (and I_shared when > 0) multiples of 64; H <= 8192;
+ * Supported shapes: H a multiple of 128, I (and I_shared when > 0) multiples of 64; H <= 8192;
  *   I, I_shared <= 4096. Otherwise MOE_ERR_UNSUPPORTED.
  * Uses the current CUDA device. *out receives the handle; release with moe_plan_destroy. */
 MOE_API moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens,
@@ -202,8 +202,8 @@ MOE_API moe_status moe_residual_add(uint16_t* x, const float* y, int T, int H, v
  * It allocates nothing: its scratch (at most 2 MiB: per-token codes, the unique-expert
  * list, row maps, fp32 SiLU(gate)*up rows) is a file-scope __device__ array inside the
  * library, present on every GPU that loads the library until the process exits. Limits:
- * T <= 8 (else MOE_ERR_CAPACITY), E <= 256, top_k <= 8, H <= 8192, I and I_shared <= 4096,
- * all multiples of 64 (else MOE_ERR_UNSUPPORTED). The first call on each device looks up
+ * T <= 8 (else MOE_ERR_CAPACITY), E <= 256, top_k <= 8, H <= 8192 and a multiple of 128,
+ * I and I_shared <= 4096 and multiples of 64 (else MOE_ERR_UNSUPPORTED). The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress); make that first call before any stream
  * capture. Every call shares the one array and keeps the previous call's contents (only
  * the error word is cleared per call): calls that overlap on the GPU - on two streams, or
