@@ -195,10 +195,11 @@ def moe_router_logits(x, w_router, logits, stream=None):
 
 
 def moe_router_pack(w_router, packed=None, stream=None):
-    """bf16 [E, 3H] split of the fp32 router weight [H, E] for moe_router_logits_packed."""
+    """bf16 [3E, H] three-part split of the fp32 router weight [H, E] (blocks of 16 experts,
+    each block hi, mid, lo rows) for moe_router_logits_packed."""
     H, E = w_router.shape
     if packed is None:
-        packed = torch.empty((E, 3 * H), dtype=torch.bfloat16, device=w_router.device)
+        packed = torch.empty((3 * E, H), dtype=torch.bfloat16, device=w_router.device)
     _check(lib().moe_router_pack(_ptr(w_router), H, E, _ptr(packed), _stream(stream)),
            "moe_router_pack")
     return packed
@@ -206,7 +207,7 @@ def moe_router_pack(w_router, packed=None, stream=None):
 
 def moe_router_logits_packed(x, packed, logits, stream=None):
     T, H = x.shape
-    E = packed.shape[0]
+    E = packed.shape[0] // 3
     _check(lib().moe_router_logits_packed(_ptr(x), _ptr(packed), T, H, E, _ptr(logits),
                                           _stream(stream)), "moe_router_logits_packed")
 

@@ -464,6 +464,7 @@ cudaError_t launch_combine(const float* yd, const int* slot_row, int T, int k, i
 __global__ void requant_kernel(const float* __restrict__ h32, int R, int T_sh, int I, int Is,
                                int Imax, __half* __restrict__ hq, float* __restrict__ sh,
                                int* __restrict__ sq_max) {
+  constexpr int kRegV = 8;  // float4 per lane held in registers: rows up to 1024 values
   __shared__ int s_sq[32];
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -471,30 +472,59 @@ __global__ void requant_kernel(const float* __restrict__ h32, int R, int T_sh, i
   if (row < R) {
     const int n = row < T_sh ? Is : I;
     const float* h = h32 + (size_t)row * Imax;
-    float amax = 0.0f;
-    for (int i = lane * 4; i < n; i += 128) {
-      const float4 v = *reinterpret_cast<const float4*>(h + i);
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-    }
-    amax = warp_max(amax);
-    const float s = __fdiv_rn(amax, 127.0f);
     __half* q = hq + (size_t)row * Imax;
-    for (int i = lane * 4; i < n; i += 128) {
-      const float4 v = *reinterpret_cast<const float4*>(h + i);
-      int c[4] = {0, 0, 0, 0};
-      if (s > 0.0f) {
-        c[0] = quant_code(v.x, s);
-        c[1] = quant_code(v.y, s);
-        c[2] = quant_code(v.z, s);
-        c[3] = quant_code(v.w, s);
+    if (n <= 128 * kRegV) {
+      float4 v[kRegV];
+#pragma unroll
+      for (int j = 0; j < kRegV; ++j)
+        v[j] = lane * 4 + j * 128 < n ? *reinterpret_cast<const float4*>(h + lane * 4 + j * 128)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      float amax = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kRegV; ++j)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+      amax = warp_max(amax);
+      const float s = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+      for (int j = 0; j < kRegV; ++j) {
+        const int i = lane * 4 + j * 128;
+        if (i >= n) break;
+        int c[4] = {0, 0, 0, 0};
+        if (s > 0.0f) {
+          c[0] = quant_code(v[j].x, s);
+          c[1] = quant_code(v[j].y, s);
+          c[2] = quant_code(v[j].z, s);
+          c[3] = quant_code(v[j].w, s);
+        }
+        sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
+        *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));
+        *reinterpret_cast<__half2*>(q + i + 2) = __halves2half2(__int2half_rn(c[2]), __int2half_rn(c[3]));
       }
-      sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
-      *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));
-      *reinterpret_cast<__half2*>(q + i + 2) =
-          __halves2half2(__int2half_rn(c[2]), __int2half_rn(c[3]));
+      if (lane == 0) sh[row] = s;
+    } else {
+      float amax = 0.0f;
+      for (int i = lane * 4; i < n; i += 128) {
+        const float4 v = *reinterpret_cast<const float4*>(h + i);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+      }
+      amax = warp_max(amax);
+      const float s = __fdiv_rn(amax, 127.0f);
+      for (int i = lane * 4; i < n; i += 128) {
+        const float4 v = *reinterpret_cast<const float4*>(h + i);
+        int c[4] = {0, 0, 0, 0};
+        if (s > 0.0f) {
+          c[0] = quant_code(v.x, s);
+          c[1] = quant_code(v.y, s);
+          c[2] = quant_code(v.z, s);
+          c[3] = quant_code(v.w, s);
+        }
+        sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
+        *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));
+        *reinterpret_cast<__half2*>(q + i + 2) = __halves2half2(__int2half_rn(c[2]), __int2half_rn(c[3]));
+      }
+      if (lane == 0) sh[row] = s;
     }
     sq = warp_sum_i(sq);
-    if (lane == 0) sh[row] = s;
   }
   if (lane == 0) s_sq[threadIdx.x / 32] = sq;
   __syncthreads();

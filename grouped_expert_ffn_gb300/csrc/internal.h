@@ -17,6 +17,7 @@ constexpr int kBK = 64;         // K elements per pipeline stage (128 bytes of f
 constexpr int kChunkK = 1024;   // K elements summed in one fp32 TMEM accumulator
 constexpr int kTokPerBlk = 64;  // tokens per histogram block (one 64-bit mask per expert)
 constexpr int kDecodeMaxRows = 8;
+constexpr int kREB = 16;  // experts per router tensor-core tile (packed router weight block)
 
 // One unit of grouped-GEMM work: token rows [row0, row0 + rows) of group `group` (expert id,
 // or E for the shared expert) against weight rows [m0, m0 + 128).

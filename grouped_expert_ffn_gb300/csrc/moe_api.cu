@@ -663,23 +663,23 @@ moe_status moe_router_logits(const uint16_t* x, const float* w_router, int T, in
 }
 
 moe_status moe_router_pack(const float* w_router, int H, int E, uint16_t* packed, void* stream) {
-  if (!w_router || !packed || H < 64 || E < 64 || H % 64 || E % 64) return MOE_ERR_INVALID_ARG;
+  if (!w_router || !packed || H < 64 || E < kREB || H % 64 || E % kREB) return MOE_ERR_INVALID_ARG;
   if (!aligned16(w_router) || !aligned16(packed)) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_router_pack(w_router, H, E, packed, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_router_logits_packed(const uint16_t* x, const uint16_t* packed, int T, int H, int E,
                                     float* logits, void* stream) {
-  if (!x || !packed || !logits || T < 1 || H < 64 || E < 64 || H % 64 || E % 64)
+  if (!x || !packed || !logits || T < 1 || H < 64 || E < kREB || H % 64 || E % kREB)
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(packed) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
   CUtensorMap ta, tb;
   const uint64_t da[2] = {(uint64_t)H, (uint64_t)T};
   const uint64_t sa[1] = {(uint64_t)H * 2};
-  const uint64_t db[2] = {(uint64_t)3 * H, (uint64_t)E};
-  const uint64_t sb[1] = {(uint64_t)3 * H * 2};
+  const uint64_t db[2] = {(uint64_t)H, (uint64_t)3 * E};
+  const uint64_t sb[1] = {(uint64_t)H * 2};
   if (!encode_2byte(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 2, da, sa, kBM) ||
-      !encode_2byte(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, packed, 2, db, sb, 64))
+      !encode_2byte(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, packed, 2, db, sb, 3 * kREB))
     return MOE_ERR_CUDA;
   return cuda_status(launch_router_tc(T, H, E, logits, ta, tb, static_cast<cudaStream_t>(stream)));
 }

@@ -37,51 +37,64 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
   }
   float sel_v[8];
   int sel_e[8];
-#pragma unroll 1
-  for (int j = 0; j < k; ++j) {
-    // lane-local best among untaken: highest value, then lowest id
-    float bv = 0.0f;
-    int be = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < kMaxEPerLane; ++i) {
-      const int e = i * 32 + lane;
-      if (!taken[i] && (be == 0x7fffffff || v[i] > bv)) {
-        bv = v[i];
-        be = e;
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      // lane-local best among untaken: highest value, then lowest id
+      float bv = 0.0f;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kMaxEPerLane; ++i) {
+        const int e = i * 32 + lane;
+        if (!taken[i] && (be == 0x7fffffff || v[i] > bv)) {
+          bv = v[i];
+          be = e;
+        }
       }
-    }
-    // warp argmax on (value desc, id asc); lanes with nothing left carry id = INT_MAX
+      // warp argmax on (value desc, id asc); lanes with nothing left carry id = INT_MAX
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      const bool better = (oe != 0x7fffffff) &&
-                          (be == 0x7fffffff || ov > bv || (ov == bv && oe < be));
-      if (better) {
-        bv = ov;
-        be = oe;
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        const bool better = (oe != 0x7fffffff) &&
+                            (be == 0x7fffffff || ov > bv || (ov == bv && oe < be));
+        if (better) {
+          bv = ov;
+          be = oe;
+        }
       }
-    }
-    sel_v[j] = bv;
-    sel_e[j] = be;
-    if ((be & 31) == lane) {
+      sel_v[j] = bv;
+      sel_e[j] = be;
+      if ((be & 31) == lane) {
 #pragma unroll
-      for (int i = 0; i < kMaxEPerLane; ++i)
-        if (i == (be >> 5)) taken[i] = true;
+        for (int i = 0; i < kMaxEPerLane; ++i)
+          if (i == (be >> 5)) taken[i] = true;
+      }
+    } else {
+      sel_v[j] = 0.0f;
+      sel_e[j] = 0;
     }
   }
-  if (lane == 0) {
-    const float m = sel_v[0];
-    float ex[8];
-    float z = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      ex[j] = expf(sel_v[j] - m);
-      z += ex[j];
+  // softmax over the selected logits: lane j < k handles slot j
+  const float m = sel_v[0];
+  float ex = 0.0f;
+  int my_e = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (lane == j && j < k) {
+      ex = expf(sel_v[j] - m);
+      my_e = sel_e[j];
     }
-    for (int j = 0; j < k; ++j) {
-      idx[(size_t)t * k + j] = sel_e[j];
-      w[(size_t)t * k + j] = ex[j] / z;
-    }
+  float z = 0.0f;
+  // sum in slot order (j = 0..k-1), identical for every lane
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float ej = __shfl_sync(0xffffffffu, ex, j);
+    if (j < k) z += ej;
+  }
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_e;
+    w[(size_t)t * k + lane] = ex / z;
   }
 }
 
@@ -119,15 +132,46 @@ __global__ void hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E
   }
 }
 
+// Exclusive scan over up to blockDim.x (<= 1024) values, one per thread; returns the
+// exclusive prefix and writes the total to *total. Every thread of the block must call it.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int wv = lane < nw ? s_warp[lane] : 0;
+    int winc = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += n;
+    }
+    if (lane < nw) s_warp[lane] = winc - wv;
+    if (lane == 31) s_warp[32] = winc;
+  }
+  __syncthreads();
+  const int r = s_warp[warp] + inc - v;
+  *total = s_warp[32];
+  __syncthreads();
+  return r;
+}
+
 // One block of 1024 threads. Turns bhist into exclusive per-expert prefixes over blocks,
 // writes counts/offsets and the two work lists (gate/up and down): per group, every
 // (128-row weight tile, token tile of at most TN rows) pair, ordered by group, then weight
 // tile, then token tile, so consecutive items of a large group reuse one weight tile from L2.
 __global__ void scan_kernel(PrepArgs a, int nblk) {
   __shared__ int s_cnt[257];
-  __shared__ int s_off[258];
+  __shared__ int s_off[257];
   __shared__ int s_base_gu[258];
   __shared__ int s_base_d[258];
+  __shared__ int s_warp[33];
   const int E = a.E;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
   // exclusive prefix over blocks of each expert's histogram (row e of [E][nblk]), warp per
@@ -161,52 +205,61 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
     }
   }
   __syncthreads();
+  // row offsets of the experts, and item bases of the groups (group g: shared when
+  // g < has_shared, else expert g - has_shared)
   const int T_sh = a.has_shared ? a.T : 0;
   const int ng = E + (a.has_shared ? 1 : 0);
+  int total;
+  const int ecnt = (int)threadIdx.x < E ? s_cnt[threadIdx.x] : 0;
+  const int eoff = block_exclusive_scan(ecnt, s_warp, &total);
+  if ((int)threadIdx.x < E) {
+    s_off[threadIdx.x] = eoff;
+    a.offsets[threadIdx.x] = eoff;
+  }
+  if (threadIdx.x == 0) a.offsets[E] = total;
+  const int g = threadIdx.x;
+  int ngu = 0, nd = 0;
+  if (g < ng) {
+    const bool sh = a.has_shared && g == 0;
+    const int cnt = sh ? a.T : s_cnt[g - a.has_shared];
+    ngu = (2 * (sh ? a.Is : a.I)) / kBM * ((cnt + a.tn_gu - 1) / a.tn_gu);
+    nd = a.H / kBM * ((cnt + a.tn_d - 1) / a.tn_d);
+  }
+  const int bgu = block_exclusive_scan(ngu, s_warp, &total);
+  if (g < ng) s_base_gu[g] = bgu;
   if (threadIdx.x == 0) {
-    int off = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = off;
-      a.offsets[e] = off;
-      off += s_cnt[e];
-    }
-    s_off[E] = off;
-    a.offsets[E] = off;
-    // group g: g < has_shared -> shared; else expert g - has_shared
-    int bg = 0, bd = 0;
-    for (int g = 0; g < ng; ++g) {
-      const bool sh = a.has_shared && g == 0;
-      const int cnt = sh ? a.T : s_cnt[g - a.has_shared];
-      const int wtg = (2 * (sh ? a.Is : a.I)) / kBM;  // gate/up weight tiles
-      const int wtd = a.H / kBM;                       // down weight tiles
-      s_base_gu[g] = bg;
-      s_base_d[g] = bd;
-      bg += wtg * ((cnt + a.tn_gu - 1) / a.tn_gu);
-      bd += wtd * ((cnt + a.tn_d - 1) / a.tn_d);
-    }
-    s_base_gu[ng] = bg;
-    s_base_d[ng] = bd;
-    a.n_items[0] = bg;
-    a.n_items[1] = bd;
+    s_base_gu[ng] = total;
+    a.n_items[0] = total;
+  }
+  const int bd = block_exclusive_scan(nd, s_warp, &total);
+  if (g < ng) s_base_d[g] = bd;
+  if (threadIdx.x == 0) {
+    s_base_d[ng] = total;
+    a.n_items[1] = total;
   }
   __syncthreads();
-  for (int g = threadIdx.x; g < ng; g += blockDim.x) {
-    const bool sh = a.has_shared && g == 0;
-    const int gid = sh ? E : g - a.has_shared;
-    const int cnt = sh ? a.T : s_cnt[gid];
-    const int row0 = sh ? 0 : T_sh + s_off[gid];
-    const int wtg = (2 * (sh ? a.Is : a.I)) / kBM;
-    const int wtd = a.H / kBM;
-    const int ttg = (cnt + a.tn_gu - 1) / a.tn_gu;
-    const int ttd = (cnt + a.tn_d - 1) / a.tn_d;
-    int p = s_base_gu[g];
-    for (int w = 0; w < wtg; ++w)
-      for (int t = 0; t < ttg; ++t)
-        a.items_gu[p++] = make_int4(gid, row0 + t * a.tn_gu, min(a.tn_gu, cnt - t * a.tn_gu), w * kBM);
-    p = s_base_d[g];
-    for (int w = 0; w < wtd; ++w)
-      for (int t = 0; t < ttd; ++t)
-        a.items_d[p++] = make_int4(gid, row0 + t * a.tn_d, min(a.tn_d, cnt - t * a.tn_d), w * kBM);
+  // items, one per thread and pass: find the group by binary search over the bases
+  for (int list = 0; list < 2; ++list) {
+    const int* base = list == 0 ? s_base_gu : s_base_d;
+    const int n = base[ng];
+    const int tn = list == 0 ? a.tn_gu : a.tn_d;
+    int4* items = list == 0 ? a.items_gu : a.items_d;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      int lo = 0, hi = ng - 1;  // last group with base <= i
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (base[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      const int gg = lo;
+      const bool sh = a.has_shared && gg == 0;
+      const int gid = sh ? E : gg - a.has_shared;
+      const int cnt = sh ? a.T : s_cnt[gid];
+      const int row0 = sh ? 0 : T_sh + s_off[gid];
+      const int tt = (cnt + tn - 1) / tn;
+      const int local = i - base[gg];
+      const int wt = local / tt, t = local % tt;
+      items[i] = make_int4(gid, row0 + t * tn, min(tn, cnt - t * tn), wt * kBM);
+    }
   }
 }
 

@@ -2,30 +2,37 @@
 //
 // logits[T, E] = x[T, H] (bf16) @ W[H, E] (fp32). The fp32 weight splits exactly enough into
 // three bf16 parts, W = hi + mid + lo (hi = bf16(W), mid = bf16(W - hi), lo = bf16(W - hi -
-// mid); the residual after lo is below 2^-26 |W|), so the product is one bf16 GEMM with the
-// reduction dimension tripled: [x | x | x] @ [hi; mid; lo]. Every bf16 x bf16 product is exact
-// and the tensor core accumulates in fp32, so the result has the accuracy of an fp32 dot
-// product. One CTA per 128-row x 64-expert tile; warp 4 feeds A (x, re-read for each part)
-// and B (packed [E, 3H] bf16) by TMA into an 8-stage ring, warp 5 issues tcgen05.mma
-// (kind::f16, bf16 inputs), warps 0-3 drain TMEM and store fp32 rows.
+// mid); the residual after lo is below 2^-26 |W|). Every bf16 x bf16 product is exact and the
+// tensor core accumulates in fp32, so x @ hi, x @ mid and x @ lo each carry the error of an
+// fp32 dot product, and their sum (hi + mid) + lo that of the fp32 projection.
+//
+// Packed weight layout: blocks of kREB experts, each block three parts of kREB rows of H bf16
+// ([E / kREB][3][kREB][H]), so one B tile of 3 * kREB rows holds all three parts of kREB
+// experts and the reduction runs over H once. One CTA per 128-row x kREB-expert tile (two per
+// SM); warp 4 feeds A (x) and B by TMA into a 4-stage ring, warp 5 issues tcgen05.mma
+// (kind::f16, bf16 inputs, N = 3 * kREB), warps 0-3 drain TMEM, add the three parts per
+// expert and store fp32 rows.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 
-constexpr int kRBN = 64;
-constexpr int kRStages = 8;
+constexpr int kRBN = 3 * kREB;  // MMA N: three parts of kREB experts
+constexpr int kRStages = 4;
 constexpr int kRA = kBM * kBK * 2;
 constexpr int kRB = kRBN * kBK * 2;
 constexpr int kRStage = kRA + kRB;
 constexpr int kRSmem = kRStages * kRStage + 256 + 1024;
+constexpr int kRTmemCols = 64;  // power of two >= kRBN
+static_assert(kRBN <= kRTmemCols && kRBN % 16 == 0, "router tile");
+static_assert(kRStage % 1024 == 0, "stages stay 1024-byte aligned for 128-byte swizzle");
 
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     router_tc_kernel(int T, int H, int E, float* __restrict__ out,
                      const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
   extern __shared__ uint8_t smem_raw[];
@@ -38,8 +45,8 @@ __global__ void __launch_bounds__(192, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kRBN;
-  const int nkb = 3 * H / kBK;
+  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kRBN, e0 = blockIdx.y * kREB;
+  const int nkb = H / kBK;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRStages; ++s) {
       mbar_init(&full[s], 1);
@@ -51,7 +58,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
   }
   if (warp == 5) {
-    tmem_alloc(tmem_slot, kRBN);
+    tmem_alloc(tmem_slot, kRTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -70,7 +77,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         mbar_arrive_expect_tx(&full[stage], kRStage);
         uint8_t* sa = smem + stage * kRStage;
-        tma_load_2d(sa, &tmA, &full[stage], (kb * kBK) % H, m0);
+        tma_load_2d(sa, &tmA, &full[stage], kb * kBK, m0);
         tma_load_2d(sa + kRA, &tmB, &full[stage], kb * kBK, n0);
         armed |= 1u << stage;
         armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -123,17 +130,23 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const int row = m0 + threadIdx.x;
       const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16);
+      static_assert(kREB == 16, "one 16-column TMEM load per part");
+      uint32_t r[3][16];
 #pragma unroll
-      for (int c = 0; c < kRBN; c += 16) {
-        uint32_t r[16];
-        tmem_ld16(tb + c, r);
-        tmem_ld_wait();
-        if (row < T) {
-          float4* dst = reinterpret_cast<float4*>(out + (size_t)row * E + n0 + c);
+      for (int p = 0; p < 3; ++p) tmem_ld16(tb + p * kREB, r[p]);
+      tmem_ld_wait();
+      if (row < T) {
+        float4* dst = reinterpret_cast<float4*>(out + (size_t)row * E + e0);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        for (int q = 0; q < kREB / 4; ++q) {
+          float v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = 4 * q + j;
+            v[j] = __fadd_rn(__fadd_rn(__uint_as_float(r[0][c]), __uint_as_float(r[1][c])),
+                             __uint_as_float(r[2][c]));
+          }
+          dst[q] = make_float4(v[0], v[1], v[2], v[3]);
         }
       }
     }
@@ -142,7 +155,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, kRBN);
+    tmem_dealloc(tmem, kRTmemCols);
   }
 }
 
@@ -151,7 +164,8 @@ __device__ __forceinline__ uint16_t bf16_rn_bits(float f) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 
-// packed[e, p*H + h] = part p of w[h, e] (p = 0 hi, 1 mid, 2 lo)
+// packed row ((e / kREB) * 3 + p) * kREB + e % kREB, column h = part p of w[h, e]
+// (p = 0 hi, 1 mid, 2 lo)
 __global__ void router_pack_kernel(const float* __restrict__ w, int H, int E,
                                    uint16_t* __restrict__ packed) {
   const size_t n = (size_t)H * E;
@@ -164,10 +178,10 @@ __global__ void router_pack_kernel(const float* __restrict__ w, int H, int E,
     const uint16_t mid = bf16_rn_bits(r1);
     const float r2 = __fsub_rn(r1, bf16_bits_to_float(mid));
     const uint16_t lo = bf16_rn_bits(r2);
-    uint16_t* row = packed + (size_t)e * 3 * H;
-    row[h] = hi;
-    row[H + h] = mid;
-    row[2 * H + h] = lo;
+    const size_t r0 = (size_t)(e / kREB) * 3 * kREB + e % kREB;
+    packed[r0 * H + h] = hi;
+    packed[(r0 + kREB) * H + h] = mid;
+    packed[(r0 + 2 * kREB) * H + h] = lo;
   }
 }
 
@@ -181,7 +195,7 @@ cudaError_t launch_router_tc(int T, int H, int E, float* out, const CUtensorMap&
   cudaError_t e = cudaFuncSetAttribute(router_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((T + kBM - 1) / kBM, E / kRBN);
+  const dim3 grid((T + kBM - 1) / kBM, E / kREB);
   router_tc_kernel<<<grid, 192, kRSmem, s>>>(T, H, E, out, tmA, tmB);
   return cudaGetLastError();
 }

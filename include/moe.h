@@ -173,10 +173,12 @@ MOE_API moe_status moe_rmsnorm_residual(uint16_t* x, const float* y, uint16_t* x
                                         void* stream);
 /* Router projection on the tensor cores. moe_router_pack splits w_router fp32 [H, E] into
  * three bf16 parts hi + mid + lo (exact to 2^-26 relative) and stores them as packed bf16
- * [E, 3H] (caller-allocated, 6*H*E bytes; a one-time step per router weight).
- * moe_router_logits_packed computes logits fp32 [T, E] = float(x bf16 [T, H]) @ W as one bf16
- * GEMM over the tripled reduction dimension (exact products, fp32 accumulation). H and E
- * multiples of 64. Encodes two TMA descriptors on the host per call. */
+ * [3E, H] (caller-allocated, 6*H*E bytes; a one-time step per router weight): blocks of 16
+ * experts, each block the hi rows, then the mid rows, then the lo rows of its experts.
+ * moe_router_logits_packed computes logits fp32 [T, E] = float(x bf16 [T, H]) @ W: per
+ * expert three bf16 dot products over H (exact products, fp32 accumulation), added as
+ * (hi + mid) + lo. H a multiple of 64, E a multiple of 16. Encodes two TMA descriptors on the
+ * host per call; MOE_ERR_INVALID_ARG on a bad size or an unaligned pointer. */
 MOE_API moe_status moe_router_pack(const float* w_router, int H, int E, uint16_t* packed,
                                    void* stream);
 MOE_API moe_status moe_router_logits_packed(const uint16_t* x, const uint16_t* packed, int T,
