@@ -80,6 +80,58 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Cluster-scope variants, for barriers that receive arrivals from the other CTA of a pair.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                             int* err) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cl(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      set_error(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+// Address of this CTA's shared-memory word `local` in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to another CTA's of the
+// cluster, completing that many transaction bytes on an mbarrier there (dst and bar from
+// mapa_shared). Asynchronous: the issuing thread does not wait for it.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void* src,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
 // ---- TMA ----------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -101,18 +153,26 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-// Bring a tensor tile into L2 ahead of its load (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(c0), "r"(c1)
-               : "memory");
+// The same 2D tile delivered to every CTA of the cluster in cta_mask, at this CTA's
+// shared-memory offsets of dst and bar (each destination's mbarrier gets the bytes it received).
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                               int c0, int c1, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%4, %5}], [%2], %3;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "h"(cta_mask), "r"(c0), "r"(c1)
+      : "memory");
 }
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; release/acquire orders shared-memory state
+// (mbarrier initialisation, last accesses) across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // ---- tcgen05 / TMEM -----------------------------------------------------------------
@@ -152,6 +212,104 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
       : "memory");
+}
+
+// Arrive once on `bar` at this shared-memory offset in every CTA of cta_mask when every
+// tcgen05 op issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// ---- the CTA pair of the 2-SM MMA (cta_group::2): every tcgen05 op of a kernel that uses
+// the pair form uses it throughout.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// D (+)= A * B^T over the pair: M = 256 rows, A rows 0-127 and B rows (columns of D)
+// [0, N/2) from the issuing CTA's shared memory, A rows 128-255 and B rows [N/2, N) from the
+// peer's at the same offsets; D rows 0-127 in the issuer's TMEM, 128-255 in the peer's.
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// The four MMAs of one k-block (K = 64: descriptors advance 32 bytes per K = 16 step), one
+// commit of them to `commit_bar`, and a non-blocking probe of phase `next_parity` of
+// `next_bar` (the barrier the issuing thread waits on for the next k-block), in one block:
+// the probe's shared-memory round trip overlaps the MMA issue instead of sitting between
+// two k-blocks with the tensor pipe idle. `accumulate` applies to the first MMA (the rest
+// accumulate). Returns whether the next k-block's operands are ready. PAIR selects the 2-SM
+// form (cta_group::2, commit multicast to both CTAs of the pair, cluster-scope probe).
+template <bool PAIR>
+__device__ __forceinline__ uint32_t mma_kblock_commit_probe(uint32_t d_tmem, uint64_t adesc,
+                                                            uint64_t bdesc, uint32_t idesc,
+                                                            uint32_t accumulate,
+                                                            uint32_t commit_bar,
+                                                            uint32_t next_bar,
+                                                            uint32_t next_parity) {
+  uint32_t ready;
+  if (PAIR) {
+    asm volatile(
+        "{\n\t.reg .pred pa, pt, pn;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 pn, [%7], %8;\n\t"
+        "setp.ne.b32 pa, %5, 0;\n\t"
+        "setp.eq.b32 pt, 1, 1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %4, pa;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], %9, %10, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], %11, %12, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], %13, %14, %4, pt;\n\t"
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%6], %15;\n\t"
+        "selp.u32 %0, 1, 0, pn;\n\t}\n"
+        : "=r"(ready)
+        : "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(commit_bar),
+          "r"(next_bar), "r"(next_parity), "l"(adesc + 2), "l"(bdesc + 2), "l"(adesc + 4),
+          "l"(bdesc + 4), "l"(adesc + 6), "l"(bdesc + 6), "h"((uint16_t)0x3)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred pa, pt, pn;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 pn, [%7], %8;\n\t"
+        "setp.ne.b32 pa, %5, 0;\n\t"
+        "setp.eq.b32 pt, 1, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pa;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], %9, %10, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], %11, %12, %4, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%1], %13, %14, %4, pt;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+        "selp.u32 %0, 1, 0, pn;\n\t}\n"
+        : "=r"(ready)
+        : "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(commit_bar),
+          "r"(next_bar), "r"(next_parity), "l"(adesc + 2), "l"(bdesc + 2), "l"(adesc + 4),
+          "l"(bdesc + 4), "l"(adesc + 6), "l"(bdesc + 6)
+        : "memory");
+  }
+  return ready;
 }
 
 // 32 lanes x 16 consecutive 32-bit columns; thread i of the warp gets lane (base lane + i).

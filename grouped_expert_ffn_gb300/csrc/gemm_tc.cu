@@ -38,168 +38,73 @@
 // same two words). With one accumulator per tile, TMEM holds two of them (2 x TN columns)
 // so the epilogue of one tile overlaps the MMAs of the next.
 //
-// Warp roles (448 threads, one CTA per SM):
+// Clusters: the token tile of an item is the same for all of an expert's weight tiles, so CS
+// CTAs (CS = 1, 2 or 4, chosen per launch from the weight-tile counts) share it: each loads a
+// share of its 64-row boxes once and multicasts it to the cluster, which divides the token
+// operand's L2-to-SM traffic by CS.
+//
+// Warp roles (672 threads, one CTA per SM):
 //   warps 0-7   epilogue: warp w reads TMEM lanes 32*(w%4).. (weight rows) and every other
 //               16-column chunk (tokens) starting at chunk w/4;
-//   warps 8-11  converters: thread r widens weight row r of each k-block;
-//   warp 12     TMA producer: int8 weight tile and fp16 token tile;
-//   warp 13     MMA issuer and TMEM owner.
-// Pipeline: 4 load stages (int8 weights + fp16 tokens, released by the MMA's commit) and 2
-// fp16 weight buffers (released by the MMA's commit). Every mbarrier wait is bounded; a wait
+//   warps 8-15  converters, two groups of four taking alternate k-blocks: thread r of a group
+//               widens weight row r;
+//   warp 16     MMA issuer and TMEM owner;
+//   warps 17-18 TMA producers of the int8 weight tiles (alternate stages);
+//   warps 19-20 TMA producers of the fp16 token tiles (alternate stages).
+// Pipeline: the weights stream from HBM through a ring of small int8 stages (4 x 8 KB,
+// released by the converters as soon as they have widened a stage); the token tiles, mostly
+// L2 hits, through a ring of large stages (4 x 32 KB), one TMA load per stage (box heights
+// 32..256 rows); one fp16 weight buffer per token stage, released together with it by the
+// MMA's commit. A TMA-issuing thread completes only a few loads per microsecond, so each ring
+// has two issuing threads and each token tile is one load rather than several 64-row ones.
+// Barrier arrivals are one per warp (after __syncwarp) and the MMA thread commits once per
+// k-block: every arrival and commit sits on the critical path of a k-block.
+// Every mbarrier wait is bounded; a wait
 // that runs out sets the plan's error word and the CTA drains its own copies and MMAs, frees
 // TMEM and returns.
 //
 // The down epilogue writes w * dequant(acc) per (row, channel) to yd; combine_kernel sums each
 // token's k routed rows and its shared-expert row in slot order (deterministic, no atomics).
-#include "common.cuh"
-#include "internal.h"
+#include "gemm_common.cuh"
 
 namespace moe {
 
-#ifndef MOE_LOAD_STAGES
-#define MOE_LOAD_STAGES 4
+#ifndef MOE_W_STAGES
+#define MOE_W_STAGES 4
 #endif
-constexpr int kTokBox = kTokenBox;                   // token rows per TMA box
+#ifndef MOE_X_STAGES
+#define MOE_X_STAGES 4
+#endif
 constexpr int kXBytesMax = kMaxTokTile * kBK * 2;    // fp16 token tile per stage (<= 32 KB)
-constexpr int kW8Bytes = kBM * kBK;                  // int8 weight tile per stage (8 KB)
-constexpr int kLoadStage = kXBytesMax + kW8Bytes;    // 40 KB
-constexpr int kLoadStages = MOE_LOAD_STAGES;
-constexpr int kW16Bytes = kBM * kBK * 2;             // fp16 weight tile (16 KB)
-constexpr int kConvBufs = 2;
-constexpr int kEpiWarps = 8;
-constexpr int kConvWarps = 4;
-constexpr int kOffConv = kLoadStages * kLoadStage;
+constexpr int kXStages = MOE_X_STAGES;
+constexpr int kWStages = MOE_W_STAGES;
+constexpr int kConvBufs = kXStages;  // fp16 weight buffer s goes with token stage s
+constexpr int kOffW8 = kXStages * kXBytesMax;
+constexpr int kOffConv = kOffW8 + kWStages * kW8Bytes;
 constexpr int kOffBar = kOffConv + kConvBufs * kW16Bytes;
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 512;
 constexpr int kGemmSmem = kOffBar + kBarBytes + 1024;
-static_assert((2 * kLoadStages + 2 * kConvBufs + 5) * 8 + 8 <= kBarBytes, "barrier area");
+static_assert((2 * kXStages + 2 * kWStages + kConvBufs + 5) * 8 + 8 <= kBarBytes, "barriers");
 static_assert(kGemmSmem <= 232448, "shared memory");
+static_assert(kOffW8 % 1024 == 0 && kOffConv % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
+static_assert(kXStages % 2 == 0 && kWStages % 2 == 0, "two producers per ring own alternate stages");
 
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kConvThreads = kConvWarps * 32;        // one thread per weight row
-constexpr int kConvWarp0 = kEpiWarps;
-constexpr int kProducerWarp = kEpiWarps + kConvWarps;
-constexpr int kMmaWarp = kProducerWarp + 1;
-constexpr int kGemmThreads = (kMmaWarp + 1) * 32;
-constexpr uint32_t kTmemCols = 512;
 
-// Whether one fp32 accumulator over the whole K is provably exact for this launch.
-__device__ __forceinline__ bool single_accumulator_exact(const GemmArgs& a) {
-  const unsigned long long r = (unsigned long long)(unsigned)*a.row_sq_max;
-  const unsigned long long w = (unsigned long long)(unsigned)*a.w_sq_max;
-  return r * w < (1ull << 48);
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// 4 int8 (one word) -> 4 fp16, exactly: bytes v+128 placed under the fp16 exponent of 1024,
-// then 1152 subtracted.
-__device__ __forceinline__ uint2 widen4(uint32_t w) {
-  const uint32_t u = w ^ 0x80808080u;
-  const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
-  const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-  const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), bias);
-  const __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), bias);
-  return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
-}
-
-// Gate/up epilogue. Lane pair (2i, 2i+1) of quadrant q holds gate and up of channel
-// m0/2 + 16q + i for every token column; the even lane finishes columns 0-7 of each 16-column
-// chunk and the odd lane columns 8-15.
-__device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
-                                                 uint32_t tbase, int half) {
-  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
-  const bool odd = lane & 1;
-  const bool shared = wi.x == a.E;
-  const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
-  const float sgc = (shared ? a.sh_s_g : a.s_g + (size_t)wi.x * a.I)[ch];
-  const float suc = (shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I)[ch];
-  const int ncols = wi.z;
-#pragma unroll 1
-  for (int c0 = half * 16; c0 < ncols; c0 += 32) {
-    int v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0;
-#pragma unroll 1
-    for (int kc = 0; kc < nch; ++kc) {
-      uint32_t r[16];
-      tmem_ld16(tbase + kc * a.TN + c0, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] += __float2int_rn(__uint_as_float(r[i]));
-    }
-    int recv[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) recv[i] = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[8 + i], 1);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int col = c0 + (odd ? 8 : 0) + i;
-      if (col < ncols) {
-        const int g = odd ? recv[i] : v[i];
-        const int u = odd ? v[8 + i] : recv[i];
-        const int row = wi.y + col;
-        const float sx = a.sx[row];
-        a.h32[(size_t)row * a.Imax + ch] = silu_mul(dequant(g, sx, sgc), dequant(u, sx, suc));
-        if (a.tap) {
-          a.tap[(size_t)row * 2 * a.Imax + ch] = g;
-          a.tap[(size_t)row * 2 * a.Imax + a.Imax + ch] = u;
-        }
-      }
-    }
-  }
-}
-
-// Down epilogue: lane = output channel m0 + 32q + lane; for each token column the warp stores
-// w * dequant(acc) for 32 consecutive channels of that row of yd (one 128-byte store). The
-// combine kernel then sums each token's rows in slot order.
-__device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase,
-                                              int half) {
-  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
-  const bool shared = wi.x == a.E;
-  const int o = wi.w + q * 32 + lane;
-  const float sdo = (shared ? a.sh_s_d : a.s_d + (size_t)wi.x * a.H)[o];
-  const int ncols = wi.z;
-#pragma unroll 1
-  for (int c0 = half * 16; c0 < ncols; c0 += 32) {
-    int v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0;
-#pragma unroll 1
-    for (int kc = 0; kc < nch; ++kc) {
-      uint32_t r[16];
-      tmem_ld16(tbase + kc * a.TN + c0, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] += __float2int_rn(__uint_as_float(r[i]));
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int col = c0 + i;
-      if (col < ncols) {
-        const int row = wi.y + col;
-        a.yd[(size_t)row * a.H + o] = __fmul_rn(a.row_w[row], dequant(v[i], a.s_h[row], sdo));
-        if (a.tap) a.tap[(size_t)row * a.H + o] = v[i];
-      }
-    }
-  }
-}
 
 template <bool GU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tmX,
+    grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ XMaps tmX,
                         const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmWs) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* empty = full + kLoadStages;
-  uint64_t* cfull = empty + kLoadStages;   // [kConvBufs]
-  uint64_t* cempty = cfull + kConvBufs;    // [kConvBufs]
-  uint64_t* acc_full = cempty + kConvBufs; // [2]
+  uint64_t* xfull = reinterpret_cast<uint64_t*>(smem + kOffBar);  // [kXStages]
+  uint64_t* xempty = xfull + kXStages;     // [kXStages]
+  uint64_t* wfull = xempty + kXStages;     // [kWStages]
+  uint64_t* wempty = wfull + kWStages;     // [kWStages]
+  uint64_t* cfull = wempty + kWStages;     // [kConvBufs]
+  uint64_t* acc_full = cfull + kConvBufs;  // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -207,17 +112,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kLoadStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kXStages; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], 1);
     }
-    for (int s = 0; s < kConvBufs; ++s) {
-      mbar_init(&cfull[s], kConvThreads);
-      mbar_init(&cempty[s], 1);
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], kConvWarps);
     }
+    for (int s = 0; s < kConvBufs; ++s) mbar_init(&cfull[s], kConvWarps);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], kEpiThreads);
+      mbar_init(&acc_empty[s], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -227,11 +133,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmX);
+  if (warp == kWProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmWs);
   }
+  if (warp == kXProducerWarp && lane < kXMaps) tma_prefetch_desc(&tmX.m[lane]);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -246,9 +152,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nslots = slot_cols <= (int)kTmemCols / 2 ? 2 : 1;
   const int kpc = single ? (1 << 30) : kChunkK / kBK;  // k-blocks per accumulator
 
-  if (warp == kProducerWarp) {
+  if (warp >= kWProducerWarp && warp < kXProducerWarp + 2) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ------- TMA producers: weights (HBM) and tokens, two threads per ring -------
+      // Producer pidx of a ring owns the ring's stages with index % 2 == pidx; both walk the
+      // whole item / k-block sequence to keep stage and phase in step.
+      const bool wprod = warp < kXProducerWarp;
+      const int pidx = warp - (wprod ? kWProducerWarp : kXProducerWarp);
+      const int nst = wprod ? kWStages : kXStages;
+      uint64_t* full = wprod ? wfull : xfull;
+      uint64_t* empty = wprod ? wempty : xempty;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;  // stages with a load issued, and its phase
@@ -257,25 +170,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int4 wi = a.items[item];
         const bool shared = wi.x == a.E;
         const int nkb = (shared ? a.K_s : a.K_r) / kBK;
-        const int nbox = (wi.z + kTokBox - 1) / kTokBox;
-        const uint32_t bytes = kW8Bytes + nbox * kTokBox * kBK * 2;
+        const int rows = (wi.z + kXStep1 - 1) / kXStep1 * kXStep1;  // box height
+        const uint32_t bytes = wprod ? (uint32_t)kW8Bytes : (uint32_t)(rows * kBK * 2);
+        const CUtensorMap* mx = &tmX.m[rows / kXStep1 - 1];
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.err)) {
-            ok = false;
-            break;
+          if ((stage & 1) == pidx) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            if (wprod) {
+              uint8_t* sw = smem + kOffW8 + stage * kW8Bytes;
+              if (shared)
+                tma_load_2d(sw, &tmWs, &full[stage], kb * kBK, wi.w);
+              else
+                tma_load_3d(sw, &tmW, &full[stage], kb * kBK, wi.w, wi.x);
+            } else {
+              tma_load_2d(smem + stage * kXBytesMax, mx, &full[stage], kb * kBK, wi.y);
+            }
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          uint8_t* sx = smem + stage * kLoadStage;
-          uint8_t* sw = sx + kXBytesMax;
-          if (shared)
-            tma_load_2d(sw, &tmWs, &full[stage], kb * kBK, wi.w);
-          else
-            tma_load_3d(sw, &tmW, &full[stage], kb * kBK, wi.w, wi.x);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(sx + b * kTokBox * kBK * 2, &tmX, &full[stage], kb * kBK, wi.y + b * kTokBox);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == kLoadStages) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1;
           }
@@ -283,7 +200,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) {
         // Let every copy this thread issued land before the CTA exits.
-        for (int s = 0; s < kLoadStages; ++s) {
+        for (int s = 0; s < nst; ++s) {
           if (!(armed >> s & 1)) continue;
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(&full[s], (armed_par >> s) & 1) &&
@@ -292,35 +209,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
+  } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvGroups * kConvWarps) {
     // ---------------- converters: int8 -> fp16 weight rows ----------------
-    const int r = threadIdx.x - kConvWarp0 * 32;  // weight row within the tile
-    const int sw8 = (r >> 1) & 3;                 // 64-byte swizzle of the int8 row
-    const int sw16 = r & 7;                       // 128-byte swizzle of the fp16 row
-    int stage = 0, cb = 0;
+    // Group g converts the k-blocks whose running index is g modulo kConvGroups, so the
+    // latency of one group's fence and arrivals overlaps the other groups' work. The fp16
+    // buffer of token stage cb is free once the MMAs of its previous use completed (the token
+    // stage's empty barrier).
+    const int cw = warp - kConvWarp0;
+    const int group = cw / kConvWarps;
+    const int r = (cw % kConvWarps) * 32 + lane;  // weight row within the tile
+    int stage = 0, cb = 0, gk = 0;
     uint32_t phase = 0, cphase = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       const int4 wi = a.items[item];
       const int nkb = (wi.x == a.E ? a.K_s : a.K_r) / kBK;
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, a.err) ||
-            !mbar_wait(&cempty[cb], cphase ^ 1, abort_flag, a.err)) {
+      for (int kb = 0; kb < nkb; ++kb, ++gk) {
+        if (gk % kConvGroups != group) {
+          if (++stage == kWStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (++cb == kConvBufs) {
+            cb = 0;
+            cphase ^= 1;
+          }
+          continue;
+        }
+        // warp-uniform outcome: the per-warp arrival below needs every lane. The token stage
+        // cb is waited for here too, so that cfull alone tells the MMA thread that both
+        // operands of the k-block are in shared memory.
+        const bool got = mbar_wait(&wfull[stage], phase, abort_flag, a.err) &&
+                         mbar_wait(&xempty[cb], cphase ^ 1, abort_flag, a.err) &&
+                         mbar_wait(&xfull[cb], cphase, abort_flag, a.err);
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        const uint8_t* src = smem + stage * kLoadStage + kXBytesMax + r * 64;
-        uint8_t* dst = smem + kOffConv + cb * kW16Bytes + r * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * (c ^ sw8));
-          const uint2 e0 = widen4(v.x), e1 = widen4(v.y), e2 = widen4(v.z), e3 = widen4(v.w);
-          *reinterpret_cast<uint4*>(dst + 16 * ((2 * c) ^ sw16)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
-          *reinterpret_cast<uint4*>(dst + 16 * ((2 * c + 1) ^ sw16)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
+        widen_row(smem + kOffW8 + stage * kW8Bytes, smem + kOffConv + cb * kW16Bytes, r);
+        fence_proxy_async_smem();  // this thread's fp16 stores, before the MMA reads them
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&cfull[cb]);
+          mbar_arrive(&wempty[stage]);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&cfull[cb]);
-        if (++stage == kLoadStages) {
+        if (++stage == kWStages) {
           stage = 0;
           phase ^= 1;
         }
@@ -333,8 +266,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      int stage = 0, cb = 0;
-      uint32_t phase = 0, cphase = 0;
+      // The issuing thread is on the tensor pipe's critical path: tcgen05.mma issue blocks
+      // once the pipe's queue is full, so every instruction between the last MMA of a k-block
+      // and the first of the next leaves the pipe idle. Per k-block it therefore waits on one
+      // barrier only (cfull: converted weights and token stage), and usually not even that:
+      // mma_kblock_commit_probe probes the next k-block's barrier while the current MMAs
+      // issue. Descriptors are a base plus a stage offset (the 14-bit start-address field
+      // does not carry).
+      const uint64_t dw0 = smem_desc_sw128(smem_u32(smem + kOffConv));
+      const uint64_t dx0 = smem_desc_sw128(smem_u32(smem));
+      int stage = 0;
+      uint32_t phase = 0, ready = 0;
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++it) {
@@ -346,30 +288,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t use = (uint32_t)(it / nslots) & 1u;
         if (!mbar_wait(&acc_empty[slot], use ^ 1, abort_flag, a.err)) break;
         tc_fence_after();
-        const uint32_t tslot = tmem + (uint32_t)(slot * slot_cols);
+        uint32_t dt = tmem + (uint32_t)(slot * slot_cols);
+        int kin = 0;  // k-block within the current accumulator chunk
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, a.err) ||
-              !mbar_wait(&cfull[cb], cphase, abort_flag, a.err)) {
+          if (!ready && !mbar_wait(&cfull[stage], phase, abort_flag, a.err)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint64_t dw = smem_desc_sw128(smem_u32(smem + kOffConv + cb * kW16Bytes));
-          const uint64_t dx = smem_desc_sw128(smem_u32(smem + stage * kLoadStage));
-          const uint32_t dt = tslot + (uint32_t)((kb / kpc) * a.TN);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_f16(dt, dw + 2 * kk, dx + 2 * kk, idesc, (kb % kpc != 0 || kk != 0) ? 1u : 0u);
-          umma_commit(&empty[stage]);
-          umma_commit(&cempty[cb]);
-          if (++stage == kLoadStages) {
-            stage = 0;
-            phase ^= 1;
+          const int ns = stage + 1 == kXStages ? 0 : stage + 1;
+          const uint32_t nph = ns == 0 ? phase ^ 1u : phase;
+          // one commit frees the token stage and the fp16 weight buffer that goes with it
+          ready = mma_kblock_commit_probe<false>(
+              dt, dw0 + (uint64_t)((stage * kW16Bytes) >> 4),
+              dx0 + (uint64_t)((stage * kXBytesMax) >> 4), idesc, kin != 0 ? 1u : 0u,
+              smem_u32(&xempty[stage]), smem_u32(&cfull[ns]), nph);
+          if (++kin == kpc) {
+            kin = 0;
+            dt += (uint32_t)a.TN;
           }
-          if (++cb == kConvBufs) {
-            cb = 0;
-            cphase ^= 1;
-          }
+          stage = ns;
+          phase = nph;
         }
         if (!ok) break;
         umma_commit(&acc_full[slot]);
@@ -391,7 +329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int nch = single ? 1 : (K + kChunkK - 1) / kChunkK;
       const int slot = it % nslots;
       const uint32_t use = (uint32_t)(it / nslots) & 1u;
-      if (!mbar_wait(&acc_full[slot], use, abort_flag, a.err)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[slot], use, abort_flag, a.err))) break;
       tc_fence_after();
       const uint32_t tbase = lane_base + (uint32_t)(slot * slot_cols);
       if (GU)
@@ -399,7 +337,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       else
         epilogue_down(a, wi, nch, tbase, half);
       tc_fence_before();
-      mbar_arrive(&acc_empty[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[slot]);
     }
   }
 
@@ -414,14 +353,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 cudaError_t gemm_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e == cudaSuccess) e = pair_set_attributes();
+  return e;
 }
 
-cudaError_t launch_grouped_gemm(bool gate_up, const GemmArgs& a, const CUtensorMap& tmX,
+// Work items that can run at once: CTAs for cs = 1, CTA pairs for cs = 2.
+cudaError_t gemm_max_clusters(bool gate_up, int cs, int* n) {
+  *n = 0;
+  if (cs == 2) return pair_max_clusters(gate_up, n);
+  if (cs != 1) return cudaErrorInvalidValue;
+  int per_sm = 0, dev = 0, sms = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, gate_up ? (const void*)grouped_gemm_kernel<true> : (const void*)grouped_gemm_kernel<false>,
+      kGemmThreads, kGemmSmem);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  *n = per_sm * sms;
+  return e;
+}
+
+// grid: a multiple of cs (whole clusters).
+cudaError_t launch_grouped_gemm(bool gate_up, int cs, const GemmArgs& a, const XMaps& tmX,
                                 const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
                                 cudaStream_t s) {
+  if (grid < cs || grid % cs) return cudaErrorInvalidValue;
+  if (cs == 2) return launch_pair_gemm(gate_up, a, tmX, tmW, tmWs, grid, s);
+  if (cs != 1) return cudaErrorInvalidValue;
   if (gate_up)
     grouped_gemm_kernel<true><<<grid, kGemmThreads, kGemmSmem, s>>>(a, tmX, tmW, tmWs);
   else

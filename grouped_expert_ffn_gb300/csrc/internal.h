@@ -12,7 +12,16 @@ namespace moe {
 
 constexpr int kBM = 128;        // tensor-core tile rows (weight rows: the MMA's M)
 constexpr int kMaxTokTile = 256;  // token rows per tile (the MMA's N), at most
-constexpr int kTokenBox = 64;   // token rows per TMA box of the GEMMs' N operand
+// Token-tile TMA boxes: one tensor map per box height over the same token-row operand, so
+// that the token tile of a k-block is one TMA load. Heights are multiples of kXStep1 (16)
+// rows up to 256 for the one-CTA kernel, and of kXStep2 (8) rows up to 128 for the CTA pair
+// (each CTA of a pair holds half of the tile).
+constexpr int kXStep1 = 16;
+constexpr int kXStep2 = 8;
+constexpr int kXMaps = 16;
+struct XMaps {
+  CUtensorMap m[kXMaps];
+};
 constexpr int kBK = 64;         // K elements per pipeline stage (128 bytes of fp16)
 constexpr int kChunkK = 1024;   // K elements summed in one fp32 TMEM accumulator
 constexpr int kTokPerBlk = 64;  // tokens per histogram block (one 64-bit mask per expert)
@@ -52,10 +61,13 @@ struct GemmArgs {
   int* err;
 };
 
-cudaError_t launch_grouped_gemm(bool gate_up, const GemmArgs& a, const CUtensorMap& tmX,
+// cs: 1 (one CTA per item of one weight tile) or 2 (a CTA pair per item of two adjacent weight
+// tiles, on the 2-SM MMA); grid a multiple of cs.
+cudaError_t launch_grouped_gemm(bool gate_up, int cs, const GemmArgs& a, const XMaps& tmX,
                                 const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
                                 cudaStream_t s);
 cudaError_t gemm_set_attributes();
+cudaError_t gemm_max_clusters(bool gate_up, int cs, int* n);
 
 cudaError_t launch_combine(const float* yd, const int* slot_row, int T, int k, int H,
                            int has_shared, float* y, cudaStream_t s);
@@ -71,6 +83,7 @@ struct PrepArgs {
   const float* w;
   const uint16_t* x;
   int T, k, E, H, I, Is, has_shared, tn_gu, tn_d;
+  int cs_gu, cs_d;            // weight tiles per work item (the GEMMs' cluster sizes)
   unsigned long long* bmask;  // [nblk, E]
   int* bhist;                 // [nblk, E]
   int* counts;                // [E]

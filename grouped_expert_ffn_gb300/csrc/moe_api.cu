@@ -17,6 +17,8 @@ struct moe_plan_s {
   int E = 0, k = 0, H = 0, I = 0, Is = 0, max_tokens = 0, Imax = 0, has_shared = 0;
   int device = 0, num_sms = 0;
   int tn_gu = 0, tn_d = 0;  // token tiles of the two GEMMs
+  int cs_gu = 1, cs_d = 1;  // cluster sizes of the two GEMMs (weight tiles per work item)
+  int grid_gu = 0, grid_d = 0;
   size_t R_max = 0;
   int max_items_gu = 0, max_items_d = 0;
   // workspace (device)
@@ -56,7 +58,9 @@ struct moe_plan_s {
   };
   std::vector<ProfRec> prof_pending;
   std::vector<cudaEvent_t> ev_pool;
-  CUtensorMap tmX_gu, tmX_d;  // token rows of the two GEMMs (N operand)
+  // token rows of the two GEMMs (N operand), one map per box height: boxes of the one-CTA
+  // kernel (16-row steps) and of the CTA pair (8-row steps)
+  XMaps tmX1_gu, tmX1_d, tmX2_gu, tmX2_d;
   std::vector<void*> allocs;
 };
 
@@ -202,6 +206,21 @@ size_t tap_bytes(const moe_plan_s* p, int which, int T) {
 
 }  // namespace
 
+namespace {
+// Grid of each GEMM for its current cluster size.
+cudaError_t size_gemm_grids(moe_plan_s* p) {
+  for (int gu = 0; gu < 2; ++gu) {
+    const int cs = gu ? p->cs_gu : p->cs_d;
+    int n = 0;
+    const cudaError_t e = gemm_max_clusters(gu != 0, cs, &n);
+    if (e != cudaSuccess) return e;
+    if (n < 1) n = std::max(1, p->num_sms / cs);
+    (gu ? p->grid_gu : p->grid_d) = n * cs;
+  }
+  return cudaSuccess;
+}
+}  // namespace
+
 extern "C" {
 
 const char* moe_status_string(moe_status s) {
@@ -296,24 +315,30 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
     free_plan(p);
     return MOE_ERR_CUDA;
   }
-  // Token-row operands of the two GEMMs (fp16 rows in the plan's row order), 64-row boxes.
+  // Token-row operands of the two GEMMs (fp16 rows in the plan's row order).
   {
     const uint64_t dims[2] = {(uint64_t)H, (uint64_t)p->R_max};
     const uint64_t st2[1] = {(uint64_t)H * 2};
-    if (!encode_f16(&p->tmX_gu, p->xq, 2, dims, st2, kTokenBox)) {
-      free_plan(p);
-      return MOE_ERR_CUDA;
-    }
     const uint64_t dims_d[2] = {(uint64_t)p->Imax, (uint64_t)p->R_max};
     const uint64_t st_d[1] = {(uint64_t)p->Imax * 2};
-    if (!encode_f16(&p->tmX_d, p->hq, 2, dims_d, st_d, kTokenBox)) {
-      free_plan(p);
-      return MOE_ERR_CUDA;
+    for (int j = 0; j < kXMaps; ++j) {
+      const uint32_t r1 = (uint32_t)(kXStep1 * (j + 1)), r2 = (uint32_t)(kXStep2 * (j + 1));
+      if (!encode_f16(&p->tmX1_gu.m[j], p->xq, 2, dims, st2, r1) ||
+          !encode_f16(&p->tmX1_d.m[j], p->hq, 2, dims_d, st_d, r1) ||
+          !encode_f16(&p->tmX2_gu.m[j], p->xq, 2, dims, st2, r2) ||
+          !encode_f16(&p->tmX2_d.m[j], p->hq, 2, dims_d, st_d, r2)) {
+        free_plan(p);
+        return MOE_ERR_CUDA;
+      }
     }
   }
   cudaError_t e = gemm_set_attributes();
   if (e == cudaSuccess) e = decode_set_attributes(H, p->Imax);
+  // One CTA per weight tile by default (moe_plan_use_cta_pairs switches a GEMM to CTA pairs);
+  // the grid is as many whole clusters as fit at once.
+  if (e == cudaSuccess) e = size_gemm_grids(p);
   if (e != cudaSuccess) {
+    cudaGetLastError();
     free_plan(p);
     return MOE_ERR_CUDA;
   }
@@ -483,6 +508,8 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   pa.has_shared = p->has_shared;
   pa.tn_gu = p->tn_gu;
   pa.tn_d = p->tn_d;
+  pa.cs_gu = p->cs_gu;
+  pa.cs_d = p->cs_d;
   pa.bmask = p->bmask;
   pa.bhist = p->bhist;
   pa.counts = p->counts;
@@ -525,7 +552,6 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.row_w = p->row_w;
   g.yd = p->yd;
   g.err = p->err;
-  const int grid = p->num_sms;
   // gate/up: K = H for every group
   g.items = p->items_gu;
   g.n_items = p->n_items;
@@ -535,7 +561,8 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.tap = p->debug ? p->tap_gu : nullptr;
   g.row_sq_max = p->sq_max;
   g.w_sq_max = pk->w_sq;
-  if ((e = launch_grouped_gemm(true, g, p->tmX_gu, pk->tmW_gu, pk->tmWs_gu, grid, s)) != cudaSuccess)
+  if ((e = launch_grouped_gemm(true, p->cs_gu, g, p->cs_gu == 2 ? p->tmX2_gu : p->tmX1_gu, pk->tmW_gu,
+                               pk->tmWs_gu, p->grid_gu, s)) != cudaSuccess)
     return cuda_status(e);
   if (ev) cudaEventRecord(ev[2], s);
   if ((e = launch_requant(p->h32, R, T_sh, p->I, p->Is, p->Imax, p->hq, p->sh, p->sq_max + 1, s)) !=
@@ -551,10 +578,25 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.tap = p->debug ? p->tap_d : nullptr;
   g.row_sq_max = p->sq_max + 1;
   g.w_sq_max = pk->w_sq + 1;
-  e = launch_grouped_gemm(false, g, p->tmX_d, pk->tmW_d, pk->tmWs_d, grid, s);
+  e = launch_grouped_gemm(false, p->cs_d, g, p->cs_d == 2 ? p->tmX2_d : p->tmX1_d, pk->tmW_d,
+                          pk->tmWs_d, p->grid_d, s);
   if (e == cudaSuccess) e = launch_combine(p->yd, p->slot_row, T, p->k, p->H, p->has_shared, y, s);
   if (ev) cudaEventRecord(ev[4], s);
   return cuda_status(e);
+}
+
+moe_status moe_plan_use_cta_pairs(moe_plan_t p, int gate_up, int down) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  const bool gu_even = (2 * p->I / kBM) % 2 == 0 && (!p->has_shared || (2 * p->Is / kBM) % 2 == 0);
+  const bool d_even = (p->H / kBM) % 2 == 0;
+  if ((gate_up && !gu_even) || (down && !d_even)) return MOE_ERR_UNSUPPORTED;
+  p->cs_gu = gate_up ? 2 : 1;
+  p->cs_d = down ? 2 : 1;
+  if (size_gemm_grids(p) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 moe_status moe_profile_enable(moe_plan_t p, int on) {

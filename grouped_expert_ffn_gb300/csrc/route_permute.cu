@@ -164,8 +164,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 
 // One block of 1024 threads. Turns bhist into exclusive per-expert prefixes over blocks,
 // writes counts/offsets and the two work lists (gate/up and down): per group, every
-// (128-row weight tile, token tile of at most TN rows) pair, ordered by group, then weight
-// tile, then token tile, so consecutive items of a large group reuse one weight tile from L2.
+// (cs adjacent 128-row weight tiles, token tile of at most TN rows) pair, ordered by group,
+// then weight tiles, then token tile, so consecutive items of a large group reuse one weight
+// tile from L2.
 __global__ void scan_kernel(PrepArgs a, int nblk) {
   __shared__ int s_cnt[257];
   __shared__ int s_off[257];
@@ -222,8 +223,8 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
   if (g < ng) {
     const bool sh = a.has_shared && g == 0;
     const int cnt = sh ? a.T : s_cnt[g - a.has_shared];
-    ngu = (2 * (sh ? a.Is : a.I)) / kBM * ((cnt + a.tn_gu - 1) / a.tn_gu);
-    nd = a.H / kBM * ((cnt + a.tn_d - 1) / a.tn_d);
+    ngu = (2 * (sh ? a.Is : a.I)) / (kBM * a.cs_gu) * ((cnt + a.tn_gu - 1) / a.tn_gu);
+    nd = a.H / (kBM * a.cs_d) * ((cnt + a.tn_d - 1) / a.tn_d);
   }
   const int bgu = block_exclusive_scan(ngu, s_warp, &total);
   if (g < ng) s_base_gu[g] = bgu;
@@ -243,6 +244,7 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
     const int* base = list == 0 ? s_base_gu : s_base_d;
     const int n = base[ng];
     const int tn = list == 0 ? a.tn_gu : a.tn_d;
+    const int wstep = kBM * (list == 0 ? a.cs_gu : a.cs_d);  // weight rows per item
     int4* items = list == 0 ? a.items_gu : a.items_d;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       int lo = 0, hi = ng - 1;  // last group with base <= i
@@ -258,7 +260,7 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
       const int tt = (cnt + tn - 1) / tn;
       const int local = i - base[gg];
       const int wt = local / tt, t = local % tt;
-      items[i] = make_int4(gid, row0 + t * tn, min(tn, cnt - t * tn), wt * kBM);
+      items[i] = make_int4(gid, row0 + t * tn, min(tn, cnt - t * tn), wt * wstep);
     }
   }
 }
