@@ -9,9 +9,11 @@
 //  decode_gu_kernel    (16 channels of one unique expert) per block: streams 16 gate and 16
 //                      up rows, dp4a against the expert's <= 8 quantised token rows held in
 //                      shared memory; fused SiLU(gate)*up.
-//  decode_down_kernel  (64 output channels of one unique expert) per block: requantises the
-//                      expert's h rows into shared memory, streams 64 down rows, dp4a, and
-//                      adds w * d into y.
+//  requant_kernel      (shared with the prefill path) requantises every h row once, warp
+//                      per row, into fp16 codes and scales.
+//  decode_down_kernel  (64 output channels of one unique expert) per block: stages the
+//                      expert's h codes as int8 in shared memory, streams 64 down rows, dp4a,
+//                      and adds w * d into y.
 #include "common.cuh"
 #include "internal.h"
 
@@ -210,24 +212,21 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
   const int8_t* Wd = shared ? a.sh_down : a.w_down + (size_t)grp.x * H * a.I;
   const float* sd = shared ? a.sh_s_down : a.s_down + (size_t)grp.x * H;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // requantise this expert's h rows (warp n handles row n)
-  if (warp < nr) {
-    const int row = row0 + warp;
-    const float* h = a.h32 + (size_t)row * Imax;
-    float amax = 0.0f;
-    for (int i = lane; i < Ig; i += 32) amax = fmaxf(amax, fabsf(h[i]));
-    amax = warp_max(amax);
-    const float s = __fdiv_rn(amax, 127.0f);
-    for (int i = lane; i < Ig; i += 32) {
-      const int q = s > 0.0f ? quant_code(h[i], s) : 0;
-      hs[(size_t)warp * Imax + i] = (int8_t)q;
-      if (a.tap_d && blockIdx.x == 0) a.hq[(size_t)row * Imax + i] = __int2half_rn(q);
+  // this expert's h codes (fp16 integers, written by the requantisation pass) -> int8
+  for (int i = threadIdx.x; i < nr * (Ig / 8); i += blockDim.x) {
+    const int n = i / (Ig / 8), u = i % (Ig / 8);
+    const uint4 v = reinterpret_cast<const uint4*>(a.hq + (size_t)(row0 + n) * Imax)[u];
+    const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+    uint32_t q[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float2 f0 = __half22float2(h2[2 * j]), f1 = __half22float2(h2[2 * j + 1]);
+      q[j] = (uint32_t)(uint8_t)(int8_t)(int)f0.x | (uint32_t)(uint8_t)(int8_t)(int)f0.y << 8 |
+             (uint32_t)(uint8_t)(int8_t)(int)f1.x << 16 | (uint32_t)(uint8_t)(int8_t)(int)f1.y << 24;
     }
-    if (lane == 0) {
-      shs[warp] = s;
-      if (a.tap_d && blockIdx.x == 0) a.sh[row] = s;
-    }
+    *reinterpret_cast<uint2*>(hs + (size_t)n * Imax + u * 8) = make_uint2(q[0], q[1]);
   }
+  if ((int)threadIdx.x < nr) shs[threadIdx.x] = a.sh[row0 + threadIdx.x];
   __syncthreads();
   const int ob = o0 + warp * 8;
   int acc[64];
@@ -265,6 +264,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) {
+  const int R = a.T * a.k + (a.has_shared ? a.T : 0);
   if (ev) cudaEventRecord(ev[0], s);
   decode_prep_kernel<<<1, 256, 0, s>>>(a);
   if (ev) cudaEventRecord(ev[1], s);
@@ -274,6 +274,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) 
   const dim3 ggu((a.Imax + kGuChannelsPerBlock - 1) / kGuChannelsPerBlock, gmax);
   decode_gu_kernel<<<ggu, 256, kDecodeMaxRows * a.H, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // one requantisation of every h row (warp per row), instead of one per down block
+  e = launch_requant(a.h32, R, a.has_shared ? a.T : 0, a.I, a.Is, a.Imax, a.hq, a.sh,
+                     a.sq_scratch, s);
+  if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[2], s);
   const dim3 gd(a.H / kDownRowsPerBlock, gmax);
   decode_down_kernel<<<gd, 256, kDecodeMaxRows * a.Imax, s>>>(a);

@@ -131,8 +131,9 @@ struct DecodeArgs {
   int8_t* qtok;      // [T, H]
   float* stok;       // [T]
   float* h32;        // [R, Imax]
-  __half* hq;        // [R, Imax] (tap only)
-  float* sh;         // [R]       (tap only)
+  __half* hq;        // [R, Imax] requantised h codes (fp16 integers)
+  float* sh;         // [R]       their scales
+  int* sq_scratch;   // one word the requantisation pass writes its sum(q^2) maximum to
   float* y;
   int32_t* tap_gu;   // NULL = off
   int32_t* tap_d;

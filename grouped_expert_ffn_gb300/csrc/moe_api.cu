@@ -488,6 +488,7 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
     a.h32 = p->h32;
     a.hq = p->hq;
     a.sh = p->sh;
+    a.sq_scratch = p->sq_max + 1;
     a.y = y;
     a.tap_gu = p->debug ? p->tap_gu : nullptr;
     a.tap_d = p->debug ? p->tap_d : nullptr;

@@ -103,6 +103,9 @@ extern "C" moe_status moe_forward_decode_static(int E, int top_k, int H, int I, 
   const size_t o_q = carve(off, (size_t)T * H);
   const size_t o_s = carve(off, sizeof(float) * T);
   const size_t o_h = carve(off, sizeof(float) * R * Imax);
+  const size_t o_hq = carve(off, sizeof(__half) * R * Imax);
+  const size_t o_sh = carve(off, sizeof(float) * R);
+  const size_t o_sq = carve(off, sizeof(int));
   if (off > kScratchBytes) return MOE_ERR_CAPACITY;
 
   unsigned char* base = nullptr;
@@ -159,8 +162,9 @@ extern "C" moe_status moe_forward_decode_static(int E, int top_k, int H, int I, 
   a.qtok = reinterpret_cast<int8_t*>(base + o_q);
   a.stok = reinterpret_cast<float*>(base + o_s);
   a.h32 = reinterpret_cast<float*>(base + o_h);
-  a.hq = nullptr;
-  a.sh = nullptr;
+  a.hq = reinterpret_cast<__half*>(base + o_hq);
+  a.sh = reinterpret_cast<float*>(base + o_sh);
+  a.sq_scratch = reinterpret_cast<int*>(base + o_sq);
   a.y = y;
   a.tap_gu = nullptr;
   a.tap_d = nullptr;
