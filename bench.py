@@ -33,6 +33,10 @@ import torch  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "MoE layer tokens/s (prefill) & µs/layer decode C=8; % int8/HBM roofline"
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up GEMM launch on the
+# stacked-prefill layer (T=2600), from one ncu capture of the kernel as it is now. Set to None
+# whenever the kernel changes, until it is captured again.
+GU_TRAFFIC_BYTES = 403.7e6
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -363,7 +367,8 @@ def run_ours(args, world, rank):
                      "requant": stage_ms[2] * 1e3, "down_gemm_combine": stage_ms[3] * 1e3},
         "roofline": {"bound": "tensor", "kernel": "grouped gate/up GEMM (tcgen05 kind::f16)",
                      "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved_tf / peak_tf, "traffic": None,
+                     "frac": achieved_tf / peak_tf, "traffic": GU_TRAFFIC_BYTES,
+                     "traffic_unit": "bytes per launch (ncu)",
                      "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 = bf16 rate)",
                      "flops_per_launch": gu_flops},
         "layer_tflops": layer_flops / (moe_ms / 1e3) / 1e12,
