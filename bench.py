@@ -101,7 +101,7 @@ class Clocks:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -249,18 +249,26 @@ def run_ours(args, world, rank):
     y = torch.empty((T, H), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def stack():
+    prof_layer = n_layers // 2
+
+    def stack(profile=False):
         # layer l: x_in = rmsnorm(x) -> logits = x_in @ W_r -> route -> y = moe(x_in) -> x += y
+        # With profile, one layer per step records the plan's per-stage CUDA events (events
+        # between every layer's kernels would add their own cost to the step).
         for l, (W, wr, packed) in enumerate(layers):
             moe.moe_rmsnorm_residual(x, y if l else None, x_in)
             moe.moe_router_logits_packed(x_in, wr, logits)
             moe.moe_route(plan, logits, idx, w)
+            if profile and l == prof_layer:
+                moe.moe_profile_enable(plan, True)
             moe.moe_forward(plan, packed, x_in, idx, w, y)
+            if profile and l == prof_layer:
+                moe.moe_profile_enable(plan, False)
         moe.moe_residual_add(x, y)
 
-    def step():
+    def step(profile=False):
         x.copy_(x0)
-        stack()
+        stack(profile)
 
     for _ in range(args.warmup):
         step()
@@ -268,7 +276,6 @@ def run_ours(args, world, rank):
     err = moe.moe_get_error(plan)
     if err:
         raise moe.MoeError(err, "stacked prefill warm-up")
-    moe.moe_profile_enable(plan, True)
     clocks = Clocks()
     barrier(world)
     torch.cuda.synchronize()
@@ -277,13 +284,12 @@ def run_ours(args, world, rank):
     torch.cuda.nvtx.range_push("timed_prefill")
     ev0.record(stream)
     for _ in range(args.steps):
-        step()
+        step(profile=True)
     ev1.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    moe.moe_profile_enable(plan, False)
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
     st, calls = moe.moe_profile_read(plan, 0)
     stage_ms = [v / max(calls, 1) for v in st]

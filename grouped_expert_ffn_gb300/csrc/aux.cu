@@ -116,6 +116,8 @@ cudaError_t launch_widen(const int8_t* src, size_t n, __half* out, cudaStream_t 
 __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
                                                             const float* __restrict__ wr, int T,
                                                             int H, int E, float* __restrict__ out) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   __shared__ float As[16][64 + 4];
   __shared__ __align__(16) float Bs[16][64];
   const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
@@ -180,11 +182,12 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, int T, int H, int E,
                                  float* out, cudaStream_t s) {
   const dim3 grid((E + 63) / 64, (T + 63) / 64);
-  router_logits_kernel<<<grid, 256, 0, s>>>(x, wr, T, H, E, out);
-  return cudaGetLastError();
+  return launch_pdl(router_logits_kernel, grid, dim3(256), 0, s, x, wr, T, H, E, out);
 }
 
 __global__ void residual_kernel(uint16_t* __restrict__ x, const float* __restrict__ y, size_t n) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n / 4;
        i += (size_t)gridDim.x * blockDim.x) {
     const float4 yv = reinterpret_cast<const float4*>(y)[i];
@@ -213,6 +216,8 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
 // Block per token: optional residual update of x, then the RMS-normalised copy x_in.
 __global__ void rmsnorm_residual_kernel(uint16_t* __restrict__ x, const float* __restrict__ y,
                                         uint16_t* __restrict__ x_in, int H) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   const int t = blockIdx.x;
   uint16_t* xr = x + (size_t)t * H;
   __shared__ float red[32];
@@ -262,13 +267,11 @@ __global__ void rmsnorm_residual_kernel(uint16_t* __restrict__ x, const float* _
 
 cudaError_t launch_rmsnorm_residual(uint16_t* x, const float* y, uint16_t* x_in, int T, int H,
                                     cudaStream_t s) {
-  rmsnorm_residual_kernel<<<T, 256, 0, s>>>(x, y, x_in, H);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_residual_kernel, dim3(T), dim3(256), 0, s, x, y, x_in, H);
 }
 
 cudaError_t launch_residual(uint16_t* x, const float* y, size_t n, cudaStream_t s) {
-  residual_kernel<<<1216, 256, 0, s>>>(x, y, n);
-  return cudaGetLastError();
+  return launch_pdl(residual_kernel, dim3(1216), dim3(256), 0, s, x, y, n);
 }
 
 }  // namespace moe

@@ -2,6 +2,7 @@
 // tensor copies and the 5th-generation tensor core (tcgen05 / TMEM), bounded waits and the
 // plan's sticky error word.
 #pragma once
+#include <utility>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -130,6 +131,31 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
           dst_cluster),
       "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
       : "memory");
+}
+
+// ---- programmatic dependent launch ------------------------------------------------------
+// Kernels of the layer chain are launched with launch_pdl: a kernel's blocks may be scheduled
+// while its predecessor on the stream drains, and wait for it (its completion and memory) in
+// pdl_wait before touching global memory. pdl_trigger lets the successor be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---- TMA ----------------------------------------------------------------------------

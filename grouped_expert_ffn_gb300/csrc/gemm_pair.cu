@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   cluster_sync();  // both CTAs' barriers and TMEM exist before either uses the other's
   tc_fence_after();
+  pdl_wait();  // the predecessor's results
+  pdl_trigger();
   const uint32_t tmem = *tmem_slot;
   const bool single = single_accumulator_exact(a);
   const int kmax = a.K_r > a.K_s ? a.K_r : a.K_s;
@@ -327,12 +329,14 @@ static cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, int grid, cudaS
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = kPairSmem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -346,7 +350,7 @@ cudaError_t pair_set_attributes() {
 }
 
 cudaError_t pair_max_clusters(bool gate_up, int* n) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg =
       pair_config(attr, 2, nullptr);
   return gate_up ? cudaOccupancyMaxActiveClusters(n, pair_gemm_kernel<true>, &cfg)
@@ -356,7 +360,7 @@ cudaError_t pair_max_clusters(bool gate_up, int* n) {
 cudaError_t launch_pair_gemm(bool gate_up, const GemmArgs& a, const XMaps& tmX,
                              const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
                              cudaStream_t s) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   if (gate_up) {
     const cudaLaunchConfig_t cfg = pair_config(attr, grid, s);
     return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<true>, a, tmX, tmW, tmWs);

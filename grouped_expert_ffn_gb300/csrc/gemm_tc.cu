@@ -141,6 +141,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the set-up above touches no global memory; from here on the predecessor's results are read
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem = *tmem_slot;
   const int n_items = *a.n_items;
   // Accumulator layout for this launch: one accumulator over the whole K (two TMEM slots,
@@ -383,16 +386,18 @@ cudaError_t launch_grouped_gemm(bool gate_up, int cs, const GemmArgs& a, const X
   if (cs == 2) return launch_pair_gemm(gate_up, a, tmX, tmW, tmWs, grid, s);
   if (cs != 1) return cudaErrorInvalidValue;
   if (gate_up)
-    grouped_gemm_kernel<true><<<grid, kGemmThreads, kGemmSmem, s>>>(a, tmX, tmW, tmWs);
-  else
-    grouped_gemm_kernel<false><<<grid, kGemmThreads, kGemmSmem, s>>>(a, tmX, tmW, tmWs);
-  return cudaGetLastError();
+    return launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, a,
+                      tmX, tmW, tmWs);
+  return launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, a,
+                    tmX, tmW, tmWs);
 }
 
 // y[t] = sum over slots j of yd[row(t, j)] + yd[t] (shared expert row), in slot order. Block per
 // token, 8 consecutive channels per thread and pass.
 __global__ void combine_kernel(const float* __restrict__ yd, const int* __restrict__ slot_row,
                                int T, int k, int H, int has_shared, float* __restrict__ y) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   const int t = blockIdx.x;
   __shared__ int rows[9];
   if (threadIdx.x < k) rows[threadIdx.x] = slot_row[(size_t)t * k + threadIdx.x];
@@ -415,8 +420,7 @@ __global__ void combine_kernel(const float* __restrict__ yd, const int* __restri
 
 cudaError_t launch_combine(const float* yd, const int* slot_row, int T, int k, int H,
                            int has_shared, float* y, cudaStream_t s) {
-  combine_kernel<<<T, 256, 0, s>>>(yd, slot_row, T, k, H, has_shared, y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(T), dim3(256), 0, s, yd, slot_row, T, k, H, has_shared, y);
 }
 
 // Per-row requantisation of h = SiLU(gate)*up: s = amax/127, q = rne(h/s) (|q| <= 127),
@@ -424,6 +428,8 @@ cudaError_t launch_combine(const float* yd, const int* slot_row, int T, int k, i
 __global__ void requant_kernel(const float* __restrict__ h32, int R, int T_sh, int I, int Is,
                                int Imax, __half* __restrict__ hq, float* __restrict__ sh,
                                int* __restrict__ sq_max) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   constexpr int kRegV = 8;  // float4 per lane held in registers: rows up to 1024 values
   __shared__ int s_sq[32];
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -500,9 +506,8 @@ cudaError_t launch_requant(const float* h32, int R, int T_sh, int I, int Is, int
                            __half* hq, float* sh, int* sq_max, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   const int rows_per_blk = 16;
-  requant_kernel<<<(R + rows_per_blk - 1) / rows_per_blk, 32 * rows_per_blk, 0, s>>>(
-      h32, R, T_sh, I, Is, Imax, hq, sh, sq_max);
-  return cudaGetLastError();
+  return launch_pdl(requant_kernel, dim3((R + rows_per_blk - 1) / rows_per_blk),
+                    dim3(32 * rows_per_blk), 0, s, h32, R, T_sh, I, Is, Imax, hq, sh, sq_max);
 }
 
 }  // namespace moe

@@ -21,8 +21,8 @@ constexpr int kMaxEPerLane = 8;  // E <= 256
 
 __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int k,
                              int32_t* __restrict__ idx, float* __restrict__ w, int* err) {
-  // a dependent decode launch may start now; it waits for this grid before reading idx / w
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (t >= T) return;
@@ -101,14 +101,16 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                          int* err, cudaStream_t s) {
   const int warps = 8;
-  route_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(logits, T, E, k, idx, w, err);
-  return cudaGetLastError();
+  return launch_pdl(route_kernel, dim3((T + warps - 1) / warps), dim3(32 * warps), 0, s, logits, T,
+                    E, k, idx, w, err);
 }
 
 // ---------------------------------------------------------------------------------------
 __global__ void hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
                             unsigned long long* __restrict__ bmask, int* __restrict__ bhist,
                             int* sq_max, int* err) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   extern __shared__ unsigned long long mask[];
   if (blockIdx.x == 0 && threadIdx.x < 2) sq_max[threadIdx.x] = 0;  // maxima of this forward
   for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0ull;
@@ -168,6 +170,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 // then weight tiles, then token tile, so consecutive items of a large group reuse one weight
 // tile from L2.
 __global__ void scan_kernel(PrepArgs a, int nblk) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   __shared__ int s_cnt[257];
   __shared__ int s_off[257];
   __shared__ int s_base_gu[258];
@@ -267,6 +271,8 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
 
 // Block per token: quantise x[t] once, write its codes (fp16 integers) to each of its rows.
 __global__ void scatter_kernel(PrepArgs a) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   const int t = blockIdx.x;
   const int H = a.H, k = a.k, E = a.E;
   const int T_sh = a.has_shared ? a.T : 0;
@@ -364,14 +370,11 @@ __global__ void scatter_kernel(PrepArgs a) {
 
 cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s) {
   const int nblk = (a.T + kTokPerBlk - 1) / kTokPerBlk;
-  hist_kernel<<<nblk, 256, a.E * sizeof(unsigned long long), s>>>(a.idx, a.T, a.k, a.E, a.bmask,
-                                                                  a.bhist, a.sq_max, a.err);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(hist_kernel, dim3(nblk), dim3(256), a.E * sizeof(unsigned long long),
+                             s, a.idx, a.T, a.k, a.E, a.bmask, a.bhist, a.sq_max, a.err);
   if (e != cudaSuccess) return e;
-  scan_kernel<<<1, 1024, 0, s>>>(a, nblk);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  scatter_kernel<<<a.T, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  if ((e = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, a, nblk)) != cudaSuccess) return e;
+  return launch_pdl(scatter_kernel, dim3(a.T), dim3(256), 0, s, a);
 }
 
 }  // namespace moe

@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(192, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // the predecessor's results (set-up above touches no global memory)
+  pdl_trigger();
   const uint32_t tmem = *tmem_slot;
   if (warp == 4) {
     if (lane == 0) {
@@ -196,8 +198,7 @@ cudaError_t launch_router_tc(int T, int H, int E, float* out, const CUtensorMap&
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
   if (e != cudaSuccess) return e;
   const dim3 grid((T + kBM - 1) / kBM, E / kREB);
-  router_tc_kernel<<<grid, 192, kRSmem, s>>>(T, H, E, out, tmA, tmB);
-  return cudaGetLastError();
+  return launch_pdl(router_tc_kernel, grid, dim3(192), kRSmem, s, T, H, E, out, tmA, tmB);
 }
 
 }  // namespace moe
