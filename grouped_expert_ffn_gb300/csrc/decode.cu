@@ -4,8 +4,9 @@
 // Halo: multi-session serving ... #145" names as the C>1 limiter (section "Status", items
 // "Batched decode doesn't scale" and "Next": expert dedup across rows plus int8 dot).
 //
-//  decode_prep_kernel  one block: per-token int8 quant, the unique-expert list (with the
-//                      shared expert as group 0), the canonical row order, y zeroed.
+//  decode_prep_kernel  block 0: the unique-expert list (with the shared expert as group 0)
+//                      and the canonical row order; block 1 + t: token t's int8 quant (the
+//                      exact per-element divisions spread over T SMs) and y's row t zeroed.
 //  decode_gu_kernel    (16 channels of one unique expert) per block: streams 16 gate and 16
 //                      up rows, dp4a against the expert's <= 8 quantised token rows held in
 //                      shared memory; fused SiLU(gate)*up.
@@ -48,13 +49,72 @@ __device__ __forceinline__ void transpose_reduce32(int (&v)[32], int lane) {
   }
 }
 
-__global__ void decode_prep_kernel(DecodeArgs a) {
+constexpr int kPrepThreads = 256;
+
+// Block 0 builds the routing metadata; block 1 + t quantises token t and zeroes y's row t.
+__device__ __forceinline__ void prep_quantise_token(const DecodeArgs& a, int t) {
+  __shared__ float s_amax[kPrepThreads / 32];
+  const int H = a.H, tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const uint16_t* xr = a.x + (size_t)t * H;
+  constexpr int kXv = 4;  // uint4 (8 bf16) per thread: rows up to 256 * 8 * 4 = 8192
+  uint4 xv[kXv];
+#pragma unroll
+  for (int c = 0; c < kXv; ++c) {
+    const int e0 = (c * kPrepThreads + tid) * 8;
+    xv[c] = e0 < H ? *reinterpret_cast<const uint4*>(xr + e0) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kXv; ++c) {
+    const uint32_t u[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_float((uint16_t)(u[i] & 0xffffu))));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_float((uint16_t)(u[i] >> 16))));
+    }
+  }
+  amax = warp_max(amax);
+  if (lane == 0) s_amax[warp] = amax;
+  __syncthreads();
+  amax = s_amax[0];
+#pragma unroll
+  for (int i = 1; i < kPrepThreads / 32; ++i) amax = fmaxf(amax, s_amax[i]);
+  const float s = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+  for (int c = 0; c < kXv; ++c) {
+    const int e0 = (c * kPrepThreads + tid) * 8;
+    if (e0 < H) {
+      const uint32_t u[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+      uint2 qv;
+      uint8_t* qb = reinterpret_cast<uint8_t*>(&qv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = bf16_bits_to_float((uint16_t)(u[i] & 0xffffu));
+        const float hi = bf16_bits_to_float((uint16_t)(u[i] >> 16));
+        qb[2 * i] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(lo, s) : 0);
+        qb[2 * i + 1] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(hi, s) : 0);
+      }
+      *reinterpret_cast<uint2*>(a.qtok + (size_t)t * H + e0) = qv;
+    }
+  }
+  if (tid == 0) a.stok[t] = s;
+  float4* y4 = reinterpret_cast<float4*>(a.y + (size_t)t * H);
+  for (int i = tid; i < H / 4; i += kPrepThreads) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(DecodeArgs a) {
+  if (blockIdx.x > 0) {
+    prep_quantise_token(a, blockIdx.x - 1);
+    return;
+  }
   __shared__ int s_cnt[256];
   __shared__ int s_off[257];
   __shared__ int s_idx[kDecodeMaxRows * 8];
-  const int T = a.T, k = a.k, E = a.E, H = a.H;
+  __shared__ int s_warp[kPrepThreads / 32];
+  const int T = a.T, k = a.k, E = a.E;
   const int T_sh = a.has_shared ? T : 0;
   const int tid = threadIdx.x;
+  const int warp = tid / 32, lane = tid % 32;
   for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
   for (int r = tid; r < T * k; r += blockDim.x) {
     int e = a.idx[r];
@@ -72,20 +132,41 @@ __global__ void decode_prep_kernel(DecodeArgs a) {
       if (s_idx[q] == s_idx[r]) set_error(a.err, kErrDevice);  // expert repeated in a token
   }
   __syncthreads();
-  if (tid == 0) {
-    int off = 0, n = 0;
-    if (a.has_shared) a.groups[n++] = make_int4(E, 0, T, 0);
-    for (int e = 0; e < E; ++e) {
+  // row offsets and group positions: block-wide exclusive scans over the experts (E <= 256,
+  // one per thread), both counts packed in one word (each is at most T * k <= 64)
+  {
+    const int e = tid;
+    const int c = e < E ? s_cnt[e] : 0;
+    const int v = (c << 16) | (c > 0 ? 1 : 0);
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += n;
+    }
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int i = 0; i < kPrepThreads / 32; ++i) {
+      if (i < warp) before += s_warp[i];
+      total += s_warp[i];
+    }
+    const int ex = before + inc - v;  // exclusive prefix of this expert
+    if (e < E) {
+      const int off = ex >> 16, gp = ex & 0xffff;
       s_off[e] = off;
       a.offsets[e] = off;
-      a.counts[e] = s_cnt[e];
+      a.counts[e] = c;
       // a group never has more rows than tokens (<= 8); more means repeated experts (flagged)
-      if (s_cnt[e] > 0) a.groups[n++] = make_int4(e, T_sh + off, min(s_cnt[e], T), 0);
-      off += s_cnt[e];
+      if (c > 0) a.groups[a.has_shared + gp] = make_int4(e, T_sh + off, min(c, T), 0);
     }
-    s_off[E] = off;
-    a.offsets[E] = off;
-    *a.n_groups = n;
+    if (tid == 0) {
+      s_off[E] = total >> 16;
+      a.offsets[E] = total >> 16;
+      *a.n_groups = (total & 0xffff) + a.has_shared;
+      if (a.has_shared) a.groups[0] = make_int4(E, 0, T, 0);
+    }
   }
   __syncthreads();
   for (int r = tid; r < T * k; r += blockDim.x) {
@@ -102,40 +183,6 @@ __global__ void decode_prep_kernel(DecodeArgs a) {
     a.row_token[tid] = tid;
     a.row_w[tid] = 1.0f;
   }
-  // per-token quantisation, warp t handles token t
-  const int warp = tid / 32, lane = tid % 32;
-  if (warp < T) {
-    const uint16_t* xr = a.x + (size_t)warp * H;
-    float amax = 0.0f;
-    for (int c = lane * 8; c < H; c += 256) {
-      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        amax = fmaxf(amax, fabsf(bf16_bits_to_float((uint16_t)(u[i] & 0xffffu))));
-        amax = fmaxf(amax, fabsf(bf16_bits_to_float((uint16_t)(u[i] >> 16))));
-      }
-    }
-    amax = warp_max(amax);
-    const float s = __fdiv_rn(amax, 127.0f);
-    for (int c = lane * 8; c < H; c += 256) {
-      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-      uint2 qv;
-      uint8_t* qb = reinterpret_cast<uint8_t*>(&qv);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = bf16_bits_to_float((uint16_t)(u[i] & 0xffffu));
-        const float hi = bf16_bits_to_float((uint16_t)(u[i] >> 16));
-        qb[2 * i] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(lo, s) : 0);
-        qb[2 * i + 1] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(hi, s) : 0);
-      }
-      *reinterpret_cast<uint2*>(a.qtok + (size_t)warp * H + c) = qv;
-    }
-    if (lane == 0) a.stok[warp] = s;
-  }
-  float4* y4 = reinterpret_cast<float4*>(a.y);
-  for (int i = tid; i < T * H / 4; i += blockDim.x) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 constexpr int kGuChannelsPerBlock = 16;  // 8 warps x 2 channels
@@ -266,7 +313,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) {
   const int R = a.T * a.k + (a.has_shared ? a.T : 0);
   if (ev) cudaEventRecord(ev[0], s);
-  decode_prep_kernel<<<1, 256, 0, s>>>(a);
+  decode_prep_kernel<<<1 + a.T, kPrepThreads, 0, s>>>(a);
   if (ev) cudaEventRecord(ev[1], s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
