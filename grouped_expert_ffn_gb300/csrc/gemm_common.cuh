@@ -8,19 +8,26 @@ namespace moe {
 
 constexpr int kW8Bytes = kBM * kBK;       // int8 weight tile per k-block (8 KB)
 constexpr int kW16Bytes = kBM * kBK * 2;  // fp16 weight tile per k-block (16 KB)
-#ifndef MOE_CONV_GROUPS
-#define MOE_CONV_GROUPS 2
-#endif
-constexpr int kEpiWarps = 8;
-constexpr int kConvWarps = 4;                  // one group: one thread per weight row
-constexpr int kConvGroups = MOE_CONV_GROUPS;   // groups take turns, one k-block each
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kConvThreads = kConvWarps * 32;
-constexpr int kConvWarp0 = kEpiWarps;
-constexpr int kMmaWarp = kEpiWarps + kConvGroups * kConvWarps;
-constexpr int kWProducerWarp = kMmaWarp + 1;        // two warps
-constexpr int kXProducerWarp = kWProducerWarp + 2;  // two warps
-constexpr int kGemmThreads = (kXProducerWarp + 2) * 32;
+// Warp roles of the grouped GEMM kernels: epilogue warps (four per TMEM lane quadrant times
+// column groups), converter groups of four warps taking turns over k-blocks, one MMA warp,
+// two weight-TMA warps, two token-TMA warps. The gate/up GEMM (32 k-blocks per item, light
+// epilogue) runs two converter groups and 8 epilogue warps; the down GEMM (8 k-blocks per
+// item, an epilogue that writes w * d for every row) one converter group and 16 epilogue
+// warps, so that its epilogue keeps up with its mainloop.
+constexpr int kConvWarps = 4;  // one converter group: one thread per weight row
+template <bool GU>
+struct GemmRoles {
+  static constexpr int kEpiWarps = GU ? 8 : 16;
+  static constexpr int kColGroups = kEpiWarps / 4;
+  static constexpr int kConvGroups = GU ? 2 : 1;
+  static constexpr int kConvWarp0 = kEpiWarps;
+  static constexpr int kMmaWarp = kEpiWarps + kConvGroups * kConvWarps;
+  static constexpr int kWProducerWarp = kMmaWarp + 1;        // two warps
+  static constexpr int kXProducerWarp = kWProducerWarp + 2;  // two warps
+  static constexpr int kThreads = (kXProducerWarp + 2) * 32;
+  static_assert(kEpiWarps % 4 == 0, "epilogue warps cover the four TMEM lane quadrants");
+  static_assert(kThreads <= 1024, "block size");
+};
 constexpr uint32_t kTmemCols = 512;
 
 // Whether one fp32 accumulator over the whole K is provably exact for this launch.
@@ -46,20 +53,46 @@ __device__ __forceinline__ uint2 widen4(uint32_t w) {
   return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
 }
 
-// Gate/up epilogue. Lane pair (2i, 2i+1) of quadrant q holds gate and up of channel
-// m0/2 + 16q + i for every token column; the even lane finishes columns 0-7 of each 16-column
-// chunk and the odd lane columns 8-15.
-__device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
-                                                 uint32_t tbase, int half) {
-  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
-  const bool odd = lane & 1;
-  const bool shared = wi.x == a.E;
-  const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
-  const float sgc = (shared ? a.sh_s_g : a.s_g + (size_t)wi.x * a.I)[ch];
-  const float suc = (shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I)[ch];
-  const int ncols = wi.z;
+// Epilogue column loop with one accumulator per tile: TMEM loads of the next 16-column chunk
+// are in flight while the current one is dequantised and stored (tcgen05.wait::ld waits for
+// all of a thread's outstanding loads, so the two register sets alternate). `store(v, c0)`
+// consumes the 16 int32 accumulators of chunk c0 (the fp32 words hold integers). With several
+// 1024-K chunks per tile, each chunk's partial sums are rounded to int32 and added in integer
+// arithmetic (the total may exceed what fp32 holds exactly).
+template <int kColGroups, typename Store>
+__device__ __forceinline__ void epilogue_columns(const GemmArgs& a, int nch, uint32_t tbase,
+                                                 int cg, int ncols, Store&& store) {
+  auto to_int = [](const uint32_t (&r)[16], int (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __float2int_rn(__uint_as_float(r[i]));
+  };
+  if (nch == 1) {
+    uint32_t ra[16], rb[16];
+    int v[16];
+    constexpr int kStep = 16 * kColGroups;  // this warp's chunks: cg, cg + kColGroups, ...
+    int c0 = cg * 16;
+    if (c0 >= ncols) return;  // uniform over the warp
+    tmem_ld16(tbase + c0, ra);
+    tmem_ld_wait();
 #pragma unroll 1
-  for (int c0 = half * 16; c0 < ncols; c0 += 32) {
+    for (; c0 < ncols; c0 += 2 * kStep) {
+      const int c1 = c0 + kStep;
+      if (c1 < ncols) tmem_ld16(tbase + c1, rb);
+      to_int(ra, v);
+      store(v, c0);
+      if (c1 >= ncols) break;
+      tmem_ld_wait();
+      const int c2 = c1 + kStep;
+      if (c2 < ncols) tmem_ld16(tbase + c2, ra);
+      to_int(rb, v);
+      store(v, c1);
+      if (c2 >= ncols) break;
+      tmem_ld_wait();
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int c0 = cg * 16; c0 < ncols; c0 += 16 * kColGroups) {
     int v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0;
@@ -71,6 +104,24 @@ __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] += __float2int_rn(__uint_as_float(r[i]));
     }
+    store(v, c0);
+  }
+}
+
+// Gate/up epilogue. Lane pair (2i, 2i+1) of quadrant q holds gate and up of channel
+// m0/2 + 16q + i for every token column; the even lane finishes columns 0-7 of each 16-column
+// chunk and the odd lane columns 8-15.
+__device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
+                                                 uint32_t tbase, int cg) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const bool odd = lane & 1;
+  const bool shared = wi.x == a.E;
+  const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
+  const float sgc = (shared ? a.sh_s_g : a.s_g + (size_t)wi.x * a.I)[ch];
+  const float suc = (shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I)[ch];
+  const int ncols = wi.z;
+  epilogue_columns<GemmRoles<true>::kColGroups>(a, nch, tbase, cg, ncols,
+                                                [&](const int (&v)[16], int c0) {
     int recv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) recv[i] = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[8 + i], 1);
@@ -89,32 +140,21 @@ __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int
         }
       }
     }
-  }
+  });
 }
 
 // Down epilogue: lane = output channel m0 + 32q + lane; for each token column the warp stores
 // w * dequant(acc) for 32 consecutive channels of that row of yd (one 128-byte store). The
 // combine kernel then sums each token's rows in slot order.
 __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase,
-                                              int half) {
+                                              int cg) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const bool shared = wi.x == a.E;
   const int o = wi.w + q * 32 + lane;
   const float sdo = (shared ? a.sh_s_d : a.s_d + (size_t)wi.x * a.H)[o];
   const int ncols = wi.z;
-#pragma unroll 1
-  for (int c0 = half * 16; c0 < ncols; c0 += 32) {
-    int v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0;
-#pragma unroll 1
-    for (int kc = 0; kc < nch; ++kc) {
-      uint32_t r[16];
-      tmem_ld16(tbase + kc * a.TN + c0, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] += __float2int_rn(__uint_as_float(r[i]));
-    }
+  epilogue_columns<GemmRoles<false>::kColGroups>(a, nch, tbase, cg, ncols,
+                                                 [&](const int (&v)[16], int c0) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int col = c0 + i;
@@ -124,7 +164,7 @@ __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nc
         if (a.tap) a.tap[(size_t)row * a.H + o] = v[i];
       }
     }
-  }
+  });
 }
 
 // Converter thread r: weight row r of one k-block, int8 (64-byte swizzled TMA tile) to fp16

@@ -9,13 +9,12 @@
 // token operand is what limits the one-CTA kernel: every token stage has to come back from L2
 // within the few k-blocks that the shared-memory ring covers.
 //
-// Roles, per CTA (672 threads):
-//   warps 0-7   epilogue of this CTA's 128 weight rows (its own TMEM lanes);
-//   warps 8-15  converters of this CTA's int8 weight tiles to fp16 (two groups of four,
-//               alternate k-blocks);
-//   warp 16     rank 0 only: MMA issuer for the pair (both CTAs allocate TMEM);
-//   warps 17-18 TMA producers of this CTA's int8 weight tiles (alternate stages);
-//   warps 19-20 TMA producers of this CTA's half token tiles (alternate stages).
+// Roles, per CTA (GemmRoles in gemm_common.cuh; gate/up 672 threads, down 800):
+//   epilogue warps of this CTA's 128 weight rows (its own TMEM lanes);
+//   converter groups of this CTA's int8 weight tiles to fp16 (alternate k-blocks);
+//   rank 0 only: the MMA issuer for the pair (both CTAs allocate TMEM);
+//   two TMA producers of this CTA's int8 weight tiles (alternate stages);
+//   two TMA producers of this CTA's half token tiles (alternate stages).
 // Synchronisation across the pair:
 //   - rank 0's MMA thread waits for its own token stage and for the fp16 weight buffer of
 //     both CTAs: cfull on rank 0 completes on the arrivals of rank 0's converter warps and on
@@ -52,10 +51,11 @@ constexpr uint16_t kPairMask = 0x3;
 constexpr uint32_t kPairTmemCols = MOE_PAIR_TMEM_COLS;  // allocated in each CTA of the pair
 
 template <bool GU>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     pair_gemm_kernel(const GemmArgs a, const __grid_constant__ XMaps tmX,
                      const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmWs) {
+  using R = GemmRoles<GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -89,21 +89,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&cfull[s], kConvWarps);  // rank 0's converter warps (+ rank 1's bytes)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 2 * kEpiWarps);
+      mbar_init(&acc_empty[s], 2 * R::kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tmem_alloc_pair(tmem_slot, kPairTmemCols);
     tmem_relinquish_pair();
   }
-  if (warp == kWProducerWarp && lane == 0) {
+  if (warp == R::kWProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmWs);
   }
-  if (warp == kXProducerWarp && lane < kXMaps) tma_prefetch_desc(&tmX.m[lane]);
+  if (warp == R::kXProducerWarp && lane < kXMaps) tma_prefetch_desc(&tmX.m[lane]);
   tc_fence_before();
   cluster_sync();  // both CTAs' barriers and TMEM exist before either uses the other's
   tc_fence_after();
@@ -120,11 +120,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (!fits && threadIdx.x == 0 && leader) set_error(a.err, kErrDevice);
   const int n_items = fits ? *a.n_items : 0;
 
-  if (warp >= kWProducerWarp && warp < kXProducerWarp + 2) {
+  if (warp >= R::kWProducerWarp && warp < R::kXProducerWarp + 2) {
     if (lane == 0) {
       // ------- TMA producers, two threads per ring, each CTA its own operands -------
-      const bool wprod = warp < kXProducerWarp;
-      const int pidx = warp - (wprod ? kWProducerWarp : kXProducerWarp);
+      const bool wprod = warp < R::kXProducerWarp;
+      const int pidx = warp - (wprod ? R::kWProducerWarp : R::kXProducerWarp);
       const int nst = wprod ? kPWStages : kPXStages;
       uint64_t* full = wprod ? wfull : xfull;
       uint64_t* empty = wprod ? wempty : xempty;
@@ -179,14 +179,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvGroups * kConvWarps) {
+  } else if (warp >= R::kConvWarp0 && warp < R::kConvWarp0 + R::kConvGroups * kConvWarps) {
     // ---------------- converters ----------------
-    // Group g converts the k-blocks whose running index is g modulo kConvGroups. On rank 0
+    // Group g converts the k-blocks whose running index is g modulo R::kConvGroups. On rank 0
     // the group's warps arrive on cfull (warp 0 also expects the 64 signal bytes of rank 1);
     // on rank 1 each warp, once its rows and rank 1's token stage are ready, copies 16 bytes
     // into rank 0's signal slot with completion on rank 0's cfull. The copy is asynchronous,
     // so no thread waits for a cluster-scope release.
-    const int cw = warp - kConvWarp0;
+    const int cw = warp - R::kConvWarp0;
     const int group = cw / kConvWarps, gw = cw % kConvWarps;
     const int r = gw * 32 + lane;
     const uint32_t cfull_leader = mapa_shared(smem_u32(cfull), 0);
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int4 wi = a.items[item];
       const int nkb = (wi.x == a.E ? a.K_s : a.K_r) / kBK;
       for (int kb = 0; kb < nkb; ++kb, ++gk) {
-        if (gk % kConvGroups == group) {
+        if (gk % R::kConvGroups == group) {
           // the buffer's previous MMAs are done (rank 0's commit), and this CTA's token stage
           // has landed: the arrival / signal below then certifies both operands of this CTA
           const bool got = mbar_wait(&wfull[ws], wph, abort_flag, a.err) &&
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == R::kMmaWarp) {
     if (leader && lane == 0) {
       // ---------------- MMA issuer of the pair ----------------
       // Same lean loop as the one-CTA kernel: one barrier per k-block (cfull: both CTAs'
@@ -283,9 +283,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
-  } else if (warp < kEpiWarps) {
+  } else if (warp < R::kEpiWarps) {
     // ---------------- epilogue of this CTA's weight rows ----------------
-    const int half = warp / 4;
+    const int cg = warp / 4;  // column group of this warp within its TMEM lane quadrant
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
     int it = 0;
@@ -300,9 +300,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tbase = lane_base + (uint32_t)(slot * slot_cols);
       if (GU)
-        epilogue_gate_up(a, wi, nch, tbase, half);
+        epilogue_gate_up(a, wi, nch, tbase, cg);
       else
-        epilogue_down(a, wi, nch, tbase, half);
+        epilogue_down(a, wi, nch, tbase, cg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -317,13 +317,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, kPairTmemCols);
   }
 }
 
-static cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, int grid, cudaStream_t s) {
+static cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, int grid, int threads,
+                                      cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -332,7 +333,7 @@ static cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, int grid, cudaS
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = kPairSmem;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -352,7 +353,8 @@ cudaError_t pair_set_attributes() {
 cudaError_t pair_max_clusters(bool gate_up, int* n) {
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg =
-      pair_config(attr, 2, nullptr);
+      pair_config(attr, 2, gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads,
+                  nullptr);
   return gate_up ? cudaOccupancyMaxActiveClusters(n, pair_gemm_kernel<true>, &cfg)
                  : cudaOccupancyMaxActiveClusters(n, pair_gemm_kernel<false>, &cfg);
 }
@@ -362,10 +364,10 @@ cudaError_t launch_pair_gemm(bool gate_up, const GemmArgs& a, const XMaps& tmX,
                              cudaStream_t s) {
   cudaLaunchAttribute attr[2];
   if (gate_up) {
-    const cudaLaunchConfig_t cfg = pair_config(attr, grid, s);
+    const cudaLaunchConfig_t cfg = pair_config(attr, grid, GemmRoles<true>::kThreads, s);
     return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<true>, a, tmX, tmW, tmWs);
   }
-  const cudaLaunchConfig_t cfg = pair_config(attr, grid, s);
+  const cudaLaunchConfig_t cfg = pair_config(attr, grid, GemmRoles<false>::kThreads, s);
   return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<false>, a, tmX, tmW, tmWs);
 }
 

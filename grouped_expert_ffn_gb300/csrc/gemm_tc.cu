@@ -43,14 +43,14 @@
 // share of its 64-row boxes once and multicasts it to the cluster, which divides the token
 // operand's L2-to-SM traffic by CS.
 //
-// Warp roles (672 threads, one CTA per SM):
-//   warps 0-7   epilogue: warp w reads TMEM lanes 32*(w%4).. (weight rows) and every other
-//               16-column chunk (tokens) starting at chunk w/4;
-//   warps 8-15  converters, two groups of four taking alternate k-blocks: thread r of a group
-//               widens weight row r;
-//   warp 16     MMA issuer and TMEM owner;
-//   warps 17-18 TMA producers of the int8 weight tiles (alternate stages);
-//   warps 19-20 TMA producers of the fp16 token tiles (alternate stages).
+// Warp roles (one CTA per SM; GemmRoles in gemm_common.cuh): gate/up 672 threads, down 800.
+//   epilogue warps (8 for gate/up, 16 for down): warp w reads TMEM lanes 32*(w%4).. (weight
+//               rows) and every (w/4)-th 16-column chunk (tokens) of its quadrant;
+//   converter groups of four warps (2 for gate/up, 1 for down) taking turns over k-blocks:
+//               thread r of a group widens weight row r;
+//   one MMA issuer and TMEM owner;
+//   two TMA producers of the int8 weight tiles (alternate stages);
+//   two TMA producers of the fp16 token tiles (alternate stages).
 // Pipeline: the weights stream from HBM through a ring of small int8 stages (4 x 8 KB,
 // released by the converters as soon as they have widened a stage); the token tiles, mostly
 // L2 hits, through a ring of large stages (4 x 32 KB), one TMA load per stage (box heights
@@ -92,10 +92,11 @@ static_assert(kXStages % 2 == 0 && kWStages % 2 == 0, "two producers per ring ow
 
 
 template <bool GU>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ XMaps tmX,
                         const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmWs) {
+  using R = GemmRoles<GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -123,21 +124,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int s = 0; s < kConvBufs; ++s) mbar_init(&cfull[s], kConvWarps);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], kEpiWarps);
+      mbar_init(&acc_empty[s], R::kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWProducerWarp && lane == 0) {
+  if (warp == R::kWProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmWs);
   }
-  if (warp == kXProducerWarp && lane < kXMaps) tma_prefetch_desc(&tmX.m[lane]);
+  if (warp == R::kXProducerWarp && lane < kXMaps) tma_prefetch_desc(&tmX.m[lane]);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -155,13 +156,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nslots = slot_cols <= (int)kTmemCols / 2 ? 2 : 1;
   const int kpc = single ? (1 << 30) : kChunkK / kBK;  // k-blocks per accumulator
 
-  if (warp >= kWProducerWarp && warp < kXProducerWarp + 2) {
+  if (warp >= R::kWProducerWarp && warp < R::kXProducerWarp + 2) {
     if (lane == 0) {
       // ------- TMA producers: weights (HBM) and tokens, two threads per ring -------
       // Producer pidx of a ring owns the ring's stages with index % 2 == pidx; both walk the
       // whole item / k-block sequence to keep stage and phase in step.
-      const bool wprod = warp < kXProducerWarp;
-      const int pidx = warp - (wprod ? kWProducerWarp : kXProducerWarp);
+      const bool wprod = warp < R::kXProducerWarp;
+      const int pidx = warp - (wprod ? R::kWProducerWarp : R::kXProducerWarp);
       const int nst = wprod ? kWStages : kXStages;
       uint64_t* full = wprod ? wfull : xfull;
       uint64_t* empty = wprod ? wempty : xempty;
@@ -212,13 +213,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvGroups * kConvWarps) {
+  } else if (warp >= R::kConvWarp0 && warp < R::kConvWarp0 + R::kConvGroups * kConvWarps) {
     // ---------------- converters: int8 -> fp16 weight rows ----------------
-    // Group g converts the k-blocks whose running index is g modulo kConvGroups, so the
+    // Group g converts the k-blocks whose running index is g modulo R::kConvGroups, so the
     // latency of one group's fence and arrivals overlaps the other groups' work. The fp16
     // buffer of token stage cb is free once the MMAs of its previous use completed (the token
     // stage's empty barrier).
-    const int cw = warp - kConvWarp0;
+    const int cw = warp - R::kConvWarp0;
     const int group = cw / kConvWarps;
     const int r = (cw % kConvWarps) * 32 + lane;  // weight row within the tile
     int stage = 0, cb = 0, gk = 0;
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int4 wi = a.items[item];
       const int nkb = (wi.x == a.E ? a.K_s : a.K_r) / kBK;
       for (int kb = 0; kb < nkb; ++kb, ++gk) {
-        if (gk % kConvGroups != group) {
+        if (gk % R::kConvGroups != group) {
           if (++stage == kWStages) {
             stage = 0;
             phase ^= 1;
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == R::kMmaWarp) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       // The issuing thread is on the tensor pipe's critical path: tcgen05.mma issue blocks
@@ -321,9 +322,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
-  } else if (warp < kEpiWarps) {
-    // ---------------- epilogue (warps 0-7) ----------------
-    const int half = warp / 4;
+  } else if (warp < R::kEpiWarps) {
+    // ---------------- epilogue ----------------
+    const int cg = warp / 4;  // column group of this warp within its TMEM lane quadrant
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     int it = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
@@ -336,9 +337,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tbase = lane_base + (uint32_t)(slot * slot_cols);
       if (GU)
-        epilogue_gate_up(a, wi, nch, tbase, half);
+        epilogue_gate_up(a, wi, nch, tbase, cg);
       else
-        epilogue_down(a, wi, nch, tbase, half);
+        epilogue_down(a, wi, nch, tbase, cg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[slot]);
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -371,7 +372,7 @@ cudaError_t gemm_max_clusters(bool gate_up, int cs, int* n) {
   int per_sm = 0, dev = 0, sms = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &per_sm, gate_up ? (const void*)grouped_gemm_kernel<true> : (const void*)grouped_gemm_kernel<false>,
-      kGemmThreads, kGemmSmem);
+      gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads, kGemmSmem);
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   *n = per_sm * sms;
@@ -386,10 +387,10 @@ cudaError_t launch_grouped_gemm(bool gate_up, int cs, const GemmArgs& a, const X
   if (cs == 2) return launch_pair_gemm(gate_up, a, tmX, tmW, tmWs, grid, s);
   if (cs != 1) return cudaErrorInvalidValue;
   if (gate_up)
-    return launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, a,
-                      tmX, tmW, tmWs);
-  return launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, a,
-                    tmX, tmW, tmWs);
+    return launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(GemmRoles<true>::kThreads),
+                      kGemmSmem, s, a, tmX, tmW, tmWs);
+  return launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(GemmRoles<false>::kThreads),
+                    kGemmSmem, s, a, tmX, tmW, tmWs);
 }
 
 // y[t] = sum over slots j of yd[row(t, j)] + yd[t] (shared expert row), in slot order. Block per
