@@ -15,11 +15,23 @@ constexpr int kW16Bytes = kBM * kBK * 2;  // fp16 weight tile per k-block (16 KB
 // item, an epilogue that writes w * d for every row) one converter group and 16 epilogue
 // warps, so that its epilogue keeps up with its mainloop.
 constexpr int kConvWarps = 4;  // one converter group: one thread per weight row
+#ifndef MOE_GU_EPI_WARPS
+#define MOE_GU_EPI_WARPS 8
+#endif
+#ifndef MOE_GU_CONV_GROUPS
+#define MOE_GU_CONV_GROUPS 2
+#endif
+#ifndef MOE_D_EPI_WARPS
+#define MOE_D_EPI_WARPS 16
+#endif
+#ifndef MOE_D_CONV_GROUPS
+#define MOE_D_CONV_GROUPS 1
+#endif
 template <bool GU>
 struct GemmRoles {
-  static constexpr int kEpiWarps = GU ? 8 : 16;
+  static constexpr int kEpiWarps = GU ? MOE_GU_EPI_WARPS : MOE_D_EPI_WARPS;
   static constexpr int kColGroups = kEpiWarps / 4;
-  static constexpr int kConvGroups = GU ? 2 : 1;
+  static constexpr int kConvGroups = GU ? MOE_GU_CONV_GROUPS : MOE_D_CONV_GROUPS;
   static constexpr int kConvWarp0 = kEpiWarps;
   static constexpr int kMmaWarp = kEpiWarps + kConvGroups * kConvWarps;
   static constexpr int kWProducerWarp = kMmaWarp + 1;        // two warps
