@@ -379,10 +379,28 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Symmetric int8 code of v with scale s (s > 0): round-half-even(v / s) clamped to +-127,
-// with an IEEE-correct division.
-__device__ __forceinline__ int quant_code(float v, float s) {
-  int q = __float2int_rn(__fdiv_rn(v, s));
+// Reciprocal of a row scale for quant_code, computed once per row. NaN (every element takes
+// the exact division) when s is so small that 1/s could overflow.
+__device__ __forceinline__ float quant_recip(float s) {
+  return s >= 0x1p-100f ? __frcp_rn(s) : __int_as_float(0x7fffffff);
+}
+
+// Symmetric int8 code of v with scale s (s > 0, r = quant_recip(s)): round-half-even of the
+// correctly rounded fp32 quotient v / s, clamped to +-127.
+// Fast path: y = v * r differs from the exact quotient q by less than 3|q|u (u = 2^-24) and the
+// fp32 quotient differs from q by at most |q|u. Every caller derives s = amax / 127 from the
+// row's amax, so |q| < 128 and the two stay within 2^-15 of each other. When y lies farther than 2^-11
+// from every half-integer, no rounding boundary separates y from the fp32 quotient and rne(y)
+// is the exact answer; otherwise (about one element in a thousand) the quotient is taken by an
+// IEEE division.
+__device__ __forceinline__ int quant_code(float v, float s, float r) {
+  const float y = __fmul_rn(v, r);
+  const float n = rintf(y);
+  int q;
+  if (fabsf(__fsub_rn(y, n)) < 0.4995f)
+    q = (int)n;
+  else
+    q = __float2int_rn(__fdiv_rn(v, s));
   return max(-127, min(127, q));
 }
 

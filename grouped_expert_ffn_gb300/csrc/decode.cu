@@ -80,6 +80,7 @@ __device__ __forceinline__ void prep_quantise_token(const DecodeArgs& a, int t) 
 #pragma unroll
   for (int i = 1; i < kPrepThreads / 32; ++i) amax = fmaxf(amax, s_amax[i]);
   const float s = __fdiv_rn(amax, 127.0f);
+  const float rs = quant_recip(s);
 #pragma unroll
   for (int c = 0; c < kXv; ++c) {
     const int e0 = (c * kPrepThreads + tid) * 8;
@@ -91,8 +92,8 @@ __device__ __forceinline__ void prep_quantise_token(const DecodeArgs& a, int t) 
       for (int i = 0; i < 4; ++i) {
         const float lo = bf16_bits_to_float((uint16_t)(u[i] & 0xffffu));
         const float hi = bf16_bits_to_float((uint16_t)(u[i] >> 16));
-        qb[2 * i] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(lo, s) : 0);
-        qb[2 * i + 1] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(hi, s) : 0);
+        qb[2 * i] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(lo, s, rs) : 0);
+        qb[2 * i + 1] = (uint8_t)(int8_t)(s > 0.0f ? quant_code(hi, s, rs) : 0);
       }
       *reinterpret_cast<uint2*>(a.qtok + (size_t)t * H + e0) = qv;
     }

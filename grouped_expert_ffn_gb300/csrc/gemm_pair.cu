@@ -199,11 +199,9 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       const int nkb = (wi.x == a.E ? a.K_s : a.K_r) / kBK;
       for (int kb = 0; kb < nkb; ++kb, ++gk) {
         if (gk % R::kConvGroups == group) {
-          // the buffer's previous MMAs are done (rank 0's commit), and this CTA's token stage
-          // has landed: the arrival / signal below then certifies both operands of this CTA
+          // the buffer's previous MMAs are done (rank 0's commit)
           const bool got = mbar_wait(&wfull[ws], wph, abort_flag, a.err) &&
-                           mbar_wait_cl(&xempty[cb], cph ^ 1, abort_flag, a.err) &&
-                           mbar_wait(&xfull[cb], cph, abort_flag, a.err);
+                           mbar_wait_cl(&xempty[cb], cph ^ 1, abort_flag, a.err);
           if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
@@ -213,8 +211,14 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
           // read of them, whichever CTA of the pair issues the MMA
           fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) mbar_arrive(&wempty[ws]);
+          // this CTA's token stage has landed (its load overlapped the conversion): the
+          // arrival / signal below then certifies both operands of this CTA
+          if (!__all_sync(0xffffffffu, lane != 0 || mbar_wait(&xfull[cb], cph, abort_flag, a.err))) {
+            ok = false;
+            break;
+          }
           if (lane == 0) {
-            mbar_arrive(&wempty[ws]);
             if (leader) {
               if (gw == 0)
                 mbar_arrive_expect_tx(&cfull[cb], 16 * kConvWarps);

@@ -240,12 +240,9 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
           }
           continue;
         }
-        // warp-uniform outcome: the per-warp arrival below needs every lane. The token stage
-        // cb is waited for here too, so that cfull alone tells the MMA thread that both
-        // operands of the k-block are in shared memory.
+        // warp-uniform outcome: the per-warp arrivals below need every lane
         const bool got = mbar_wait(&wfull[stage], phase, abort_flag, a.err) &&
-                         mbar_wait(&xempty[cb], cphase ^ 1, abort_flag, a.err) &&
-                         mbar_wait(&xfull[cb], cphase, abort_flag, a.err);
+                         mbar_wait(&xempty[cb], cphase ^ 1, abort_flag, a.err);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -253,10 +250,14 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
         widen_row(smem + kOffW8 + stage * kW8Bytes, smem + kOffConv + cb * kW16Bytes, r);
         fence_proxy_async_smem();  // this thread's fp16 stores, before the MMA reads them
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&cfull[cb]);
-          mbar_arrive(&wempty[stage]);
+        if (lane == 0) mbar_arrive(&wempty[stage]);
+        // The token stage cb is waited for after the conversion (which overlaps its load), so
+        // that cfull alone tells the MMA thread that both operands are in shared memory.
+        if (!__all_sync(0xffffffffu, lane != 0 || mbar_wait(&xfull[cb], cphase, abort_flag, a.err))) {
+          ok = false;
+          break;
         }
+        if (lane == 0) mbar_arrive(&cfull[cb]);
         if (++stage == kWStages) {
           stage = 0;
           phase ^= 1;
@@ -452,16 +453,17 @@ __global__ void requant_kernel(const float* __restrict__ h32, int R, int T_sh, i
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
       amax = warp_max(amax);
       const float s = __fdiv_rn(amax, 127.0f);
+      const float rs = quant_recip(s);
 #pragma unroll
       for (int j = 0; j < kRegV; ++j) {
         const int i = lane * 4 + j * 128;
         if (i >= n) break;
         int c[4] = {0, 0, 0, 0};
         if (s > 0.0f) {
-          c[0] = quant_code(v[j].x, s);
-          c[1] = quant_code(v[j].y, s);
-          c[2] = quant_code(v[j].z, s);
-          c[3] = quant_code(v[j].w, s);
+          c[0] = quant_code(v[j].x, s, rs);
+          c[1] = quant_code(v[j].y, s, rs);
+          c[2] = quant_code(v[j].z, s, rs);
+          c[3] = quant_code(v[j].w, s, rs);
         }
         sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
         *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));
@@ -476,14 +478,15 @@ __global__ void requant_kernel(const float* __restrict__ h32, int R, int T_sh, i
       }
       amax = warp_max(amax);
       const float s = __fdiv_rn(amax, 127.0f);
+      const float rs = quant_recip(s);
       for (int i = lane * 4; i < n; i += 128) {
         const float4 v = *reinterpret_cast<const float4*>(h + i);
         int c[4] = {0, 0, 0, 0};
         if (s > 0.0f) {
-          c[0] = quant_code(v.x, s);
-          c[1] = quant_code(v.y, s);
-          c[2] = quant_code(v.z, s);
-          c[3] = quant_code(v.w, s);
+          c[0] = quant_code(v.x, s, rs);
+          c[1] = quant_code(v.y, s, rs);
+          c[2] = quant_code(v.z, s, rs);
+          c[3] = quant_code(v.w, s, rs);
         }
         sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
         *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));

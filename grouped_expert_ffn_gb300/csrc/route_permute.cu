@@ -325,6 +325,7 @@ __global__ void scatter_kernel(PrepArgs a) {
   }
   __syncthreads();
   const float s = __fdiv_rn(s_red[0], 127.0f);
+  const float rs = quant_recip(s);
   const int nrows = k + (a.has_shared ? 1 : 0);
   if (threadIdx.x < nrows) a.sx[s_rows[threadIdx.x]] = s;
   if (threadIdx.x == 0 && a.stok) a.stok[t] = s;
@@ -337,8 +338,8 @@ __global__ void scatter_kernel(PrepArgs a) {
     for (int i = 0; i < 4; ++i) {
       const float lo = bf16_bits_to_float((uint16_t)(u[i] & 0xffffu));
       const float hi = bf16_bits_to_float((uint16_t)(u[i] >> 16));
-      q[2 * i] = s > 0.0f ? quant_code(lo, s) : 0;
-      q[2 * i + 1] = s > 0.0f ? quant_code(hi, s) : 0;
+      q[2 * i] = s > 0.0f ? quant_code(lo, s, rs) : 0;
+      q[2 * i + 1] = s > 0.0f ? quant_code(hi, s, rs) : 0;
       sq += q[2 * i] * q[2 * i] + q[2 * i + 1] * q[2 * i + 1];
     }
     uint4 hv;

@@ -144,6 +144,43 @@ def test_decode_and_prefill_give_identical_integers():
         lay.close()
 
 
+def _tie_rows(x, seed):
+    """Rows whose elements sit on (or next to) the rounding boundaries of the int8 code: with a
+    power-of-two amax the scale is exact and (m + 1/2) * scale is an exact tie; with another
+    amax the bf16 value nearest a tie lands a fraction of an ulp from it."""
+    g = torch.Generator().manual_seed(seed)
+    T, H = x.shape
+    x = x.clone()
+    for t in range(T):
+        c = 2.0 ** (t % 9 - 4)
+        m = torch.randint(-127, 127, (H,), generator=g).double() + 0.5
+        if t % 3 == 2:  # non-exact scale: amax 100 c, targets next to (m + 1/2) * fl(amax / 127)
+            s = float(np.float32(np.float32(100.0 * c) / np.float32(127.0)))
+            row = m.clamp(-99.5, 99.5) * s
+            row[0] = 100.0 * c
+        else:
+            row = m * c
+            row[0] = -127.0 * c if t % 2 else 127.0 * c
+        row[1::7] = torch.randint(-127, 128, (len(range(1, H, 7)),), generator=g).double() * c
+        x[t] = row.to(torch.bfloat16)
+    return x
+
+
+@pytest.mark.parametrize("T", [8, 40])
+def test_activation_codes_on_rounding_ties(T):
+    # decode (T=8) and prefill (T=40) token quantisation at exact and near ties, bit-exact
+    # against the oracle's round-half-even of the fp32 quotient, and the layer downstream
+    sh = synth.LayerShape(T=T, H=1024, E=32, k=4, I=256, Is=256)
+    d = synth.small_layer(T, 1024, 32, 4, 256, 256, seed=31 + T)
+    x = _tie_rows(d["x"], 7 + T)
+    W = weights_to(d["weights"], "cuda")
+    q_o, s_o = oracle.quant_rows(x)
+    xf = x.float().numpy()
+    ties = np.abs(np.abs(xf / s_o[:, None]) % 1.0 - 0.5) < 1e-3
+    assert ties.sum() > T * 1024 // 2  # most elements are (near) ties
+    check_layer(sh, x, d["logits"], W, oracle_layer(d["weights"], sh))
+
+
 def test_capacity_and_argument_errors():
     sh = synth.LayerShape(T=16, H=256, E=8, k=2, I=128, Is=0)
     d = synth.small_layer(16, 256, 8, 2, 128, 0, seed=3)
