@@ -12,8 +12,9 @@ constexpr int kW16Bytes = kBM * kBK * 2;  // fp16 weight tile per k-block (16 KB
 // column groups), converter groups of four warps taking turns over k-blocks, one MMA warp,
 // two weight-TMA warps, two token-TMA warps. The gate/up GEMM (32 k-blocks per item, light
 // epilogue) runs two converter groups and 8 epilogue warps; the down GEMM (8 k-blocks per
-// item, an epilogue that writes w * d for every row) one converter group and 16 epilogue
-// warps, so that its epilogue keeps up with its mainloop.
+// item, an epilogue that writes w * d for every row) two converter groups and 12 epilogue
+// warps, so that its epilogue keeps up with its mainloop (the register file caps a block of
+// 25 warps at 72 registers a thread).
 constexpr int kConvWarps = 4;  // one converter group: one thread per weight row
 #ifndef MOE_GU_EPI_WARPS
 #define MOE_GU_EPI_WARPS 8
@@ -22,10 +23,10 @@ constexpr int kConvWarps = 4;  // one converter group: one thread per weight row
 #define MOE_GU_CONV_GROUPS 2
 #endif
 #ifndef MOE_D_EPI_WARPS
-#define MOE_D_EPI_WARPS 16
+#define MOE_D_EPI_WARPS 12
 #endif
 #ifndef MOE_D_CONV_GROUPS
-#define MOE_D_CONV_GROUPS 1
+#define MOE_D_CONV_GROUPS 2
 #endif
 template <bool GU>
 struct GemmRoles {
@@ -165,15 +166,22 @@ __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nc
   const int o = wi.w + q * 32 + lane;
   const float sdo = (shared ? a.sh_s_d : a.s_d + (size_t)wi.x * a.H)[o];
   const int ncols = wi.z;
+  const int last = wi.y + ncols - 1;
   epilogue_columns<GemmRoles<false>::kColGroups>(a, nch, tbase, cg, ncols,
                                                  [&](const int (&v)[16], int c0) {
+    // One load per lane before any store of the chunk (the stores might alias the scales as
+    // far as the compiler knows): lanes 0-15 hold the rows' h scales, lanes 16-31 their
+    // routing weights; each column takes its two by shuffle.
+    const int lrow = min(wi.y + c0 + (lane & 15), last);
+    const float lv = lane < 16 ? a.s_h[lrow] : a.row_w[lrow];
+    float* dst = a.yd + (size_t)(wi.y + c0) * a.H + o;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int col = c0 + i;
-      if (col < ncols) {
-        const int row = wi.y + col;
-        a.yd[(size_t)row * a.H + o] = __fmul_rn(a.row_w[row], dequant(v[i], a.s_h[row], sdo));
-        if (a.tap) a.tap[(size_t)row * a.H + o] = v[i];
+      const float shr = __shfl_sync(0xffffffffu, lv, i);
+      const float wr = __shfl_sync(0xffffffffu, lv, 16 + i);
+      if (c0 + i < ncols) {
+        dst[(size_t)i * a.H] = __fmul_rn(wr, dequant(v[i], shr, sdo));
+        if (a.tap) a.tap[(size_t)(wi.y + c0 + i) * a.H + o] = v[i];
       }
     }
   });
