@@ -36,7 +36,7 @@ METRIC = "MoE layer tokens/s (prefill) & µs/layer decode C=8; % int8/HBM roofli
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up GEMM launch on the
 # stacked-prefill layer (T=2600), from one ncu capture of the kernel as it is now. Set to None
 # whenever the kernel changes, until it is captured again.
-GU_TRAFFIC_BYTES = None
+GU_TRAFFIC_BYTES = 404.7e6  # 367.4 MB read + 37.2 MB written (ncu, commit 1c2e286)
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 

@@ -426,76 +426,105 @@ cudaError_t launch_combine(const float* yd, const int* slot_row, int T, int k, i
 }
 
 // Per-row requantisation of h = SiLU(gate)*up: s = amax/127, q = rne(h/s) (|q| <= 127),
-// written as fp16 integers for the down GEMM's token operand. One warp per row.
-__global__ void requant_kernel(const float* __restrict__ h32, int R, int T_sh, int I, int Is,
-                               int Imax, __half* __restrict__ hq, float* __restrict__ sh,
-                               int* __restrict__ sq_max) {
+// written as fp16 integers for the down GEMM's token operand, and the running maximum of the
+// rows' sums of squared codes (the down GEMM's exactness bound).
+
+// Codes of one row of n values held in registers (lane owns values lane*4 + 128j .. +3).
+template <int kRegV>
+__device__ __forceinline__ float requant_row_regs(const float4 (&v)[kRegV], int n, int lane,
+                                                  __half* __restrict__ q, int& sq) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kRegV; ++j)
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+  amax = warp_max(amax);
+  const float s = __fdiv_rn(amax, 127.0f);
+  const float rs = quant_recip(s);
+#pragma unroll
+  for (int j = 0; j < kRegV; ++j) {
+    const int i = lane * 4 + j * 128;
+    if (i >= n) break;
+    int c[4] = {0, 0, 0, 0};
+    if (s > 0.0f) {
+      c[0] = quant_code(v[j].x, s, rs);
+      c[1] = quant_code(v[j].y, s, rs);
+      c[2] = quant_code(v[j].z, s, rs);
+      c[3] = quant_code(v[j].w, s, rs);
+    }
+    sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
+    *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));
+    *reinterpret_cast<__half2*>(q + i + 2) = __halves2half2(__int2half_rn(c[2]), __int2half_rn(c[3]));
+  }
+  return s;
+}
+
+// The same for a row too long for the registers: two passes over global memory.
+__device__ __forceinline__ float requant_row_loop(const float* __restrict__ h, int n, int lane,
+                                                  __half* __restrict__ q, int& sq) {
+  float amax = 0.0f;
+  for (int i = lane * 4; i < n; i += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(h + i);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  amax = warp_max(amax);
+  const float s = __fdiv_rn(amax, 127.0f);
+  const float rs = quant_recip(s);
+  for (int i = lane * 4; i < n; i += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(h + i);
+    int c[4] = {0, 0, 0, 0};
+    if (s > 0.0f) {
+      c[0] = quant_code(v.x, s, rs);
+      c[1] = quant_code(v.y, s, rs);
+      c[2] = quant_code(v.z, s, rs);
+      c[3] = quant_code(v.w, s, rs);
+    }
+    sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
+    *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));
+    *reinterpret_cast<__half2*>(q + i + 2) = __halves2half2(__int2half_rn(c[2]), __int2half_rn(c[3]));
+  }
+  return s;
+}
+
+// Each warp takes kRows consecutive rows and issues the loads of all of them before reducing
+// any (more bytes in flight per warp); rows of up to 128 * kRegV values stay in registers.
+constexpr int kRequantRows = 2;
+constexpr int kRequantThreads = 512;
+
+template <int kRegV>
+__global__ void __launch_bounds__(kRequantThreads) requant_kernel(
+    const float* __restrict__ h32, int R, int T_sh, int I, int Is, int Imax,
+    __half* __restrict__ hq, float* __restrict__ sh, int* __restrict__ sq_max) {
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
-  constexpr int kRegV = 8;  // float4 per lane held in registers: rows up to 1024 values
   __shared__ int s_sq[32];
-  const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const int row0 = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * kRequantRows;
   int sq = 0;
-  if (row < R) {
-    const int n = row < T_sh ? Is : I;
+  float4 v[kRequantRows][kRegV];
+  int n[kRequantRows];
+#pragma unroll
+  for (int r = 0; r < kRequantRows; ++r) {
+    const int row = row0 + r;
+    n[r] = row < R ? (row < T_sh ? Is : I) : 0;
+    const bool regs = n[r] <= 128 * kRegV;
     const float* h = h32 + (size_t)row * Imax;
-    __half* q = hq + (size_t)row * Imax;
-    if (n <= 128 * kRegV) {
-      float4 v[kRegV];
 #pragma unroll
-      for (int j = 0; j < kRegV; ++j)
-        v[j] = lane * 4 + j * 128 < n ? *reinterpret_cast<const float4*>(h + lane * 4 + j * 128)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-      float amax = 0.0f;
-#pragma unroll
-      for (int j = 0; j < kRegV; ++j)
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
-      amax = warp_max(amax);
-      const float s = __fdiv_rn(amax, 127.0f);
-      const float rs = quant_recip(s);
-#pragma unroll
-      for (int j = 0; j < kRegV; ++j) {
-        const int i = lane * 4 + j * 128;
-        if (i >= n) break;
-        int c[4] = {0, 0, 0, 0};
-        if (s > 0.0f) {
-          c[0] = quant_code(v[j].x, s, rs);
-          c[1] = quant_code(v[j].y, s, rs);
-          c[2] = quant_code(v[j].z, s, rs);
-          c[3] = quant_code(v[j].w, s, rs);
-        }
-        sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
-        *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));
-        *reinterpret_cast<__half2*>(q + i + 2) = __halves2half2(__int2half_rn(c[2]), __int2half_rn(c[3]));
-      }
-      if (lane == 0) sh[row] = s;
-    } else {
-      float amax = 0.0f;
-      for (int i = lane * 4; i < n; i += 128) {
-        const float4 v = *reinterpret_cast<const float4*>(h + i);
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-      }
-      amax = warp_max(amax);
-      const float s = __fdiv_rn(amax, 127.0f);
-      const float rs = quant_recip(s);
-      for (int i = lane * 4; i < n; i += 128) {
-        const float4 v = *reinterpret_cast<const float4*>(h + i);
-        int c[4] = {0, 0, 0, 0};
-        if (s > 0.0f) {
-          c[0] = quant_code(v.x, s, rs);
-          c[1] = quant_code(v.y, s, rs);
-          c[2] = quant_code(v.z, s, rs);
-          c[3] = quant_code(v.w, s, rs);
-        }
-        sq += c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3];
-        *reinterpret_cast<__half2*>(q + i) = __halves2half2(__int2half_rn(c[0]), __int2half_rn(c[1]));
-        *reinterpret_cast<__half2*>(q + i + 2) = __halves2half2(__int2half_rn(c[2]), __int2half_rn(c[3]));
-      }
-      if (lane == 0) sh[row] = s;
-    }
-    sq = warp_sum_i(sq);
+    for (int j = 0; j < kRegV; ++j)
+      v[r][j] = regs && lane * 4 + j * 128 < n[r]
+                    ? *reinterpret_cast<const float4*>(h + lane * 4 + j * 128)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+#pragma unroll
+  for (int r = 0; r < kRequantRows; ++r) {
+    const int row = row0 + r;
+    if (row >= R) break;  // uniform over the warp
+    __half* q = hq + (size_t)row * Imax;
+    const float s = n[r] <= 128 * kRegV
+                        ? requant_row_regs<kRegV>(v[r], n[r], lane, q, sq)
+                        : requant_row_loop(h32 + (size_t)row * Imax, n[r], lane, q, sq);
+    if (lane == 0) sh[row] = s;
+  }
+  sq = warp_sum_i(sq);
   if (lane == 0) s_sq[threadIdx.x / 32] = sq;
   __syncthreads();
   // one guarded atomic per block: most blocks do not raise the running maximum
@@ -509,9 +538,11 @@ __global__ void requant_kernel(const float* __restrict__ h32, int R, int T_sh, i
 cudaError_t launch_requant(const float* h32, int R, int T_sh, int I, int Is, int Imax,
                            __half* hq, float* sh, int* sq_max, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
-  const int rows_per_blk = 16;
-  return launch_pdl(requant_kernel, dim3((R + rows_per_blk - 1) / rows_per_blk),
-                    dim3(32 * rows_per_blk), 0, s, h32, R, T_sh, I, Is, Imax, hq, sh, sq_max);
+  const int rows_per_blk = (kRequantThreads / 32) * kRequantRows;
+  const dim3 grid((R + rows_per_blk - 1) / rows_per_blk), block(kRequantThreads);
+  if (Imax <= 512)
+    return launch_pdl(requant_kernel<4>, grid, block, 0, s, h32, R, T_sh, I, Is, Imax, hq, sh, sq_max);
+  return launch_pdl(requant_kernel<8>, grid, block, 0, s, h32, R, T_sh, I, Is, Imax, hq, sh, sq_max);
 }
 
 }  // namespace moe
