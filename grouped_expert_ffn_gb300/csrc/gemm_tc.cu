@@ -87,7 +87,8 @@ constexpr int kGemmSmem = kOffBar + kBarBytes + 1024;
 static_assert((2 * kXStages + 2 * kWStages + kConvBufs + 5) * 8 + 8 <= kBarBytes, "barriers");
 static_assert(kGemmSmem <= 232448, "shared memory");
 static_assert(kOffW8 % 1024 == 0 && kOffConv % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
-static_assert(kXStages % 2 == 0 && kWStages % 2 == 0, "two producers per ring own alternate stages");
+// Two producers per ring: stage s belongs to producer s % 2 (any stage count >= 2 works).
+static_assert(kXStages >= 2 && kWStages >= 2, "two producers per ring");
 
 
 

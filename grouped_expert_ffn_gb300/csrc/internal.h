@@ -11,7 +11,11 @@
 namespace moe {
 
 constexpr int kBM = 128;        // tensor-core tile rows (weight rows: the MMA's M)
-constexpr int kMaxTokTile = 256;  // token rows per tile (the MMA's N), at most
+#ifndef MOE_MAX_TOK_TILE
+#define MOE_MAX_TOK_TILE 256
+#endif
+constexpr int kMaxTokTile = MOE_MAX_TOK_TILE;  // token rows per tile (the MMA's N), at most
+static_assert(kMaxTokTile % 32 == 0 && kMaxTokTile <= 256, "token tile");
 // Token-tile TMA boxes: one tensor map per box height over the same token-row operand, so
 // that the token tile of a k-block is one TMA load. Heights are multiples of kXStep1 (16)
 // rows up to 256 for the one-CTA kernel, and of kXStep2 (8) rows up to 128 for the CTA pair
