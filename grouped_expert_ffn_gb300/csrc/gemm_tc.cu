@@ -73,22 +73,32 @@ namespace moe {
 #define MOE_W_STAGES 4
 #endif
 #ifndef MOE_X_STAGES
-#define MOE_X_STAGES 4
+#define MOE_X_STAGES 4  // token stages of the gate/up GEMM
+#endif
+#ifndef MOE_D_X_STAGES
+#define MOE_D_X_STAGES 4  // token stages of the down GEMM
 #endif
 constexpr int kXBytesMax = kMaxTokTile * kBK * 2;    // fp16 token tile per stage (<= 32 KB)
-constexpr int kXStages = MOE_X_STAGES;
-constexpr int kWStages = MOE_W_STAGES;
-constexpr int kConvBufs = kXStages;  // fp16 weight buffer s goes with token stage s
-constexpr int kOffW8 = kXStages * kXBytesMax;
-constexpr int kOffConv = kOffW8 + kWStages * kW8Bytes;
-constexpr int kOffBar = kOffConv + kConvBufs * kW16Bytes;
-constexpr int kBarBytes = 512;
-constexpr int kGemmSmem = kOffBar + kBarBytes + 1024;
-static_assert((2 * kXStages + 2 * kWStages + kConvBufs + 5) * 8 + 8 <= kBarBytes, "barriers");
-static_assert(kGemmSmem <= 232448, "shared memory");
-static_assert(kOffW8 % 1024 == 0 && kOffConv % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
-// Two producers per ring: stage s belongs to producer s % 2 (any stage count >= 2 works).
-static_assert(kXStages >= 2 && kWStages >= 2, "two producers per ring");
+
+// Shared-memory layout of one GEMM instance: token stages, int8 weight stages, fp16 weight
+// buffers (buffer s goes with token stage s), barriers.
+template <bool GU>
+struct GemmSmem {
+  static constexpr int kXStages = GU ? MOE_X_STAGES : MOE_D_X_STAGES;
+  static constexpr int kWStages = MOE_W_STAGES;
+  static constexpr int kConvBufs = kXStages;
+  static constexpr int kOffW8 = kXStages * kXBytesMax;
+  static constexpr int kOffConv = kOffW8 + kWStages * kW8Bytes;
+  static constexpr int kOffBar = kOffConv + kConvBufs * kW16Bytes;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kBytes = kOffBar + kBarBytes + 1024;
+  static_assert((2 * kXStages + 2 * kWStages + kConvBufs + 5) * 8 + 8 <= kBarBytes, "barriers");
+  static_assert(kBytes <= 232448, "shared memory");
+  static_assert(kOffW8 % 1024 == 0 && kOffConv % 1024 == 0,
+                "swizzled tiles stay 1024-byte aligned");
+  // Two producers per ring: stage s belongs to producer s % 2 (any stage count >= 2 works).
+  static_assert(kXStages >= 2 && kWStages >= 2, "two producers per ring");
+};
 
 
 
@@ -97,6 +107,10 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ XMaps tmX,
                         const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmWs) {
+  constexpr int kXStages = GemmSmem<GU>::kXStages, kWStages = GemmSmem<GU>::kWStages;
+  constexpr int kConvBufs = GemmSmem<GU>::kConvBufs;
+  constexpr int kOffW8 = GemmSmem<GU>::kOffW8, kOffConv = GemmSmem<GU>::kOffConv;
+  constexpr int kOffBar = GemmSmem<GU>::kOffBar;
   using R = GemmRoles<GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -358,10 +372,10 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
 
 cudaError_t gemm_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem<true>::kBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem<false>::kBytes);
   if (e == cudaSuccess) e = pair_set_attributes();
   return e;
 }
@@ -374,7 +388,8 @@ cudaError_t gemm_max_clusters(bool gate_up, int cs, int* n) {
   int per_sm = 0, dev = 0, sms = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &per_sm, gate_up ? (const void*)grouped_gemm_kernel<true> : (const void*)grouped_gemm_kernel<false>,
-      gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads, kGemmSmem);
+      gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads,
+      gate_up ? GemmSmem<true>::kBytes : GemmSmem<false>::kBytes);
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   *n = per_sm * sms;
@@ -390,9 +405,9 @@ cudaError_t launch_grouped_gemm(bool gate_up, int cs, const GemmArgs& a, const X
   if (cs != 1) return cudaErrorInvalidValue;
   if (gate_up)
     return launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(GemmRoles<true>::kThreads),
-                      kGemmSmem, s, a, tmX, tmW, tmWs);
+                      GemmSmem<true>::kBytes, s, a, tmX, tmW, tmWs);
   return launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(GemmRoles<false>::kThreads),
-                    kGemmSmem, s, a, tmX, tmW, tmWs);
+                    GemmSmem<false>::kBytes, s, a, tmX, tmW, tmWs);
 }
 
 // y[t] = sum over slots j of yd[row(t, j)] + yd[t] (shared expert row), in slot order. Block per
