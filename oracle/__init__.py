@@ -30,9 +30,12 @@ class _Taps(C.Structure):
 
 
 def lib():
+    """The oracle's shared library: built from moe_oracle.cpp, or the build named by the
+    environment variable MOE_ORACLE_LIB (the mutation test loads deliberately broken copies
+    that way)."""
     global _lib
     if _lib is None:
-        _lib = C.CDLL(build())
+        _lib = C.CDLL(os.environ.get("MOE_ORACLE_LIB") or build())
         for name in ("oracle_route", "oracle_quant_rows", "oracle_permute", "oracle_forward",
                      "oracle_dense", "oracle_router_logits", "oracle_rmsnorm_residual"):
             getattr(_lib, name).restype = C.c_int

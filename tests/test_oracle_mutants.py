@@ -1,0 +1,83 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each mutant is a copy of the oracle with one planted mistake (a wrong constant, rounding
+rule, sign, index, operand or dropped term). It is built on the CPU into a temporary
+directory and the pin suite (test_oracle_pins.py) runs against it in a subprocess; every
+mutant must make at least one pin fail. Nothing here touches a GPU or the library.
+"""
+import importlib
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+oracle_build = importlib.import_module("oracle.build")  # the module (the package re-exports its function)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
+
+# (name, original text, planted mistake); the original occurs exactly once in the source.
+MUTANTS = [
+    ("quant_scale_128", "const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),
+    ("quant_ties_away", "std::nearbyint(v[i] / s)", "std::round(v[i] / s)"),
+    ("quant_amax_no_abs", "amax = std::max(amax, std::fabs(v[i]));", "amax = std::max(amax, v[i]);"),
+    ("quant_clamp_126", "if (r > 127.0f) r = 127.0f;", "if (r > 126.0f) r = 126.0f;"),
+    ("route_ties_to_highest_id", "(best < 0 || l[e] > l[best])", "(best < 0 || l[e] >= l[best])"),
+    ("route_unnormalised", "static_cast<float>(ex[j] / z)", "static_cast<float>(ex[j])"),
+    ("gate_without_token_scale", "const float g = (static_cast<float>(ag) * sx) * sg[i];",
+     "const float g = static_cast<float>(ag) * sg[i];"),
+    ("up_with_gate_scale", "const float u = (static_cast<float>(au) * sx) * su[i];",
+     "const float u = (static_cast<float>(au) * sx) * sg[i];"),
+    ("silu_sign", "g / (1.0f + std::exp(-g))", "g / (1.0f + std::exp(g))"),
+    ("gate_up_swapped", "const float silu = g / (1.0f + std::exp(-g));\n    h[i] = silu * u;",
+     "const float silu = u / (1.0f + std::exp(-u));\n    h[i] = silu * g;"),
+    ("gate_weight_transposed", "Wg[(size_t)i * H + c]", "Wg[(size_t)c * I + i]"),
+    ("down_weight_transposed", "Wd[(size_t)o * I + i]", "Wd[(size_t)i * H + o]"),
+    ("down_without_h_scale", "d[o] = (static_cast<float>(ad) * sh) * sd[o];",
+     "d[o] = static_cast<float>(ad) * sd[o];"),
+    ("combine_ignores_route_weights",
+     "const double wt = shared ? 1.0 : static_cast<double>(w[(size_t)t * k + s]);",
+     "const double wt = 1.0;"),
+    ("shared_expert_dropped", "const int S = k + (Is > 0 ? 1 : 0);", "const int S = k;"),
+    ("permute_unstable_within_expert",
+     "for (long r = 0; r < R; ++r)\n      if (idx[r] == e) perm[pos++] = (int32_t)r;",
+     "for (long r = R - 1; r >= 0; --r)\n      if (idx[r] == e) perm[pos++] = (int32_t)r;"),
+    ("rmsnorm_sample_variance", "std::sqrt(ss / H + 1e-6)", "std::sqrt(ss / (H - 1) + 1e-6)"),
+    ("residual_ignored",
+     "bf16_to_float(xr[h]) + static_cast<float>(y[(size_t)t * H + h])", "bf16_to_float(xr[h])"),
+    ("bf16_ties_away", "u += 0x7fffu + ((u >> 16) & 1u);", "u += 0x8000u;"),
+    ("router_weight_transposed", "Wr[(size_t)h * E + e]", "Wr[(size_t)e * H + h]"),
+]
+
+
+def _run_mutant(tmp, name, old, new):
+    src = open(oracle_build.SRC).read()
+    assert src.count(old) == 1, (name, src.count(old))
+    d = os.path.join(tmp, name)
+    os.makedirs(d, exist_ok=True)
+    cpp = os.path.join(d, "moe_oracle.cpp")
+    so = os.path.join(d, "libmoe_oracle.so")
+    with open(cpp, "w") as f:
+        f.write(src.replace(old, new))
+    subprocess.run(["g++", *oracle_build.FLAGS, cpp, "-o", so], check=True)
+    env = dict(os.environ, MOE_ORACLE_LIB=so)
+    r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-x", "-q", "-p", "no:cacheprovider"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return name, r.returncode, r.stdout[-600:]
+
+
+def test_every_mutant_fails_a_pin(tmp_path):
+    workers = max(1, min(8, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 4))
+    with ThreadPoolExecutor(workers) as ex:
+        results = list(ex.map(lambda m: _run_mutant(str(tmp_path), *m), MUTANTS))
+    survivors = [(n, out) for n, rc, out in results if rc == 0]
+    assert not survivors, "mutants not caught by any pin: " + ", ".join(n for n, _ in survivors)
+    # a caught mutant fails a test (rc 1) or crashes the run; it must not break collection
+    for n, rc, out in results:
+        assert rc == 1 or rc < 0, (n, rc, out)
+
+
+def test_unmutated_oracle_passes_the_pins():
+    r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-q", "-p", "no:cacheprovider"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-600:]

@@ -387,3 +387,23 @@ def test_residual_is_fp32_add_rounded_to_bf16():
     assert (torch.from_numpy(x2.view(np.int16)) == ref.view(torch.int16)).all()
     _, x_in2 = oracle.rmsnorm_residual(x2)
     assert (x_in == x_in2).all()
+
+
+def test_residual_rounding_ties_go_to_even():
+    # x + y landing exactly halfway between two bf16 neighbours rounds to the even one
+    # (bf16 spacing is 2^-7 on [1, 2), 2^-6 on [2, 4), 2^-9 on [0.5, 1)); just above the
+    # halfway point rounds up. Expected values worked by hand.
+    cases = [  # (x, y, x + y rounded to bf16)
+        (1.0, 2.0 ** -8, 1.0),
+        (1.0078125, 2.0 ** -8, 1.015625),
+        (-1.0, -(2.0 ** -8), -1.0),
+        (-1.0078125, -(2.0 ** -8), -1.015625),
+        (2.0, 2.0 ** -7, 2.0),
+        (3.0, 2.0 ** -7, 3.0),
+        (0.5, 2.0 ** -10, 0.5),
+        (1.0, 2.0 ** -8 + 2.0 ** -20, 1.0078125),
+    ]
+    x = bf16_bits([[c[0] for c in cases]])
+    y = np.array([[c[1] for c in cases]], np.float64)
+    x2, _ = oracle.rmsnorm_residual(x, y)
+    assert _bf16_to_f32(x2).numpy()[0].tolist() == [c[2] for c in cases]
