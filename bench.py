@@ -57,8 +57,12 @@ def dist_init(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
-        torch.cuda.set_device(local)
-        torch.distributed.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            torch.distributed.init_process_group("nccl")
+        else:
+            # host-only runs (the tests of this plumbing): the same path over gloo
+            torch.distributed.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank
@@ -72,9 +76,16 @@ def barrier(world):
 def max_over_ranks(v, world):
     if world == 1:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return t.item()
+
+
+def replica_throughput(units_per_step, world, ms_step):
+    """Whole-job rate of `world` independent replicas (weak scaling): every rank processes
+    units_per_step per step, and the step takes the slowest rank's time ms_step."""
+    return units_per_step * world / (ms_step / 1e3)
 
 
 # ---------------------------------------------------------------- clocks
@@ -296,7 +307,7 @@ def run_ours(args, world, rank):
     assert moe.moe_get_error(plan) == 0
     ms_step = ms_total / args.steps
     layer_tokens = T * n_layers
-    value = layer_tokens * world / (ms_step / 1e3)
+    value = replica_throughput(layer_tokens, world, ms_step)
 
     # roofline of the dominant kernel (gate/up GEMM): 2*R*2I*H flops per launch
     R = T * k + T
@@ -329,7 +340,7 @@ def run_ours(args, world, rank):
         e1.record(stream)
         torch.cuda.synchronize()
         ms_e2e = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
-        e2e_value = layer_tokens * world / (ms_e2e / 1e3)
+        e2e_value = replica_throughput(layer_tokens, world, ms_e2e)
 
         e2e = {"value": e2e_value, "unit": "MoE-layer tokens/s",
                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2}
@@ -368,7 +379,7 @@ def run_ours(args, world, rank):
                    "l2": "inputs larger than L2 (each layer's weights > 129 MB)"},
         "per_layer_us": ms_step * 1e3 / n_layers,
         "moe_layer_us": moe_ms * 1e3,
-        "stack_prompt_tokens_per_s": T * world / (ms_step / 1e3),
+        "stack_prompt_tokens_per_s": replica_throughput(T, world, ms_step),
         "stage_us": {"permute_quant": stage_ms[0] * 1e3, "gate_up_gemm": stage_ms[1] * 1e3,
                      "requant": stage_ms[2] * 1e3, "down_gemm_combine": stage_ms[3] * 1e3},
         "roofline": {"bound": "tensor", "kernel": "grouped gate/up GEMM (tcgen05 kind::f16)",
