@@ -59,6 +59,7 @@ def lib() -> C.CDLL:
             "moe_forward": ([vp, vp, vp, i32, vp, vp, vp, vp], i32),
             "moe_get_error": ([vp], i32),
             "moe_clear_error": ([vp], i32),
+            "moe_selftest_wait_timeout": ([vp, vp], i32),
             "moe_status_string": ([i32], C.c_char_p),
             "moe_debug_enable": ([vp, i32], i32),
             "moe_debug_tap_bytes": ([vp, i32], sz),
@@ -165,6 +166,11 @@ def moe_get_error(plan: int) -> int:
 
 def moe_clear_error(plan: int):
     _check(lib().moe_clear_error(plan), "moe_clear_error")
+
+
+def moe_selftest_wait_timeout(plan: int, stream=None):
+    """Queue the bounded-wait self-test: the plan's error word becomes MOE_ERR_TIMEOUT."""
+    _check(lib().moe_selftest_wait_timeout(plan, _stream(stream)), "moe_selftest_wait_timeout")
 
 
 def moe_debug_enable(plan: int, on: bool = True):

@@ -274,4 +274,24 @@ cudaError_t launch_residual(uint16_t* x, const float* y, size_t n, cudaStream_t 
   return launch_pdl(residual_kernel, dim3(1216), dim3(256), 0, s, x, y, n);
 }
 
+// Self-test of the bounded waits: one thread waits, with the kernels' own bounded wait, on
+// an mbarrier that nothing ever arrives on. The wait gives up after its time limit and
+// records MOE_ERR_TIMEOUT in `err`; nothing is in flight when the kernel returns.
+__global__ void selftest_wait_kernel(int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, err);
+}
+
+cudaError_t launch_selftest_wait(int* err, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(err);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -157,6 +157,7 @@ cudaError_t launch_row_sq_max(const int8_t* w, size_t rows, int cols, int* out, 
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, int T, int H, int E,
                                  float* out, cudaStream_t s);
 cudaError_t launch_residual(uint16_t* x, const float* y, size_t n, cudaStream_t s);
+cudaError_t launch_selftest_wait(int* err, cudaStream_t s);
 cudaError_t launch_router_pack(const float* w, int H, int E, uint16_t* packed, cudaStream_t s);
 cudaError_t launch_router_tc(int T, int H, int E, float* out, const CUtensorMap& tmA,
                              const CUtensorMap& tmB, cudaStream_t s);

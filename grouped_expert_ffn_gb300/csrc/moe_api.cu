@@ -646,6 +646,11 @@ moe_status moe_clear_error(moe_plan_t p) {
   return cudaMemset(p->err, 0, sizeof(int)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status moe_selftest_wait_timeout(moe_plan_t p, void* stream) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_selftest_wait(p->err, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_debug_enable(moe_plan_t p, int on) {
   if (!p) return MOE_ERR_INVALID_ARG;
   if (on && !p->tap_gu) {

@@ -122,6 +122,12 @@ MOE_API moe_status moe_forward(moe_plan_t plan, moe_packed_t packed, const uint1
 MOE_API moe_status moe_get_error(moe_plan_t plan);
 /* Clear the sticky error word (synchronises the device). */
 MOE_API moe_status moe_clear_error(moe_plan_t plan);
+/* Self-test of device-side failure detection: queues on `stream` one kernel whose single
+ * thread waits, with the library's bounded wait, on a barrier that nothing completes. After
+ * the wait's time limit (2 s) it gives up and sets the plan's sticky error word to
+ * MOE_ERR_TIMEOUT; the context stays usable (moe_clear_error, then any other call). Returns
+ * MOE_ERR_INVALID_ARG for a NULL plan, MOE_ERR_CUDA if the launch fails. Asynchronous. */
+MOE_API moe_status moe_selftest_wait_timeout(moe_plan_t plan, void* stream);
 
 /* Short static description of a status code. */
 MOE_API const char* moe_status_string(moe_status s);

@@ -224,6 +224,26 @@ def test_out_of_range_expert_sets_device_error():
         lay.close()
 
 
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    # Failure detection without a fault: a wait on a barrier that nothing completes gives up
+    # after its limit and sets the plan's sticky MOE_ERR_TIMEOUT; the host reads it, clears
+    # it, and the same plan then computes a full layer correctly.
+    wl, d = _host_layer("tiny")
+    sh = wl.shape
+    W = weights_to(d["weights"], "cuda")
+    lay = moe.MoELayer(sh.E, sh.k, sh.H, sh.I, sh.Is, sh.T, W)
+    try:
+        assert moe.moe_get_error(lay.plan) == 0
+        moe.moe_selftest_wait_timeout(lay.plan)
+        assert moe.moe_get_error(lay.plan) == moe.MOE_ERR_TIMEOUT
+        assert moe.moe_get_error(lay.plan) == moe.MOE_ERR_TIMEOUT  # sticky
+        moe.moe_clear_error(lay.plan)
+        assert moe.moe_get_error(lay.plan) == 0
+        check_layer(sh, d["x"], d["logits"], W, oracle_layer(d["weights"], sh), layer=lay)
+    finally:
+        lay.close()
+
+
 def test_residual_add():
     x = synth.make_activations(37, 256, 5)
     y = torch.randn(37, 256, generator=torch.Generator().manual_seed(1))
