@@ -1,8 +1,9 @@
 // Grouped W8A8 GEMMs of the prefill path on the 5th-generation tensor cores (tcgen05).
 //
 // One persistent kernel runs every (expert group, 128-row weight tile, token tile) work item
-// of a layer: the gate/up GEMM with a fused SiLU(gate)*up epilogue, or the down GEMM with a
-// fused router-weighted scatter-combine into y. This is the concatenated-expert computation
+// of a layer: the gate/up GEMM with a fused SiLU(gate)*up epilogue, or the down GEMM whose
+// epilogue writes every row's router-weighted output (combine_kernel then sums each token's
+// rows). This is the concatenated-expert computation
 // of the page "Qwen3.6-35B-A3B Linux v1.0.4: ~2.7s fixed per-request TTFT ...", section
 // "The fix (concatenated-expert dispatch)": one launch per operator and layer instead of one
 // per expert, with gate and up concatenated along the weight dimension.
@@ -19,8 +20,8 @@
 // 128-byte-swizzled tile the MMA reads. The widening is exact: byte v+128 becomes the fp16
 // bit pattern 0x6400|(v+128) = 1024 + v + 128, and subtracting 1152 leaves v. Token rows are
 // already fp16 integers (written by the permutation step / requantisation) and go straight
-// from TMA (64-row boxes, 128-byte swizzle) to the MMA: widening them in shared memory too
-// would triple the shared-memory traffic of a k-block (measured slower).
+// from TMA (one box per stage, 128-byte swizzle) to the MMA: widening them in shared memory
+// too would triple the shared-memory traffic of a k-block (measured slower).
 //
 // Exact integer products on an fp16 tensor pipe. sm_103a has no int8 tcgen05 MMA, so the
 // int8 operands are held as fp16 (every int8 value is an fp16 integer) and multiplied with
@@ -38,24 +39,24 @@
 // same two words). With one accumulator per tile, TMEM holds two of them (2 x TN columns)
 // so the epilogue of one tile overlaps the MMAs of the next.
 //
-// Clusters: the token tile of an item is the same for all of an expert's weight tiles, so CS
-// CTAs (CS = 1, 2 or 4, chosen per launch from the weight-tile counts) share it: each loads a
-// share of its 64-row boxes once and multicasts it to the cluster, which divides the token
-// operand's L2-to-SM traffic by CS.
+// The 2-SM form of the same items (one MMA of M = 256 over two CTAs, each holding half of the
+// token tile) is in gemm_pair.cu; a plan selects it per GEMM.
 //
 // Warp roles (one CTA per SM; GemmRoles in gemm_common.cuh): gate/up 672 threads, down 800.
-//   epilogue warps (8 for gate/up, 16 for down): warp w reads TMEM lanes 32*(w%4).. (weight
+//   epilogue warps (8 for gate/up, 12 for down): warp w reads TMEM lanes 32*(w%4).. (weight
 //               rows) and every (w/4)-th 16-column chunk (tokens) of its quadrant;
-//   converter groups of four warps (2 for gate/up, 1 for down) taking turns over k-blocks:
-//               thread r of a group widens weight row r;
+//   converter groups of four warps (2 for each GEMM) taking turns over k-blocks: thread r of
+//               a group widens weight row r;
 //   one MMA issuer and TMEM owner;
 //   two TMA producers of the int8 weight tiles (alternate stages);
 //   two TMA producers of the fp16 token tiles (alternate stages).
 // Pipeline: the weights stream from HBM through a ring of small int8 stages (4 x 8 KB,
 // released by the converters as soon as they have widened a stage); the token tiles, mostly
 // L2 hits, through a ring of large stages (4 x 32 KB), one TMA load per stage (box heights
-// 32..256 rows); one fp16 weight buffer per token stage, released together with it by the
-// MMA's commit. A TMA-issuing thread completes only a few loads per microsecond, so each ring
+// 16..256 rows); one fp16 weight buffer per token stage, released together with it by the
+// MMA's commit. A converter group widens its k-block as soon as the int8 tile and the fp16
+// buffer are free and waits for the token tile only afterwards, so the token load overlaps
+// the conversion. A TMA-issuing thread completes only a few loads per microsecond, so each ring
 // has two issuing threads and each token tile is one load rather than several 64-row ones.
 // Barrier arrivals are one per warp (after __syncwarp) and the MMA thread commits once per
 // k-block: every arrival and commit sits on the critical path of a k-block.
