@@ -5,13 +5,13 @@
 // "Batched decode doesn't scale" and "Next": expert dedup across rows plus int8 dot).
 //
 //  decode_prep_kernel  block 0: the unique-expert list (with the shared expert as group 0)
-//                      and the canonical row order; block 1 + t: token t's int8 quant (the
-//                      exact per-element divisions spread over T SMs) and y's row t zeroed.
+//                      and the canonical row order; block 1 + t: token t's int8 quant
+//                      (spread over T SMs) and y's row t zeroed.
 //  decode_gu_kernel    (16 channels of one unique expert) per block: streams 16 gate and 16
 //                      up rows, dp4a against the expert's <= 8 quantised token rows held in
 //                      shared memory; fused SiLU(gate)*up.
-//  requant_kernel      (shared with the prefill path) requantises every h row once, warp
-//                      per row, into fp16 codes and scales.
+//  requant_kernel      (shared with the prefill path) requantises every h row once, two
+//                      rows per warp, into fp16 codes and scales.
 //  decode_down_kernel  (64 output channels of one unique expert) per block: stages the
 //                      expert's h codes as int8 in shared memory, streams 64 down rows, dp4a,
 //                      and adds w * d into y.
