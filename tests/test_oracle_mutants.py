@@ -47,6 +47,20 @@ MUTANTS = [
      "bf16_to_float(xr[h]) + static_cast<float>(y[(size_t)t * H + h])", "bf16_to_float(xr[h])"),
     ("bf16_ties_away", "u += 0x7fffu + ((u >> 16) & 1u);", "u += 0x8000u;"),
     ("router_weight_transposed", "Wr[(size_t)h * E + e]", "Wr[(size_t)e * H + h]"),
+    ("quant_scale_by_reciprocal", "const float s = amax / 127.0f;",
+     "const float s = amax * (1.0f / 127.0f);"),
+    ("quant_multiply_by_reciprocal", "std::nearbyint(v[i] / s)", "std::nearbyint(v[i] * (1.0f / s))"),
+    ("route_repeats_best", "taken[best] = 1;", "taken[best] = 0;"),
+    ("route_skips_last_expert", "for (int e = 0; e < E; ++e)\n        if (!taken[e]",
+     "for (int e = 0; e < E - 1; ++e)\n        if (!taken[e]"),
+    ("gate_drops_last_term", "for (int c = 0; c < H; ++c) {\n      ag +=",
+     "for (int c = 0; c < H - 1; ++c) {\n      ag +="),
+    ("down_drops_last_term", "for (int i = 0; i < I; ++i)\n      ad +=",
+     "for (int i = 1; i < I; ++i)\n      ad +="),
+    ("rmsnorm_without_eps", "std::sqrt(ss / H + 1e-6)", "std::sqrt(ss / H)"),
+    ("router_float_accumulation", "double acc = 0.0;\n      for (int h = 0; h < H; ++h)",
+     "float acc = 0.0f;\n      for (int h = 0; h < H; ++h)"),
+    ("dense_drops_shared_expert", "if (Is > 0) {\n      expert_ffn", "if (Is < 0) {\n      expert_ffn"),
 ]
 
 
