@@ -110,7 +110,9 @@ MOE_API moe_status moe_route(moe_plan_t plan, const float* logits, int T, int32_
 
 /* The MoE layer: y fp32 [T, H] = sum_j w[t,j] * expert_{idx[t,j]}(x[t]) + shared(x[t]).
  *   x bf16 [T, H] (raw bf16 bits); idx, w as produced by moe_route (any valid top-k
- *   routing: idx[t,*] distinct, in [0, E)); y is overwritten.
+ *   routing: idx[t,*] distinct, in [0, E)); y is overwritten. 1 <= T <= max_tokens: an
+ *   empty batch (T = 0) is MOE_ERR_INVALID_ARG, a larger one MOE_ERR_CAPACITY, both
+ *   returned before any work is queued.
  * T <= 8 runs the deduplicated weight-streaming decode kernels; larger T runs the grouped
  * tensor-core GEMMs. Both give identical integer accumulators. Allocates nothing, never
  * synchronises, and may be captured in a CUDA graph. The workspace is per plan: calls on

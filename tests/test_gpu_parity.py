@@ -203,6 +203,12 @@ def test_capacity_and_argument_errors():
         st = moe.lib().moe_forward(lay.plan, lay.packed, x[:8].data_ptr(), 8, idx.data_ptr(),
                                    w.data_ptr(), yb.data_ptr(), None)
         assert st == moe.MOE_ERR_INVALID_ARG
+        # empty batch: refused on the host, nothing queued, no sticky error
+        st = moe.lib().moe_route(lay.plan, lg.data_ptr(), 0, idx.data_ptr(), w.data_ptr(), None)
+        assert st == moe.MOE_ERR_INVALID_ARG
+        st = moe.lib().moe_forward(lay.plan, lay.packed, x.data_ptr(), 0, idx.data_ptr(),
+                                   w.data_ptr(), y.data_ptr(), None)
+        assert st == moe.MOE_ERR_INVALID_ARG
         assert moe.moe_get_error(lay.plan) == 0
     finally:
         lay.close()
