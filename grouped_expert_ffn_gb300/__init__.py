@@ -99,10 +99,17 @@ def _check(st: int, where: str):
 
 
 def _ptr(t):
+    """Device address of a tensor argument (None and raw integer addresses pass through).
+    The kernels read row-major contiguous device memory, so a strided view or a host tensor
+    is refused here instead of being read with the wrong layout or from the wrong memory."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError(f"tensor argument of shape {tuple(t.shape)} is not contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"tensor argument of shape {tuple(t.shape)} is on {t.device}, not CUDA")
     return t.data_ptr()
 
 

@@ -69,3 +69,17 @@ def test_null_handles_rejected(lib):
     # misaligned pointers are rejected before any launch
     assert lib.moe_router_logits(16 + 2, 32, 4, 64, 8, 64, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_residual_add(18, 32, 4, 64, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_binding_refuses_host_and_strided_tensors(lib):
+    import torch
+    import grouped_expert_ffn_gb300 as moe
+    lg = torch.zeros((4, 8), dtype=torch.float32)
+    idx = torch.zeros((4, 2), dtype=torch.int32)
+    w = torch.zeros((4, 2), dtype=torch.float32)
+    with pytest.raises(ValueError, match="not CUDA"):
+        moe.moe_route(1, lg, idx, w, stream=0)
+    with pytest.raises(ValueError, match="not contiguous"):
+        moe.moe_route(1, torch.zeros((8, 4)).t(), idx, w, stream=0)
+    with pytest.raises(ValueError, match="not CUDA"):
+        moe.moe_residual_add(torch.zeros((2, 8), dtype=torch.bfloat16), torch.zeros((2, 8)), stream=0)
