@@ -37,6 +37,9 @@ METRIC = "MoE layer tokens/s (prefill) & µs/layer decode C=8; % int8/HBM roofli
 # stacked-prefill layer (T=2600), from one ncu capture of the kernel as it is now. Set to None
 # whenever the kernel changes, until it is captured again.
 GU_TRAFFIC_BYTES = 404.7e6  # 367.4 MB read + 37.2 MB written (ncu, commit 1c2e286)
+# Kernels one stacked-prefill layer launches: RMS pre-norm, router projection, routing, and
+# the forward's histogram, scan, scatter, gate/up GEMM, requantisation, down GEMM, combine.
+LAUNCHES_PER_LAYER = 10
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -242,6 +245,90 @@ def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
             "kernel_gbs": uniq_bytes / (kern_us * 1e-6) / 1e9 if kern_us > 0 else None}
 
 
+def layer_work(sh, counts=None):
+    """(int-ops of the layer, weight bytes the layer touches) for routing counts `counts`
+    (experts with no row touch no bytes); 2*M*N*K over routed rows plus the shared expert."""
+    R = sh.T * sh.k
+    ops = 2.0 * R * 3 * sh.I * sh.H + 2.0 * sh.T * 3 * sh.Is * sh.H
+    used = sh.E if counts is None else int((counts > 0).sum())
+    wbytes = used * (3 * sh.H * sh.I + 4 * (2 * sh.I + sh.H))
+    if sh.Is:
+        wbytes += 3 * sh.H * sh.Is + 4 * (2 * sh.Is + sh.H)
+    return ops, wbytes
+
+
+def measure_layer(moe, name, peaks, steps):
+    """One layer of a single-layer workload (the 256-token prefill chunk, the 8192-token
+    stress layer): routing once, then `steps` timed forwards (CUDA events on the stream);
+    tokens/s, microseconds per layer, and the layer's tensor and HBM roofline fractions."""
+    dev = torch.device("cuda")
+    wl = synth.WORKLOADS[name]
+    sh = wl.shape
+    W = synth.make_weights(sh, wl.seed, device=dev)
+    x = synth.make_activations(sh.T, sh.H, wl.seed, wl.outliers, dev)
+    lg = synth.make_logits(sh.T, sh.E, wl.seed, wl.zipf_s, dev)
+    lay = moe.MoELayer(sh.E, sh.k, sh.H, sh.I, sh.Is, sh.T, W)
+    try:
+        idx, w = lay.route(lg)
+        y = torch.empty((sh.T, sh.H), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            lay.forward(x, idx, w, y)
+        torch.cuda.synchronize()
+        counts = moe.moe_debug_tap(lay.plan, moe.TAP_COUNTS)
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(steps, 10)
+        e0.record(stream)
+        for _ in range(reps):
+            lay.forward(x, idx, w, y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        moe.moe_profile_enable(lay.plan, True)
+        for _ in range(3):
+            lay.forward(x, idx, w, y)
+        torch.cuda.synchronize()
+        st, calls = moe.moe_profile_read(lay.plan, 0)
+        moe.moe_profile_enable(lay.plan, False)
+        if moe.moe_get_error(lay.plan):
+            raise moe.MoeError(moe.moe_get_error(lay.plan), name)
+    finally:
+        lay.close()
+    ops, wbytes = layer_work(sh, counts)
+    act_bytes = sh.T * sh.H * 2 + sh.T * sh.H * 4  # x in (bf16), y out (fp32)
+    tf = ops / (us * 1e-6) / 1e12
+    gbs = (wbytes + act_bytes) / (us * 1e-6) / 1e9
+    return {"workload": wl.note, "tokens_per_s": sh.T / (us * 1e-6), "us_per_layer": us,
+            "int_ops": ops, "achieved_tops": tf,
+            "tensor_frac": tf / peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]),
+            "hbm_bytes": wbytes + act_bytes, "achieved_gbs": gbs,
+            "hbm_frac": gbs / peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]),
+            "experts_used": int((counts > 0).sum()),
+            "stage_us": [v * 1e3 / max(calls, 1) for v in st]}
+
+
+def oracle_one_core(names, max_tokens):
+    """The oracle (as it stands) on one host core: MoE-layer tokens/s per workload, on the
+    first min(T, max_tokens[name]) tokens of the workload's layer."""
+    import oracle
+    out = {}
+    for name in names:
+        wl = synth.WORKLOADS[name]
+        sh = wl.shape
+        d = synth.make_layer(wl, device="cpu")
+        n = min(sh.T, max_tokens.get(name, sh.T))
+        L = oracle.Layer(d["weights"], sh.E, sh.k, sh.H, sh.I, sh.Is)
+        x = d["x"][:n].contiguous()
+        lg = d["logits"][:n].contiguous()
+        t0 = time.perf_counter()
+        idx, w = oracle.route(lg, sh.k)
+        oracle.forward(L, x, idx, w, nthreads=1)
+        dt = time.perf_counter() - t0
+        out[name] = {"value": n / dt, "unit": "MoE-layer tokens/s", "cores": 1, "kind": "oracle",
+                     "sample": f"{n} of {sh.T} tokens of the {name} layer (route + layer), {dt:.2f} s"}
+    return out
+
+
 def run_ours(args, world, rank):
     import grouped_expert_ffn_gb300 as moe
     peaks, peak_src = load_peaks()
@@ -313,11 +400,13 @@ def run_ours(args, world, rank):
     R = T * k + T
     gu_flops = 2.0 * R * 2 * sh.I * H
     gu_ms = stage_ms[1]
-    peak_tf = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    peak_tf = peaks.get("bf16_tflops", FALLBACK["bf16_tflops"])
+    peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
     achieved_tf = gu_flops / (gu_ms / 1e3) / 1e12
     down_flops = 2.0 * R * H * sh.I
     layer_flops = gu_flops + down_flops
     moe_ms = sum(stage_ms)
+    layer_tf = layer_flops / (moe_ms / 1e3) / 1e12
 
     # ---- e2e: host (pinned) x in, host result out, inside the timed region
     e2e = None
@@ -358,7 +447,15 @@ def run_ours(args, world, rank):
                "sample": f"{n_tok} tokens of layer 0 of the stack (router projection + route + "
                          f"layer), {secs:.1f} s"}
 
-    n_launch = (n_layers * 10 + 1) * args.steps  # norm, router, route, 7 forward kernels; residual
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        extra["prefill_chunk_T256"] = measure_layer(moe, "prefill", peaks, args.steps)
+        extra["stress_T8192"] = measure_layer(moe, "stress", peaks, args.steps)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        extra["cpu_baseline_1core"] = oracle_one_core(["tiny", "decode", "prefill"],
+                                                      {"prefill": args.cpu_tokens_1core})
+
+    n_launch = (n_layers * LAUNCHES_PER_LAYER + 1) * args.steps
     line = {
         "metric": METRIC,
         "value": value,
@@ -386,14 +483,22 @@ def run_ours(args, world, rank):
                      "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved_tf / peak_tf, "traffic": GU_TRAFFIC_BYTES,
                      "traffic_unit": "bytes per launch (ncu)",
-                     "peak_source": f"{peak_src} bf16_tflops_sustained (fp16 = bf16 rate)",
+                     "peak_source": f"{peak_src} bf16_tflops (burst; fp16 = bf16 rate)",
+                     "frac_of_sustained": achieved_tf / peak_sus,
                      "flops_per_launch": gu_flops},
-        "layer_tflops": layer_flops / (moe_ms / 1e3) / 1e12,
+        "layer_roofline": {"bound": "tensor", "achieved": layer_tf, "unit": "TFLOP/s",
+                           "flops_per_layer": layer_flops, "layer_us": moe_ms * 1e3,
+                           "frac": layer_tf / peak_tf, "frac_of_sustained": layer_tf / peak_sus,
+                           "gate_up_frac": achieved_tf / peak_tf,
+                           "down_frac": down_flops / (stage_ms[3] / 1e3) / 1e12 / peak_tf,
+                           "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "layer_tflops": layer_tf,
         "decode": decode,
         "e2e": e2e,
         "gpu_launches": n_launch,
         "clocks": clk,
         "cpu_baseline": cpu,
+        **extra,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -458,6 +563,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the T=256 prefill-chunk and T=8192 stress layer lines")
+    ap.add_argument("--cpu-tokens-1core", type=int, default=48,
+                    help="tokens of the T=256 prefill layer the one-core oracle runs")
     args = ap.parse_args()
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

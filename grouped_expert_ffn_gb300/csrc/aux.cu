@@ -1,55 +1,10 @@
-// Weight packing for the tensor-core path, and the two steps around the layer in a stacked
-// prefill (router projection and the bf16 residual update).
+// Weight packing for the tensor-core path (gate/up rows interleaved in channel pairs, row
+// sum-of-squares maxima), and the steps around the layer in a stacked prefill (router
+// projection, RMS pre-norm and the bf16 residual update).
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
-
-// Gate/up rows interleaved in pairs: packed row 2i is gate channel i and row 2i+1 up channel
-// i, so the tensor-core tile of 128 weight rows yields SiLU(gate)*up for 64 channels with
-// gate and up in adjacent TMEM lanes. int8 values widened to fp16 (exact). 8 elements per
-// thread.
-__global__ void pack_gu_kernel(const int8_t* __restrict__ gate, const int8_t* __restrict__ up,
-                               int n_mats, int I, int H, __half* __restrict__ out) {
-  const size_t n8 = (size_t)n_mats * 2 * I * H / 8;
-  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8;
-       v += (size_t)gridDim.x * blockDim.x) {
-    const size_t el = v * 8;
-    const int h = (int)(el % H);
-    const size_t prow = el / H;  // packed row over all matrices
-    const int m = (int)(prow / (2 * I));
-    const int p = (int)(prow % (2 * I));
-    const int ch = p >> 1;
-    const int8_t* src = ((p & 1) ? up : gate) + ((size_t)m * I + ch) * H + h;
-    const uint2 raw = *reinterpret_cast<const uint2*>(src);
-    const int8_t* q = reinterpret_cast<const int8_t*>(&raw);
-    uint4 o;
-    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2 h2 = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
-      ow[i] = *reinterpret_cast<const uint32_t*>(&h2);
-    }
-    *reinterpret_cast<uint4*>(out + el) = o;
-  }
-}
-
-__global__ void widen_kernel(const int8_t* __restrict__ src, size_t n, __half* __restrict__ out) {
-  const size_t n8 = n / 8;
-  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n8;
-       v += (size_t)gridDim.x * blockDim.x) {
-    const uint2 raw = reinterpret_cast<const uint2*>(src)[v];
-    const int8_t* q = reinterpret_cast<const int8_t*>(&raw);
-    uint4 o;
-    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2 h2 = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
-      ow[i] = *reinterpret_cast<const uint32_t*>(&h2);
-    }
-    reinterpret_cast<uint4*>(out)[v] = o;
-  }
-}
 
 // max over rows of sum(q^2) of an int8 matrix [rows, cols], into *out (atomicMax). Warp per
 // row; cols a multiple of 16.
@@ -97,17 +52,6 @@ __global__ void pack_gu8_kernel(const int8_t* __restrict__ gate, const int8_t* _
 cudaError_t launch_pack_gu8(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,
                             int8_t* out, cudaStream_t s) {
   pack_gu8_kernel<<<1216, 256, 0, s>>>(gate, up, n_mats, I, H, out);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,
-                           __half* out, cudaStream_t s) {
-  pack_gu_kernel<<<1216, 256, 0, s>>>(gate, up, n_mats, I, H, out);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_widen(const int8_t* src, size_t n, __half* out, cudaStream_t s) {
-  widen_kernel<<<1216, 256, 0, s>>>(src, n, out);
   return cudaGetLastError();
 }
 

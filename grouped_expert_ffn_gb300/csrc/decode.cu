@@ -333,14 +333,17 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) 
   return cudaGetLastError();
 }
 
-bool decode_shape_supported(int H, int Imax) { return H <= 8192 && Imax <= 4096; }
+bool decode_shape_supported(int H, int Imax) { return H <= kDecodeMaxH && Imax <= kDecodeMaxI; }
 
-cudaError_t decode_set_attributes(int H, int Imax) {
+// The kernels' dynamic shared-memory limit is a process-wide attribute: it is set once to the
+// largest shapes the library accepts (never per plan, so that a plan with smaller shapes
+// cannot lower it under a plan with larger ones).
+cudaError_t decode_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(decode_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kDecodeMaxRows * H);
+                                       kDecodeMaxRows * kDecodeMaxH);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kDecodeMaxRows * Imax);
+                              kDecodeMaxRows * kDecodeMaxI);
 }
 
 }  // namespace moe

@@ -30,6 +30,8 @@ constexpr int kBK = 64;         // K elements per pipeline stage (128 bytes of f
 constexpr int kChunkK = 1024;   // K elements summed in one fp32 TMEM accumulator
 constexpr int kTokPerBlk = 64;  // tokens per histogram block (one 64-bit mask per expert)
 constexpr int kDecodeMaxRows = 8;
+constexpr int kDecodeMaxH = 8192;  // largest H and intermediate size the decode kernels take
+constexpr int kDecodeMaxI = 4096;
 constexpr int kREB = 16;  // experts per router tensor-core tile (packed router weight block)
 
 // One unit of grouped-GEMM work: token rows [row0, row0 + rows) of group `group` (expert id,
@@ -144,13 +146,10 @@ struct DecodeArgs {
   int* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev);
-cudaError_t decode_set_attributes(int H, int Imax);
+cudaError_t decode_set_attributes();
 bool decode_shape_supported(int H, int Imax);  // shapes the T <= 8 streaming kernels take
 
 // weight packing and the stacked-prefill helpers
-cudaError_t launch_pack_gu(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,
-                           __half* out, cudaStream_t s);
-cudaError_t launch_widen(const int8_t* src, size_t n, __half* out, cudaStream_t s);
 cudaError_t launch_pack_gu8(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,
                             int8_t* out, cudaStream_t s);
 cudaError_t launch_row_sq_max(const int8_t* w, size_t rows, int cols, int* out, cudaStream_t s);

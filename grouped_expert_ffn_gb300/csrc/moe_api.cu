@@ -333,7 +333,7 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
     }
   }
   cudaError_t e = gemm_set_attributes();
-  if (e == cudaSuccess) e = decode_set_attributes(H, p->Imax);
+  if (e == cudaSuccess) e = decode_set_attributes();
   // One CTA per weight tile by default (moe_plan_use_cta_pairs switches a GEMM to CTA pairs);
   // the grid is as many whole clusters as fit at once.
   if (e == cudaSuccess) e = size_gemm_grids(p);

@@ -2,11 +2,10 @@
 // memory carved out of one file-scope device array instead of a plan's workspace.
 //
 // Who needs it: callers that must not allocate device memory on the call path. Examples are
-// a host program whose stream is being captured into a CUDA graph (allocation calls are not
-// allowed while capturing), a plugin running inside another runtime that owns every device
-// allocation and forbids its guests from calling cudaMalloc, and latency-critical serving
-// loops where cudaMalloc/cudaFree would implicitly synchronise the device and stall other
-// streams. moe_plan allocates a workspace, so those callers cannot use it on the call path.
+// a plugin running inside another runtime that owns every device allocation and forbids its
+// guests from calling cudaMalloc, and latency-critical serving loops where cudaMalloc/cudaFree
+// would implicitly synchronise the device and stall other streams. moe_plan allocates a
+// workspace, so those callers cannot use it on the call path.
 //
 // The scratch array lives in this library's device image: every GPU that loads the library
 // holds kScratchBytes of it until the process exits, whether or not this entry point is used.
@@ -117,9 +116,8 @@ extern "C" moe_status moe_forward_decode_static(int E, int top_k, int H, int I, 
                                                                        : MOE_ERR_CUDA;
   }
   // The decode kernels take up to 8 rows x H (gate/up) and 8 rows x Imax (down) bytes of
-  // dynamic shared memory; raise their limit to this library's largest shapes (set per call:
-  // a plan created later may have lowered it).
-  if ((e = decode_set_attributes(8192, 4096)) != cudaSuccess) return MOE_ERR_CUDA;
+  // dynamic shared memory; their limit is set to this library's largest shapes.
+  if ((e = decode_set_attributes()) != cudaSuccess) return MOE_ERR_CUDA;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* err = reinterpret_cast<int*>(base + o_err);

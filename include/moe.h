@@ -79,7 +79,10 @@ typedef struct {
 } moe_weights;
 
 /* Create a plan for one layer shape and allocate its workspace for up to max_tokens
- * tokens per call (the only allocation on the forward path's behalf).
+ * tokens per call (the only allocation on the forward path's behalf). The plan is the
+ * persistent per-layer-shape state that the page "Qwen3.6-35B-A3B Linux v1.0.4: ~2.7s fixed
+ * per-request TTFT ..." (section "Evidence", item 1, and "Request" (b)) finds missing: no
+ * buffer is created or destroyed per call.
  *   E: routed experts (1..256); top_k: 1..min(E, 8); H: hidden size; I: routed expert
  *   intermediate size; I_shared: shared expert intermediate size, 0 = no shared expert.
  * Supported shapes: H a multiple of 128, I (and I_shared when > 0) multiples of 64; H <= 8192;
@@ -92,15 +95,19 @@ MOE_API moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int ma
 MOE_API moe_status moe_plan_destroy(moe_plan_t plan);
 
 /* Register one layer's weights with the plan's shapes. Allocates and fills (on `stream`)
- * the device copy the tensor-core path reads (gate/up rows interleaved in N-tile blocks, the
- * int8 values widened to fp16, which represents every int8 exactly); the decode path reads
- * the caller's int8 arrays and scales directly, so they must stay alive and unchanged while
- * the packed handle is in use. Release with moe_packed_destroy. */
+ * the device copy the tensor-core path reads: the int8 gate and up rows interleaved in
+ * channel pairs (row 2i = gate channel i, row 2i+1 = up channel i, per expert; the shared
+ * expert likewise), still int8, plus the maxima over weight rows of the sum of squared codes
+ * that the GEMMs' exactness test uses. The down GEMM and the decode path read the caller's
+ * int8 arrays and scales directly, so they must stay alive and unchanged while the packed
+ * handle is in use. Release with moe_packed_destroy. */
 MOE_API moe_status moe_pack_weights(moe_plan_t plan, const moe_weights* w, void* stream,
                             moe_packed_t* out);
 MOE_API moe_status moe_packed_destroy(moe_packed_t packed);
 
-/* Top-k softmax routing (warp per token).
+/* Top-k softmax routing (warp per token): the "top-8" selection of routed experts per token
+ * that the page "Qwen3.6-35B-A3B Linux v1.0.4 ..." (section "The fix (concatenated-expert
+ * dispatch)") dispatches, with the softmax weights of the selected experts.
  *   logits fp32 [T, E] -> idx int32 [T, top_k], w fp32 [T, top_k].
  * Selection compares the fp32 logits; ties go to the lowest expert id; slots are ordered by
  * logit descending, then id ascending. w is a softmax over the selected logits, so each
@@ -108,7 +115,11 @@ MOE_API moe_status moe_packed_destroy(moe_packed_t packed);
 MOE_API moe_status moe_route(moe_plan_t plan, const float* logits, int T, int32_t* idx, float* w,
                      void* stream);
 
-/* The MoE layer: y fp32 [T, H] = sum_j w[t,j] * expert_{idx[t,j]}(x[t]) + shared(x[t]).
+/* The MoE layer: y fp32 [T, H] = sum_j w[t,j] * expert_{idx[t,j]}(x[t]) + shared(x[t]),
+ * computed as one grouped (concatenated-expert) computation per operator, as the page
+ * "Qwen3.6-35B-A3B Linux v1.0.4 ..." proposes in section "The fix (concatenated-expert
+ * dispatch)": gate and up concatenated (N = top_k x 2 x I per token), one GLU region over
+ * all experts, then the down projection and the weighted combine.
  *   x bf16 [T, H] (raw bf16 bits); idx, w as produced by moe_route (any valid top-k
  *   routing: idx[t,*] distinct, in [0, E)); y is overwritten. 1 <= T <= max_tokens: an
  *   empty batch (T = 0) is MOE_ERR_INVALID_ARG, a larger one MOE_ERR_CAPACITY, both
@@ -206,11 +217,11 @@ MOE_API moe_status moe_residual_add(uint16_t* x, const float* y, int T, int H, v
 
 /* ---- allocation-free batched decode ---------------------------------------------------
  * The source pages have no counterpart of this entry point; it exists for callers that
- * cannot allocate device memory on their call path (a stream being captured into a CUDA
- * graph, where allocation calls are not allowed; a plugin inside a host runtime that owns
- * all device allocations; serving loops that cannot afford the implicit device
- * synchronisation of cudaMalloc/cudaFree). moe_plan allocates a workspace, so such callers
- * use this instead for decode-sized batches.
+ * cannot allocate device memory on their call path: a plugin inside a host runtime that owns
+ * every device allocation and forbids its guests from calling cudaMalloc, or a serving loop
+ * that cannot afford the implicit device synchronisation of cudaMalloc/cudaFree between
+ * steps. moe_plan allocates a workspace, so such callers use this instead for decode-sized
+ * batches.
  *
  * Computes exactly what moe_forward computes for 1 <= T <= 8 rows (the deduplicated
  * weight-streaming decode kernels), taking the shapes directly instead of a plan:
@@ -222,11 +233,13 @@ MOE_API moe_status moe_residual_add(uint16_t* x, const float* y, int T, int H, v
  * list, row maps, fp32 SiLU(gate)*up rows) is a file-scope __device__ array inside the
  * library, present on every GPU that loads the library until the process exits. Limits:
  * T <= 8 (else MOE_ERR_CAPACITY), E <= 256, top_k <= 8, H <= 8192 and a multiple of 128,
- * I and I_shared <= 4096 and multiples of 64 (else MOE_ERR_UNSUPPORTED). The first call on each device looks up
- * the array's device address (cudaGetSymbolAddress); make that first call before any stream
- * capture. Every call shares the one array and keeps the previous call's contents (only
- * the error word is cleared per call): calls that overlap on the GPU - on two streams, or
- * from two host threads - race and corrupt each other's results; serialise them. */
+ * I and I_shared <= 4096 and multiples of 64 (else MOE_ERR_UNSUPPORTED). The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress) and keeps it for
+ * the life of the process; make that first call before any stream capture, and do not call
+ * this entry point again on a device after cudaDeviceReset (the array may then move). Every
+ * call shares the one array and keeps the previous call's contents (only the error word is
+ * cleared per call): calls that overlap on the GPU - on two streams, or from two host
+ * threads - race and corrupt each other's results; serialise them. */
 MOE_API moe_status moe_forward_decode_static(int E, int top_k, int H, int I, int I_shared,
                                              const moe_weights* w, const uint16_t* x, int T,
                                              const int32_t* idx, const float* wts, float* y,

@@ -40,17 +40,52 @@ def test_layer_parity_full(name):
 
 
 def test_stress_layer_sampled():
+    # T=8192, E=256, Zipf 1.5: the persistent scheduler under heavy skew with empty experts.
+    # Full oracle parity on a sample of tokens that includes, for every empty expert, the
+    # first and last token of the nearest non-empty expert on each side (their rows sit at
+    # the segment boundaries around the empty group); and every gate/up accumulator of the
+    # heaviest expert's rows against the exact integer sums of the oracle's activation codes
+    # with that expert's int8 weights (fp64 products and sums of integers below 2^53 are exact).
     wl = synth.WORKLOADS["stress"]
     sh = wl.shape
     W = synth.make_weights(sh, wl.seed, device="cuda")
     x = synth.make_activations(sh.T, sh.H, wl.seed, wl.outliers, "cpu")
     lg = synth.make_logits(sh.T, sh.E, wl.seed, wl.zipf_s, "cpu")
     L = oracle_layer(W, sh)
+    idx_o, _ = oracle.route(lg, sh.k)
+    counts_o = np.bincount(idx_o.ravel(), minlength=sh.E)
+    toks_of = lambda e: np.nonzero((idx_o == e).any(axis=1))[0]
+    edge = []
+    for e in np.nonzero(counts_o == 0)[0]:
+        for step in (-1, 1):
+            n = e + step
+            while 0 <= n < sh.E and counts_o[n] == 0:
+                n += step
+            if 0 <= n < sh.E:
+                t = toks_of(n)
+                edge += [t[0], t[-1]]
     rng = np.random.default_rng(0)
-    sample = np.sort(np.concatenate([[0, sh.T - 1], rng.choice(sh.T, 22, replace=False)]))
+    sample = np.unique(np.concatenate([[0, sh.T - 1], rng.choice(sh.T, 22, replace=False),
+                                       np.asarray(edge, np.int64)[:40]]))
     st = check_layer(sh, x, lg, W, L, sample=sample)
     counts = st["tap"]["counts"]
     assert (counts == 0).any() and np.sort(counts)[::-1][:4].sum() > 0.4 * sh.T * sh.k
+    # every row of the heaviest expert
+    e = int(np.argmax(counts_o))
+    rows_tok = toks_of(e)
+    q_o, _ = oracle.quant_rows(x)
+    qx = q_o[rows_tok].astype(np.float64)
+    ref_g = qx @ W["w_gate"][e].cpu().numpy().astype(np.float64).T
+    ref_u = qx @ W["w_up"][e].cpu().numpy().astype(np.float64).T
+    perm = st["tap"]["perm"]
+    R = sh.T * sh.k + sh.T
+    acc_gu = st["tap"]["acc_gu"].reshape(R, 2, max(sh.I, sh.Is))
+    off = st["tap"]["offsets"]
+    seg = np.arange(off[e], off[e + 1])
+    assert (perm[seg] // sh.k == rows_tok).all()   # rows of expert e in token order
+    rows = sh.T + seg                              # shared rows come first
+    assert (acc_gu[rows, 0, :sh.I] == ref_g).all()
+    assert (acc_gu[rows, 1, :sh.I] == ref_u).all()
 
 
 def test_stack_layer0_sampled():
@@ -179,6 +214,21 @@ def test_activation_codes_on_rounding_ties(T):
     ties = np.abs(np.abs(xf / s_o[:, None]) % 1.0 - 0.5) < 1e-3
     assert ties.sum() > T * 1024 // 2  # most elements are (near) ties
     check_layer(sh, x, d["logits"], W, oracle_layer(d["weights"], sh))
+
+
+def test_decode_after_a_smaller_plan_was_created():
+    # The decode kernels' shared-memory limit is process-wide: creating a plan with small
+    # shapes after one with large shapes must not break decode on the large plan.
+    big = synth.LayerShape(T=8, H=4096, E=16, k=4, I=2048, Is=0)
+    d = synth.small_layer(8, big.H, big.E, big.k, big.I, 0, seed=61, zipf_s=1.1)
+    W = weights_to(d["weights"], "cuda")
+    lay = moe.MoELayer(big.E, big.k, big.H, big.I, 0, 8, W)
+    small = moe.moe_plan(8, 2, 256, 128, 0, 16)
+    try:
+        check_layer(big, d["x"], d["logits"], W, oracle_layer(d["weights"], big), layer=lay)
+    finally:
+        moe.moe_plan_destroy(small)
+        lay.close()
 
 
 def test_capacity_and_argument_errors():
