@@ -67,7 +67,6 @@ def lib() -> C.CDLL:
             "moe_profile_enable": ([vp, i32], i32),
             "moe_profile_read": ([vp, i32, C.POINTER(C.c_float), C.POINTER(C.c_int)], i32),
             "moe_router_logits": ([vp, vp, i32, i32, i32, vp, vp], i32),
-            "moe_plan_use_cta_pairs": ([vp, i32, i32], i32),
             "moe_router_pack": ([vp, i32, i32, vp, vp], i32),
             "moe_router_logits_packed": ([vp, vp, i32, i32, i32, vp, vp], i32),
             "moe_residual_add": ([vp, vp, i32, i32, vp], i32),
@@ -127,12 +126,6 @@ def moe_plan(E: int, top_k: int, H: int, I: int, I_shared: int, max_tokens: int)
     h = C.c_void_p()
     _check(lib().moe_plan(E, top_k, H, I, I_shared, max_tokens, C.byref(h)), "moe_plan")
     return h.value
-
-
-def moe_plan_use_cta_pairs(plan: int, gate_up: bool, down: bool):
-    """Run the gate/up and/or down GEMM on CTA pairs (2-SM MMA); same results."""
-    _check(lib().moe_plan_use_cta_pairs(plan, int(bool(gate_up)), int(bool(down))),
-           "moe_plan_use_cta_pairs")
 
 
 def moe_plan_destroy(plan: int):

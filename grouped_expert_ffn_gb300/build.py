@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["moe_api.cu", "gemm_tc.cu", "gemm_pair.cu", "route_permute.cu", "decode.cu", "aux.cu", "no_alloc.cu", "router_tc.cu"]
+SOURCES = ["moe_api.cu", "gemm_tc.cu", "route_permute.cu", "decode.cu", "aux.cu", "no_alloc.cu", "router_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

@@ -81,58 +81,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Cluster-scope variants, for barriers that receive arrivals from the other CTA of a pair.
-__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                             int* err) {
-  if (mbar_try_wait_cl(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait_cl(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      set_error(err, kErrTimeout);
-      return false;
-    }
-  }
-}
-// Address of this CTA's shared-memory word `local` in the CTA of cluster rank `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to another CTA's of the
-// cluster, completing that many transaction bytes on an mbarrier there (dst and bar from
-// mapa_shared). Asynchronous: the issuing thread does not wait for it.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void* src,
-                                                  uint32_t bytes, uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst_cluster),
-      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
-
 // ---- programmatic dependent launch ------------------------------------------------------
 // Kernels of the layer chain are launched with launch_pdl: a kernel's blocks may be scheduled
 // while its predecessor on the stream drains, and wait for it (its completion and memory) in
@@ -179,17 +127,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster; release/acquire orders shared-memory state
-// (mbarrier initialisation, last accesses) across the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
 // ---- tcgen05 / TMEM -----------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -229,79 +166,61 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// ---- the CTA pair of the 2-SM MMA (cta_group::2): every tcgen05 op of a kernel that uses
-// the pair form uses it throughout.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(slot)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+// 32 lanes x 32 consecutive 32-bit columns written from 32 registers per thread (thread i of
+// the warp writes lane base + i). Asynchronous: tmem_st_wait waits for the thread's stores.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+      " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+      " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+      "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 
-// The four MMAs of one k-block (K = 64: descriptors advance 32 bytes per K = 16 step), one
-// commit of them to `commit_bar`, and a non-blocking probe of phase `next_parity` of
-// `next_bar` (the barrier the issuing thread waits on for the next k-block), in one block:
-// the probe's shared-memory round trip overlaps the MMA issue instead of sitting between
-// two k-blocks with the tensor pipe idle. `accumulate` applies to the first MMA (the rest
-// accumulate). Returns whether the next k-block's operands are ready. PAIR selects the 2-SM
-// form (cta_group::2, commit multicast to both CTAs of the pair, cluster-scope probe).
-template <bool PAIR>
-__device__ __forceinline__ uint32_t mma_kblock_commit_probe(uint32_t d_tmem, uint64_t adesc,
-                                                            uint64_t bdesc, uint32_t idesc,
-                                                            uint32_t accumulate,
-                                                            uint32_t commit_bar,
-                                                            uint32_t next_bar,
-                                                            uint32_t next_parity) {
+// One pipeline stage of the grouped GEMM (128 K): eight MMAs of K = 16 with the A operand
+// (weights, fp16) in TMEM, a_tmem + 8 columns per MMA, and B (tokens) in shared memory, two
+// 64-K sub-tiles b0 and b1 (descriptors advance 32 bytes per MMA); one commit to `commit_x`
+// (the token stage is free once these MMAs completed) and one to `commit_a` (the TMEM A stage
+// is free); and a non-blocking probe of phase `next_parity` of `next_bar` (the barrier of the
+// next stage), all in one block, so that the probe's shared-memory round trip overlaps the
+// MMA issue. The block opens with tcgen05.fence::after_thread_sync: the A stage was written
+// by other threads (tcgen05.st) and observed complete through an mbarrier. `accumulate`
+// applies to the first MMA. Returns whether the next stage is ready.
+__device__ __forceinline__ uint32_t mma_stage_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                                 uint64_t b1, uint32_t idesc, uint32_t accumulate,
+                                                 uint32_t commit_x, uint32_t commit_a,
+                                                 uint32_t next_bar, uint32_t next_parity) {
   uint32_t ready;
-  if (PAIR) {
-    asm volatile(
-        "{\n\t.reg .pred pa, pt, pn;\n\t"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 pn, [%7], %8;\n\t"
-        "setp.ne.b32 pa, %5, 0;\n\t"
-        "setp.eq.b32 pt, 1, 1;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %4, pa;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %9, %10, %4, pt;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %11, %12, %4, pt;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %13, %14, %4, pt;\n\t"
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%6], %15;\n\t"
-        "selp.u32 %0, 1, 0, pn;\n\t}\n"
-        : "=r"(ready)
-        : "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(commit_bar),
-          "r"(next_bar), "r"(next_parity), "l"(adesc + 2), "l"(bdesc + 2), "l"(adesc + 4),
-          "l"(bdesc + 4), "l"(adesc + 6), "l"(bdesc + 6), "h"((uint16_t)0x3)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred pa, pt, pn;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 pn, [%7], %8;\n\t"
-        "setp.ne.b32 pa, %5, 0;\n\t"
-        "setp.eq.b32 pt, 1, 1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pa;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], %9, %10, %4, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], %11, %12, %4, pt;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%1], %13, %14, %4, pt;\n\t"
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-        "selp.u32 %0, 1, 0, pn;\n\t}\n"
-        : "=r"(ready)
-        : "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(commit_bar),
-          "r"(next_bar), "r"(next_parity), "l"(adesc + 2), "l"(bdesc + 2), "l"(adesc + 4),
-          "l"(bdesc + 4), "l"(adesc + 6), "l"(bdesc + 6)
-        : "memory");
-  }
+  asm volatile(
+      "{\n\t.reg .pred pa, pt, pn;\n\t"
+      "tcgen05.fence::after_thread_sync;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\t"
+      "setp.eq.b32 pt, 1, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, pa;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%10], %11, %4, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%12], %13, %4, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%14], %15, %4, pt;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 pn, [%8], %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%16], %17, %4, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%18], %19, %4, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%20], %21, %4, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%22], %23, %4, pt;\n\t"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+      "selp.u32 %0, 1, 0, pn;\n\t}\n"
+      : "=r"(ready)
+      : "r"(d_tmem), "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate), "r"(commit_x),
+        "r"(commit_a), "r"(next_bar), "r"(next_parity), "r"(a_tmem + 8), "l"(b0 + 2),
+        "r"(a_tmem + 16), "l"(b0 + 4), "r"(a_tmem + 24), "l"(b0 + 6), "r"(a_tmem + 32), "l"(b1),
+        "r"(a_tmem + 40), "l"(b1 + 2), "r"(a_tmem + 48), "l"(b1 + 4), "r"(a_tmem + 56),
+        "l"(b1 + 6)
+      : "memory");
   return ready;
 }
 

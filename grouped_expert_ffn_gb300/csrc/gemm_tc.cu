@@ -2,26 +2,27 @@
 //
 // One persistent kernel runs every (expert group, 128-row weight tile, token tile) work item
 // of a layer: the gate/up GEMM with a fused SiLU(gate)*up epilogue, or the down GEMM whose
-// epilogue writes every row's router-weighted output (combine_kernel then sums each token's
-// rows). This is the concatenated-expert computation
-// of the page "Qwen3.6-35B-A3B Linux v1.0.4: ~2.7s fixed per-request TTFT ...", section
-// "The fix (concatenated-expert dispatch)": one launch per operator and layer instead of one
-// per expert, with gate and up concatenated along the weight dimension.
+// epilogue adds every row's router-weighted output into the layer output y. This is the
+// concatenated-expert computation of the page "Qwen3.6-35B-A3B Linux v1.0.4: ~2.7s fixed
+// per-request TTFT ...", section "The fix (concatenated-expert dispatch)": one launch per
+// operator and layer instead of one per expert, gate and up concatenated along the weight
+// dimension, one GLU region over all experts.
 //
 // Orientation: the weights are the MMA's M operand (128 rows per tile) and an expert's tokens
-// its N operand (N = the expert's row count rounded up to 16, at most the token tile TN <=
-// 256), so an expert with 162 tokens costs one 176-wide tile instead of two 128-row tiles.
-// The accumulator holds weight rows in TMEM lanes and tokens in columns. Gate and up rows are
-// interleaved in pairs (row 2i = gate channel i, row 2i+1 = up channel i), so SiLU(gate)*up
-// is formed by one lane-pair exchange.
+// its N operand (N = the tile's row count rounded up to 16, at most the token tile TN <= 192;
+// an expert's rows are split into equal tiles), so an expert with 162 tokens costs one
+// 176-wide tile. The accumulator holds weight rows in TMEM lanes and tokens in columns. Gate
+// and up rows are interleaved in pairs (row 2i = gate channel i, row 2i+1 = up channel i), so
+// SiLU(gate)*up is formed by one lane-pair exchange.
 //
-// int8 weights stay int8 in HBM (half the bytes of fp16): TMA brings each 128 x 64 int8 weight
-// tile into shared memory (64-byte swizzle), and four converter warps widen it to the fp16
-// 128-byte-swizzled tile the MMA reads. The widening is exact: byte v+128 becomes the fp16
-// bit pattern 0x6400|(v+128) = 1024 + v + 128, and subtracting 1152 leaves v. Token rows are
-// already fp16 integers (written by the permutation step / requantisation) and go straight
-// from TMA (one box per stage, 128-byte swizzle) to the MMA: widening them in shared memory
-// too would triple the shared-memory traffic of a k-block (measured slower).
+// Weights: int8 in HBM, A operand in TMEM. TMA brings each 128-row x 128-K int8 weight tile
+// into shared memory (128-byte swizzle); converter warps read one row each, widen it exactly
+// to fp16 in registers (byte v+128 placed under the fp16 exponent of 1024, then 1152
+// subtracted) and store it into TMEM with tcgen05.st, where the MMA reads it as its A operand.
+// Shared memory then carries only the int8 tile (written by TMA, read once) and the token
+// tile (written by TMA, read by the MMA): the tensor core's shared-memory reads are the token
+// operand alone. Tokens (the B operand) are fp16 integer codes written by the permutation step
+// / requantisation, TMA-loaded in 64-K boxes with the 128-byte swizzle.
 //
 // Exact integer products on an fp16 tensor pipe. sm_103a has no int8 tcgen05 MMA, so the
 // int8 operands are held as fp16 (every int8 value is an fp16 integer) and multiplied with
@@ -39,79 +40,262 @@
 // same two words). With one accumulator per tile, TMEM holds two of them (2 x TN columns)
 // so the epilogue of one tile overlaps the MMAs of the next.
 //
-// The 2-SM form of the same items (one MMA of M = 256 over two CTAs, each holding half of the
-// token tile) is in gemm_pair.cu; a plan selects it per GEMM.
+// TMEM (512 columns): accumulator slots in columns [0, 384), two A stages of 64 columns
+// (128 rows x 128 K of fp16) in [384, 512).
 //
-// Warp roles (one CTA per SM; GemmRoles in gemm_common.cuh): gate/up 672 threads, down 800.
+// Warp roles (one CTA per SM; GemmRoles):
 //   epilogue warps (8 for gate/up, 12 for down): warp w reads TMEM lanes 32*(w%4).. (weight
 //               rows) and every (w/4)-th 16-column chunk (tokens) of its quadrant;
-//   converter groups of four warps (2 for each GEMM) taking turns over k-blocks: thread r of
-//               a group widens weight row r;
+//   two converter groups of four warps: group g fills A stage g for every stage index of
+//               parity g, thread r of a group widening weight row r;
 //   one MMA issuer and TMEM owner;
-//   two TMA producers of the int8 weight tiles (alternate stages);
-//   two TMA producers of the fp16 token tiles (alternate stages).
-// Pipeline: the weights stream from HBM through a ring of small int8 stages (4 x 8 KB,
-// released by the converters as soon as they have widened a stage); the token tiles, mostly
-// L2 hits, through a ring of large stages (4 x 32 KB), one TMA load per stage (box heights
-// 16..256 rows); one fp16 weight buffer per token stage, released together with it by the
-// MMA's commit. A converter group widens its k-block as soon as the int8 tile and the fp16
-// buffer are free and waits for the token tile only afterwards, so the token load overlaps
-// the conversion. A TMA-issuing thread completes only a few loads per microsecond, so each ring
-// has two issuing threads and each token tile is one load rather than several 64-row ones.
-// Barrier arrivals are one per warp (after __syncwarp) and the MMA thread commits once per
-// k-block: every arrival and commit sits on the critical path of a k-block.
-// Every mbarrier wait is bounded; a wait
-// that runs out sets the plan's error word and the CTA drains its own copies and MMAs, frees
-// TMEM and returns.
+//   one TMA producer of the int8 weight tiles, two of the token tiles (alternate stages).
+// Pipeline per 128-K stage: the weight tile lands in a ring of 4 int8 stages (released by the
+// converters once read); the token tile (two 64-K boxes) in a ring of 3 stages (released by
+// the MMA's commit); a converter group widens the weight tile into its A stage as soon as the
+// MMAs that last read that stage completed, then waits for the token tile and signals the MMA
+// thread, which issues the stage's 8 MMAs and two commits (token stage, A stage) in one asm
+// block. Every mbarrier wait is bounded; a wait that runs out sets the plan's error word and
+// the CTA drains its own copies and MMAs, frees TMEM and returns.
 //
-// The down epilogue writes w * dequant(acc) per (row, channel) to yd; combine_kernel sums each
-// token's k routed rows and its shared-expert row in slot order (deterministic, no atomics).
-#include "gemm_common.cuh"
+// The down epilogue adds w * dequant(acc) of every (row, channel) into y[token, channel] with
+// fp32 reductions (y is zeroed by the permutation step), so the per-row outputs never go to
+// HBM and no separate combine pass runs; the order of the additions into y is not fixed.
+#include "common.cuh"
+#include "internal.h"
 
 namespace moe {
 
+constexpr int kW8Bytes = kBM * kKS;                  // int8 weight tile per stage (16 KB)
+constexpr int kXSubBytes = kMaxTokTile * kBK * 2;    // one 64-K token box (<= 24 KB)
+constexpr int kXStageBytes = 2 * kXSubBytes;         // token tile per stage (<= 48 KB)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACols = kKS / 2;                 // one A stage: 128 K of fp16 pairs
+constexpr int kAStages = 2;
+static_assert(kAccCols + kAStages * kACols == kTmemCols, "TMEM columns");
+static_assert(2 * kMaxTokTile <= kAccCols, "two accumulator slots");
+static_assert(kXSubBytes % 1024 == 0, "swizzled token boxes stay 1024-byte aligned");
+
+constexpr int kConvWarps = 4;  // one converter group: one thread per weight row
+#ifndef MOE_GU_EPI_WARPS
+#define MOE_GU_EPI_WARPS 8
+#endif
+#ifndef MOE_D_EPI_WARPS
+#define MOE_D_EPI_WARPS 12
+#endif
+template <bool GU>
+struct GemmRoles {
+  static constexpr int kEpiWarps = GU ? MOE_GU_EPI_WARPS : MOE_D_EPI_WARPS;
+  static constexpr int kColGroups = kEpiWarps / 4;
+  static constexpr int kConvGroups = kAStages;  // group g fills A stage g
+  static constexpr int kConvWarp0 = kEpiWarps;
+  static constexpr int kMmaWarp = kEpiWarps + kConvGroups * kConvWarps;
+  static constexpr int kWProducerWarp = kMmaWarp + 1;
+  static constexpr int kXProducerWarp = kWProducerWarp + 1;  // two warps
+  static constexpr int kThreads = (kXProducerWarp + 2) * 32;
+  static_assert(kEpiWarps % 4 == 0, "epilogue warps cover the four TMEM lane quadrants");
+  static_assert(kConvWarp0 % 4 == 0, "converter warp q%4 writes TMEM lane quadrant q%4");
+  static_assert(kThreads <= 1024, "block size");
+};
+
+#ifndef MOE_X_STAGES
+#define MOE_X_STAGES 3
+#endif
 #ifndef MOE_W_STAGES
 #define MOE_W_STAGES 4
 #endif
-#ifndef MOE_X_STAGES
-#define MOE_X_STAGES 4  // token stages of the gate/up GEMM
-#endif
-#ifndef MOE_D_X_STAGES
-#define MOE_D_X_STAGES 4  // token stages of the down GEMM
-#endif
-constexpr int kXBytesMax = kMaxTokTile * kBK * 2;    // fp16 token tile per stage (<= 32 KB)
-
-// Shared-memory layout of one GEMM instance: token stages, int8 weight stages, fp16 weight
-// buffers (buffer s goes with token stage s), barriers.
-template <bool GU>
+// Shared-memory layout: token stages, int8 weight stages, barriers.
 struct GemmSmem {
-  static constexpr int kXStages = GU ? MOE_X_STAGES : MOE_D_X_STAGES;
+  static constexpr int kXStages = MOE_X_STAGES;
   static constexpr int kWStages = MOE_W_STAGES;
-  static constexpr int kConvBufs = kXStages;
-  static constexpr int kOffW8 = kXStages * kXBytesMax;
-  static constexpr int kOffConv = kOffW8 + kWStages * kW8Bytes;
-  static constexpr int kOffBar = kOffConv + kConvBufs * kW16Bytes;
-  static constexpr int kBarBytes = 512;
+  static constexpr int kOffW8 = kXStages * kXStageBytes;
+  static constexpr int kOffBar = kOffW8 + kWStages * kW8Bytes;
+  static constexpr int kBarBytes = 256;
   static constexpr int kBytes = kOffBar + kBarBytes + 1024;
-  static_assert((2 * kXStages + 2 * kWStages + kConvBufs + 5) * 8 + 8 <= kBarBytes, "barriers");
+  static_assert((2 * kXStages + 2 * kWStages + 2 * kAStages + 5) * 8 + 8 <= kBarBytes, "barriers");
   static_assert(kBytes <= 232448, "shared memory");
-  static_assert(kOffW8 % 1024 == 0 && kOffConv % 1024 == 0,
-                "swizzled tiles stay 1024-byte aligned");
-  // Two producers per ring: stage s belongs to producer s % 2 (any stage count >= 2 works).
-  static_assert(kXStages >= 2 && kWStages >= 2, "two producers per ring");
+  static_assert(kOffW8 % 1024 == 0 && kOffBar % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
+  static_assert(kXStages >= 2 && kWStages >= 2, "two token producers");
 };
 
+// Whether one fp32 accumulator over the whole K is provably exact for this launch.
+__device__ __forceinline__ bool single_accumulator_exact(const GemmArgs& a) {
+  const unsigned long long r = (unsigned long long)(unsigned)*a.row_sq_max;
+  const unsigned long long w = (unsigned long long)(unsigned)*a.w_sq_max;
+  return r * w < (1ull << 48);
+}
 
+// 4 int8 (one word) -> 4 fp16, exactly: bytes v+128 placed under the fp16 exponent of 1024,
+// then 1152 subtracted. Element 0 lands in the low half of the first word.
+__device__ __forceinline__ uint2 widen4(uint32_t w) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+  const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), bias);
+  const __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), bias);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+
+// Converter thread of weight row r: one 128-K int8 row (128-byte-swizzled TMA tile) widened
+// to fp16 and stored as 64 TMEM columns of the thread's lane (K elements 2c, 2c+1 in column
+// c, the even element in the low half), in two halves of 32 columns.
+__device__ __forceinline__ void widen_row_to_tmem(const uint8_t* w8_tile, int r, uint32_t taddr) {
+  const uint8_t* src = w8_tile + r * 128;
+  const int sw = r & 7;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t o[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * ((4 * h + c) ^ sw));
+      const uint2 e0 = widen4(v.x), e1 = widen4(v.y), e2 = widen4(v.z), e3 = widen4(v.w);
+      o[8 * c + 0] = e0.x;
+      o[8 * c + 1] = e0.y;
+      o[8 * c + 2] = e1.x;
+      o[8 * c + 3] = e1.y;
+      o[8 * c + 4] = e2.x;
+      o[8 * c + 5] = e2.y;
+      o[8 * c + 6] = e3.x;
+      o[8 * c + 7] = e3.y;
+    }
+    tmem_st32(taddr + 32 * h, o);
+  }
+}
+
+// Epilogue column loop with one accumulator per tile: TMEM loads of the next 16-column chunk
+// are in flight while the current one is dequantised and stored (tcgen05.wait::ld waits for
+// all of a thread's outstanding loads, so the two register sets alternate). `store(v, c0)`
+// consumes the 16 int32 accumulators of chunk c0 (the fp32 words hold integers). With several
+// 1024-K chunks per tile, each chunk's partial sums are rounded to int32 and added in integer
+// arithmetic (the total may exceed what fp32 holds exactly).
+template <int kColGroups, typename Store>
+__device__ __forceinline__ void epilogue_columns(const GemmArgs& a, int nch, uint32_t tbase,
+                                                 int cg, int ncols, Store&& store) {
+  auto to_int = [](const uint32_t (&r)[16], int (&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __float2int_rn(__uint_as_float(r[i]));
+  };
+  if (nch == 1) {
+    uint32_t ra[16], rb[16];
+    int v[16];
+    constexpr int kStep = 16 * kColGroups;  // this warp's chunks: cg, cg + kColGroups, ...
+    int c0 = cg * 16;
+    if (c0 >= ncols) return;  // uniform over the warp
+    tmem_ld16(tbase + c0, ra);
+    tmem_ld_wait();
+#pragma unroll 1
+    for (; c0 < ncols; c0 += 2 * kStep) {
+      const int c1 = c0 + kStep;
+      if (c1 < ncols) tmem_ld16(tbase + c1, rb);
+      to_int(ra, v);
+      store(v, c0);
+      if (c1 >= ncols) break;
+      tmem_ld_wait();
+      const int c2 = c1 + kStep;
+      if (c2 < ncols) tmem_ld16(tbase + c2, ra);
+      to_int(rb, v);
+      store(v, c1);
+      if (c2 >= ncols) break;
+      tmem_ld_wait();
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int c0 = cg * 16; c0 < ncols; c0 += 16 * kColGroups) {
+    int v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0;
+#pragma unroll 1
+    for (int kc = 0; kc < nch; ++kc) {
+      uint32_t r[16];
+      tmem_ld16(tbase + kc * a.TN + c0, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] += __float2int_rn(__uint_as_float(r[i]));
+    }
+    store(v, c0);
+  }
+}
+
+// Gate/up epilogue. Lane pair (2i, 2i+1) of quadrant q holds gate and up of channel
+// m0/2 + 16q + i for every token column; the even lane finishes columns 0-7 of each 16-column
+// chunk and the odd lane columns 8-15. The rows' activation scales come from one load per
+// lane per chunk (lanes 0-15), taken by shuffle.
+__device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
+                                                 uint32_t tbase, int cg) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const bool odd = lane & 1;
+  const bool shared = wi.x == a.E;
+  const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
+  const float sgc = (shared ? a.sh_s_g : a.s_g + (size_t)wi.x * a.I)[ch];
+  const float suc = (shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I)[ch];
+  const int ncols = wi.z;
+  const int last = wi.y + ncols - 1;
+  epilogue_columns<GemmRoles<true>::kColGroups>(a, nch, tbase, cg, ncols,
+                                                [&](const int (&v)[16], int c0) {
+    const float lsx = a.sx[min(wi.y + c0 + (lane & 15), last)];
+    int recv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) recv[i] = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[8 + i], 1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int cc = (odd ? 8 : 0) + i;
+      const float sx = __shfl_sync(0xffffffffu, lsx, cc);
+      const int col = c0 + cc;
+      if (col < ncols) {
+        const int g = odd ? recv[i] : v[i];
+        const int u = odd ? v[8 + i] : recv[i];
+        const int row = wi.y + col;
+        a.h32[(size_t)row * a.Imax + ch] = silu_mul(dequant(g, sx, sgc), dequant(u, sx, suc));
+        if (a.tap) {
+          a.tap[(size_t)row * 2 * a.Imax + ch] = g;
+          a.tap[(size_t)row * 2 * a.Imax + a.Imax + ch] = u;
+        }
+      }
+    }
+  });
+}
+
+// Down epilogue: lane = output channel m0 + 32q + lane; for each token column the warp adds
+// w * dequant(acc) for 32 consecutive channels into that row's token row of y (one coalesced
+// 128-byte reduction). Each column's h scale, routing weight and token come from one or two
+// loads per lane per chunk, taken by shuffle.
+__device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase,
+                                              int cg) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const bool shared = wi.x == a.E;
+  const int o = wi.w + q * 32 + lane;
+  const float sdo = (shared ? a.sh_s_d : a.s_d + (size_t)wi.x * a.H)[o];
+  const int ncols = wi.z;
+  const int last = wi.y + ncols - 1;
+  epilogue_columns<GemmRoles<false>::kColGroups>(a, nch, tbase, cg, ncols,
+                                                 [&](const int (&v)[16], int c0) {
+    // lanes 0-15 hold the rows' h scales, lanes 16-31 their routing weights; every lane the
+    // token of row (lane & 15)
+    const int lrow = min(wi.y + c0 + (lane & 15), last);
+    const float lv = lane < 16 ? a.s_h[lrow] : a.row_w[lrow];
+    const int ltok = a.row_token[lrow];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float shr = __shfl_sync(0xffffffffu, lv, i);
+      const float wr = __shfl_sync(0xffffffffu, lv, 16 + i);
+      const int tok = __shfl_sync(0xffffffffu, ltok, i);
+      if (c0 + i < ncols) {
+        atomicAdd(a.y + (size_t)tok * a.H + o, __fmul_rn(wr, dequant(v[i], shr, sdo)));
+        if (a.tap) a.tap[(size_t)(wi.y + c0 + i) * a.H + o] = v[i];
+      }
+    }
+  });
+}
 
 template <bool GU>
 __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ XMaps tmX,
                         const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmWs) {
-  constexpr int kXStages = GemmSmem<GU>::kXStages, kWStages = GemmSmem<GU>::kWStages;
-  constexpr int kConvBufs = GemmSmem<GU>::kConvBufs;
-  constexpr int kOffW8 = GemmSmem<GU>::kOffW8, kOffConv = GemmSmem<GU>::kOffConv;
-  constexpr int kOffBar = GemmSmem<GU>::kOffBar;
+  constexpr int kXStages = GemmSmem::kXStages, kWStages = GemmSmem::kWStages;
+  constexpr int kOffW8 = GemmSmem::kOffW8, kOffBar = GemmSmem::kOffBar;
   using R = GemmRoles<GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -120,8 +304,9 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
   uint64_t* xempty = xfull + kXStages;     // [kXStages]
   uint64_t* wfull = xempty + kXStages;     // [kWStages]
   uint64_t* wempty = wfull + kWStages;     // [kWStages]
-  uint64_t* cfull = wempty + kWStages;     // [kConvBufs]
-  uint64_t* acc_full = cfull + kConvBufs;  // [2]
+  uint64_t* afull = wempty + kWStages;     // [kAStages]
+  uint64_t* aempty = afull + kAStages;     // [kAStages]
+  uint64_t* acc_full = aempty + kAStages;  // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -137,7 +322,10 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], kConvWarps);
     }
-    for (int s = 0; s < kConvBufs; ++s) mbar_init(&cfull[s], kConvWarps);
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&afull[s], kConvWarps);
+      mbar_init(&aempty[s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], R::kEpiWarps);
@@ -165,36 +353,36 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
   const int n_items = *a.n_items;
   // Accumulator layout for this launch: one accumulator over the whole K (two TMEM slots,
   // double-buffered) when the bound proves it exact, else 1024-K chunks (the host sizes the
-  // token tile so that the chunks of one tile fit the 512 columns).
+  // token tile so that the chunks of one tile fit the accumulator columns).
   const bool single = single_accumulator_exact(a);
   const int kmax = a.K_r > a.K_s ? a.K_r : a.K_s;
   const int slot_cols = single ? a.TN : ((kmax + kChunkK - 1) / kChunkK) * a.TN;
-  const int nslots = slot_cols <= (int)kTmemCols / 2 ? 2 : 1;
-  const int kpc = single ? (1 << 30) : kChunkK / kBK;  // k-blocks per accumulator
+  const int nslots = slot_cols <= kAccCols / 2 ? 2 : 1;
+  const int kpc = single ? (1 << 30) : kChunkK / kKS;  // stages per accumulator
 
   if (warp >= R::kWProducerWarp && warp < R::kXProducerWarp + 2) {
     if (lane == 0) {
-      // ------- TMA producers: weights (HBM) and tokens, two threads per ring -------
-      // Producer pidx of a ring owns the ring's stages with index % 2 == pidx; both walk the
-      // whole item / k-block sequence to keep stage and phase in step.
-      const bool wprod = warp < R::kXProducerWarp;
-      const int pidx = warp - (wprod ? R::kWProducerWarp : R::kXProducerWarp);
+      // ------- TMA producers: weights (HBM) and tokens (two threads, alternate stages) -------
+      // Every producer walks the whole item / stage sequence to keep stage and phase in step.
+      const bool wprod = warp == R::kWProducerWarp;
+      const int pidx = warp - R::kXProducerWarp;  // token producers only
       const int nst = wprod ? kWStages : kXStages;
       uint64_t* full = wprod ? wfull : xfull;
       uint64_t* empty = wprod ? wempty : xempty;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;  // stages with a load issued, and its phase
+      uint32_t ks = 0;                    // running stage index
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         const int4 wi = a.items[item];
         const bool shared = wi.x == a.E;
-        const int nkb = (shared ? a.K_s : a.K_r) / kBK;
-        const int rows = (wi.z + kXStep1 - 1) / kXStep1 * kXStep1;  // box height
-        const uint32_t bytes = wprod ? (uint32_t)kW8Bytes : (uint32_t)(rows * kBK * 2);
-        const CUtensorMap* mx = &tmX.m[rows / kXStep1 - 1];
-        for (int kb = 0; kb < nkb; ++kb) {
-          if ((stage & 1) == pidx) {
+        const int nks = ((shared ? a.K_s : a.K_r) + kKS - 1) / kKS;
+        const int rows = (wi.z + kXStep - 1) / kXStep * kXStep;  // box height
+        const uint32_t bytes = wprod ? (uint32_t)kW8Bytes : (uint32_t)(2 * rows * kBK * 2);
+        const CUtensorMap* mx = &tmX.m[rows / kXStep - 1];
+        for (int kb = 0; kb < nks; ++kb, ++ks) {
+          if (wprod || (int)(ks & 1) == pidx) {
             if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.err)) {
               ok = false;
               break;
@@ -203,11 +391,14 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
             if (wprod) {
               uint8_t* sw = smem + kOffW8 + stage * kW8Bytes;
               if (shared)
-                tma_load_2d(sw, &tmWs, &full[stage], kb * kBK, wi.w);
+                tma_load_2d(sw, &tmWs, &full[stage], kb * kKS, wi.w);
               else
-                tma_load_3d(sw, &tmW, &full[stage], kb * kBK, wi.w, wi.x);
+                tma_load_3d(sw, &tmW, &full[stage], kb * kKS, wi.w, wi.x);
             } else {
-              tma_load_2d(smem + stage * kXBytesMax, mx, &full[stage], kb * kBK, wi.y);
+              // the second box of a last stage past K reads zeros (out of bounds)
+              uint8_t* sx = smem + stage * kXStageBytes;
+              tma_load_2d(sx, mx, &full[stage], kb * kKS, wi.y);
+              tma_load_2d(sx + kXSubBytes, mx, &full[stage], kb * kKS + kBK, wi.y);
             }
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -230,57 +421,54 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       }
     }
   } else if (warp >= R::kConvWarp0 && warp < R::kConvWarp0 + R::kConvGroups * kConvWarps) {
-    // ---------------- converters: int8 -> fp16 weight rows ----------------
-    // Group g converts the k-blocks whose running index is g modulo R::kConvGroups, so the
-    // latency of one group's fence and arrivals overlaps the other groups' work. The fp16
-    // buffer of token stage cb is free once the MMAs of its previous use completed (the token
-    // stage's empty barrier).
+    // ---------------- converters: int8 weight rows -> fp16 A operand in TMEM ----------------
+    // Group g handles the stages of parity g and fills A stage g. The A stage is free once the
+    // MMAs of its previous use completed (aempty, committed by the MMA thread).
     const int cw = warp - R::kConvWarp0;
-    const int group = cw / kConvWarps;
-    const int r = (cw % kConvWarps) * 32 + lane;  // weight row within the tile
-    int stage = 0, cb = 0, gk = 0;
-    uint32_t phase = 0, cphase = 0;
+    const int g = cw / kConvWarps;
+    const int r = (cw % kConvWarps) * 32 + lane;  // weight row within the tile = TMEM lane
+    const uint32_t ta = tmem + ((uint32_t)((cw % kConvWarps) * 32) << 16) +
+                        (uint32_t)(kAccCols + g * kACols);
+    int ws = 0, xs = 0;
+    uint32_t wph = 0, xph = 0, aph = 0;
+    uint32_t ks = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       const int4 wi = a.items[item];
-      const int nkb = (wi.x == a.E ? a.K_s : a.K_r) / kBK;
-      for (int kb = 0; kb < nkb; ++kb, ++gk) {
-        if (gk % R::kConvGroups != group) {
-          if (++stage == kWStages) {
-            stage = 0;
-            phase ^= 1;
+      const int nks = ((wi.x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
+      for (int kb = 0; kb < nks; ++kb, ++ks) {
+        if ((int)(ks & 1) == g) {
+          // warp-uniform outcome: the per-warp arrivals below need every lane
+          const bool got = mbar_wait(&wfull[ws], wph, abort_flag, a.err) &&
+                           mbar_wait(&aempty[g], aph ^ 1, abort_flag, a.err);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
           }
-          if (++cb == kConvBufs) {
-            cb = 0;
-            cphase ^= 1;
+          tc_fence_after();  // the MMAs that read this A stage before have completed
+          widen_row_to_tmem(smem + kOffW8 + ws * kW8Bytes, r, ta);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&wempty[ws]);  // int8 tile read (values consumed)
+          tmem_st_wait();
+          tc_fence_before();
+          // The token stage is waited for after the conversion (which overlaps its load), so
+          // that afull alone tells the MMA thread that both operands are in place.
+          if (!__all_sync(0xffffffffu,
+                          lane != 0 || mbar_wait(&xfull[xs], xph, abort_flag, a.err))) {
+            ok = false;
+            break;
           }
-          continue;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afull[g]);
+          aph ^= 1;
         }
-        // warp-uniform outcome: the per-warp arrivals below need every lane
-        const bool got = mbar_wait(&wfull[stage], phase, abort_flag, a.err) &&
-                         mbar_wait(&xempty[cb], cphase ^ 1, abort_flag, a.err);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
+        if (++ws == kWStages) {
+          ws = 0;
+          wph ^= 1;
         }
-        widen_row(smem + kOffW8 + stage * kW8Bytes, smem + kOffConv + cb * kW16Bytes, r);
-        fence_proxy_async_smem();  // this thread's fp16 stores, before the MMA reads them
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&wempty[stage]);
-        // The token stage cb is waited for after the conversion (which overlaps its load), so
-        // that cfull alone tells the MMA thread that both operands are in shared memory.
-        if (!__all_sync(0xffffffffu, lane != 0 || mbar_wait(&xfull[cb], cphase, abort_flag, a.err))) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) mbar_arrive(&cfull[cb]);
-        if (++stage == kWStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-        if (++cb == kConvBufs) {
-          cb = 0;
-          cphase ^= 1;
+        if (++xs == kXStages) {
+          xs = 0;
+          xph ^= 1;
         }
       }
     }
@@ -288,21 +476,20 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       // The issuing thread is on the tensor pipe's critical path: tcgen05.mma issue blocks
-      // once the pipe's queue is full, so every instruction between the last MMA of a k-block
-      // and the first of the next leaves the pipe idle. Per k-block it therefore waits on one
-      // barrier only (cfull: converted weights and token stage), and usually not even that:
-      // mma_kblock_commit_probe probes the next k-block's barrier while the current MMAs
-      // issue. Descriptors are a base plus a stage offset (the 14-bit start-address field
-      // does not carry).
-      const uint64_t dw0 = smem_desc_sw128(smem_u32(smem + kOffConv));
+      // once the pipe's queue is full, so every instruction between the last MMA of a stage
+      // and the first of the next leaves the pipe idle. Per stage it waits on one barrier
+      // (afull: A stage written and token stage landed), and usually not even that:
+      // mma_stage_ts probes the next stage's barrier while the current MMAs issue.
+      // Descriptors are a base plus a stage offset (the 14-bit start-address field does not
+      // carry).
       const uint64_t dx0 = smem_desc_sw128(smem_u32(smem));
-      int stage = 0;
-      uint32_t phase = 0, ready = 0;
+      int xs = 0;
+      uint32_t ks = 0, ready = 0;
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++it) {
         const int4 wi = a.items[item];
-        const int nkb = (wi.x == a.E ? a.K_s : a.K_r) / kBK;
+        const int nks = ((wi.x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
         const int n_mma = (wi.z + 15) & ~15;
         const uint32_t idesc = idesc_f16_f32(kBM, n_mma);
         const int slot = it % nslots;
@@ -310,25 +497,24 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
         if (!mbar_wait(&acc_empty[slot], use ^ 1, abort_flag, a.err)) break;
         tc_fence_after();
         uint32_t dt = tmem + (uint32_t)(slot * slot_cols);
-        int kin = 0;  // k-block within the current accumulator chunk
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!ready && !mbar_wait(&cfull[stage], phase, abort_flag, a.err)) {
+        int kin = 0;  // stage within the current accumulator chunk
+        for (int kb = 0; kb < nks; ++kb, ++ks) {
+          const int g = (int)(ks & 1);
+          if (!ready && !mbar_wait(&afull[g], (ks >> 1) & 1u, abort_flag, a.err)) {
             ok = false;
             break;
           }
-          const int ns = stage + 1 == kXStages ? 0 : stage + 1;
-          const uint32_t nph = ns == 0 ? phase ^ 1u : phase;
-          // one commit frees the token stage and the fp16 weight buffer that goes with it
-          ready = mma_kblock_commit_probe<false>(
-              dt, dw0 + (uint64_t)((stage * kW16Bytes) >> 4),
-              dx0 + (uint64_t)((stage * kXBytesMax) >> 4), idesc, kin != 0 ? 1u : 0u,
-              smem_u32(&xempty[stage]), smem_u32(&cfull[ns]), nph);
+          const uint32_t kn = ks + 1;
+          const uint64_t b0 = dx0 + (uint64_t)((xs * kXStageBytes) >> 4);
+          ready = mma_stage_ts(dt, tmem + (uint32_t)(kAccCols + g * kACols), b0,
+                               b0 + (uint64_t)(kXSubBytes >> 4), idesc, kin != 0 ? 1u : 0u,
+                               smem_u32(&xempty[xs]), smem_u32(&aempty[g]),
+                               smem_u32(&afull[kn & 1]), (kn >> 1) & 1u);
           if (++kin == kpc) {
             kin = 0;
             dt += (uint32_t)a.TN;
           }
-          stage = ns;
-          phase = nph;
+          if (++xs == kXStages) xs = 0;
         }
         if (!ok) break;
         umma_commit(&acc_full[slot]);
@@ -373,73 +559,35 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
 
 cudaError_t gemm_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem<true>::kBytes);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem::kBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem<false>::kBytes);
-  if (e == cudaSuccess) e = pair_set_attributes();
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem::kBytes);
   return e;
 }
 
-// Work items that can run at once: CTAs for cs = 1, CTA pairs for cs = 2.
-cudaError_t gemm_max_clusters(bool gate_up, int cs, int* n) {
+// CTAs of the GEMM that can run at once (one per SM).
+cudaError_t gemm_max_ctas(bool gate_up, int* n) {
   *n = 0;
-  if (cs == 2) return pair_max_clusters(gate_up, n);
-  if (cs != 1) return cudaErrorInvalidValue;
   int per_sm = 0, dev = 0, sms = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &per_sm, gate_up ? (const void*)grouped_gemm_kernel<true> : (const void*)grouped_gemm_kernel<false>,
-      gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads,
-      gate_up ? GemmSmem<true>::kBytes : GemmSmem<false>::kBytes);
+      gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads, GemmSmem::kBytes);
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   *n = per_sm * sms;
   return e;
 }
 
-// grid: a multiple of cs (whole clusters).
-cudaError_t launch_grouped_gemm(bool gate_up, int cs, const GemmArgs& a, const XMaps& tmX,
+cudaError_t launch_grouped_gemm(bool gate_up, const GemmArgs& a, const XMaps& tmX,
                                 const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
                                 cudaStream_t s) {
-  if (grid < cs || grid % cs) return cudaErrorInvalidValue;
-  if (cs == 2) return launch_pair_gemm(gate_up, a, tmX, tmW, tmWs, grid, s);
-  if (cs != 1) return cudaErrorInvalidValue;
+  if (grid < 1) return cudaErrorInvalidValue;
   if (gate_up)
     return launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(GemmRoles<true>::kThreads),
-                      GemmSmem<true>::kBytes, s, a, tmX, tmW, tmWs);
+                      GemmSmem::kBytes, s, a, tmX, tmW, tmWs);
   return launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(GemmRoles<false>::kThreads),
-                    GemmSmem<false>::kBytes, s, a, tmX, tmW, tmWs);
-}
-
-// y[t] = sum over slots j of yd[row(t, j)] + yd[t] (shared expert row), in slot order. Block per
-// token, 8 consecutive channels per thread and pass.
-__global__ void combine_kernel(const float* __restrict__ yd, const int* __restrict__ slot_row,
-                               int T, int k, int H, int has_shared, float* __restrict__ y) {
-  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
-  pdl_trigger();
-  const int t = blockIdx.x;
-  __shared__ int rows[9];
-  if (threadIdx.x < k) rows[threadIdx.x] = slot_row[(size_t)t * k + threadIdx.x];
-  if (threadIdx.x == k) rows[k] = has_shared ? t : -1;
-  __syncthreads();
-  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j <= k; ++j) {
-      const int r = rows[j];
-      if (r < 0) continue;
-      const float4 v = *reinterpret_cast<const float4*>(yd + (size_t)r * H + c);
-      acc.x = __fadd_rn(acc.x, v.x);
-      acc.y = __fadd_rn(acc.y, v.y);
-      acc.z = __fadd_rn(acc.z, v.z);
-      acc.w = __fadd_rn(acc.w, v.w);
-    }
-    *reinterpret_cast<float4*>(y + (size_t)t * H + c) = acc;
-  }
-}
-
-cudaError_t launch_combine(const float* yd, const int* slot_row, int T, int k, int H,
-                           int has_shared, float* y, cudaStream_t s) {
-  return launch_pdl(combine_kernel, dim3(T), dim3(256), 0, s, yd, slot_row, T, k, H, has_shared, y);
+                    GemmSmem::kBytes, s, a, tmX, tmW, tmWs);
 }
 
 // Per-row requantisation of h = SiLU(gate)*up: s = amax/127, q = rne(h/s) (|q| <= 127),

@@ -12,22 +12,24 @@ namespace moe {
 
 constexpr int kBM = 128;        // tensor-core tile rows (weight rows: the MMA's M)
 #ifndef MOE_MAX_TOK_TILE
-#define MOE_MAX_TOK_TILE 256
+#define MOE_MAX_TOK_TILE 192
 #endif
 constexpr int kMaxTokTile = MOE_MAX_TOK_TILE;  // token rows per tile (the MMA's N), at most
-static_assert(kMaxTokTile % 32 == 0 && kMaxTokTile <= 256, "token tile");
-// Token-tile TMA boxes: one tensor map per box height over the same token-row operand, so
-// that the token tile of a k-block is one TMA load. Heights are multiples of kXStep1 (16)
-// rows up to 256 for the one-CTA kernel, and of kXStep2 (8) rows up to 128 for the CTA pair
-// (each CTA of a pair holds half of the tile).
-constexpr int kXStep1 = 16;
-constexpr int kXStep2 = 8;
-constexpr int kXMaps = 16;
+static_assert(kMaxTokTile % 16 == 0 && kMaxTokTile <= 192, "token tile");
+// Token-tile TMA boxes: one tensor map per box height (multiples of kXStep rows up to the
+// token tile) over the same token-row operand, so that each 64-K half of a token stage is one
+// TMA load.
+constexpr int kXStep = 16;
+constexpr int kXMaps = kMaxTokTile / kXStep;
 struct XMaps {
   CUtensorMap m[kXMaps];
 };
-constexpr int kBK = 64;         // K elements per pipeline stage (128 bytes of fp16)
+constexpr int kBK = 64;         // K elements per token TMA box (128 bytes of fp16)
+constexpr int kKS = 128;        // K elements per pipeline stage (two token boxes, 8 MMAs)
 constexpr int kChunkK = 1024;   // K elements summed in one fp32 TMEM accumulator
+// TMEM columns of the GEMMs: two accumulator slots of up to kMaxTokTile columns each, then
+// the A-operand stages (one 128-row x 128-K fp16 weight tile = 64 columns each).
+constexpr int kAccCols = 384;
 constexpr int kTokPerBlk = 64;  // tokens per histogram block (one 64-bit mask per expert)
 constexpr int kDecodeMaxRows = 8;
 constexpr int kDecodeMaxH = 8192;  // largest H and intermediate size the decode kernels take
@@ -58,7 +60,7 @@ struct GemmArgs {
   const float* sh_s_d;   // [H]
   const int* row_token;  // per row
   const float* row_w;    // per row
-  float* yd;             // [R, H] weighted per-row down outputs
+  float* y;              // [T, H] layer output: every row adds w * d into its token's row
   // exactness bound of one fp32 accumulator over the whole K (see gemm_tc.cu)
   const int* row_sq_max;  // max over A rows of sum(q^2), written by the row producer
   const int* w_sq_max;    // max over weight rows of sum(q_w^2), written at packing
@@ -67,16 +69,12 @@ struct GemmArgs {
   int* err;
 };
 
-// cs: 1 (one CTA per item of one weight tile) or 2 (a CTA pair per item of two adjacent weight
-// tiles, on the 2-SM MMA); grid a multiple of cs.
-cudaError_t launch_grouped_gemm(bool gate_up, int cs, const GemmArgs& a, const XMaps& tmX,
+cudaError_t launch_grouped_gemm(bool gate_up, const GemmArgs& a, const XMaps& tmX,
                                 const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
                                 cudaStream_t s);
 cudaError_t gemm_set_attributes();
-cudaError_t gemm_max_clusters(bool gate_up, int cs, int* n);
+cudaError_t gemm_max_ctas(bool gate_up, int* n);
 
-cudaError_t launch_combine(const float* yd, const int* slot_row, int T, int k, int H,
-                           int has_shared, float* y, cudaStream_t s);
 cudaError_t launch_requant(const float* h32, int R, int T_sh, int I, int Is, int Imax,
                            __half* hq, float* sh, int* sq_max, cudaStream_t s);
 
@@ -89,7 +87,6 @@ struct PrepArgs {
   const float* w;
   const uint16_t* x;
   int T, k, E, H, I, Is, has_shared, tn_gu, tn_d;
-  int cs_gu, cs_d;            // weight tiles per work item (the GEMMs' cluster sizes)
   unsigned long long* bmask;  // [nblk, E]
   int* bhist;                 // [nblk, E]
   int* counts;                // [E]
@@ -102,7 +99,7 @@ struct PrepArgs {
   float* sx;                  // [R]
   int* row_token;             // [R]
   float* row_w;               // [R]
-  int* slot_row;              // [T*k] row of each routed slot
+  float* y;                   // [T, H] layer output, zeroed here (the down GEMM adds into it)
   int8_t* qtok;               // [T, H] or NULL
   float* stok;                // [T]   or NULL
   int* sq_max;                // [2] row sum(q^2) maxima (gate/up rows, down rows), reset here

@@ -17,7 +17,6 @@ struct moe_plan_s {
   int E = 0, k = 0, H = 0, I = 0, Is = 0, max_tokens = 0, Imax = 0, has_shared = 0;
   int device = 0, num_sms = 0;
   int tn_gu = 0, tn_d = 0;  // token tiles of the two GEMMs
-  int cs_gu = 1, cs_d = 1;  // cluster sizes of the two GEMMs (weight tiles per work item)
   int grid_gu = 0, grid_d = 0;
   size_t R_max = 0;
   int max_items_gu = 0, max_items_d = 0;
@@ -26,8 +25,6 @@ struct moe_plan_s {
   float* sx = nullptr;
   int* row_token = nullptr;
   float* row_w = nullptr;
-  int* slot_row = nullptr;   // [max_tokens * k]
-  float* yd = nullptr;       // [R, H] weighted per-row down outputs
   float* h32 = nullptr;
   __half* hq = nullptr;  // [R, Imax] codes of SiLU(gate)*up (fp16 integers)
   float* sh = nullptr;
@@ -58,9 +55,8 @@ struct moe_plan_s {
   };
   std::vector<ProfRec> prof_pending;
   std::vector<cudaEvent_t> ev_pool;
-  // token rows of the two GEMMs (N operand), one map per box height: boxes of the one-CTA
-  // kernel (16-row steps) and of the CTA pair (8-row steps)
-  XMaps tmX1_gu, tmX1_d, tmX2_gu, tmX2_d;
+  // token rows of the two GEMMs (N operand), one map per box height (16-row steps)
+  XMaps tmX_gu, tmX_d;
   std::vector<void*> allocs;
 };
 
@@ -111,17 +107,17 @@ bool encode_2byte(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int 
   return r == CUDA_SUCCESS;
 }
 
-// int8 weight tiles: box {64 bytes, box_rows[, 1]}, 64-byte swizzle.
+// int8 weight tiles: box {128 bytes (one 128-K stage), box_rows[, 1]}, 128-byte swizzle.
 bool encode_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                const uint64_t* strides_bytes, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[3], st[2];
-  cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, 1}, es[3] = {1, 1, 1};
+  cuuint32_t box[3] = {(cuuint32_t)kKS, box_rows, 1}, es[3] = {1, 1, 1};
   for (int i = 0; i < rank; ++i) d[i] = dims[i];
   for (int i = 0; i < rank - 1; ++i) st[i] = strides_bytes[i];
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), d, st, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -156,11 +152,12 @@ void free_plan(moe_plan_s* p) {
   delete p;
 }
 
-// Token tile: 256 rows, or fewer when the exact 1024-K chunks of one tile would not fit the
-// 512 TMEM columns (chunks x tile <= 512), a multiple of 32.
+// Token tile of a GEMM with reduction length K: kMaxTokTile rows, or fewer when the exact
+// 1024-K chunks of one tile would not fit the accumulator columns (chunks x tile <= kAccCols),
+// a multiple of 16.
 int token_tile(int K) {
   const int nch = (K + kChunkK - 1) / kChunkK;
-  int tn = (512 / nch) & ~31;
+  int tn = (kAccCols / nch) & ~15;
   return tn > kMaxTokTile ? kMaxTokTile : tn;
 }
 
@@ -207,15 +204,13 @@ size_t tap_bytes(const moe_plan_s* p, int which, int T) {
 }  // namespace
 
 namespace {
-// Grid of each GEMM for its current cluster size.
+// Grid of each GEMM: as many CTAs as fit at once (one per SM).
 cudaError_t size_gemm_grids(moe_plan_s* p) {
   for (int gu = 0; gu < 2; ++gu) {
-    const int cs = gu ? p->cs_gu : p->cs_d;
     int n = 0;
-    const cudaError_t e = gemm_max_clusters(gu != 0, cs, &n);
+    const cudaError_t e = gemm_max_ctas(gu != 0, &n);
     if (e != cudaSuccess) return e;
-    if (n < 1) n = std::max(1, p->num_sms / cs);
-    (gu ? p->grid_gu : p->grid_d) = n * cs;
+    (gu ? p->grid_gu : p->grid_d) = n < 1 ? p->num_sms : n;
   }
   return cudaSuccess;
 }
@@ -290,8 +285,6 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   ALLOC(sx, p->R_max);
   ALLOC(row_token, p->R_max);
   ALLOC(row_w, p->R_max);
-  ALLOC(slot_row, T * top_k);
-  ALLOC(yd, p->R_max * H);
   ALLOC(h32, p->R_max * p->Imax);
   ALLOC(hq, p->R_max * p->Imax);
   ALLOC(sh, p->R_max);
@@ -322,11 +315,9 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
     const uint64_t dims_d[2] = {(uint64_t)p->Imax, (uint64_t)p->R_max};
     const uint64_t st_d[1] = {(uint64_t)p->Imax * 2};
     for (int j = 0; j < kXMaps; ++j) {
-      const uint32_t r1 = (uint32_t)(kXStep1 * (j + 1)), r2 = (uint32_t)(kXStep2 * (j + 1));
-      if (!encode_f16(&p->tmX1_gu.m[j], p->xq, 2, dims, st2, r1) ||
-          !encode_f16(&p->tmX1_d.m[j], p->hq, 2, dims_d, st_d, r1) ||
-          !encode_f16(&p->tmX2_gu.m[j], p->xq, 2, dims, st2, r2) ||
-          !encode_f16(&p->tmX2_d.m[j], p->hq, 2, dims_d, st_d, r2)) {
+      const uint32_t r1 = (uint32_t)(kXStep * (j + 1));
+      if (!encode_f16(&p->tmX_gu.m[j], p->xq, 2, dims, st2, r1) ||
+          !encode_f16(&p->tmX_d.m[j], p->hq, 2, dims_d, st_d, r1)) {
         free_plan(p);
         return MOE_ERR_CUDA;
       }
@@ -334,8 +325,6 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   }
   cudaError_t e = gemm_set_attributes();
   if (e == cudaSuccess) e = decode_set_attributes();
-  // One CTA per weight tile by default (moe_plan_use_cta_pairs switches a GEMM to CTA pairs);
-  // the grid is as many whole clusters as fit at once.
   if (e == cudaSuccess) e = size_gemm_grids(p);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -509,8 +498,6 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   pa.has_shared = p->has_shared;
   pa.tn_gu = p->tn_gu;
   pa.tn_d = p->tn_d;
-  pa.cs_gu = p->cs_gu;
-  pa.cs_d = p->cs_d;
   pa.bmask = p->bmask;
   pa.bhist = p->bhist;
   pa.counts = p->counts;
@@ -523,7 +510,7 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   pa.sx = p->sx;
   pa.row_token = p->row_token;
   pa.row_w = p->row_w;
-  pa.slot_row = p->slot_row;
+  pa.y = y;
   pa.qtok = p->debug ? p->qtok : nullptr;
   pa.stok = p->debug ? p->stok : nullptr;
   pa.sq_max = p->sq_max;
@@ -551,7 +538,7 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.sh_s_d = pk->w.sh_s_down;
   g.row_token = p->row_token;
   g.row_w = p->row_w;
-  g.yd = p->yd;
+  g.y = y;
   g.err = p->err;
   // gate/up: K = H for every group
   g.items = p->items_gu;
@@ -562,8 +549,8 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.tap = p->debug ? p->tap_gu : nullptr;
   g.row_sq_max = p->sq_max;
   g.w_sq_max = pk->w_sq;
-  if ((e = launch_grouped_gemm(true, p->cs_gu, g, p->cs_gu == 2 ? p->tmX2_gu : p->tmX1_gu, pk->tmW_gu,
-                               pk->tmWs_gu, p->grid_gu, s)) != cudaSuccess)
+  if ((e = launch_grouped_gemm(true, g, p->tmX_gu, pk->tmW_gu, pk->tmWs_gu, p->grid_gu, s)) !=
+      cudaSuccess)
     return cuda_status(e);
   if (ev) cudaEventRecord(ev[2], s);
   if ((e = launch_requant(p->h32, R, T_sh, p->I, p->Is, p->Imax, p->hq, p->sh, p->sq_max + 1, s)) !=
@@ -579,25 +566,9 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   g.tap = p->debug ? p->tap_d : nullptr;
   g.row_sq_max = p->sq_max + 1;
   g.w_sq_max = pk->w_sq + 1;
-  e = launch_grouped_gemm(false, p->cs_d, g, p->cs_d == 2 ? p->tmX2_d : p->tmX1_d, pk->tmW_d,
-                          pk->tmWs_d, p->grid_d, s);
-  if (e == cudaSuccess) e = launch_combine(p->yd, p->slot_row, T, p->k, p->H, p->has_shared, y, s);
+  e = launch_grouped_gemm(false, g, p->tmX_d, pk->tmW_d, pk->tmWs_d, p->grid_d, s);
   if (ev) cudaEventRecord(ev[4], s);
   return cuda_status(e);
-}
-
-moe_status moe_plan_use_cta_pairs(moe_plan_t p, int gate_up, int down) {
-  if (!p) return MOE_ERR_INVALID_ARG;
-  const bool gu_even = (2 * p->I / kBM) % 2 == 0 && (!p->has_shared || (2 * p->Is / kBM) % 2 == 0);
-  const bool d_even = (p->H / kBM) % 2 == 0;
-  if ((gate_up && !gu_even) || (down && !d_even)) return MOE_ERR_UNSUPPORTED;
-  p->cs_gu = gate_up ? 2 : 1;
-  p->cs_d = down ? 2 : 1;
-  if (size_gemm_grids(p) != cudaSuccess) {
-    cudaGetLastError();
-    return MOE_ERR_CUDA;
-  }
-  return MOE_OK;
 }
 
 moe_status moe_profile_enable(moe_plan_t p, int on) {

@@ -8,7 +8,8 @@
 //                    experts, and the grouped-GEMM work lists (expert-tile queue).
 //  scatter_kernel    block per token: per-token int8 quantisation of x, the codes written as
 //                    fp16 integers into every row the token occupies (one per routed slot plus
-//                    the shared expert's row) with 16-byte stores; row metadata.
+//                    the shared expert's row) with 16-byte stores; row metadata; the token's
+//                    row of y zeroed (the down GEMM adds every row's output into it).
 // Row order: the shared expert's rows [0, T) first (row t = token t), then the routed
 // assignments grouped by expert id and, inside an expert, by token. This is the order a
 // stable sort of the flattened idx by expert id gives.
@@ -166,9 +167,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 
 // One block of 1024 threads. Turns bhist into exclusive per-expert prefixes over blocks,
 // writes counts/offsets and the two work lists (gate/up and down): per group, every
-// (cs adjacent 128-row weight tiles, token tile of at most TN rows) pair, ordered by group,
-// then weight tiles, then token tile, so consecutive items of a large group reuse one weight
-// tile from L2.
+// (128-row weight tile, token tile) pair, ordered by group, then weight tile, then token tile,
+// so consecutive items of a large group reuse one weight tile from L2. A group of cnt rows is
+// split into ceil(cnt / TN) token tiles of equal size (within one row), so no tile is a thin
+// remainder.
 __global__ void scan_kernel(PrepArgs a, int nblk) {
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
@@ -227,8 +229,8 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
   if (g < ng) {
     const bool sh = a.has_shared && g == 0;
     const int cnt = sh ? a.T : s_cnt[g - a.has_shared];
-    ngu = (2 * (sh ? a.Is : a.I)) / (kBM * a.cs_gu) * ((cnt + a.tn_gu - 1) / a.tn_gu);
-    nd = a.H / (kBM * a.cs_d) * ((cnt + a.tn_d - 1) / a.tn_d);
+    ngu = (2 * (sh ? a.Is : a.I)) / kBM * ((cnt + a.tn_gu - 1) / a.tn_gu);
+    nd = a.H / kBM * ((cnt + a.tn_d - 1) / a.tn_d);
   }
   const int bgu = block_exclusive_scan(ngu, s_warp, &total);
   if (g < ng) s_base_gu[g] = bgu;
@@ -248,7 +250,6 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
     const int* base = list == 0 ? s_base_gu : s_base_d;
     const int n = base[ng];
     const int tn = list == 0 ? a.tn_gu : a.tn_d;
-    const int wstep = kBM * (list == 0 ? a.cs_gu : a.cs_d);  // weight rows per item
     int4* items = list == 0 ? a.items_gu : a.items_d;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       int lo = 0, hi = ng - 1;  // last group with base <= i
@@ -264,7 +265,8 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
       const int tt = (cnt + tn - 1) / tn;
       const int local = i - base[gg];
       const int wt = local / tt, t = local % tt;
-      items[i] = make_int4(gid, row0 + t * tn, min(tn, cnt - t * tn), wt * wstep);
+      const int r0 = (int)((long long)t * cnt / tt), r1 = (int)((long long)(t + 1) * cnt / tt);
+      items[i] = make_int4(gid, row0 + r0, r1 - r0, wt * kBM);
     }
   }
 }
@@ -295,7 +297,6 @@ __global__ void scatter_kernel(PrepArgs a) {
     a.perm[pos] = t * k + j;
     const int row = T_sh + pos;
     s_rows[j] = row;
-    a.slot_row[(size_t)t * k + j] = row;
     a.row_token[row] = t;
     a.row_w[row] = a.w[(size_t)t * k + j];
   } else if (threadIdx.x == k && a.has_shared) {
@@ -303,6 +304,8 @@ __global__ void scatter_kernel(PrepArgs a) {
     a.row_token[t] = t;
     a.row_w[t] = 1.0f;
   }
+  float4* y4 = reinterpret_cast<float4*>(a.y + (size_t)t * H);
+  for (int c = threadIdx.x; c < H / 4; c += blockDim.x) y4[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   // amax over the row (8 bf16 per thread per pass)
   const uint16_t* xr = a.x + (size_t)t * H;
   float amax = 0.0f;

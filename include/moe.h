@@ -169,22 +169,13 @@ MOE_API moe_status moe_debug_enable(moe_plan_t plan, int on);
 MOE_API size_t moe_debug_tap_bytes(moe_plan_t plan, int which);
 MOE_API moe_status moe_debug_tap(moe_plan_t plan, int which, void* dst_host, size_t bytes);
 
-/* Run the gate/up GEMM and/or the down GEMM on CTA pairs: the 2-SM tcgen05 MMA (cta_group::2),
- * one work item = two adjacent 128-row weight tiles of one token tile, each CTA of the pair
- * holding its own weight rows and half of the tokens. Results are identical to the default
- * (one CTA per weight tile). Needs an even weight-tile count in every group of that GEMM
- * (2*I/128 and 2*I_shared/128 for gate/up, H/128 for down), else MOE_ERR_UNSUPPORTED and the
- * plan is unchanged; 0 switches a GEMM back. Default: both off (faster on the workloads
- * measured so far). Call while no forward on the plan is in flight. */
-MOE_API moe_status moe_plan_use_cta_pairs(moe_plan_t plan, int gate_up, int down);
-
 /* ---- per-stage device timing (benchmark instrument) ----------------------------------
  * When enabled, every moe_forward also records CUDA events around its kernels on the call's
  * stream (no extra synchronisation). moe_profile_read synchronises on those events and
  * writes, for the chosen path (0 = prefill, 1 = decode), the summed device milliseconds of
  * each stage over all forwards since the previous read into ms_out[4] and their number into
  * *calls, then starts a new accumulation. Stages: prefill {permute+quant, gate/up GEMM,
- * requant, down GEMM + combine}; decode {dedup+quant, gate/up stream, down stream +
+ * requant, down GEMM adding into y}; decode {dedup+quant, gate/up stream, down stream +
  * combine, 0}. Not for use inside CUDA graph capture. */
 MOE_API moe_status moe_profile_enable(moe_plan_t plan, int on);
 MOE_API moe_status moe_profile_read(moe_plan_t plan, int path, float* ms_out, int* calls);

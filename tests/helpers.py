@@ -16,6 +16,7 @@ Y_RMSE_REL = 5e-3     # rms(dy) <= Y_RMSE_REL * rms(y_ref)
 W_ABS = 1e-6          # routing weights
 HQ_MISMATCH_FRAC = 1e-3
 DOWN_SKIP_FRAC = 1e-3   # rows left out of the bit-exact down comparison by an h-code tie
+SH_ULPS = 4             # h scales: amax / 127 of SiLU outputs that may differ in the last ulp
 
 
 def weights_to(W: dict, device) -> dict:
@@ -99,7 +100,13 @@ def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L: oracle.
                 assert dq.max() <= 1, (t, s)
                 n_hq_diff += int((dq != 0).sum())
                 n_hq += Ig
-                if dq.max() == 0 and shs[r] == tp["sh"][i, s]:
+                # the row's scale comes from an amax over SiLU outputs whose exp may differ in
+                # the last ulp between the CUDA and host math libraries
+                s_o = np.float32(tp["sh"][i, s])
+                assert abs(float(shs[r]) - float(s_o)) <= SH_ULPS * float(np.spacing(s_o)), (t, s)
+                # the down accumulators depend only on the h codes (not on their scale): compared
+                # bit-exactly on every row whose codes agree
+                if dq.max() == 0:
                     assert (acc_d[r] == tp["acc_d"][i, s]).all(), (t, s)
                     n_rows_d += 1
         assert n_hq_diff <= HQ_MISMATCH_FRAC * n_hq, (n_hq_diff, n_hq)
@@ -111,6 +118,8 @@ def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L: oracle.
         yg = y.cpu().numpy().astype(np.float64)[toks]
         mx, rm = y_errors(yg, y_o)
         assert mx <= Y_MAX_REL and rm <= Y_RMSE_REL, (mx, rm)
+        print(f"parity: y max_rel {mx:.2e} rmse_rel {rm:.2e}; h codes differing {n_hq_diff} of "
+              f"{n_hq}; down rows compared bit-exactly {n_rows_d} of {n_rows}")
         return dict(max_rel=mx, rmse_rel=rm, hq_diff=n_hq_diff, hq_total=n_hq,
                     rows_down_exact=n_rows_d, y=y, idx=idx_g, w=w_g, tap=tap)
     finally:

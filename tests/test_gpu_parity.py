@@ -309,8 +309,7 @@ def test_residual_add():
     assert torch.equal(xd.cpu().view(torch.int16), ref.view(torch.int16))
 
 
-@pytest.mark.parametrize("pairs", [False, True])
-def test_adversarial_rows_take_the_exact_chunked_path(pairs):
+def test_adversarial_rows_take_the_exact_chunked_path():
     # Constant token rows quantise to +-127 everywhere and one gate row of expert 0 is all 127:
     # the gate accumulator reaches 2048 * 127^2 > 2^24, beyond what one fp32 accumulator holds
     # exactly, and the product of the row/weight sum-of-squares bounds exceeds 2^48, so the
@@ -329,40 +328,11 @@ def test_adversarial_rows_take_the_exact_chunked_path(pairs):
     Wd = weights_to(W, "cuda")
     layer = moe.MoELayer(sh.E, sh.k, sh.H, sh.I, sh.Is, sh.T, Wd)
     try:
-        if pairs:
-            moe.moe_plan_use_cta_pairs(layer.plan, True, True)
         st = check_layer(sh, x, lg, Wd, oracle_layer(W, sh), layer=layer)
     finally:
         layer.close()
     gu = st["tap"]["acc_gu"]
     assert np.abs(gu).max() == 2048 * 127 * 127
-
-
-@pytest.mark.parametrize("name", ["tiny", "prefill"])
-def test_cta_pair_gemms_match_the_oracle(name):
-    # The 2-SM MMA path (two CTAs per item of two weight tiles, each holding half of the
-    # tokens) against the oracle: the same bit-exact integers and y tolerances.
-    wl, d = _host_layer(name)
-    sh = wl.shape
-    W = weights_to(d["weights"], "cuda")
-    layer = moe.MoELayer(sh.E, sh.k, sh.H, sh.I, sh.Is, sh.T, W)
-    try:
-        moe.moe_plan_use_cta_pairs(layer.plan, True, True)
-        check_layer(sh, d["x"], d["logits"], W, oracle_layer(d["weights"], sh), layer=layer)
-    finally:
-        layer.close()
-
-
-def test_cta_pairs_need_even_weight_tile_counts():
-    # shared expert with 2 * 192 / 128 = 3 gate/up weight tiles: no pairs for gate/up
-    plan = moe.moe_plan(16, 4, 256, 128, 192, 64)
-    try:
-        with pytest.raises(moe.MoeError):
-            moe.moe_plan_use_cta_pairs(plan, True, False)
-        moe.moe_plan_use_cta_pairs(plan, False, True)  # down: H / 128 = 2 tiles
-        moe.moe_plan_use_cta_pairs(plan, False, False)
-    finally:
-        moe.moe_plan_destroy(plan)
 
 
 @pytest.mark.parametrize("T", [2600, 77])
