@@ -44,23 +44,23 @@
 // (128 rows x 128 K of fp16) in [384, 512).
 //
 // Warp roles (one CTA per SM; GemmRoles):
-//   epilogue warps (8 for gate/up, 12 for down): warp w reads TMEM lanes 32*(w%4).. (weight
+//   epilogue warps (12 for each GEMM): warp w reads TMEM lanes 32*(w%4).. (weight
 //               rows) and every (w/4)-th 16-column chunk (tokens) of its quadrant;
-//   two converter groups of four warps: group g fills A stage g for every stage index of
-//               parity g, thread r of a group widening weight row r;
+//   two converter groups of four warps: group h widens K half h (64 K) of every stage into
+//               the stage's A stage, thread r of a group widening weight row r;
 //   one MMA issuer and TMEM owner;
 //   one TMA producer of the int8 weight tiles, two of the token tiles (alternate stages).
 // Pipeline per 128-K stage: the weight tile lands in a ring of 4 int8 stages (released by the
 // converters once read); the token tile (two 64-K boxes) in a ring of 3 stages (released by
-// the MMA's commit); a converter group widens the weight tile into its A stage as soon as the
-// MMAs that last read that stage completed, then waits for the token tile and signals the MMA
-// thread, which issues the stage's 8 MMAs and two commits (token stage, A stage) in one asm
-// block. Every mbarrier wait is bounded; a wait that runs out sets the plan's error word and
+// the MMA's commit); the two converter groups widen their K halves of the next stage into
+// registers ahead and store them into A stage ks % 2 as soon as the MMAs that last read it
+// completed; the MMA thread waits for the A stage and the token stage and issues the stage's
+// 8 MMAs and two commits (token stage, A stage) in one asm block. Every mbarrier wait is bounded; a wait that runs out sets the plan's error word and
 // the CTA drains its own copies and MMAs, frees TMEM and returns.
 //
 // The down epilogue adds w * dequant(acc) of every (row, channel) into y[token, channel] with
-// fp32 reductions (y is zeroed by the permutation step), so the per-row outputs never go to
-// HBM and no separate combine pass runs; the order of the additions into y is not fixed.
+// 16-byte fp32 reductions (y is zeroed by the permutation step), so the per-row outputs never
+// go to HBM and no separate combine pass runs; the order of the additions into y is not fixed.
 #include "common.cuh"
 #include "internal.h"
 
@@ -78,7 +78,7 @@ static_assert(kXSubBytes % 1024 == 0, "swizzled token boxes stay 1024-byte align
 
 constexpr int kConvWarps = 4;  // one converter group: one thread per weight row
 #ifndef MOE_GU_EPI_WARPS
-#define MOE_GU_EPI_WARPS 8
+#define MOE_GU_EPI_WARPS 12
 #endif
 #ifndef MOE_D_EPI_WARPS
 #define MOE_D_EPI_WARPS 12
@@ -87,7 +87,7 @@ template <bool GU>
 struct GemmRoles {
   static constexpr int kEpiWarps = GU ? MOE_GU_EPI_WARPS : MOE_D_EPI_WARPS;
   static constexpr int kColGroups = kEpiWarps / 4;
-  static constexpr int kConvGroups = kAStages;  // group g fills A stage g
+  static constexpr int kConvGroups = 2;  // group h widens K half h of every stage
   static constexpr int kConvWarp0 = kEpiWarps;
   static constexpr int kMmaWarp = kEpiWarps + kConvGroups * kConvWarps;
   static constexpr int kWProducerWarp = kMmaWarp + 1;
@@ -137,36 +137,63 @@ __device__ __forceinline__ uint2 widen4(uint32_t w) {
   return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
 }
 
-// Converter thread of weight row r: one 128-K int8 row (128-byte-swizzled TMA tile) widened
-// to fp16 and stored as 64 TMEM columns of the thread's lane (K elements 2c, 2c+1 in column
-// c, the even element in the low half), in two halves of 32 columns.
-__device__ __forceinline__ void widen_row_to_tmem(const uint8_t* w8_tile, int r, uint32_t taddr) {
+// Converter thread of weight row r, half h of a 128-K stage: 64 int8 weights of the row
+// (128-byte-swizzled TMA tile) widened to fp16 pairs in 32 registers, laid out as the 32
+// TMEM columns of the thread's lane that the MMA reads (K elements 2c, 2c+1 in column c, the
+// even element in the low half).
+__device__ __forceinline__ void widen_half_row(const uint8_t* w8_tile, int r, int h,
+                                               uint32_t (&o)[32]) {
   const uint8_t* src = w8_tile + r * 128;
   const int sw = r & 7;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t o[32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * ((4 * h + c) ^ sw));
-      const uint2 e0 = widen4(v.x), e1 = widen4(v.y), e2 = widen4(v.z), e3 = widen4(v.w);
-      o[8 * c + 0] = e0.x;
-      o[8 * c + 1] = e0.y;
-      o[8 * c + 2] = e1.x;
-      o[8 * c + 3] = e1.y;
-      o[8 * c + 4] = e2.x;
-      o[8 * c + 5] = e2.y;
-      o[8 * c + 6] = e3.x;
-      o[8 * c + 7] = e3.y;
-    }
-    tmem_st32(taddr + 32 * h, o);
+  for (int c = 0; c < 4; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * ((4 * h + c) ^ sw));
+    const uint2 e0 = widen4(v.x), e1 = widen4(v.y), e2 = widen4(v.z), e3 = widen4(v.w);
+    o[8 * c + 0] = e0.x;
+    o[8 * c + 1] = e0.y;
+    o[8 * c + 2] = e1.x;
+    o[8 * c + 3] = e1.y;
+    o[8 * c + 4] = e2.x;
+    o[8 * c + 5] = e2.y;
+    o[8 * c + 6] = e3.x;
+    o[8 * c + 7] = e3.y;
   }
+}
+
+// 16-column chunks one epilogue warp handles per tile (its column group takes every
+// kColGroups-th chunk of at most kMaxTokTile columns).
+template <int kColGroups>
+__host__ __device__ constexpr int kEpiChunks() {
+  return (kMaxTokTile / 16 + kColGroups - 1) / kColGroups;
+}
+
+// Per-item values an epilogue lane needs, loaded before the accumulator is ready so that
+// their latency overlaps the wait: the output channel's weight scales, and per chunk j the
+// row values of column (lane & 15) of the chunk.
+template <bool GU>
+struct EpiMeta {
+  static constexpr int kJ = kEpiChunks<(GU ? MOE_GU_EPI_WARPS : MOE_D_EPI_WARPS) / 4>();
+  float s0, s1;       // gate/up: gate and up scale of the channel; down: scale of the channel
+  float rv[kJ];       // gate/up: the row's activation scale; down: h scale (lanes 0-15) or
+                      // routing weight (lanes 16-31) of the row
+  int tok[GU ? 1 : kJ];  // down: the row's token
+};
+
+// a[j] without dynamic register indexing (j is a compile-time constant in the common path).
+template <typename T, int N>
+__device__ __forceinline__ T pick(const T (&a)[N], int j) {
+  T r = a[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i)
+    if (j == i) r = a[i];
+  return r;
 }
 
 // Epilogue column loop with one accumulator per tile: TMEM loads of the next 16-column chunk
 // are in flight while the current one is dequantised and stored (tcgen05.wait::ld waits for
-// all of a thread's outstanding loads, so the two register sets alternate). `store(v, c0)`
-// consumes the 16 int32 accumulators of chunk c0 (the fp32 words hold integers). With several
+// all of a thread's outstanding loads, so the two register sets alternate). `store(v, c0, j)`
+// consumes the 16 int32 accumulators of chunk c0, this warp's j-th chunk (the fp32 words hold
+// integers). With several
 // 1024-K chunks per tile, each chunk's partial sums are rounded to int32 and added in integer
 // arithmetic (the total may exceed what fp32 holds exactly).
 template <int kColGroups, typename Store>
@@ -184,25 +211,25 @@ __device__ __forceinline__ void epilogue_columns(const GemmArgs& a, int nch, uin
     if (c0 >= ncols) return;  // uniform over the warp
     tmem_ld16(tbase + c0, ra);
     tmem_ld_wait();
-#pragma unroll 1
-    for (; c0 < ncols; c0 += 2 * kStep) {
+#pragma unroll
+    for (int j = 0; j < kEpiChunks<kColGroups>(); j += 2, c0 += 2 * kStep) {
       const int c1 = c0 + kStep;
       if (c1 < ncols) tmem_ld16(tbase + c1, rb);
       to_int(ra, v);
-      store(v, c0);
+      store(v, c0, j);
       if (c1 >= ncols) break;
       tmem_ld_wait();
       const int c2 = c1 + kStep;
       if (c2 < ncols) tmem_ld16(tbase + c2, ra);
       to_int(rb, v);
-      store(v, c1);
+      store(v, c1, j + 1);
       if (c2 >= ncols) break;
       tmem_ld_wait();
     }
     return;
   }
 #pragma unroll 1
-  for (int c0 = cg * 16; c0 < ncols; c0 += 16 * kColGroups) {
+  for (int c0 = cg * 16, j = 0; c0 < ncols; c0 += 16 * kColGroups, ++j) {
     int v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0;
@@ -214,40 +241,50 @@ __device__ __forceinline__ void epilogue_columns(const GemmArgs& a, int nch, uin
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] += __float2int_rn(__uint_as_float(r[i]));
     }
-    store(v, c0);
+    store(v, c0, j);
   }
 }
 
 // Gate/up epilogue. Lane pair (2i, 2i+1) of quadrant q holds gate and up of channel
 // m0/2 + 16q + i for every token column; the even lane finishes columns 0-7 of each 16-column
-// chunk and the odd lane columns 8-15. The rows' activation scales come from one load per
-// lane per chunk (lanes 0-15), taken by shuffle.
-__device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
-                                                 uint32_t tbase, int cg) {
+// chunk and the odd lane columns 8-15. Each column's activation scale is taken by shuffle from
+// the lane that loaded it.
+__device__ __forceinline__ void load_meta_gate_up(const GemmArgs& a, int4 wi, int cg,
+                                                  EpiMeta<true>& m) {
+  constexpr int kCG = GemmRoles<true>::kColGroups;
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
-  const bool odd = lane & 1;
   const bool shared = wi.x == a.E;
   const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
-  const float sgc = (shared ? a.sh_s_g : a.s_g + (size_t)wi.x * a.I)[ch];
-  const float suc = (shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I)[ch];
+  m.s0 = (shared ? a.sh_s_g : a.s_g + (size_t)wi.x * a.I)[ch];
+  m.s1 = (shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I)[ch];
+  const int last = wi.y + wi.z - 1;
+#pragma unroll
+  for (int j = 0; j < EpiMeta<true>::kJ; ++j)
+    m.rv[j] = a.sx[min(wi.y + cg * 16 + j * 16 * kCG + (lane & 15), last)];
+}
+
+__device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
+                                                 uint32_t tbase, int cg, const EpiMeta<true>& m) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const bool odd = lane & 1;
+  const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
   const int ncols = wi.z;
-  const int last = wi.y + ncols - 1;
   epilogue_columns<GemmRoles<true>::kColGroups>(a, nch, tbase, cg, ncols,
-                                                [&](const int (&v)[16], int c0) {
-    const float lsx = a.sx[min(wi.y + c0 + (lane & 15), last)];
+                                                [&](const int (&v)[16], int c0, int j) {
     int recv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) recv[i] = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[8 + i], 1);
+    const float rvj = pick(m.rv, j);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int cc = (odd ? 8 : 0) + i;
-      const float sx = __shfl_sync(0xffffffffu, lsx, cc);
+      const float sx = __shfl_sync(0xffffffffu, rvj, cc);
       const int col = c0 + cc;
       if (col < ncols) {
         const int g = odd ? recv[i] : v[i];
         const int u = odd ? v[8 + i] : recv[i];
         const int row = wi.y + col;
-        a.h32[(size_t)row * a.Imax + ch] = silu_mul(dequant(g, sx, sgc), dequant(u, sx, suc));
+        a.h32[(size_t)row * a.Imax + ch] = silu_mul(dequant(g, sx, m.s0), dequant(u, sx, m.s1));
         if (a.tap) {
           a.tap[(size_t)row * 2 * a.Imax + ch] = g;
           a.tap[(size_t)row * 2 * a.Imax + a.Imax + ch] = u;
@@ -257,34 +294,83 @@ __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int
   });
 }
 
-// Down epilogue: lane = output channel m0 + 32q + lane; for each token column the warp adds
-// w * dequant(acc) for 32 consecutive channels into that row's token row of y (one coalesced
-// 128-byte reduction). Each column's h scale, routing weight and token come from one or two
-// loads per lane per chunk, taken by shuffle.
-__device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase,
-                                              int cg) {
+// y[0..3] += v, one 16-byte fp32 reduction (the address is 16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* p, float a0, float a1, float a2, float a3) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a0), "f"(a1),
+               "f"(a2), "f"(a3)
+               : "memory");
+}
+
+// 4 x 4 transpose within each lane quad: on entry lane b (= lane % 4) holds v[i] = M[b][i],
+// on exit v[i] = M[i][b]. Two butterfly stages (partners b^1, then b^2), two shuffles each.
+__device__ __forceinline__ void quad_transpose(float (&v)[4], int lane) {
+  const bool h1 = (lane & 1) != 0, h2 = (lane & 2) != 0;
+#pragma unroll
+  for (int p = 0; p < 4; p += 2) {
+    const float recv = __shfl_xor_sync(0xffffffffu, h1 ? v[p] : v[p + 1], 1);
+    if (h1)
+      v[p] = recv;
+    else
+      v[p + 1] = recv;
+  }
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const float recv = __shfl_xor_sync(0xffffffffu, h2 ? v[p] : v[p + 2], 2);
+    if (h2)
+      v[p] = recv;
+    else
+      v[p + 2] = recv;
+  }
+}
+
+// Down epilogue: lane = output channel m0 + 32q + lane holds w * dequant(acc) of 16 token
+// columns per chunk. A 4 x 4 transpose within each lane quad gives every lane four
+// consecutive channels of one token, added into y with one 16-byte reduction: each warp
+// instruction adds 128 contiguous bytes into each of four token rows of y. Each column's h
+// scale, routing weight and token are taken by shuffle from the lanes that loaded them.
+__device__ __forceinline__ void load_meta_down(const GemmArgs& a, int4 wi, int cg,
+                                               EpiMeta<false>& m) {
+  constexpr int kCG = GemmRoles<false>::kColGroups;
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const bool shared = wi.x == a.E;
-  const int o = wi.w + q * 32 + lane;
-  const float sdo = (shared ? a.sh_s_d : a.s_d + (size_t)wi.x * a.H)[o];
-  const int ncols = wi.z;
-  const int last = wi.y + ncols - 1;
-  epilogue_columns<GemmRoles<false>::kColGroups>(a, nch, tbase, cg, ncols,
-                                                 [&](const int (&v)[16], int c0) {
-    // lanes 0-15 hold the rows' h scales, lanes 16-31 their routing weights; every lane the
-    // token of row (lane & 15)
-    const int lrow = min(wi.y + c0 + (lane & 15), last);
-    const float lv = lane < 16 ? a.s_h[lrow] : a.row_w[lrow];
-    const int ltok = a.row_token[lrow];
+  m.s0 = (shared ? a.sh_s_d : a.s_d + (size_t)wi.x * a.H)[wi.w + q * 32 + lane];
+  const int last = wi.y + wi.z - 1;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float shr = __shfl_sync(0xffffffffu, lv, i);
-      const float wr = __shfl_sync(0xffffffffu, lv, 16 + i);
-      const int tok = __shfl_sync(0xffffffffu, ltok, i);
-      if (c0 + i < ncols) {
-        atomicAdd(a.y + (size_t)tok * a.H + o, __fmul_rn(wr, dequant(v[i], shr, sdo)));
-        if (a.tap) a.tap[(size_t)(wi.y + c0 + i) * a.H + o] = v[i];
+  for (int j = 0; j < EpiMeta<false>::kJ; ++j) {
+    const int lrow = min(wi.y + cg * 16 + j * 16 * kCG + (lane & 15), last);
+    m.rv[j] = lane < 16 ? a.s_h[lrow] : a.row_w[lrow];
+    m.tok[j] = a.row_token[lrow];
+  }
+}
+
+__device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase,
+                                              int cg, const EpiMeta<false>& m) {
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+  const int o = wi.w + q * 32 + lane;
+  const int ncols = wi.z;
+  const int b = lane & 3;
+  float* yq = a.y + (o - b);  // first channel of this lane's quad
+  epilogue_columns<GemmRoles<false>::kColGroups>(a, nch, tbase, cg, ncols,
+                                                 [&](const int (&v)[16], int c0, int j) {
+    if (a.tap) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (c0 + i < ncols) a.tap[(size_t)(wi.y + c0 + i) * a.H + o] = v[i];
+    }
+    const float rvj = pick(m.rv, j);
+    const int tokj = pick(m.tok, j);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      float t[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float shr = __shfl_sync(0xffffffffu, rvj, 4 * jj + i);
+        const float wr = __shfl_sync(0xffffffffu, rvj, 16 + 4 * jj + i);
+        t[i] = __fmul_rn(wr, dequant(v[4 * jj + i], shr, m.s0));
       }
+      quad_transpose(t, lane);  // t[i]: channel (o - b + i), column 4jj + b
+      const int tok = __shfl_sync(0xffffffffu, tokj, 4 * jj + b);
+      if (c0 + 4 * jj + b < ncols) red_add_v4(yq + (size_t)tok * a.H, t[0], t[1], t[2], t[3]);
     }
   });
 }
@@ -320,10 +406,10 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     }
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(&wfull[s], 1);
-      mbar_init(&wempty[s], kConvWarps);
+      mbar_init(&wempty[s], R::kConvGroups * kConvWarps);  // every converter warp reads it
     }
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&afull[s], kConvWarps);
+      mbar_init(&afull[s], R::kConvGroups * kConvWarps);
       mbar_init(&aempty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -422,69 +508,64 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     }
   } else if (warp >= R::kConvWarp0 && warp < R::kConvWarp0 + R::kConvGroups * kConvWarps) {
     // ---------------- converters: int8 weight rows -> fp16 A operand in TMEM ----------------
-    // Group g handles the stages of parity g and fills A stage g. The A stage is free once the
-    // MMAs of its previous use completed (aempty, committed by the MMA thread).
+    // Both groups work on every stage: group h widens K half h (64 K) of each weight row into
+    // the stage's A stage (ks % 2). A group widens the next stage's half into registers as
+    // soon as its int8 tile has landed, and only then waits for the A stage to be free (the
+    // MMAs that last read it completed, aempty): after that wait just the TMEM store, its
+    // completion and the arrival remain on the path from one stage's MMAs to the next's.
     const int cw = warp - R::kConvWarp0;
-    const int g = cw / kConvWarps;
+    const int h = cw / kConvWarps;                // K half of every stage
     const int r = (cw % kConvWarps) * 32 + lane;  // weight row within the tile = TMEM lane
     const uint32_t ta = tmem + ((uint32_t)((cw % kConvWarps) * 32) << 16) +
-                        (uint32_t)(kAccCols + g * kACols);
-    int ws = 0, xs = 0;
-    uint32_t wph = 0, xph = 0, aph = 0;
+                        (uint32_t)(kAccCols + 32 * h);
+    uint32_t o[32];
+    int item = blockIdx.x, kb = 0;
+    int nks = item < n_items ? ((a.items[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS : 0;
     uint32_t ks = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      const int4 wi = a.items[item];
-      const int nks = ((wi.x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
-      for (int kb = 0; kb < nks; ++kb, ++ks) {
-        if ((int)(ks & 1) == g) {
-          // warp-uniform outcome: the per-warp arrivals below need every lane
-          const bool got = mbar_wait(&wfull[ws], wph, abort_flag, a.err) &&
-                           mbar_wait(&aempty[g], aph ^ 1, abort_flag, a.err);
-          if (!__all_sync(0xffffffffu, got)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();  // the MMAs that read this A stage before have completed
-          widen_row_to_tmem(smem + kOffW8 + ws * kW8Bytes, r, ta);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&wempty[ws]);  // int8 tile read (values consumed)
-          tmem_st_wait();
-          tc_fence_before();
-          // The token stage is waited for after the conversion (which overlaps its load), so
-          // that afull alone tells the MMA thread that both operands are in place.
-          if (!__all_sync(0xffffffffu,
-                          lane != 0 || mbar_wait(&xfull[xs], xph, abort_flag, a.err))) {
-            ok = false;
-            break;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&afull[g]);
-          aph ^= 1;
-        }
-        if (++ws == kWStages) {
-          ws = 0;
-          wph ^= 1;
-        }
-        if (++xs == kXStages) {
-          xs = 0;
-          xph ^= 1;
-        }
+    // widen stage k's half into o and release the int8 tile
+    auto load = [&](uint32_t k) -> bool {
+      const int ws = (int)(k % kWStages);
+      if (!__all_sync(0xffffffffu, mbar_wait(&wfull[ws], (k / kWStages) & 1u, abort_flag, a.err)))
+        return false;
+      widen_half_row(smem + kOffW8 + ws * kW8Bytes, r, h, o);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wempty[ws]);  // values consumed: the int8 tile may be reused
+      return true;
+    };
+    bool ok = item < n_items && load(0);
+    while (ok) {
+      const int as = (int)(ks & 1);
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&aempty[as], ((ks >> 1) & 1u) ^ 1u, abort_flag, a.err)))
+        break;
+      tc_fence_after();  // the MMAs that read this A stage before have completed
+      tmem_st32(ta + (uint32_t)(as * kACols), o);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[as]);
+      ++ks;
+      if (++kb == nks) {
+        kb = 0;
+        item += gridDim.x;
+        if (item >= n_items) break;
+        nks = ((a.items[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
       }
+      ok = load(ks);
     }
   } else if (warp == R::kMmaWarp) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       // The issuing thread is on the tensor pipe's critical path: tcgen05.mma issue blocks
       // once the pipe's queue is full, so every instruction between the last MMA of a stage
-      // and the first of the next leaves the pipe idle. Per stage it waits on one barrier
-      // (afull: A stage written and token stage landed), and usually not even that:
-      // mma_stage_ts probes the next stage's barrier while the current MMAs issue.
+      // and the first of the next leaves the pipe idle. Per stage it waits for the A stage
+      // (afull; usually already seen by the probe inside the previous stage's issue block)
+      // and for the token stage (xfull).
       // Descriptors are a base plus a stage offset (the 14-bit start-address field does not
       // carry).
       const uint64_t dx0 = smem_desc_sw128(smem_u32(smem));
       int xs = 0;
-      uint32_t ks = 0, ready = 0;
+      uint32_t xph = 0, ks = 0, ready = 0;
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++it) {
@@ -504,6 +585,10 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
             ok = false;
             break;
           }
+          if (!mbar_test(&xfull[xs], xph) && !mbar_wait(&xfull[xs], xph, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
           const uint32_t kn = ks + 1;
           const uint64_t b0 = dx0 + (uint64_t)((xs * kXStageBytes) >> 4);
           ready = mma_stage_ts(dt, tmem + (uint32_t)(kAccCols + g * kACols), b0,
@@ -514,7 +599,10 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
             kin = 0;
             dt += (uint32_t)a.TN;
           }
-          if (++xs == kXStages) xs = 0;
+          if (++xs == kXStages) {
+            xs = 0;
+            xph ^= 1;
+          }
         }
         if (!ok) break;
         umma_commit(&acc_full[slot]);
@@ -536,13 +624,18 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       const int nch = single ? 1 : (K + kChunkK - 1) / kChunkK;
       const int slot = it % nslots;
       const uint32_t use = (uint32_t)(it / nslots) & 1u;
+      EpiMeta<GU> m;
+      if constexpr (GU)
+        load_meta_gate_up(a, wi, cg, m);
+      else
+        load_meta_down(a, wi, cg, m);
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[slot], use, abort_flag, a.err))) break;
       tc_fence_after();
       const uint32_t tbase = lane_base + (uint32_t)(slot * slot_cols);
-      if (GU)
-        epilogue_gate_up(a, wi, nch, tbase, cg);
+      if constexpr (GU)
+        epilogue_gate_up(a, wi, nch, tbase, cg, m);
       else
-        epilogue_down(a, wi, nch, tbase, cg);
+        epilogue_down(a, wi, nch, tbase, cg, m);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[slot]);
