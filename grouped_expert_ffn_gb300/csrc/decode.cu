@@ -3,6 +3,8 @@
 // int8 dot (dp4a) into exact int32 accumulators. This is the kernel the page "[job] Strix
 // Halo: multi-session serving ... #145" names as the C>1 limiter (section "Status", items
 // "Batched decode doesn't scale" and "Next": expert dedup across rows plus int8 dot).
+// All four launches use programmatic dependent launch: each kernel's blocks may be scheduled
+// while its predecessor drains and wait for it in pdl_wait before touching global memory.
 //
 //  decode_prep_kernel  block 0: the unique-expert list (with the shared expert as group 0)
 //                      and the canonical row order; block 1 + t: token t's int8 quant
@@ -104,6 +106,8 @@ __device__ __forceinline__ void prep_quantise_token(const DecodeArgs& a, int t) 
 }
 
 __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(DecodeArgs a) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   if (blockIdx.x > 0) {
     prep_quantise_token(a, blockIdx.x - 1);
     return;
@@ -191,6 +195,8 @@ constexpr int kDownRowsPerBlock = 64;    // 8 warps x 8 output rows
 
 __global__ void __launch_bounds__(256) decode_gu_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) int8_t xs[];  // [8][H]
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   const int g = blockIdx.y;
   if (g >= *a.n_groups) return;
   const int4 grp = a.groups[g];
@@ -250,6 +256,8 @@ __global__ void __launch_bounds__(256) decode_gu_kernel(DecodeArgs a) {
 __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) int8_t hs[];  // [8][Imax]
   __shared__ float shs[kDecodeMaxRows];
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
   const int g = blockIdx.y;
   if (g >= *a.n_groups) return;
   const int4 grp = a.groups[g];
@@ -314,23 +322,23 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) {
   const int R = a.T * a.k + (a.has_shared ? a.T : 0);
   if (ev) cudaEventRecord(ev[0], s);
-  decode_prep_kernel<<<1 + a.T, kPrepThreads, 0, s>>>(a);
+  cudaError_t e = launch_pdl(decode_prep_kernel, dim3(1 + a.T), dim3(kPrepThreads), 0, s, a);
   if (ev) cudaEventRecord(ev[1], s);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int gmax = min(a.E, a.T * a.k) + (a.has_shared ? 1 : 0);
   const dim3 ggu((a.Imax + kGuChannelsPerBlock - 1) / kGuChannelsPerBlock, gmax);
-  decode_gu_kernel<<<ggu, 256, kDecodeMaxRows * a.H, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(decode_gu_kernel, ggu, dim3(256), (size_t)kDecodeMaxRows * a.H, s, a)) !=
+      cudaSuccess)
+    return e;
   // one requantisation of every h row (warp per row), instead of one per down block
   e = launch_requant(a.h32, R, a.has_shared ? a.T : 0, a.I, a.Is, a.Imax, a.hq, a.sh,
                      a.sq_scratch, s);
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[2], s);
   const dim3 gd(a.H / kDownRowsPerBlock, gmax);
-  decode_down_kernel<<<gd, 256, kDecodeMaxRows * a.Imax, s>>>(a);
+  e = launch_pdl(decode_down_kernel, gd, dim3(256), (size_t)kDecodeMaxRows * a.Imax, s, a);
   if (ev) cudaEventRecord(ev[3], s);
-  return cudaGetLastError();
+  return e;
 }
 
 bool decode_shape_supported(int H, int Imax) { return H <= kDecodeMaxH && Imax <= kDecodeMaxI; }
