@@ -101,6 +101,9 @@ struct GemmRoles {
 #ifndef MOE_X_STAGES
 #define MOE_X_STAGES 3
 #endif
+#ifndef MOE_L2_HINTS
+#define MOE_L2_HINTS 1  // weight tiles evict-first, h32 evict-last (read again by requant)
+#endif
 #ifndef MOE_W_STAGES
 #define MOE_W_STAGES 4
 #endif
@@ -174,6 +177,7 @@ template <bool GU>
 struct EpiMeta {
   static constexpr int kJ = kEpiChunks<(GU ? MOE_GU_EPI_WARPS : MOE_D_EPI_WARPS) / 4>();
   float s0, s1;       // gate/up: gate and up scale of the channel; down: scale of the channel
+  uint64_t pol;       // gate/up: L2 policy of the h32 stores
   float rv[kJ];       // gate/up: the row's activation scale; down: h scale (lanes 0-15) or
                       // routing weight (lanes 16-31) of the row
   int tok[GU ? 1 : kJ];  // down: the row's token
@@ -257,6 +261,7 @@ __device__ __forceinline__ void load_meta_gate_up(const GemmArgs& a, int4 wi, in
   const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
   m.s0 = (shared ? a.sh_s_g : a.s_g + (size_t)wi.x * a.I)[ch];
   m.s1 = (shared ? a.sh_s_u : a.s_u + (size_t)wi.x * a.I)[ch];
+  m.pol = l2_policy_evict_last();
   const int last = wi.y + wi.z - 1;
 #pragma unroll
   for (int j = 0; j < EpiMeta<true>::kJ; ++j)
@@ -284,7 +289,11 @@ __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int
         const int g = odd ? recv[i] : v[i];
         const int u = odd ? v[8 + i] : recv[i];
         const int row = wi.y + col;
-        a.h32[(size_t)row * a.Imax + ch] = silu_mul(dequant(g, sx, m.s0), dequant(u, sx, m.s1));
+        const float hv = silu_mul(dequant(g, sx, m.s0), dequant(u, sx, m.s1));
+        if (MOE_L2_HINTS)
+          st_f32_hint(a.h32 + (size_t)row * a.Imax + ch, hv, m.pol);  // read again by requant
+        else
+          a.h32[(size_t)row * a.Imax + ch] = hv;
         if (a.tap) {
           a.tap[(size_t)row * 2 * a.Imax + ch] = g;
           a.tap[(size_t)row * 2 * a.Imax + a.Imax + ch] = u;
@@ -459,6 +468,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;  // stages with a load issued, and its phase
       uint32_t ks = 0;                    // running stage index
+      const uint64_t pol_first = l2_policy_evict_first();  // weights: read once
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         const int4 wi = a.items[item];
@@ -476,7 +486,12 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
             mbar_arrive_expect_tx(&full[stage], bytes);
             if (wprod) {
               uint8_t* sw = smem + kOffW8 + stage * kW8Bytes;
-              if (shared)
+              if (MOE_L2_HINTS) {
+                if (shared)
+                  tma_load_2d_hint(sw, &tmWs, &full[stage], kb * kKS, wi.w, pol_first);
+                else
+                  tma_load_3d_hint(sw, &tmW, &full[stage], kb * kKS, wi.w, wi.x, pol_first);
+              } else if (shared)
                 tma_load_2d(sw, &tmWs, &full[stage], kb * kKS, wi.w);
               else
                 tma_load_3d(sw, &tmW, &full[stage], kb * kKS, wi.w, wi.x);
