@@ -758,10 +758,11 @@ __device__ __forceinline__ float requant_row_loop(const float* __restrict__ h, i
   return s;
 }
 
-// Each warp takes kRows consecutive rows and issues the loads of all of them before reducing
-// any (more bytes in flight per warp); rows of up to 128 * kRegV values stay in registers.
-constexpr int kRequantRows = 2;
-constexpr int kRequantThreads = 512;
+// Each warp takes kRequantRows consecutive rows and issues the loads of all of them before
+// reducing any; rows of up to 128 * kRegV values stay in registers. Small blocks of one row per
+// warp give many short waves, so that no second wave runs nearly alone.
+constexpr int kRequantRows = 1;
+constexpr int kRequantThreads = 256;
 
 template <int kRegV>
 __global__ void __launch_bounds__(kRequantThreads) requant_kernel(

@@ -171,7 +171,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 // so consecutive items of a large group reuse one weight tile from L2. A group of cnt rows is
 // split into ceil(cnt / TN) token tiles of equal size (within one row), so no tile is a thin
 // remainder.
-__global__ void scan_kernel(PrepArgs a, int nblk) {
+__global__ void __launch_bounds__(1024) scan_kernel(PrepArgs a, int nblk) {
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
   __shared__ int s_cnt[257];
@@ -182,33 +182,48 @@ __global__ void scan_kernel(PrepArgs a, int nblk) {
   const int E = a.E;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
   // exclusive prefix over blocks of each expert's histogram (row e of [E][nblk]), warp per
-  // expert, 128 blocks per pass with independent loads
-  for (int e = warp; e < E; e += nwarps) {
-    int* row = a.bhist + (size_t)e * nblk;
-    int carry = 0;
-    for (int b0 = 0; b0 < nblk; b0 += 128) {
-      int v[4];
+  // expert; a warp takes its experts kSE at a time with all their loads issued together
+  // (128 blocks per pass), so the load latency is paid once per pass, not once per expert
+  constexpr int kSE = 4;
+  for (int e0 = warp; e0 < E; e0 += nwarps * kSE) {
+    int carry[kSE];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int b = b0 + i * 32 + lane;
-        v[i] = b < nblk ? row[b] : 0;
+    for (int x = 0; x < kSE; ++x) carry[x] = 0;
+    for (int b0 = 0; b0 < nblk; b0 += 128) {
+      int v[kSE][4];
+#pragma unroll
+      for (int x = 0; x < kSE; ++x) {
+        const int e = e0 + x * nwarps;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int b = b0 + i * 32 + lane;
+          v[x][i] = e < E && b < nblk ? a.bhist[(size_t)e * nblk + b] : 0;
+        }
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        int incl = v[i];
+      for (int x = 0; x < kSE; ++x) {
+        const int e = e0 + x * nwarps;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int n = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += n;
+        for (int i = 0; i < 4; ++i) {
+          int incl = v[x][i];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+          }
+          const int b = b0 + i * 32 + lane;
+          if (e < E && b < nblk) a.bhist[(size_t)e * nblk + b] = carry[x] + incl - v[x][i];
+          carry[x] += __shfl_sync(0xffffffffu, incl, 31);
         }
-        const int b = b0 + i * 32 + lane;
-        if (b < nblk) row[b] = carry + incl - v[i];
-        carry += __shfl_sync(0xffffffffu, incl, 31);
       }
     }
-    if (lane == 0) {
-      s_cnt[e] = carry;
-      a.counts[e] = carry;
+#pragma unroll
+    for (int x = 0; x < kSE; ++x) {
+      const int e = e0 + x * nwarps;
+      if (lane == 0 && e < E) {
+        s_cnt[e] = carry[x];
+        a.counts[e] = carry[x];
+      }
     }
   }
   __syncthreads();
