@@ -40,6 +40,8 @@ GU_TRAFFIC_BYTES = 403.0e6
 # Kernels one stacked-prefill layer launches: RMS pre-norm, router projection, routing, and
 # the forward's histogram, scan, scatter, gate/up GEMM, requantisation, down GEMM.
 LAUNCHES_PER_LAYER = 9
+# moe_forward's default dispatch threshold (T <= this runs the weight-streaming kernels).
+DEFAULT_DECODE_ROWS = 32
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -240,9 +242,61 @@ def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
             "us_per_layer": us_layer, "unique_experts": U,
             "unique_bytes_per_layer": uniq_bytes, "achieved_gbs": dec_gbs,
             "hbm_peak_gbs": hbm, "frac": dec_gbs / hbm,
-            "stage_us": {"dedup_quant": dstage_us[0], "gate_up_stream": dstage_us[1],
-                         "down_stream_combine": dstage_us[2]},
+            "stage_us": {"dedup_quant": dstage_us[0], "gate_up_stream_requant": dstage_us[1],
+                         "down_stream_into_y": dstage_us[2]},
             "kernel_gbs": uniq_bytes / (kern_us * 1e-6) / 1e9 if kern_us > 0 else None}
+
+
+def measure_crossover(moe, plan, layers, H, E, k, steps, stream,
+                      Ts=(1, 2, 4, 8, 12, 16, 24, 32, 48, 64)):
+    """Both paths of moe_forward at small T (the decode/grouped-GEMM crossover): each T runs
+    through the stack's 40 layers' weights (CUDA graph of route + forward per layer) once on
+    the weight-streaming decode kernels and once on the grouped GEMMs; microseconds per
+    layer. Zipf(1.1) routing as in the decode workload."""
+    dev = torch.device("cuda")
+    dwl = synth.WORKLOADS["decode"]
+    out = {"T": [], "stream_us": [], "grouped_us": []}
+    for T in Ts:
+        xd = synth.make_activations(T, H, 500 + T, dwl.outliers, dev)
+        lgd = synth.make_logits(T, E, 500 + T, dwl.zipf_s, dev)
+        idd = torch.empty((T, k), dtype=torch.int32, device=dev)
+        wd = torch.empty((T, k), dtype=torch.float32, device=dev)
+        yd = torch.empty((T, H), dtype=torch.float32, device=dev)
+
+        def run():
+            for (W, wr, packed) in layers:
+                moe.moe_route(plan, lgd, idd, wd)
+                moe.moe_forward(plan, packed, xd, idd, wd, yd)
+
+        out["T"].append(T)
+        for rows, key in ((64, "stream_us"), (0, "grouped_us")):
+            moe.moe_plan_set_decode_rows(plan, rows)
+            run()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            s2 = torch.cuda.Stream()
+            s2.wait_stream(stream)
+            with torch.cuda.stream(s2):
+                with torch.cuda.graph(g, stream=s2):
+                    run()
+            torch.cuda.synchronize()
+            for _ in range(3):
+                g.replay()
+            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(steps, 10)
+            d0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            d1.record(stream)
+            torch.cuda.synchronize()
+            out[key].append(round(d0.elapsed_time(d1) * 1e3 / reps / len(layers), 2))
+            del g
+    moe.moe_plan_set_decode_rows(plan, DEFAULT_DECODE_ROWS)
+    assert moe.moe_get_error(plan) == 0
+    faster = [T for T, a, b in zip(out["T"], out["stream_us"], out["grouped_us"]) if b < a]
+    out["grouped_faster_from_T"] = min(faster) if faster else None
+    out["plan_default_decode_rows"] = DEFAULT_DECODE_ROWS
+    return out
 
 
 def layer_work(sh, counts=None):
@@ -451,6 +505,7 @@ def run_ours(args, world, rank):
     if rank == 0 and not args.no_extra:
         extra["prefill_chunk_T256"] = measure_layer(moe, "prefill", peaks, args.steps)
         extra["stress_T8192"] = measure_layer(moe, "stress", peaks, args.steps)
+        extra["decode_crossover"] = measure_crossover(moe, plan, layers, H, E, k, args.steps, stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         extra["cpu_baseline_1core"] = oracle_one_core(["tiny", "decode", "prefill"],
                                                       {"prefill": args.cpu_tokens_1core})

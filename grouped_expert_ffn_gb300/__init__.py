@@ -53,6 +53,7 @@ def lib() -> C.CDLL:
         sig = {
             "moe_plan": ([i32, i32, i32, i32, i32, i32, C.POINTER(vp)], i32),
             "moe_plan_destroy": ([vp], i32),
+            "moe_plan_set_decode_rows": ([vp, i32], i32),
             "moe_pack_weights": ([vp, C.POINTER(Weights), vp, C.POINTER(vp)], i32),
             "moe_packed_destroy": ([vp], i32),
             "moe_route": ([vp, vp, i32, vp, vp, vp], i32),
@@ -130,6 +131,11 @@ def moe_plan(E: int, top_k: int, H: int, I: int, I_shared: int, max_tokens: int)
 
 def moe_plan_destroy(plan: int):
     _check(lib().moe_plan_destroy(plan), "moe_plan_destroy")
+
+
+def moe_plan_set_decode_rows(plan: int, rows: int):
+    """T <= rows runs the weight-streaming decode kernels, larger T the grouped GEMMs."""
+    _check(lib().moe_plan_set_decode_rows(plan, rows), "moe_plan_set_decode_rows")
 
 
 def make_weights_struct(W: dict) -> Weights:

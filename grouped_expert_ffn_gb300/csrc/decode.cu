@@ -1,8 +1,10 @@
-// Batched decode (T <= 8 rows): experts deduplicated across rows, each unique expert's int8
-// weights streamed from HBM exactly once and applied to every row that routed to it, with an
-// int8 dot (dp4a) into exact int32 accumulators. This is the kernel the page "[job] Strix
-// Halo: multi-session serving ... #145" names as the C>1 limiter (section "Status", items
-// "Batched decode doesn't scale" and "Next": expert dedup across rows plus int8 dot).
+// Batched decode and small batches (T <= 64 rows): experts deduplicated across rows, each
+// unique expert's int8 weights streamed from HBM exactly once and applied to every row that
+// routed to it, with an int8 dot (dp4a) into exact int32 accumulators. This is the kernel the
+// page "[job] Strix Halo: multi-session serving ... #145" names as the C>1 limiter (section
+// "Status", items "Batched decode doesn't scale" and "Next": expert dedup across rows plus
+// int8 dot). An expert's rows are taken kChunk (8) at a time; with more than 8 rows (the
+// batched verify arms of the same page, "Plan") the later passes re-read its weights from L2.
 // All four launches use programmatic dependent launch: each kernel's blocks may be scheduled
 // while its predecessor drains and wait for it in pdl_wait before touching global memory.
 //
@@ -10,13 +12,13 @@
 //                      and the canonical row order; block 1 + t: token t's int8 quant
 //                      (spread over T SMs) and y's row t zeroed.
 //  decode_gu_kernel    (16 channels of one unique expert) per block: streams 16 gate and 16
-//                      up rows, dp4a against the expert's <= 8 quantised token rows held in
-//                      shared memory; fused SiLU(gate)*up.
+//                      up rows, dp4a against up to 8 of the expert's quantised token rows held
+//                      in shared memory per pass; fused SiLU(gate)*up.
 //  requant_kernel      (shared with the prefill path) requantises every h row once, two
 //                      rows per warp, into fp16 codes and scales.
-//  decode_down_kernel  (64 output channels of one unique expert) per block: stages the
-//                      expert's h codes as int8 in shared memory, streams 64 down rows, dp4a,
-//                      and adds w * d into y.
+//  decode_down_kernel  (64 output channels of one unique expert) per block: stages up to 8 of
+//                      the expert's h code rows as int8 in shared memory per pass, streams 64
+//                      down rows, dp4a, and adds w * d into y.
 #include "common.cuh"
 #include "internal.h"
 
@@ -52,6 +54,7 @@ __device__ __forceinline__ void transpose_reduce32(int (&v)[32], int lane) {
 }
 
 constexpr int kPrepThreads = 256;
+constexpr int kChunk = 8;  // rows per pass over an expert's weights
 
 // Block 0 builds the routing metadata; block 1 + t quantises token t and zeroes y's row t.
 __device__ __forceinline__ void prep_quantise_token(const DecodeArgs& a, int t) {
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(DecodeArgs a)
   }
   __syncthreads();
   // row offsets and group positions: block-wide exclusive scans over the experts (E <= 256,
-  // one per thread), both counts packed in one word (each is at most T * k <= 64)
+  // one per thread), both counts packed in one word (each is at most T * k <= 512)
   {
     const int e = tid;
     const int c = e < E ? s_cnt[e] : 0;
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(DecodeArgs a)
       s_off[e] = off;
       a.offsets[e] = off;
       a.counts[e] = c;
-      // a group never has more rows than tokens (<= 8); more means repeated experts (flagged)
+      // a group never has more rows than tokens; more means repeated experts (flagged)
       if (c > 0) a.groups[a.has_shared + gp] = make_int4(e, T_sh + off, min(c, T), 0);
     }
     if (tid == 0) {
@@ -193,8 +196,8 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(DecodeArgs a)
 constexpr int kGuChannelsPerBlock = 16;  // 8 warps x 2 channels
 constexpr int kDownRowsPerBlock = 64;    // 8 warps x 8 output rows
 
-__global__ void __launch_bounds__(256) decode_gu_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) int8_t xs[];  // [8][H]
+__global__ void __launch_bounds__(256, 3) decode_gu_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) int8_t xs[];  // [kChunk][H] token codes of one pass
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
   const int g = blockIdx.y;
@@ -209,53 +212,58 @@ __global__ void __launch_bounds__(256) decode_gu_kernel(DecodeArgs a) {
   const int8_t* Wu = shared ? a.sh_up : a.w_up + (size_t)grp.x * a.I * H;
   const float* sg = shared ? a.sh_s_gate : a.s_gate + (size_t)grp.x * a.I;
   const float* su = shared ? a.sh_s_up : a.s_up + (size_t)grp.x * a.I;
-  for (int i = threadIdx.x; i < nr * H / 16; i += blockDim.x) {
-    const int n = i / (H / 16), u = i % (H / 16);
-    const int tok = a.row_token[row0 + n];
-    reinterpret_cast<int4*>(xs + (size_t)n * H)[u] =
-        reinterpret_cast<const int4*>(a.qtok + (size_t)tok * H)[u];
-  }
-  __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int c = c0 + 2 * warp;
   const int8_t* rows[4] = {Wg + (size_t)c * H, Wu + (size_t)c * H, Wg + (size_t)(c + 1) * H,
                            Wu + (size_t)(c + 1) * H};
-  int acc[32];
+  for (int n0 = 0; n0 < nr; n0 += kChunk) {
+    const int nc = min(kChunk, nr - n0);
+    if (n0 > 0) __syncthreads();  // the previous pass no longer reads xs
+    for (int i = threadIdx.x; i < nc * H / 16; i += blockDim.x) {
+      const int n = i / (H / 16), u = i % (H / 16);
+      const int tok = a.row_token[row0 + n0 + n];
+      reinterpret_cast<int4*>(xs + (size_t)n * H)[u] =
+          reinterpret_cast<const int4*>(a.qtok + (size_t)tok * H)[u];
+    }
+    __syncthreads();
+    int acc[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0;
+    for (int i = 0; i < 32; ++i) acc[i] = 0;
 #pragma unroll 4
-  for (int u = lane; u < H / 16; u += 32) {
-    int4 wv[4];
+    for (int u = lane; u < H / 16; u += 32) {
+      int4 wv[4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) wv[r] = ld_stream(rows[r] + (size_t)u * 16);
+      for (int r = 0; r < 4; ++r) wv[r] = ld_stream(rows[r] + (size_t)u * 16);
 #pragma unroll
-    for (int n = 0; n < kDecodeMaxRows; ++n) {
-      if (n < nr) {
-        const int4 xv = *reinterpret_cast<const int4*>(xs + (size_t)n * H + u * 16);
+      for (int n = 0; n < kChunk; ++n) {
+        if (n < nc) {
+          const int4 xv = *reinterpret_cast<const int4*>(xs + (size_t)n * H + u * 16);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) acc[r * 8 + n] = dot16(wv[r], xv, acc[r * 8 + n]);
+          for (int r = 0; r < 4; ++r) acc[r * 8 + n] = dot16(wv[r], xv, acc[r * 8 + n]);
+        }
       }
     }
-  }
-  transpose_reduce32(acc, lane);
-  const int mine = acc[0];
-  const int other = __shfl_down_sync(0xffffffffu, mine, 8);
-  const int r = lane >> 3, n = lane & 7;
-  if ((r & 1) == 0 && n < nr) {
-    const int ch = c + (r >> 1);
-    const int row = row0 + n;
-    const float sx = a.stok[a.row_token[row]];
-    a.h32[(size_t)row * a.Imax + ch] = silu_mul(dequant(mine, sx, sg[ch]), dequant(other, sx, su[ch]));
-    if (a.tap_gu) {
-      a.tap_gu[(size_t)row * 2 * a.Imax + ch] = mine;
-      a.tap_gu[(size_t)row * 2 * a.Imax + a.Imax + ch] = other;
+    transpose_reduce32(acc, lane);
+    const int mine = acc[0];
+    const int other = __shfl_down_sync(0xffffffffu, mine, 8);
+    const int r = lane >> 3, n = lane & 7;
+    if ((r & 1) == 0 && n < nc) {
+      const int ch = c + (r >> 1);
+      const int row = row0 + n0 + n;
+      const float sx = a.stok[a.row_token[row]];
+      a.h32[(size_t)row * a.Imax + ch] =
+          silu_mul(dequant(mine, sx, sg[ch]), dequant(other, sx, su[ch]));
+      if (a.tap_gu) {
+        a.tap_gu[(size_t)row * 2 * a.Imax + ch] = mine;
+        a.tap_gu[(size_t)row * 2 * a.Imax + a.Imax + ch] = other;
+      }
     }
   }
 }
 
 __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) int8_t hs[];  // [8][Imax]
-  __shared__ float shs[kDecodeMaxRows];
+  extern __shared__ __align__(16) int8_t hs[];  // [kChunk][Imax] h codes of one pass
+  __shared__ float shs[kChunk];
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
   const int g = blockIdx.y;
@@ -268,58 +276,64 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
   const int8_t* Wd = shared ? a.sh_down : a.w_down + (size_t)grp.x * H * a.I;
   const float* sd = shared ? a.sh_s_down : a.s_down + (size_t)grp.x * H;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // this expert's h codes (fp16 integers, written by the requantisation pass) -> int8
-  for (int i = threadIdx.x; i < nr * (Ig / 8); i += blockDim.x) {
-    const int n = i / (Ig / 8), u = i % (Ig / 8);
-    const uint4 v = reinterpret_cast<const uint4*>(a.hq + (size_t)(row0 + n) * Imax)[u];
-    const __half2* h2 = reinterpret_cast<const __half2*>(&v);
-    uint32_t q[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float2 f0 = __half22float2(h2[2 * j]), f1 = __half22float2(h2[2 * j + 1]);
-      q[j] = (uint32_t)(uint8_t)(int8_t)(int)f0.x | (uint32_t)(uint8_t)(int8_t)(int)f0.y << 8 |
-             (uint32_t)(uint8_t)(int8_t)(int)f1.x << 16 | (uint32_t)(uint8_t)(int8_t)(int)f1.y << 24;
-    }
-    *reinterpret_cast<uint2*>(hs + (size_t)n * Imax + u * 8) = make_uint2(q[0], q[1]);
-  }
-  if ((int)threadIdx.x < nr) shs[threadIdx.x] = a.sh[row0 + threadIdx.x];
-  __syncthreads();
   const int ob = o0 + warp * 8;
-  int acc[64];
+  for (int n0 = 0; n0 < nr; n0 += kChunk) {
+    const int nc = min(kChunk, nr - n0);
+    if (n0 > 0) __syncthreads();  // the previous pass no longer reads hs and shs
+    // up to kChunk of this expert's h code rows (fp16 integers, written by the
+    // requantisation pass) -> int8
+    for (int i = threadIdx.x; i < nc * (Ig / 8); i += blockDim.x) {
+      const int n = i / (Ig / 8), u = i % (Ig / 8);
+      const uint4 v = reinterpret_cast<const uint4*>(a.hq + (size_t)(row0 + n0 + n) * Imax)[u];
+      const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+      uint32_t q[2];
 #pragma unroll
-  for (int i = 0; i < 64; ++i) acc[i] = 0;
+      for (int j = 0; j < 2; ++j) {
+        const float2 f0 = __half22float2(h2[2 * j]), f1 = __half22float2(h2[2 * j + 1]);
+        q[j] = (uint32_t)(uint8_t)(int8_t)(int)f0.x | (uint32_t)(uint8_t)(int8_t)(int)f0.y << 8 |
+               (uint32_t)(uint8_t)(int8_t)(int)f1.x << 16 | (uint32_t)(uint8_t)(int8_t)(int)f1.y << 24;
+      }
+      *reinterpret_cast<uint2*>(hs + (size_t)n * Imax + u * 8) = make_uint2(q[0], q[1]);
+    }
+    if ((int)threadIdx.x < nc) shs[threadIdx.x] = a.sh[row0 + n0 + threadIdx.x];
+    __syncthreads();
+    int acc[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) acc[i] = 0;
 #pragma unroll 1
-  for (int u = lane; u < Ig / 16; u += 32) {
-    int4 wv[8];
+    for (int u = lane; u < Ig / 16; u += 32) {
+      int4 wv[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) wv[r] = ld_stream(Wd + (size_t)(ob + r) * Ig + (size_t)u * 16);
+      for (int r = 0; r < 8; ++r) wv[r] = ld_stream(Wd + (size_t)(ob + r) * Ig + (size_t)u * 16);
 #pragma unroll
-    for (int n = 0; n < kDecodeMaxRows; ++n) {
-      if (n < nr) {
-        const int4 xv = *reinterpret_cast<const int4*>(hs + (size_t)n * Imax + u * 16);
+      for (int n = 0; n < kChunk; ++n) {
+        if (n < nc) {
+          const int4 xv = *reinterpret_cast<const int4*>(hs + (size_t)n * Imax + u * 16);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) acc[r * 8 + n] = dot16(wv[r], xv, acc[r * 8 + n]);
+          for (int r = 0; r < 8; ++r) acc[r * 8 + n] = dot16(wv[r], xv, acc[r * 8 + n]);
+        }
       }
     }
-  }
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    int v[32];
+    for (int half = 0; half < 2; ++half) {
+      int v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = acc[half * 32 + i];
-    transpose_reduce32(v, lane);
-    const int r = half * 4 + (lane >> 3), n = lane & 7;
-    if (n < nr) {
-      const int o = ob + r;
-      const int row = row0 + n;
-      const float d = dequant(v[0], shs[n], sd[o]);
-      atomicAdd(a.y + (size_t)a.row_token[row] * H + o, __fmul_rn(a.row_w[row], d));
-      if (a.tap_d) a.tap_d[(size_t)row * H + o] = v[0];
+      for (int i = 0; i < 32; ++i) v[i] = acc[half * 32 + i];
+      transpose_reduce32(v, lane);
+      const int r = half * 4 + (lane >> 3), n = lane & 7;
+      if (n < nc) {
+        const int o = ob + r;
+        const int row = row0 + n0 + n;
+        const float d = dequant(v[0], shs[n], sd[o]);
+        atomicAdd(a.y + (size_t)a.row_token[row] * H + o, __fmul_rn(a.row_w[row], d));
+        if (a.tap_d) a.tap_d[(size_t)row * H + o] = v[0];
+      }
     }
   }
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) {
+  if (a.T < 1 || a.T > kDecodeMaxRows || a.k > 8 || a.E > 256) return cudaErrorInvalidValue;
   const int R = a.T * a.k + (a.has_shared ? a.T : 0);
   if (ev) cudaEventRecord(ev[0], s);
   cudaError_t e = launch_pdl(decode_prep_kernel, dim3(1 + a.T), dim3(kPrepThreads), 0, s, a);
@@ -327,7 +341,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) 
   if (e != cudaSuccess) return e;
   const int gmax = min(a.E, a.T * a.k) + (a.has_shared ? 1 : 0);
   const dim3 ggu((a.Imax + kGuChannelsPerBlock - 1) / kGuChannelsPerBlock, gmax);
-  if ((e = launch_pdl(decode_gu_kernel, ggu, dim3(256), (size_t)kDecodeMaxRows * a.H, s, a)) !=
+  if ((e = launch_pdl(decode_gu_kernel, ggu, dim3(256), (size_t)kChunk * a.H, s, a)) !=
       cudaSuccess)
     return e;
   // one requantisation of every h row (warp per row), instead of one per down block
@@ -336,7 +350,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) 
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[2], s);
   const dim3 gd(a.H / kDownRowsPerBlock, gmax);
-  e = launch_pdl(decode_down_kernel, gd, dim3(256), (size_t)kDecodeMaxRows * a.Imax, s, a);
+  e = launch_pdl(decode_down_kernel, gd, dim3(256), (size_t)kChunk * a.Imax, s, a);
   if (ev) cudaEventRecord(ev[3], s);
   return e;
 }
@@ -348,10 +362,10 @@ bool decode_shape_supported(int H, int Imax) { return H <= kDecodeMaxH && Imax <
 // cannot lower it under a plan with larger ones).
 cudaError_t decode_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(decode_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kDecodeMaxRows * kDecodeMaxH);
+                                       kChunk * kDecodeMaxH);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kDecodeMaxRows * kDecodeMaxI);
+                              kChunk * kDecodeMaxI);
 }
 
 }  // namespace moe

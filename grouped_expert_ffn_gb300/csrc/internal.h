@@ -31,7 +31,13 @@ constexpr int kChunkK = 1024;   // K elements summed in one fp32 TMEM accumulato
 // the A-operand stages (one 128-row x 128-K fp16 weight tile = 64 columns each).
 constexpr int kAccCols = 384;
 constexpr int kTokPerBlk = 64;  // tokens per histogram block (one 64-bit mask per expert)
-constexpr int kDecodeMaxRows = 8;
+// Largest T the deduplicated weight-streaming kernels take, and the default dispatch
+// threshold of a plan (T <= threshold runs them, larger T the grouped GEMMs). Measured on
+// GB300 for the 35B-A3B-shaped layer (H=2048, E=128, k=8, I=512, Zipf 1.1 routing, weights
+// streamed from HBM): streaming 66.8 us against grouped 76.0 us per layer at T=32, 97.7
+// against 81.2 at T=48.
+constexpr int kDecodeMaxRows = 64;
+constexpr int kDecodeDefaultRows = 32;
 constexpr int kDecodeMaxH = 8192;  // largest H and intermediate size the decode kernels take
 constexpr int kDecodeMaxI = 4096;
 constexpr int kREB = 16;  // experts per router tensor-core tile (packed router weight block)
@@ -144,7 +150,7 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev);
 cudaError_t decode_set_attributes();
-bool decode_shape_supported(int H, int Imax);  // shapes the T <= 8 streaming kernels take
+bool decode_shape_supported(int H, int Imax);  // shapes the streaming kernels take
 
 // weight packing and the stacked-prefill helpers
 cudaError_t launch_pack_gu8(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,

@@ -47,6 +47,7 @@ struct moe_plan_s {
   int32_t* tap_gu = nullptr;
   int32_t* tap_d = nullptr;
   int last_T = 0;
+  int decode_rows = kDecodeDefaultRows;  // T <= decode_rows runs the streaming decode kernels
   // per-stage timing
   int profile = 0;
   struct ProfRec {
@@ -335,6 +336,12 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   return MOE_OK;
 }
 
+moe_status moe_plan_set_decode_rows(moe_plan_t p, int rows) {
+  if (!p || rows < 0 || rows > kDecodeMaxRows) return MOE_ERR_INVALID_ARG;
+  p->decode_rows = rows;
+  return MOE_OK;
+}
+
 moe_status moe_plan_destroy(moe_plan_t plan) {
   if (!plan) return MOE_ERR_INVALID_ARG;
   free_plan(plan);
@@ -439,7 +446,7 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   const int R = T * p->k + T_sh;
   p->last_T = T;
   cudaError_t e;
-  if (T <= kDecodeMaxRows && decode_shape_supported(p->H, p->Imax)) {
+  if (T <= p->decode_rows && decode_shape_supported(p->H, p->Imax)) {
     DecodeArgs a;
     a.idx = idx;
     a.w = w;

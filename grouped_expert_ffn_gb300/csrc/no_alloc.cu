@@ -17,6 +17,7 @@
 namespace moe {
 
 constexpr size_t kScratchBytes = 2u << 20;  // 2 MiB
+constexpr int kStaticMaxRows = 8;           // largest T this entry point takes
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
@@ -70,7 +71,7 @@ extern "C" moe_status moe_forward_decode_static(int E, int top_k, int H, int I, 
                                                 int32_t* status, void* stream) {
   if (!wt || !x || !idx || !w || !y) return MOE_ERR_INVALID_ARG;
   if (E < 1 || top_k < 1 || top_k > E || H < 1 || I < 1 || I_shared < 0) return MOE_ERR_INVALID_ARG;
-  if (T < 1 || T > kDecodeMaxRows) return MOE_ERR_CAPACITY;
+  if (T < 1 || T > kStaticMaxRows) return MOE_ERR_CAPACITY;
   if (E > 256 || top_k > 8 || H % 128 || I % 64 || I_shared % 64 ||
       !decode_shape_supported(H, I > I_shared ? I : I_shared))
     return MOE_ERR_UNSUPPORTED;

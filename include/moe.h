@@ -8,9 +8,10 @@
  * instead of one launch per expert: the remedy the page "Qwen3.6-35B-A3B Linux v1.0.4:
  * ~2.7s fixed per-request TTFT = ~4,900 serialized per-expert NPU execs ..." proposes in
  * section "The fix (concatenated-expert dispatch)" (one run per operator per layer-block,
- * N = TOP_K x 2 x IM_EXP). Batched decode (T <= 8 rows) deduplicates experts across rows
- * and streams each unique expert's int8 weights once with an int8 dot, as the page
- * "[job] Strix Halo: multi-session serving ... #145", section "Status", item "Next" asks.
+ * N = TOP_K x 2 x IM_EXP). Batched decode and small batches (T <= 64 rows) deduplicate
+ * experts across rows and stream each unique expert's int8 weights once with an int8 dot,
+ * as the page "[job] Strix Halo: multi-session serving ... #145", section "Status", item
+ * "Next" asks.
  *
  * Conventions (every entry point):
  *  - Data pointers are DEVICE pointers unless a comment says host. Tensors are row-major
@@ -124,12 +125,23 @@ MOE_API moe_status moe_route(moe_plan_t plan, const float* logits, int T, int32_
  *   routing: idx[t,*] distinct, in [0, E)); y is overwritten. 1 <= T <= max_tokens: an
  *   empty batch (T = 0) is MOE_ERR_INVALID_ARG, a larger one MOE_ERR_CAPACITY, both
  *   returned before any work is queued.
- * T <= 8 runs the deduplicated weight-streaming decode kernels; larger T runs the grouped
- * tensor-core GEMMs. Both give identical integer accumulators. Allocates nothing, never
+ * T <= the plan's decode threshold (moe_plan_set_decode_rows; default 32) runs the
+ * deduplicated weight-streaming decode kernels; larger T runs the grouped tensor-core GEMMs.
+ * Both give identical integer accumulators. Allocates nothing, never
  * synchronises, and may be captured in a CUDA graph. The workspace is per plan: calls on
  * one plan must not overlap in time (use one plan per concurrent stream). */
 MOE_API moe_status moe_forward(moe_plan_t plan, moe_packed_t packed, const uint16_t* x, int T,
                        const int32_t* idx, const float* w, float* y, void* stream);
+
+/* Dispatch threshold of moe_forward on this plan: T <= rows runs the weight-streaming decode
+ * kernels (each unique expert's weights read once, rows applied 8 at a time), larger T the
+ * grouped GEMMs. 0 <= rows <= 64 (else MOE_ERR_INVALID_ARG); 0 sends every call to the
+ * grouped GEMMs. Default 32: measured on GB300 for a 35B-A3B-shaped layer, streaming is the
+ * faster path up to T=32 and the grouped GEMMs from T=48. The crossover between the two paths is a measured property of the GPU and
+ * the layer shape (the page "[job] Strix Halo ... #145", "Done / measured", on the grouped
+ * threshold), so it is a setting rather than a constant. Host-only; takes effect on the next
+ * moe_forward. */
+MOE_API moe_status moe_plan_set_decode_rows(moe_plan_t plan, int rows);
 
 /* Sticky device-side error word of the plan (synchronises the device). MOE_OK if none. */
 MOE_API moe_status moe_get_error(moe_plan_t plan);
@@ -175,8 +187,8 @@ MOE_API moe_status moe_debug_tap(moe_plan_t plan, int which, void* dst_host, siz
  * writes, for the chosen path (0 = prefill, 1 = decode), the summed device milliseconds of
  * each stage over all forwards since the previous read into ms_out[4] and their number into
  * *calls, then starts a new accumulation. Stages: prefill {permute+quant, gate/up GEMM,
- * requant, down GEMM adding into y}; decode {dedup+quant, gate/up stream, down stream +
- * combine, 0}. Not for use inside CUDA graph capture. */
+ * requant, down GEMM adding into y}; decode {dedup + quant, gate/up stream +
+ * requant, down stream adding into y, 0}. Not for use inside CUDA graph capture. */
 MOE_API moe_status moe_profile_enable(moe_plan_t plan, int on);
 MOE_API moe_status moe_profile_read(moe_plan_t plan, int path, float* ms_out, int* calls);
 

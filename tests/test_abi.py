@@ -61,6 +61,7 @@ def test_null_handles_rejected(lib):
     assert lib.moe_route(None, None, 4, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_forward(None, None, None, 4, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_plan_destroy(None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_plan_set_decode_rows(None, 8) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_packed_destroy(None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_get_error(None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_debug_tap_bytes(None, 0) == 0

@@ -149,12 +149,13 @@ def test_all_tokens_one_expert_and_empty_experts():
 
 
 def test_decode_and_prefill_give_identical_integers():
-    # the same 8 tokens through the decode kernels (T=8) and inside a 9-token prefill call
-    sh9 = synth.LayerShape(T=9, H=2048, E=128, k=8, I=512, Is=512)
+    # the same 8 tokens through the decode kernels (T=8) and inside a 9-token call on the
+    # grouped GEMMs (the plan's threshold set to 8)
     d = synth.small_layer(9, 2048, 128, 8, 512, 512, seed=21, zipf_s=1.1, outliers=8)
     W = weights_to(d["weights"], "cuda")
     lay = moe.MoELayer(128, 8, 2048, 512, 512, 16, W)
     try:
+        moe.moe_plan_set_decode_rows(lay.plan, 8)
         moe.moe_debug_enable(lay.plan, True)
         x = d["x"].cuda()
         lg = d["logits"].cuda()
@@ -175,6 +176,69 @@ def test_decode_and_prefill_give_identical_integers():
                 assert (gu9[r9[t, s]] == gu8[r8[t, s]]).all()
         dy = (y9[:8] - y8).abs().max().item()
         assert dy <= 1e-5 * y9[:8].abs().max().item()
+    finally:
+        lay.close()
+
+
+@pytest.mark.parametrize("T,E,k", [(9, 128, 8), (16, 128, 8), (33, 128, 8), (64, 128, 8),
+                                   (64, 16, 4)])
+def test_decode_kernels_up_to_64_rows_match_the_oracle(T, E, k):
+    # the weight-streaming kernels above 8 rows: an expert's rows are taken 8 per pass (the
+    # shared expert has all T rows; with E=16, k=4 every routed expert has about 16)
+    sh = synth.LayerShape(T=T, H=2048, E=E, k=k, I=512, Is=512)
+    d = synth.small_layer(T, 2048, E, k, 512, 512, seed=40 + T + E, zipf_s=1.1, outliers=8)
+    W = weights_to(d["weights"], "cuda")
+    lay = moe.MoELayer(E, k, 2048, 512, 512, T, W)
+    try:
+        moe.moe_plan_set_decode_rows(lay.plan, 64)
+        st = check_layer(sh, d["x"], d["logits"], W, oracle_layer(d["weights"], sh), layer=lay)
+        assert st["tap"]["counts"].max() > 8  # some routed expert took more than one pass
+    finally:
+        lay.close()
+
+
+def _path_taps(lay, x, idx, w, rows):
+    moe.moe_plan_set_decode_rows(lay.plan, rows)
+    y = lay.forward(x, idx, w)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(lay.plan) == 0
+    taps = {n: moe.moe_debug_tap(lay.plan, i) for n, i in (
+        ("counts", moe.TAP_COUNTS), ("offsets", moe.TAP_OFFSETS), ("perm", moe.TAP_PERM),
+        ("qx", moe.TAP_QX), ("sx", moe.TAP_SX), ("acc_gu", moe.TAP_ACC_GU), ("hq", moe.TAP_HQ),
+        ("sh", moe.TAP_SH), ("acc_d", moe.TAP_ACC_D))}
+    return y, taps
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 9, 24, 64])
+def test_decode_and_grouped_paths_give_identical_integers(T):
+    # the same call through the weight-streaming kernels and through the grouped GEMMs, on
+    # both sides of every dispatch threshold a plan can take: permutation, activation codes,
+    # every gate/up and down accumulator, the h codes and their scales are bit-identical (the
+    # two paths use the same rounding rules and the same h formula); y agrees up to the order
+    # of the fp32 additions
+    H, E, k, I, Is = 2048, 128, 8, 512, 512
+    d = synth.small_layer(T, H, E, k, I, Is, seed=70 + T, zipf_s=1.1, outliers=8)
+    W = weights_to(d["weights"], "cuda")
+    lay = moe.MoELayer(E, k, H, I, Is, T, W)
+    try:
+        moe.moe_debug_enable(lay.plan, True)
+        x = d["x"].cuda()
+        idx, w = lay.route(d["logits"].cuda())
+        y_s, ts = _path_taps(lay, x, idx, w, 64)
+        y_g, tg = _path_taps(lay, x, idx, w, 0)
+        for n in ("counts", "offsets", "perm", "qx", "sx"):
+            assert (ts[n] == tg[n]).all(), n
+        R = T * k + T
+        ig = np.full(R, I)
+        ig[:T] = Is  # shared rows first
+        gu_s, gu_g = ts["acc_gu"].reshape(R, 2, -1), tg["acc_gu"].reshape(R, 2, -1)
+        hq_s, hq_g = ts["hq"].reshape(R, -1), tg["hq"].reshape(R, -1)
+        for r in range(R):
+            assert (gu_s[r, :, :ig[r]] == gu_g[r, :, :ig[r]]).all(), r
+            assert (hq_s[r, :ig[r]] == hq_g[r, :ig[r]]).all(), r
+        assert (ts["sh"][:R] == tg["sh"][:R]).all()
+        assert (ts["acc_d"].reshape(R, H) == tg["acc_d"].reshape(R, H)).all()
+        assert (y_s - y_g).abs().max().item() <= 1e-5 * y_g.abs().max().item()
     finally:
         lay.close()
 
@@ -229,6 +293,18 @@ def test_decode_after_a_smaller_plan_was_created():
     finally:
         moe.moe_plan_destroy(small)
         lay.close()
+
+
+def test_decode_threshold_range():
+    lay_plan = moe.moe_plan(8, 2, 256, 128, 0, 16)
+    try:
+        for bad in (-1, 65):
+            with pytest.raises(moe.MoeError):
+                moe.moe_plan_set_decode_rows(lay_plan, bad)
+        for ok in (0, 1, 32, 64):
+            moe.moe_plan_set_decode_rows(lay_plan, ok)
+    finally:
+        moe.moe_plan_destroy(lay_plan)
 
 
 def test_capacity_and_argument_errors():
