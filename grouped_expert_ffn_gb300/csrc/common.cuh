@@ -344,6 +344,11 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 __device__ __forceinline__ float dequant(int acc, float s_row, float s_col) {
   return __fmul_rn(__fmul_rn(__int2float_rn(acc), s_row), s_col);
 }
+// The same from accf = float(acc) (round to nearest even), e.g. an fp32 accumulator that
+// holds the integer exactly.
+__device__ __forceinline__ float dequant_f(float accf, float s_row, float s_col) {
+  return __fmul_rn(__fmul_rn(accf, s_row), s_col);
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

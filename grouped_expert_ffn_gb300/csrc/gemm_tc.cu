@@ -61,6 +61,8 @@
 // The down epilogue adds w * dequant(acc) of every (row, channel) into y[token, channel] with
 // 16-byte fp32 reductions (y is zeroed by the permutation step), so the per-row outputs never
 // go to HBM and no separate combine pass runs; the order of the additions into y is not fixed.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -193,23 +195,31 @@ __device__ __forceinline__ T pick(const T (&a)[N], int j) {
   return r;
 }
 
-// Epilogue column loop with one accumulator per tile: TMEM loads of the next 16-column chunk
-// are in flight while the current one is dequantised and stored (tcgen05.wait::ld waits for
-// all of a thread's outstanding loads, so the two register sets alternate). `store(v, c0, j)`
-// consumes the 16 int32 accumulators of chunk c0, this warp's j-th chunk (the fp32 words hold
-// integers). With several
-// 1024-K chunks per tile, each chunk's partial sums are rounded to int32 and added in integer
-// arithmetic (the total may exceed what fp32 holds exactly).
+// An accumulator value as the epilogues consume it: either the fp32 TMEM word, which holds the
+// integer exactly (one accumulator over the whole K), or an int32 sum of 1024-K chunks.
+// acc_f gives float(acc) as the dequantisation rounds it, acc_i the int32 (for debug taps).
+__device__ __forceinline__ float acc_f(float x) { return x; }
+__device__ __forceinline__ float acc_f(int x) { return __int2float_rn(x); }
+__device__ __forceinline__ int acc_i(float x) { return __float2int_rn(x); }
+__device__ __forceinline__ int acc_i(int x) { return x; }
+
+// Drains the accumulator tile chunk by chunk: this warp's 16-column chunks c0 = 16 cg,
+// 16 (cg + kColGroups), ..., the next chunk's TMEM load issued before the current one is
+// consumed. store(v, c0, j) consumes chunk c0 (this warp's j-th). With one accumulator over
+// the whole K, v is the fp32 TMEM words themselves (exact integers: no conversion); with
+// several 1024-K chunks, each chunk's partial sums are rounded to int32 and added in integer
+// arithmetic (the total may exceed what fp32 holds exactly) and v is the int32 sums.
 template <int kColGroups, typename Store>
 __device__ __forceinline__ void epilogue_columns(const GemmArgs& a, int nch, uint32_t tbase,
                                                  int cg, int ncols, Store&& store) {
-  auto to_int = [](const uint32_t (&r)[16], int (&v)[16]) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __float2int_rn(__uint_as_float(r[i]));
-  };
   if (nch == 1) {
     uint32_t ra[16], rb[16];
-    int v[16];
+    auto emit = [&](const uint32_t (&r)[16], int c, int j) {
+      float f[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(r[i]);
+      store(f, c, j);
+    };
     constexpr int kStep = 16 * kColGroups;  // this warp's chunks: cg, cg + kColGroups, ...
     int c0 = cg * 16;
     if (c0 >= ncols) return;  // uniform over the warp
@@ -219,14 +229,12 @@ __device__ __forceinline__ void epilogue_columns(const GemmArgs& a, int nch, uin
     for (int j = 0; j < kEpiChunks<kColGroups>(); j += 2, c0 += 2 * kStep) {
       const int c1 = c0 + kStep;
       if (c1 < ncols) tmem_ld16(tbase + c1, rb);
-      to_int(ra, v);
-      store(v, c0, j);
+      emit(ra, c0, j);
       if (c1 >= ncols) break;
       tmem_ld_wait();
       const int c2 = c1 + kStep;
       if (c2 < ncols) tmem_ld16(tbase + c2, ra);
-      to_int(rb, v);
-      store(v, c1, j + 1);
+      emit(rb, c1, j + 1);
       if (c2 >= ncols) break;
       tmem_ld_wait();
     }
@@ -275,8 +283,9 @@ __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int
   const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
   const int ncols = wi.z;
   epilogue_columns<GemmRoles<true>::kColGroups>(a, nch, tbase, cg, ncols,
-                                                [&](const int (&v)[16], int c0, int j) {
-    int recv[8];
+                                                [&](const auto& v, int c0, int j) {
+    using V = typename std::remove_cv<typename std::remove_reference<decltype(v[0])>::type>::type;
+    V recv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) recv[i] = __shfl_xor_sync(0xffffffffu, odd ? v[i] : v[8 + i], 1);
     const float rvj = pick(m.rv, j);
@@ -286,17 +295,17 @@ __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int
       const float sx = __shfl_sync(0xffffffffu, rvj, cc);
       const int col = c0 + cc;
       if (col < ncols) {
-        const int g = odd ? recv[i] : v[i];
-        const int u = odd ? v[8 + i] : recv[i];
+        const V g = odd ? recv[i] : v[i];
+        const V u = odd ? v[8 + i] : recv[i];
         const int row = wi.y + col;
-        const float hv = silu_mul(dequant(g, sx, m.s0), dequant(u, sx, m.s1));
+        const float hv = silu_mul(dequant_f(acc_f(g), sx, m.s0), dequant_f(acc_f(u), sx, m.s1));
         if (MOE_L2_HINTS)
           st_f32_hint(a.h32 + (size_t)row * a.Imax + ch, hv, m.pol);  // read again by requant
         else
           a.h32[(size_t)row * a.Imax + ch] = hv;
         if (a.tap) {
-          a.tap[(size_t)row * 2 * a.Imax + ch] = g;
-          a.tap[(size_t)row * 2 * a.Imax + a.Imax + ch] = u;
+          a.tap[(size_t)row * 2 * a.Imax + ch] = acc_i(g);
+          a.tap[(size_t)row * 2 * a.Imax + a.Imax + ch] = acc_i(u);
         }
       }
     }
@@ -312,11 +321,12 @@ __device__ __forceinline__ void red_add_v4(float* p, float a0, float a1, float a
 
 // 4 x 4 transpose within each lane quad: on entry lane b (= lane % 4) holds v[i] = M[b][i],
 // on exit v[i] = M[i][b]. Two butterfly stages (partners b^1, then b^2), two shuffles each.
-__device__ __forceinline__ void quad_transpose(float (&v)[4], int lane) {
+template <typename V>
+__device__ __forceinline__ void quad_transpose(V (&v)[4], int lane) {
   const bool h1 = (lane & 1) != 0, h2 = (lane & 2) != 0;
 #pragma unroll
   for (int p = 0; p < 4; p += 2) {
-    const float recv = __shfl_xor_sync(0xffffffffu, h1 ? v[p] : v[p + 1], 1);
+    const V recv = __shfl_xor_sync(0xffffffffu, h1 ? v[p] : v[p + 1], 1);
     if (h1)
       v[p] = recv;
     else
@@ -324,7 +334,7 @@ __device__ __forceinline__ void quad_transpose(float (&v)[4], int lane) {
   }
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
-    const float recv = __shfl_xor_sync(0xffffffffu, h2 ? v[p] : v[p + 2], 2);
+    const V recv = __shfl_xor_sync(0xffffffffu, h2 ? v[p] : v[p + 2], 2);
     if (h2)
       v[p] = recv;
     else
@@ -332,11 +342,13 @@ __device__ __forceinline__ void quad_transpose(float (&v)[4], int lane) {
   }
 }
 
-// Down epilogue: lane = output channel m0 + 32q + lane holds w * dequant(acc) of 16 token
-// columns per chunk. A 4 x 4 transpose within each lane quad gives every lane four
-// consecutive channels of one token, added into y with one 16-byte reduction: each warp
-// instruction adds 128 contiguous bytes into each of four token rows of y. Each column's h
-// scale, routing weight and token are taken by shuffle from the lanes that loaded them.
+// Down epilogue: lane = output channel m0 + 32q + lane holds the accumulators of 16 token
+// columns per chunk. A 4 x 4 transpose of the accumulators within each lane quad gives
+// every lane four consecutive channels of one column; it dequantises them with that column's
+// h scale and routing weight (three shuffles per four columns from the lanes that loaded the
+// column metadata) and the four channels' weight scales (taken from the quad once per item),
+// and adds them into y with one 16-byte reduction: each warp instruction adds 128 contiguous
+// bytes into each of four token rows of y.
 __device__ __forceinline__ void load_meta_down(const GemmArgs& a, int4 wi, int cg,
                                                EpiMeta<false>& m) {
   constexpr int kCG = GemmRoles<false>::kColGroups;
@@ -359,27 +371,31 @@ __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nc
   const int ncols = wi.z;
   const int b = lane & 3;
   float* yq = a.y + (o - b);  // first channel of this lane's quad
+  float sw[4];                // weight-row scales of the quad's channels o - b + i
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sw[i] = __shfl_sync(0xffffffffu, m.s0, (lane & ~3) + i);
   epilogue_columns<GemmRoles<false>::kColGroups>(a, nch, tbase, cg, ncols,
-                                                 [&](const int (&v)[16], int c0, int j) {
+                                                 [&](const auto& v, int c0, int j) {
+    using V = typename std::remove_cv<typename std::remove_reference<decltype(v[0])>::type>::type;
     if (a.tap) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (c0 + i < ncols) a.tap[(size_t)(wi.y + c0 + i) * a.H + o] = v[i];
+        if (c0 + i < ncols) a.tap[(size_t)(wi.y + c0 + i) * a.H + o] = acc_i(v[i]);
     }
     const float rvj = pick(m.rv, j);
     const int tokj = pick(m.tok, j);
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-      float t[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float shr = __shfl_sync(0xffffffffu, rvj, 4 * jj + i);
-        const float wr = __shfl_sync(0xffffffffu, rvj, 16 + 4 * jj + i);
-        t[i] = __fmul_rn(wr, dequant(v[4 * jj + i], shr, m.s0));
-      }
+      V t[4] = {v[4 * jj], v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]};
       quad_transpose(t, lane);  // t[i]: channel (o - b + i), column 4jj + b
-      const int tok = __shfl_sync(0xffffffffu, tokj, 4 * jj + b);
-      if (c0 + 4 * jj + b < ncols) red_add_v4(yq + (size_t)tok * a.H, t[0], t[1], t[2], t[3]);
+      const int col = 4 * jj + b;
+      const float shr = __shfl_sync(0xffffffffu, rvj, col);
+      const float wr = __shfl_sync(0xffffffffu, rvj, 16 + col);
+      const int tok = __shfl_sync(0xffffffffu, tokj, col);
+      float d[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[i] = __fmul_rn(wr, dequant_f(acc_f(t[i]), shr, sw[i]));
+      if (c0 + col < ncols) red_add_v4(yq + (size_t)tok * a.H, d[0], d[1], d[2], d[3]);
     }
   });
 }
