@@ -37,9 +37,9 @@ METRIC = "MoE layer tokens/s (prefill) & µs/layer decode C=8; % int8/HBM roofli
 # stacked-prefill layer (T=2600), from one ncu capture of the kernel as it is now. Set to None
 # whenever the kernel changes, until it is captured again.
 GU_TRAFFIC_BYTES = 403.0e6
-# Kernels one stacked-prefill layer launches: RMS pre-norm, router projection, routing, and
-# the forward's histogram, scan, scatter, gate/up GEMM, requantisation, down GEMM.
-LAUNCHES_PER_LAYER = 9
+# Kernels one stacked-prefill layer launches: RMS pre-norm, router projection, and the
+# forward's routing + histogram + scan, scatter, gate/up GEMM, requantisation, down GEMM.
+LAUNCHES_PER_LAYER = 7
 # moe_forward's default dispatch threshold (T <= this runs the weight-streaming kernels).
 DEFAULT_DECODE_ROWS = 32
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -184,8 +184,9 @@ def oracle_sample_rate(W_dev, wl, n_tokens, nthreads):
 
 
 def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
-    """Batched decode, C=8 rows, through the same layers' weights (CUDA graph of
-    route + forward per layer); microseconds per layer and the HBM roofline."""
+    """Batched decode, C=8 rows, through the same layers' weights (CUDA graph of one
+    moe_route_forward per layer: routing from the logits inside the forward); microseconds
+    per layer and the HBM roofline."""
     dev = torch.device("cuda")
     n_layers = len(layers)
     dwl = synth.WORKLOADS["decode"]
@@ -197,8 +198,7 @@ def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
 
     def decode_stack():
         for (W, wr, packed) in layers:
-            moe.moe_route(plan, lgd, idd, wd)
-            moe.moe_forward(plan, packed, xd, idd, wd, yd)
+            moe.moe_route_forward(plan, packed, xd, lgd, idd, wd, yd)
 
     decode_stack()
     torch.cuda.synchronize()
@@ -242,7 +242,7 @@ def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
             "us_per_layer": us_layer, "unique_experts": U,
             "unique_bytes_per_layer": uniq_bytes, "achieved_gbs": dec_gbs,
             "hbm_peak_gbs": hbm, "frac": dec_gbs / hbm,
-            "stage_us": {"dedup_quant": dstage_us[0], "gate_up_stream_requant": dstage_us[1],
+            "stage_us": {"route_dedup_quant": dstage_us[0], "gate_up_stream_requant": dstage_us[1],
                          "down_stream_into_y": dstage_us[2]},
             "kernel_gbs": uniq_bytes / (kern_us * 1e-6) / 1e9 if kern_us > 0 else None}
 
@@ -250,7 +250,7 @@ def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
 def measure_crossover(moe, plan, layers, H, E, k, steps, stream,
                       Ts=(1, 2, 4, 8, 12, 16, 24, 32, 48, 64)):
     """Both paths of moe_forward at small T (the decode/grouped-GEMM crossover): each T runs
-    through the stack's 40 layers' weights (CUDA graph of route + forward per layer) once on
+    through the stack's 40 layers' weights (CUDA graph of moe_route_forward per layer) once on
     the weight-streaming decode kernels and once on the grouped GEMMs; microseconds per
     layer. Zipf(1.1) routing as in the decode workload."""
     dev = torch.device("cuda")
@@ -265,8 +265,7 @@ def measure_crossover(moe, plan, layers, H, E, k, steps, stream,
 
         def run():
             for (W, wr, packed) in layers:
-                moe.moe_route(plan, lgd, idd, wd)
-                moe.moe_forward(plan, packed, xd, idd, wd, yd)
+                moe.moe_route_forward(plan, packed, xd, lgd, idd, wd, yd)
 
         out["T"].append(T)
         for rows, key in ((64, "stream_us"), (0, "grouped_us")):
@@ -404,16 +403,16 @@ def run_ours(args, world, rank):
     prof_layer = n_layers // 2
 
     def stack(profile=False):
-        # layer l: x_in = rmsnorm(x) -> logits = x_in @ W_r -> route -> y = moe(x_in) -> x += y
+        # layer l: x_in = rmsnorm(x) -> logits = x_in @ W_r -> routing and y = moe(x_in), the
+        # routing inside the forward's first kernel -> x += y
         # With profile, one layer per step records the plan's per-stage CUDA events (events
         # between every layer's kernels would add their own cost to the step).
         for l, (W, wr, packed) in enumerate(layers):
             moe.moe_rmsnorm_residual(x, y if l else None, x_in)
             moe.moe_router_logits_packed(x_in, wr, logits)
-            moe.moe_route(plan, logits, idx, w)
             if profile and l == prof_layer:
                 moe.moe_profile_enable(plan, True)
-            moe.moe_forward(plan, packed, x_in, idx, w, y)
+            moe.moe_route_forward(plan, packed, x_in, logits, idx, w, y)
             if profile and l == prof_layer:
                 moe.moe_profile_enable(plan, False)
         moe.moe_residual_add(x, y)

@@ -58,6 +58,7 @@ def lib() -> C.CDLL:
             "moe_packed_destroy": ([vp], i32),
             "moe_route": ([vp, vp, i32, vp, vp, vp], i32),
             "moe_forward": ([vp, vp, vp, i32, vp, vp, vp, vp], i32),
+            "moe_route_forward": ([vp, vp, vp, i32, vp, vp, vp, vp, vp], i32),
             "moe_get_error": ([vp], i32),
             "moe_clear_error": ([vp], i32),
             "moe_selftest_wait_timeout": ([vp, vp], i32),
@@ -164,6 +165,14 @@ def moe_forward(plan: int, packed: int, x, idx, w, y, stream=None):
     T = x.shape[0]
     _check(lib().moe_forward(plan, packed, _ptr(x), T, _ptr(idx), _ptr(w), _ptr(y),
                              _stream(stream)), "moe_forward")
+
+
+def moe_route_forward(plan: int, packed: int, x, logits, idx, w, y, stream=None):
+    """Routing (written to idx, w) and the layer (y) in one call; the routing runs inside
+    the forward's first kernel."""
+    T = x.shape[0]
+    _check(lib().moe_route_forward(plan, packed, _ptr(x), T, _ptr(logits), _ptr(idx), _ptr(w),
+                                   _ptr(y), _stream(stream)), "moe_route_forward")
 
 
 def moe_get_error(plan: int) -> int:

@@ -361,4 +361,85 @@ __device__ __forceinline__ int warp_sum_i(int v) {
   return v;
 }
 
+// ---- top-k softmax routing of one token, one warp ---------------------------------------
+// The k (<= 8) largest of the E (<= 256) fp32 logits l[0..E) (ties to the lowest expert id;
+// slots ordered by logit descending, then id ascending) and their softmax weights
+// exp(l_j - l_max) / sum_i exp(l_i - l_max), the sum taken in slot order. Lane j < k writes
+// slot j of idx[0..k) and w[0..k). Every lane of the warp must call it.
+constexpr int kMaxEPerLane = 8;  // E <= 256
+
+__device__ __forceinline__ void route_token_warp(const float* __restrict__ l, int E, int k,
+                                                 int32_t* __restrict__ idx, float* __restrict__ w,
+                                                 int lane) {
+  float v[kMaxEPerLane];
+  bool taken[kMaxEPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxEPerLane; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = e < E ? l[e] : 0.0f;
+    taken[i] = e >= E;
+  }
+  float sel_v[8];
+  int sel_e[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      // lane-local best among untaken: highest value, then lowest id
+      float bv = 0.0f;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kMaxEPerLane; ++i) {
+        const int e = i * 32 + lane;
+        if (!taken[i] && (be == 0x7fffffff || v[i] > bv)) {
+          bv = v[i];
+          be = e;
+        }
+      }
+      // warp argmax on (value desc, id asc); lanes with nothing left carry id = INT_MAX
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        const bool better = (oe != 0x7fffffff) &&
+                            (be == 0x7fffffff || ov > bv || (ov == bv && oe < be));
+        if (better) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      sel_v[j] = bv;
+      sel_e[j] = be;
+      if ((be & 31) == lane) {
+#pragma unroll
+        for (int i = 0; i < kMaxEPerLane; ++i)
+          if (i == (be >> 5)) taken[i] = true;
+      }
+    } else {
+      sel_v[j] = 0.0f;
+      sel_e[j] = 0;
+    }
+  }
+  // softmax over the selected logits: lane j < k handles slot j
+  const float m = sel_v[0];
+  float ex = 0.0f;
+  int my_e = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (lane == j && j < k) {
+      ex = expf(sel_v[j] - m);
+      my_e = sel_e[j];
+    }
+  float z = 0.0f;
+  // sum in slot order (j = 0..k-1), identical for every lane
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float ej = __shfl_sync(0xffffffffu, ex, j);
+    if (j < k) z += ej;
+  }
+  if (lane < k) {
+    idx[lane] = my_e;
+    w[lane] = ex / z;
+  }
+}
+
 }  // namespace moe

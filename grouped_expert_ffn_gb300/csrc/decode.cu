@@ -8,8 +8,9 @@
 // All four launches use programmatic dependent launch: each kernel's blocks may be scheduled
 // while its predecessor drains and wait for it in pdl_wait before touching global memory.
 //
-//  decode_prep_kernel  block 0: the unique-expert list (with the shared expert as group 0)
-//                      and the canonical row order; block 1 + t: token t's int8 quant
+//  decode_prep_kernel  block 0: the tokens' routing when logits are given, then the
+//                      unique-expert list (with the shared expert as group 0) and the
+//                      canonical row order; block 1 + t: token t's int8 quant
 //                      (spread over T SMs) and y's row t zeroed.
 //  decode_gu_kernel    (16 channels of one unique expert) per block: streams 16 gate and 16
 //                      up rows, dp4a against up to 8 of the expert's quantised token rows held
@@ -123,6 +124,12 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(DecodeArgs a)
   const int T_sh = a.has_shared ? T : 0;
   const int tid = threadIdx.x;
   const int warp = tid / 32, lane = tid % 32;
+  if (a.logits) {  // the tokens' routing first (warp per token); idx, w = idx_out, w_out
+    for (int t = warp; t < T; t += kPrepThreads / 32)
+      route_token_warp(a.logits + (size_t)t * E, E, k, a.idx_out + (size_t)t * k,
+                       a.w_out + (size_t)t * k, lane);
+    __syncthreads();
+  }
   for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
   for (int r = tid; r < T * k; r += blockDim.x) {
     int e = a.idx[r];

@@ -30,7 +30,7 @@ constexpr int kChunkK = 1024;   // K elements summed in one fp32 TMEM accumulato
 // TMEM columns of the GEMMs: two accumulator slots of up to kMaxTokTile columns each, then
 // the A-operand stages (one 128-row x 128-K fp16 weight tile = 64 columns each).
 constexpr int kAccCols = 384;
-constexpr int kTokPerBlk = 64;  // tokens per histogram block (one 64-bit mask per expert)
+constexpr int kTokPerBlk = 32;  // tokens per routing/histogram block (a 64-bit mask per expert holds them)
 // Largest T the deduplicated weight-streaming kernels take, and the default dispatch
 // threshold of a plan (T <= threshold runs them, larger T the grouped GEMMs). Measured on
 // GB300 for the 35B-A3B-shaped layer (H=2048, E=128, k=8, I=512, Zipf 1.1 routing, weights
@@ -91,6 +91,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
 struct PrepArgs {
   const int32_t* idx;
   const float* w;
+  const float* logits = nullptr;  // [T, E]: route here into idx_out / w_out (idx, w = those)
+  int32_t* idx_out = nullptr;
+  float* w_out = nullptr;
+  int* scan_ctr = nullptr;        // one zero-initialised counter, left at zero
   const uint16_t* x;
   int T, k, E, H, I, Is, has_shared, tn_gu, tn_d;
   unsigned long long* bmask;  // [nblk, E]
@@ -116,6 +120,9 @@ cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s);
 struct DecodeArgs {
   const int32_t* idx;
   const float* w;
+  const float* logits = nullptr;  // [T, E]: route in the prep kernel into idx_out / w_out
+  int32_t* idx_out = nullptr;
+  float* w_out = nullptr;
   const uint16_t* x;
   int T, k, E, H, I, Is, Imax, has_shared, num_sms;
   const int8_t* w_gate;

@@ -41,6 +41,7 @@ struct moe_plan_s {
   int4* groups = nullptr;
   int* n_groups = nullptr;
   int* sq_max = nullptr;  // [2] per-forward maxima of row sum(q^2): gate/up rows, down rows
+  int* scan_ctr = nullptr;  // blocks of the routing/histogram kernel counted in (zero between calls)
   int* err = nullptr;
   // taps
   int debug = 0;
@@ -303,8 +304,10 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   ALLOC(n_groups, 1);
   ALLOC(sq_max, 2);
   ALLOC(err, 1);
+  ALLOC(scan_ctr, 1);
 #undef ALLOC
   if (cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess ||
+      cudaMemset(p->scan_ctr, 0, sizeof(int)) != cudaSuccess ||
       cudaMemset(p->hq, 0, p->R_max * p->Imax * sizeof(__half)) != cudaSuccess) {
     free_plan(p);
     return MOE_ERR_CUDA;
@@ -434,8 +437,11 @@ moe_status moe_route(moe_plan_t p, const float* logits, int T, int32_t* idx, flo
                                   static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
-                       const int32_t* idx, const float* w, float* y, void* stream) {
+// moe_forward, and moe_route_forward when logits is not null (then idx, w are the outputs
+// the routing writes, read back by the later kernels).
+static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
+                        const float* logits, const int32_t* idx, const float* w, float* y,
+                        void* stream) {
   if (!p || !pk || !x || !idx || !w || !y || pk->plan != p) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(idx) || !aligned16(w) || !aligned16(y))
     return MOE_ERR_INVALID_ARG;
@@ -450,6 +456,9 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
     DecodeArgs a;
     a.idx = idx;
     a.w = w;
+    a.logits = logits;
+    a.idx_out = const_cast<int32_t*>(idx);
+    a.w_out = const_cast<float*>(w);
     a.x = x;
     a.T = T;
     a.k = p->k;
@@ -495,6 +504,10 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   PrepArgs pa;
   pa.idx = idx;
   pa.w = w;
+  pa.logits = logits;
+  pa.idx_out = const_cast<int32_t*>(idx);
+  pa.w_out = const_cast<float*>(w);
+  pa.scan_ctr = p->scan_ctr;
   pa.x = x;
   pa.T = T;
   pa.k = p->k;
@@ -578,6 +591,18 @@ moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
   return cuda_status(e);
 }
 
+moe_status moe_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
+                       const int32_t* idx, const float* w, float* y, void* stream) {
+  return forward_impl(p, pk, x, T, nullptr, idx, w, y, stream);
+}
+
+moe_status moe_route_forward(moe_plan_t p, moe_packed_t pk, const uint16_t* x, int T,
+                             const float* logits, int32_t* idx, float* w, float* y,
+                             void* stream) {
+  if (!logits || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  return forward_impl(p, pk, x, T, logits, idx, w, y, stream);
+}
+
 moe_status moe_profile_enable(moe_plan_t p, int on) {
   if (!p) return MOE_ERR_INVALID_ARG;
   p->profile = on ? 1 : 0;
@@ -621,6 +646,7 @@ moe_status moe_get_error(moe_plan_t p) {
 moe_status moe_clear_error(moe_plan_t p) {
   if (!p) return MOE_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(p->scan_ctr, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaMemset(p->err, 0, sizeof(int)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

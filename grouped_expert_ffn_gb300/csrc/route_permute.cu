@@ -2,10 +2,12 @@
 //
 //  route_kernel      warp per token: top-k of the fp32 logits (ties to the lowest expert id),
 //                    softmax over the selected logits.
-//  hist_kernel       per block of 64 tokens, one 64-bit token mask per expert (which of the
-//                    block's tokens chose it); its popcount is the block's histogram.
-//  scan_kernel       one block: per-expert counts, exclusive prefixes over blocks and over
-//                    experts, and the grouped-GEMM work lists (expert-tile queue).
+//  route_hist_scan_kernel
+//                    per block of 64 tokens: the tokens' routing (when logits are given), one
+//                    64-bit token mask per expert (which of the block's tokens chose it; its
+//                    popcount is the block's histogram); the last block to finish runs the
+//                    scan: per-expert counts, exclusive prefixes over blocks and over experts,
+//                    and the grouped-GEMM work lists (expert-tile queue).
 //  scatter_kernel    block per token: per-token int8 quantisation of x, the codes written as
 //                    fp16 integers into every row the token occupies (one per routed slot plus
 //                    the shared expert's row) with 16-byte stores; row metadata; the token's
@@ -18,8 +20,6 @@
 
 namespace moe {
 
-constexpr int kMaxEPerLane = 8;  // E <= 256
-
 __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int k,
                              int32_t* __restrict__ idx, float* __restrict__ w, int* err) {
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
@@ -27,76 +27,7 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (t >= T) return;
-  const float* l = logits + (size_t)t * E;
-  float v[kMaxEPerLane];
-  bool taken[kMaxEPerLane];
-#pragma unroll
-  for (int i = 0; i < kMaxEPerLane; ++i) {
-    const int e = i * 32 + lane;
-    v[i] = e < E ? l[e] : 0.0f;
-    taken[i] = e >= E;
-  }
-  float sel_v[8];
-  int sel_e[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j < k) {
-      // lane-local best among untaken: highest value, then lowest id
-      float bv = 0.0f;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kMaxEPerLane; ++i) {
-        const int e = i * 32 + lane;
-        if (!taken[i] && (be == 0x7fffffff || v[i] > bv)) {
-          bv = v[i];
-          be = e;
-        }
-      }
-      // warp argmax on (value desc, id asc); lanes with nothing left carry id = INT_MAX
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        const bool better = (oe != 0x7fffffff) &&
-                            (be == 0x7fffffff || ov > bv || (ov == bv && oe < be));
-        if (better) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      sel_v[j] = bv;
-      sel_e[j] = be;
-      if ((be & 31) == lane) {
-#pragma unroll
-        for (int i = 0; i < kMaxEPerLane; ++i)
-          if (i == (be >> 5)) taken[i] = true;
-      }
-    } else {
-      sel_v[j] = 0.0f;
-      sel_e[j] = 0;
-    }
-  }
-  // softmax over the selected logits: lane j < k handles slot j
-  const float m = sel_v[0];
-  float ex = 0.0f;
-  int my_e = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (lane == j && j < k) {
-      ex = expf(sel_v[j] - m);
-      my_e = sel_e[j];
-    }
-  float z = 0.0f;
-  // sum in slot order (j = 0..k-1), identical for every lane
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float ej = __shfl_sync(0xffffffffu, ex, j);
-    if (j < k) z += ej;
-  }
-  if (lane < k) {
-    idx[(size_t)t * k + lane] = my_e;
-    w[(size_t)t * k + lane] = ex / z;
-  }
+  route_token_warp(logits + (size_t)t * E, E, k, idx + (size_t)t * k, w + (size_t)t * k, lane);
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
@@ -104,35 +35,6 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* idx,
   const int warps = 8;
   return launch_pdl(route_kernel, dim3((T + warps - 1) / warps), dim3(32 * warps), 0, s, logits, T,
                     E, k, idx, w, err);
-}
-
-// ---------------------------------------------------------------------------------------
-__global__ void hist_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
-                            unsigned long long* __restrict__ bmask, int* __restrict__ bhist,
-                            int* sq_max, int* err) {
-  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
-  pdl_trigger();
-  extern __shared__ unsigned long long mask[];
-  if (blockIdx.x == 0 && threadIdx.x < 2) sq_max[threadIdx.x] = 0;  // maxima of this forward
-  for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0ull;
-  __syncthreads();
-  const int t0 = blockIdx.x * kTokPerBlk;
-  const int n = min(kTokPerBlk, T - t0) * k;
-  for (int r = threadIdx.x; r < n; r += blockDim.x) {
-    const int e = idx[(size_t)t0 * k + r];
-    if (e < 0 || e >= E) {
-      set_error(err, kErrDevice);
-      continue;
-    }
-    const unsigned long long bit = 1ull << (r / k);
-    const unsigned long long old = atomicOr(&mask[e], bit);
-    if (old & bit) set_error(err, kErrDevice);  // an expert repeated within a token
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    bmask[(size_t)blockIdx.x * E + e] = mask[e];
-    bhist[(size_t)e * gridDim.x + blockIdx.x] = __popcll(mask[e]);  // [E][nblk]
-  }
 }
 
 // Exclusive scan over up to blockDim.x (<= 1024) values, one per thread; returns the
@@ -165,15 +67,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return r;
 }
 
-// One block of 1024 threads. Turns bhist into exclusive per-expert prefixes over blocks,
+// The last block of route_hist_scan_kernel (1024 threads). Turns bhist into exclusive
+// per-expert prefixes over blocks,
 // writes counts/offsets and the two work lists (gate/up and down): per group, every
 // (128-row weight tile, token tile) pair, ordered by group, then weight tile, then token tile,
 // so consecutive items of a large group reuse one weight tile from L2. A group of cnt rows is
 // split into ceil(cnt / TN) token tiles of equal size (within one row), so no tile is a thin
 // remainder.
-__global__ void __launch_bounds__(1024) scan_kernel(PrepArgs a, int nblk) {
-  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
-  pdl_trigger();
+__device__ __forceinline__ void scan_block(const PrepArgs& a, int nblk) {
   __shared__ int s_cnt[257];
   __shared__ int s_off[257];
   __shared__ int s_base_gu[258];
@@ -197,7 +98,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(PrepArgs a, int nblk) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int b = b0 + i * 32 + lane;
-          v[x][i] = e < E && b < nblk ? a.bhist[(size_t)e * nblk + b] : 0;
+          v[x][i] = e < E && b < nblk ? __ldcg(a.bhist + (size_t)e * nblk + b) : 0;
         }
       }
 #pragma unroll
@@ -284,6 +185,56 @@ __global__ void __launch_bounds__(1024) scan_kernel(PrepArgs a, int nblk) {
       items[i] = make_int4(gid, row0 + r0, r1 - r0, wt * kBM);
     }
   }
+}
+
+// Block of kTokPerBlk tokens, 1024 threads: the tokens' routing when logits are given (warp per
+// token), the block's per-expert token masks and their popcounts (the block's histogram),
+// then a per-layer counter; the last block to count in runs scan_block over every block's
+// histogram (no block waits for another) and resets the counter for the next call.
+__global__ void __launch_bounds__(1024) route_hist_scan_kernel(PrepArgs a, int nblk) {
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
+  __shared__ unsigned long long s_mask[256];
+  __shared__ int s_last;
+  const int T = a.T, k = a.k, E = a.E;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
+  if (blockIdx.x == 0 && threadIdx.x < 2) a.sq_max[threadIdx.x] = 0;  // maxima of this forward
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
+  const int t0 = blockIdx.x * kTokPerBlk;
+  const int nt = min(kTokPerBlk, T - t0);
+  if (a.logits) {
+    for (int tt = warp; tt < nt; tt += nwarps) {
+      const size_t t = (size_t)(t0 + tt);
+      route_token_warp(a.logits + t * E, E, k, a.idx_out + t * k, a.w_out + t * k, lane);
+    }
+  }
+  __syncthreads();  // this block's routing and the cleared masks are visible to the block
+  const int32_t* idx = a.logits ? a.idx_out : a.idx;
+  for (int r = threadIdx.x; r < nt * k; r += blockDim.x) {
+    const int e = idx[(size_t)t0 * k + r];
+    if (e < 0 || e >= E) {
+      set_error(a.err, kErrDevice);
+      continue;
+    }
+    const unsigned long long bit = 1ull << (r / k);
+    const unsigned long long old = atomicOr(&s_mask[e], bit);
+    if (old & bit) set_error(a.err, kErrDevice);  // an expert repeated within a token
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    a.bmask[(size_t)blockIdx.x * E + e] = s_mask[e];
+    a.bhist[(size_t)e * nblk + blockIdx.x] = __popcll(s_mask[e]);  // [E][nblk]
+  }
+  __threadfence();  // this thread's histogram stores visible device-wide before the count
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_last = atomicAdd(a.scan_ctr, 1) == nblk - 1;
+    if (s_last) *a.scan_ctr = 0;  // every block has counted: ready for the next call
+  }
+  __syncthreads();
+  if (!s_last) return;  // uniform over the block
+  __threadfence();
+  scan_block(a, nblk);
 }
 
 // Block per token: quantise x[t] once, write its codes (fp16 integers) to each of its rows.
@@ -389,10 +340,8 @@ __global__ void scatter_kernel(PrepArgs a) {
 
 cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s) {
   const int nblk = (a.T + kTokPerBlk - 1) / kTokPerBlk;
-  cudaError_t e = launch_pdl(hist_kernel, dim3(nblk), dim3(256), a.E * sizeof(unsigned long long),
-                             s, a.idx, a.T, a.k, a.E, a.bmask, a.bhist, a.sq_max, a.err);
+  cudaError_t e = launch_pdl(route_hist_scan_kernel, dim3(nblk), dim3(1024), 0, s, a, nblk);
   if (e != cudaSuccess) return e;
-  if ((e = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, a, nblk)) != cudaSuccess) return e;
   return launch_pdl(scatter_kernel, dim3(a.T), dim3(256), 0, s, a);
 }
 

@@ -133,6 +133,18 @@ MOE_API moe_status moe_route(moe_plan_t plan, const float* logits, int T, int32_
 MOE_API moe_status moe_forward(moe_plan_t plan, moe_packed_t packed, const uint16_t* x, int T,
                        const int32_t* idx, const float* w, float* y, void* stream);
 
+/* moe_route followed by moe_forward, with the routing done inside the forward's first kernel
+ * (the step before the layer fused into it; page "Qwen3.6-35B-A3B Linux v1.0.4 ...",
+ * section "The fix (concatenated-expert dispatch)": fewer dispatches per layer). logits fp32
+ * [T, E] in; idx int32 [T, k] and w fp32 [T, k] are written exactly as moe_route writes them
+ * (the same selection and softmax code) and y as moe_forward computes it from them. Same
+ * arguments, errors and conditions as moe_forward; logits must be 16-byte aligned. Uses a
+ * per-plan counter (calls on one plan must not overlap in time; moe_clear_error resets it
+ * after a call that failed). */
+MOE_API moe_status moe_route_forward(moe_plan_t plan, moe_packed_t packed, const uint16_t* x,
+                                     int T, const float* logits, int32_t* idx, float* w, float* y,
+                                     void* stream);
+
 /* Dispatch threshold of moe_forward on this plan: T <= rows runs the weight-streaming decode
  * kernels (each unique expert's weights read once, rows applied 8 at a time), larger T the
  * grouped GEMMs. 0 <= rows <= 64 (else MOE_ERR_INVALID_ARG); 0 sends every call to the

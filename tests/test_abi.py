@@ -60,6 +60,8 @@ def test_plan_without_gpu_reports_no_device(lib):
 def test_null_handles_rejected(lib):
     assert lib.moe_route(None, None, 4, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_forward(None, None, None, 4, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_forward(None, None, None, 4, None, None, None, None, None) == \
+        moe.MOE_ERR_INVALID_ARG
     assert lib.moe_plan_destroy(None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_plan_set_decode_rows(None, 8) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_packed_destroy(None) == moe.MOE_ERR_INVALID_ARG

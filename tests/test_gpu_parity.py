@@ -243,6 +243,43 @@ def test_decode_and_grouped_paths_give_identical_integers(T):
         lay.close()
 
 
+@pytest.mark.parametrize("T,rows", [(8, 32), (40, 32), (40, 0), (2600, 32)])
+def test_route_forward_matches_route_then_forward(T, rows):
+    # moe_route_forward (routing inside the forward's first kernel) against moe_route followed
+    # by moe_forward: idx and w bit-identical, every tapped integer and scale bit-identical,
+    # y equal up to the order of the fp32 additions; on the weight-streaming path (T <= rows)
+    # and on the grouped GEMMs, twice in a row (the histogram kernel's counter returns to zero)
+    H, E, k, I, Is = 2048, 128, 8, 512, 512
+    d = synth.small_layer(T, H, E, k, I, Is, seed=90 + T, zipf_s=1.1, outliers=8)
+    W = weights_to(d["weights"], "cuda")
+    lay = moe.MoELayer(E, k, H, I, Is, T, W)
+    names = (("counts", moe.TAP_COUNTS), ("offsets", moe.TAP_OFFSETS), ("perm", moe.TAP_PERM),
+             ("qx", moe.TAP_QX), ("sx", moe.TAP_SX), ("acc_gu", moe.TAP_ACC_GU), ("hq", moe.TAP_HQ),
+             ("sh", moe.TAP_SH), ("acc_d", moe.TAP_ACC_D))
+    try:
+        moe.moe_plan_set_decode_rows(lay.plan, rows)
+        moe.moe_debug_enable(lay.plan, True)
+        x = d["x"].cuda()
+        lg = d["logits"].cuda()
+        idx_r, w_r = lay.route(lg)
+        y_r = lay.forward(x, idx_r, w_r)
+        torch.cuda.synchronize()
+        ref = {n: moe.moe_debug_tap(lay.plan, i) for n, i in names}
+        for _ in range(2):
+            idx = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+            w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+            y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+            moe.moe_route_forward(lay.plan, lay.packed, x, lg, idx, w, y)
+            torch.cuda.synchronize()
+            assert moe.moe_get_error(lay.plan) == 0
+            assert torch.equal(idx, idx_r) and torch.equal(w, w_r)
+            for n, i in names:
+                assert (moe.moe_debug_tap(lay.plan, i) == ref[n]).all(), n
+            assert (y - y_r).abs().max().item() <= 1e-5 * y_r.abs().max().item()
+    finally:
+        lay.close()
+
+
 def _tie_rows(x, seed):
     """Rows whose elements sit on (or next to) the rounding boundaries of the int8 code: with a
     power-of-two amax the scale is exact and (m + 1/2) * scale is an exact tie; with another
