@@ -572,6 +572,12 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       tc_fence_after();  // the MMAs that read this A stage before have completed
       tmem_st32(ta + (uint32_t)(as * kACols), o);
       tmem_st_wait();
+      // Converter warp 0 also waits for the stage's token tile, so that afull implies it and
+      // the MMA thread has a single barrier to check per stage (the converters run far ahead).
+      if (cw == 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(&xfull[ks % kXStages], (ks / kXStages) & 1u,
+                                             abort_flag, a.err)))
+        break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[as]);
@@ -589,14 +595,14 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       // ---------------- MMA issuer ----------------
       // The issuing thread is on the tensor pipe's critical path: tcgen05.mma issue blocks
       // once the pipe's queue is full, so every instruction between the last MMA of a stage
-      // and the first of the next leaves the pipe idle. Per stage it waits for the A stage
-      // (afull; usually already seen by the probe inside the previous stage's issue block)
-      // and for the token stage (xfull).
+      // and the first of the next leaves the pipe idle. Per stage it waits on one barrier,
+      // afull (usually already seen by the probe inside the previous stage's issue block),
+      // which the converters complete only once the stage's token tile has landed too.
       // Descriptors are a base plus a stage offset (the 14-bit start-address field does not
       // carry).
       const uint64_t dx0 = smem_desc_sw128(smem_u32(smem));
       int xs = 0;
-      uint32_t xph = 0, ks = 0, ready = 0;
+      uint32_t ks = 0, ready = 0;
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++it) {
@@ -612,11 +618,8 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
         int kin = 0;  // stage within the current accumulator chunk
         for (int kb = 0; kb < nks; ++kb, ++ks) {
           const int g = (int)(ks & 1);
+          // afull also covers the token stage (converter warp 0 waits for it before arriving)
           if (!ready && !mbar_wait(&afull[g], (ks >> 1) & 1u, abort_flag, a.err)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_test(&xfull[xs], xph) && !mbar_wait(&xfull[xs], xph, abort_flag, a.err)) {
             ok = false;
             break;
           }
@@ -630,10 +633,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
             kin = 0;
             dt += (uint32_t)a.TN;
           }
-          if (++xs == kXStages) {
-            xs = 0;
-            xph ^= 1;
-          }
+          if (++xs == kXStages) xs = 0;
         }
         if (!ok) break;
         umma_commit(&acc_full[slot]);
