@@ -280,6 +280,24 @@ def test_route_forward_matches_route_then_forward(T, rows):
         lay.close()
 
 
+@pytest.mark.parametrize("T,rows", [(8, 32), (8, 0), (40, 0)])
+def test_largest_supported_shape(T, rows):
+    # H = 8192 and I = I_shared = 4096, the largest shapes a plan accepts: the decode kernels'
+    # largest shared-memory staging (8 x H token codes, 8 x I h codes) and the grouped GEMMs'
+    # longest reduction (the 1024-K chunked accumulators when the exactness bound needs them),
+    # on the weight-streaming path and on the grouped GEMMs
+    sh = synth.LayerShape(T=T, H=8192, E=4, k=2, I=4096, Is=4096)
+    W = synth.make_weights(sh, 123, device="cuda")
+    x = synth.make_activations(T, sh.H, 123, 0, "cpu")
+    lg = synth.make_logits(T, sh.E, 123, 0.0, "cpu")
+    lay = moe.MoELayer(sh.E, sh.k, sh.H, sh.I, sh.Is, T, W)
+    try:
+        moe.moe_plan_set_decode_rows(lay.plan, rows)
+        check_layer(sh, x, lg, W, oracle_layer(W, sh), layer=lay)
+    finally:
+        lay.close()
+
+
 def _tie_rows(x, seed):
     """Rows whose elements sit on (or next to) the rounding boundaries of the int8 code: with a
     power-of-two amax the scale is exact and (m + 1/2) * scale is an exact tie; with another
