@@ -44,7 +44,7 @@
 // (128 rows x 128 K of fp16) in [384, 512).
 //
 // Warp roles (one CTA per SM; GemmRoles):
-//   epilogue warps (12 for each GEMM): warp w reads TMEM lanes 32*(w%4).. (weight
+//   epilogue warps (8 for gate/up, 12 for down): warp w reads TMEM lanes 32*(w%4).. (weight
 //               rows) and every (w/4)-th 16-column chunk (tokens) of its quadrant;
 //   two converter groups of four warps: group h widens K half h (64 K) of every stage into
 //               the stage's A stage, thread r of a group widening weight row r;
@@ -80,7 +80,7 @@ static_assert(kXSubBytes % 1024 == 0, "swizzled token boxes stay 1024-byte align
 
 constexpr int kConvWarps = 4;  // one converter group: one thread per weight row
 #ifndef MOE_GU_EPI_WARPS
-#define MOE_GU_EPI_WARPS 12
+#define MOE_GU_EPI_WARPS 8
 #endif
 #ifndef MOE_D_EPI_WARPS
 #define MOE_D_EPI_WARPS 12
