@@ -24,6 +24,16 @@ class _Layer(C.Structure):
                 ("sh_s_gate", C.c_void_p), ("sh_s_up", C.c_void_p), ("sh_s_down", C.c_void_p)]
 
 
+class _LayerNvfp4(C.Structure):
+    _fields_ = [("E", C.c_int), ("k", C.c_int), ("H", C.c_int), ("I", C.c_int), ("Is", C.c_int),
+                ("w_gate", C.c_void_p), ("w_up", C.c_void_p), ("w_down", C.c_void_p),
+                ("b_gate", C.c_void_p), ("b_up", C.c_void_p), ("b_down", C.c_void_p),
+                ("g_gate", C.c_void_p), ("g_up", C.c_void_p), ("g_down", C.c_void_p),
+                ("sh_gate", C.c_void_p), ("sh_up", C.c_void_p), ("sh_down", C.c_void_p),
+                ("sh_b_gate", C.c_void_p), ("sh_b_up", C.c_void_p), ("sh_b_down", C.c_void_p),
+                ("sh_g", C.c_void_p)]
+
+
 class _Taps(C.Structure):
     _fields_ = [("qx", C.c_void_p), ("sx", C.c_void_p), ("acc_gu", C.c_void_p),
                 ("hq", C.c_void_p), ("sh", C.c_void_p), ("acc_d", C.c_void_p)]
@@ -37,8 +47,12 @@ def lib():
     if _lib is None:
         _lib = C.CDLL(os.environ.get("MOE_ORACLE_LIB") or build())
         for name in ("oracle_route", "oracle_quant_rows", "oracle_permute", "oracle_forward",
-                     "oracle_dense", "oracle_router_logits", "oracle_rmsnorm_residual"):
+                     "oracle_dense", "oracle_router_logits", "oracle_rmsnorm_residual",
+                     "oracle_forward_nvfp4"):
             getattr(_lib, name).restype = C.c_int
+        for name in ("oracle_e2m1_value", "oracle_e4m3_value"):
+            getattr(_lib, name).restype = C.c_double
+            getattr(_lib, name).argtypes = [C.c_int]
     return _lib
 
 
@@ -170,3 +184,56 @@ def rmsnorm_residual(x_bf16, y=None):
     x_in = np.zeros_like(x)
     lib().oracle_rmsnorm_residual(_p(x), _p(yy), _p(x_in), T, H)
     return x, x_in
+
+
+def e2m1_value(code: int) -> float:
+    return lib().oracle_e2m1_value(int(code))
+
+
+def e4m3_value(byte: int) -> float:
+    return lib().oracle_e4m3_value(int(byte))
+
+
+class LayerNvfp4:
+    """Host copies of one layer's NVFP4 expert weights (see synth.make_weights_nvfp4)."""
+
+    def __init__(self, W: dict, E: int, k: int, H: int, I: int, Is: int):
+        self.E, self.k, self.H, self.I, self.Is = E, k, H, I, Is
+        self.arrs = {}
+        for key in ("w_gate", "w_up", "w_down", "b_gate", "b_up", "b_down"):
+            self.arrs[key] = _np(W[key], np.uint8)
+        for key in ("g_gate", "g_up", "g_down"):
+            self.arrs[key] = _np(W[key], np.float32)
+        if Is > 0:
+            for key in ("sh_gate", "sh_up", "sh_down", "sh_b_gate", "sh_b_up", "sh_b_down"):
+                self.arrs[key] = _np(W[key], np.uint8)
+            self.arrs["sh_g"] = _np(W["sh_g"], np.float32)
+        self.c = _LayerNvfp4(E, k, H, I, Is,
+                             *[_p(self.arrs.get(f)) for f, _ in _LayerNvfp4._fields_[5:]])
+
+
+def forward_nvfp4(layer: LayerNvfp4, x_bf16, idx, w, taps: bool = False,
+                  nthreads: int | None = None):
+    """The layer with NVFP4 expert weights. Returns y (float64 [T,H]) and, with taps=True,
+    the intermediates; acc_gu and acc_d are the exact sums of q * e2m1 * e4m3 (float64)."""
+    x = _np(x_bf16, np.uint16)
+    ix = _np(idx, np.int32)
+    ww = _np(w, np.float32)
+    T, H = x.shape
+    k = layer.k
+    S = k + (1 if layer.Is > 0 else 0)
+    Imax = max(layer.I, layer.Is)
+    y = np.zeros((T, H), np.float64)
+    t = None
+    tp = None
+    if taps:
+        t = dict(qx=np.zeros((T, H), np.int8), sx=np.zeros(T, np.float32),
+                 acc_gu=np.zeros((T, S, 2, Imax), np.float64), hq=np.zeros((T, S, Imax), np.int8),
+                 sh=np.zeros((T, S), np.float32), acc_d=np.zeros((T, S, H), np.float64))
+        tp = _Taps(*[_p(t[f]) for f, _ in _Taps._fields_])
+    rc = lib().oracle_forward_nvfp4(C.byref(layer.c), _p(x), T, _p(ix), _p(ww), _p(y),
+                                    C.byref(tp) if tp is not None else None,
+                                    nthreads or default_threads())
+    if rc:
+        raise ValueError(f"oracle_forward_nvfp4 rc={rc}")
+    return (y, t) if taps else y

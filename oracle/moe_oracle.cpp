@@ -28,6 +28,18 @@
 // implements: W8A8 with per-output-channel weight scales, per-token activation scales,
 // fp32 scales and an fp32 output.
 //
+// NVFP4 experts. The same layer with its expert weights (routed and shared) in NVFP4 instead
+// of int8: the format the page "[job] Strix Halo: multi-session serving ... #145" keeps for
+// the routed experts (comment of Oct 19, "FP4 dtype survey on the AMD track ... decided: stay
+// on NVFP4"). A weight row is a sequence of 4-bit E2M1 codes, two per byte (element 2j in the
+// low nibble), with one E4M3 block scale per 16 consecutive elements and one fp32 scale per
+// weight matrix. Dequantised weight = e2m1(code) * e4m3(block scale) * matrix scale. The
+// activations stay int8 as above. With w' = e2m1 * e4m3 (the weight without the matrix
+// scale), every product q * w' is a multiple of 2^-10 below 2^19 in magnitude, so a row's
+// sum over up to 2^13 elements is exact in double; the oracle forms it in double (h
+// ascending) and then applies the scales as the int8 layer does:
+//   g = (float(acc_g) * s_x) * gs_gate,  u likewise,  d = (float(acc_d) * s_h) * gs_down.
+//
 // Built with -O2 -ffp-contract=off and no fast-math, so every fp32 operation is a single
 // IEEE-rounded operation in the order written.
 
@@ -66,6 +78,38 @@ typedef struct {
   float* sh;       // [T, S]
   int32_t* acc_d;  // [T, S, H]
 } oracle_taps;
+
+// NVFP4 layer: codes uint8 [rows, K/2] (two E2M1 codes per byte, element 2j in the low
+// nibble), block scales uint8 E4M3 [rows, K/16], one fp32 scale per matrix.
+typedef struct {
+  int E, k, H, I, Is;
+  const uint8_t* w_gate;              // [E, I, H/2]
+  const uint8_t* w_up;                // [E, I, H/2]
+  const uint8_t* w_down;              // [E, H, I/2]
+  const uint8_t* b_gate;              // [E, I, H/16]
+  const uint8_t* b_up;                // [E, I, H/16]
+  const uint8_t* b_down;              // [E, H, I/16]
+  const float* g_gate;                // [E]
+  const float* g_up;                  // [E]
+  const float* g_down;                // [E]
+  const uint8_t* sh_gate;             // [Is, H/2]
+  const uint8_t* sh_up;               // [Is, H/2]
+  const uint8_t* sh_down;             // [H, Is/2]
+  const uint8_t* sh_b_gate;           // [Is, H/16]
+  const uint8_t* sh_b_up;             // [Is, H/16]
+  const uint8_t* sh_b_down;           // [H, Is/16]
+  const float* sh_g;                  // [3]: gate, up, down matrix scales
+} oracle_layer_nvfp4;
+
+// Intermediates of the NVFP4 layer; the accumulators are the exact sums of q * w' (double).
+typedef struct {
+  int8_t* qx;      // [T, H]
+  float* sx;       // [T]
+  double* acc_gu;  // [T, S, 2, Imax]
+  int8_t* hq;      // [T, S, Imax]
+  float* sh;       // [T, S]
+  double* acc_d;   // [T, S, H]
+} oracle_taps_nvfp4;
 
 }  // extern "C"
 
@@ -130,6 +174,72 @@ void expert_ffn(const int8_t* qx, float sx, int H, int I,
       ad += static_cast<int32_t>(hq[i]) * static_cast<int32_t>(Wd[(size_t)o * I + i]);
     if (acc_d_tap) acc_d_tap[o] = ad;
     d[o] = (static_cast<float>(ad) * sh) * sd[o];
+  }
+}
+
+// E2M1 (OCP Microscaling Formats v1.0, FP4): bit 3 sign, bits 2-1 exponent with bias 1,
+// bit 0 mantissa; exponent 0 encodes the subnormals 0 and 0.5.
+double e2m1_value(unsigned code) {
+  const unsigned sgn = (code >> 3) & 1u, ex = (code >> 1) & 3u, man = code & 1u;
+  const double mag = ex == 0 ? 0.5 * man : std::ldexp(1.0 + 0.5 * man, (int)ex - 1);
+  return sgn ? -mag : mag;
+}
+
+// E4M3 (OCP FP8, the "fn" variant without infinities): bit 7 sign, bits 6-3 exponent with
+// bias 7, bits 2-0 mantissa; exponent 0 encodes subnormals f/8 * 2^-6; S.1111.111 is NaN.
+double e4m3_value(unsigned b) {
+  const unsigned sgn = (b >> 7) & 1u, ex = (b >> 3) & 15u, man = b & 7u;
+  if (ex == 15 && man == 7) return std::nan("");
+  const double mag = ex == 0 ? std::ldexp(man / 8.0, -6) : std::ldexp(1.0 + man / 8.0, (int)ex - 7);
+  return sgn ? -mag : mag;
+}
+
+// Element j of an NVFP4 row without the matrix scale: e2m1(code j) * e4m3(block scale j/16).
+double nvfp4_element(const uint8_t* codes, const uint8_t* bscale, int j) {
+  const unsigned code = (codes[j / 2] >> (4 * (j % 2))) & 15u;
+  return e2m1_value(code) * e4m3_value(bscale[j / 16]);
+}
+
+// A block scale must be a finite, non-negative E4M3 value.
+bool block_scales_valid(const uint8_t* b, size_t n) {
+  for (size_t i = 0; i < n; ++i)
+    if (b[i] >= 0x7f) return false;
+  return true;
+}
+
+// One expert with NVFP4 weights applied to one quantised token row (the int8 expert_ffn with
+// each weight row read through nvfp4_element and the sums formed exactly in double).
+void expert_ffn_nvfp4(const int8_t* qx, float sx, int H, int I, const uint8_t* Wg,
+                      const uint8_t* Wu, const uint8_t* Wd, const uint8_t* Bg, const uint8_t* Bu,
+                      const uint8_t* Bd, float gg, float gu, float gd, float* d,
+                      double* acc_gu_tap, int8_t* hq_tap, float* sh_tap, double* acc_d_tap,
+                      int Imax) {
+  std::vector<float> h(I);
+  for (int i = 0; i < I; ++i) {
+    double ag = 0.0, au = 0.0;
+    for (int hh = 0; hh < H; ++hh) {
+      ag += qx[hh] * nvfp4_element(Wg + (size_t)i * (H / 2), Bg + (size_t)i * (H / 16), hh);
+      au += qx[hh] * nvfp4_element(Wu + (size_t)i * (H / 2), Bu + (size_t)i * (H / 16), hh);
+    }
+    if (acc_gu_tap) {
+      acc_gu_tap[i] = ag;
+      acc_gu_tap[Imax + i] = au;
+    }
+    const float g4 = (static_cast<float>(ag) * sx) * gg;
+    const float u4 = (static_cast<float>(au) * sx) * gu;
+    h[i] = g4 / (1.0f + std::exp(-g4)) * u4;
+  }
+  std::vector<int8_t> hq(I);
+  float sh = 0.0f;
+  quantize_row(h.data(), I, hq.data(), &sh);
+  if (hq_tap) std::memcpy(hq_tap, hq.data(), I);
+  if (sh_tap) *sh_tap = sh;
+  for (int o = 0; o < H; ++o) {
+    double ad = 0.0;
+    for (int j = 0; j < I; ++j)
+      ad += hq[j] * nvfp4_element(Wd + (size_t)o * (I / 2), Bd + (size_t)o * (I / 16), j);
+    if (acc_d_tap) acc_d_tap[o] = ad;
+    d[o] = (static_cast<float>(ad) * sh) * gd;
   }
 }
 
@@ -340,6 +450,67 @@ int oracle_router_logits(const uint16_t* x, const float* Wr, int T, int H, int E
         acc += static_cast<double>(bf16_to_float(x[(size_t)t * H + h])) *
                static_cast<double>(Wr[(size_t)h * E + e]);
       logits[(size_t)t * E + e] = acc;
+    }
+  });
+  return 0;
+}
+
+// Value of one E2M1 code (0..15) and of one E4M3 byte (0..255; NaN for the NaN encodings).
+double oracle_e2m1_value(int code) { return e2m1_value((unsigned)code & 15u); }
+double oracle_e4m3_value(int byte) { return e4m3_value((unsigned)byte & 255u); }
+
+// The layer with NVFP4 expert weights (see the file header). Same arguments as
+// oracle_forward; returns -3 when a block scale is negative or NaN.
+int oracle_forward_nvfp4(const oracle_layer_nvfp4* L, const uint16_t* x, int T,
+                         const int32_t* idx, const float* w, double* y,
+                         const oracle_taps_nvfp4* taps, int nthreads) {
+  if (!L || L->E <= 0 || L->k <= 0 || L->k > L->E || L->H <= 0 || L->I <= 0 || L->Is < 0 ||
+      L->H % 16 || L->I % 16 || L->Is % 16)
+    return -1;
+  const int H = L->H, I = L->I, Is = L->Is, k = L->k, E = L->E;
+  const int S = Is > 0 ? k + 1 : k;
+  const int Imax = std::max(I, Is);
+  for (long r = 0; r < (long)T * k; ++r)
+    if (idx[r] < 0 || idx[r] >= E) return -2;
+  if (!block_scales_valid(L->b_gate, (size_t)E * I * (H / 16)) ||
+      !block_scales_valid(L->b_up, (size_t)E * I * (H / 16)) ||
+      !block_scales_valid(L->b_down, (size_t)E * H * (I / 16)))
+    return -3;
+  if (Is > 0 && (!block_scales_valid(L->sh_b_gate, (size_t)Is * (H / 16)) ||
+                 !block_scales_valid(L->sh_b_up, (size_t)Is * (H / 16)) ||
+                 !block_scales_valid(L->sh_b_down, (size_t)H * (Is / 16))))
+    return -3;
+  parallel_tokens(T, nthreads, [&](int t) {
+    std::vector<float> xf(H), d(H);
+    std::vector<int8_t> qx(H);
+    for (int c = 0; c < H; ++c) xf[c] = bf16_to_float(x[(size_t)t * H + c]);
+    float sx = 0.0f;
+    quantize_row(xf.data(), H, qx.data(), &sx);
+    if (taps && taps->qx) std::memcpy(taps->qx + (size_t)t * H, qx.data(), H);
+    if (taps && taps->sx) taps->sx[t] = sx;
+    double* yt = y + (size_t)t * H;
+    for (int o = 0; o < H; ++o) yt[o] = 0.0;
+    for (int s = 0; s < S; ++s) {
+      const bool shared = (s == k);
+      const size_t slot = (size_t)t * S + s;
+      double* agu = (taps && taps->acc_gu) ? taps->acc_gu + slot * 2 * Imax : nullptr;
+      int8_t* hq = (taps && taps->hq) ? taps->hq + slot * Imax : nullptr;
+      float* sh = (taps && taps->sh) ? taps->sh + slot : nullptr;
+      double* ad = (taps && taps->acc_d) ? taps->acc_d + slot * H : nullptr;
+      if (shared) {
+        expert_ffn_nvfp4(qx.data(), sx, H, Is, L->sh_gate, L->sh_up, L->sh_down, L->sh_b_gate,
+                         L->sh_b_up, L->sh_b_down, L->sh_g[0], L->sh_g[1], L->sh_g[2], d.data(),
+                         agu, hq, sh, ad, Imax);
+      } else {
+        const int e = idx[(size_t)t * k + s];
+        expert_ffn_nvfp4(qx.data(), sx, H, I, L->w_gate + (size_t)e * I * (H / 2),
+                         L->w_up + (size_t)e * I * (H / 2), L->w_down + (size_t)e * H * (I / 2),
+                         L->b_gate + (size_t)e * I * (H / 16), L->b_up + (size_t)e * I * (H / 16),
+                         L->b_down + (size_t)e * H * (I / 16), L->g_gate[e], L->g_up[e],
+                         L->g_down[e], d.data(), agu, hq, sh, ad, Imax);
+      }
+      const double wt4 = shared ? 1.0 : static_cast<double>(w[(size_t)t * k + s]);
+      for (int o = 0; o < H; ++o) yt[o] += wt4 * static_cast<double>(d[o]);
     }
   });
   return 0;

@@ -190,6 +190,85 @@ def small_layer(T, H, E, k, I, Is, seed, zipf_s=0.0, outliers=0, device="cpu") -
     return make_layer(wl, device)
 
 
+# NVFP4 expert weights. The same N(0, 0.02) draws quantised to NVFP4 instead of int8 (input
+# preparation, as for int8): per weight matrix a fp32 scale gs = amax / (6 * 448); per block
+# of 16 consecutive elements of a row an E4M3 scale = amax_block / (6 * gs) rounded to E4M3
+# (torch's float8_e4m3fn conversion, round to nearest even); each element w / (scale * gs)
+# rounded to the nearest E2M1 magnitude (0, 0.5, 1, 1.5, 2, 3, 4, 6; saturating at 6) with
+# its sign. Codes are packed two per byte, element 2j in the low nibble.
+_E2M1_BOUNDS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
+def quantize_nvfp4_rows(w: torch.Tensor, gs: torch.Tensor):
+    """NVFP4 codes (uint8 [..., K/2]) and E4M3 block scales (uint8 [..., K/16]) of weight
+    rows w [..., K] under the matrix scale gs (fp32 scalar tensor)."""
+    w = w.float()
+    shp = w.shape
+    blk = w.reshape(*shp[:-1], shp[-1] // 16, 16)
+    bs = (blk.abs().amax(-1) / (6.0 * gs)).clamp_(max=448.0)
+    bs8 = bs.to(torch.float8_e4m3fn)
+    bsd = bs8.float()
+    safe = torch.where(bsd > 0, bsd, torch.ones_like(bsd))
+    v = blk / (safe * gs)[..., None]
+    bounds = torch.tensor(_E2M1_BOUNDS, dtype=torch.float32, device=w.device)
+    mag = torch.bucketize(v.abs(), bounds, right=False)
+    mag = torch.where(bsd[..., None] > 0, mag, torch.zeros_like(mag))
+    code = (mag | torch.where(v < 0, 8, 0)).to(torch.uint8).reshape(shp)
+    packed = code[..., 0::2] | (code[..., 1::2] << 4)
+    return packed.contiguous(), bs8.view(torch.uint8).contiguous()
+
+
+def _normal_nvfp4(shape, g, device, std=0.02, chunk_rows=None):
+    """N(0,std) fp32 draws [n0, rows, K] (or [rows, K]) quantised to NVFP4 with one matrix
+    scale per index of dim 0 (per expert) or one for the whole 2-D matrix."""
+    three = len(shape) == 3
+    n0 = shape[0] if three else 1
+    rows, K = shape[-2], shape[-1]
+    codes = torch.empty((n0, rows, K // 2), dtype=torch.uint8, device=device)
+    bsc = torch.empty((n0, rows, K // 16), dtype=torch.uint8, device=device)
+    gsv = torch.empty((n0,), dtype=torch.float32, device=device)
+    step = chunk_rows or n0
+    for a in range(0, n0, step):
+        b = min(n0, a + step)
+        w = torch.randn((b - a, rows, K), generator=g, device=device, dtype=torch.float32) * std
+        for i in range(b - a):
+            am = w[i].abs().amax()
+            gs = torch.where(am > 0, am / (6.0 * 448.0), torch.ones_like(am))
+            codes[a + i], bsc[a + i] = quantize_nvfp4_rows(w[i], gs)
+            gsv[a + i] = gs
+        del w
+    if not three:
+        return codes[0], bsc[0], gsv
+    return codes, bsc, gsv
+
+
+def make_weights_nvfp4(shape: LayerShape, seed: int, device="cpu", slab: int = 16) -> dict:
+    """NVFP4 routed + shared expert weights for one layer:
+    w_gate, w_up uint8 [E, I, H/2], b_gate, b_up uint8 [E, I, H/16], g_gate, g_up fp32 [E];
+    w_down uint8 [E, H, I/2], b_down uint8 [E, H, I/16], g_down fp32 [E]; shared expert
+    sh_gate, sh_up [Is, H/2], sh_b_gate, sh_b_up [Is, H/16], sh_down [H, Is/2],
+    sh_b_down [H, Is/16] and sh_g fp32 [3] (gate, up, down)."""
+    g = _gen(seed * 1000 + 19, device)
+    E, H, I, Is = shape.E, shape.H, shape.I, shape.Is
+    wg, bg, gg = _normal_nvfp4((E, I, H), g, device, chunk_rows=slab)
+    wu, bu, gu = _normal_nvfp4((E, I, H), g, device, chunk_rows=slab)
+    wd, bd, gd = _normal_nvfp4((E, H, I), g, device, chunk_rows=slab)
+    W = dict(w_gate=wg, b_gate=bg, g_gate=gg, w_up=wu, b_up=bu, g_up=gu,
+             w_down=wd, b_down=bd, g_down=gd)
+    if Is > 0:
+        shg, shbg, shgg = _normal_nvfp4((Is, H), g, device)
+        shu, shbu, shgu = _normal_nvfp4((Is, H), g, device)
+        shd, shbd, shgd = _normal_nvfp4((H, Is), g, device)
+        W.update(sh_gate=shg, sh_b_gate=shbg, sh_up=shu, sh_b_up=shbu, sh_down=shd,
+                 sh_b_down=shbd, sh_g=torch.cat([shgg, shgu, shgd]).contiguous())
+    return W
+
+
+def weight_bytes_per_expert_nvfp4(H: int, I: int) -> int:
+    """Bytes one NVFP4 expert occupies in HBM: packed codes plus E4M3 block scales."""
+    return 3 * H * I // 2 + 3 * H * I // 16
+
+
 def weight_bytes_per_expert(H: int, I: int) -> int:
     """Bytes one expert occupies in HBM: int8 gate+up+down plus fp32 scales."""
     return 3 * H * I + 4 * (2 * I + H)

@@ -61,6 +61,21 @@ MUTANTS = [
     ("router_float_accumulation", "double acc = 0.0;\n      for (int h = 0; h < H; ++h)",
      "float acc = 0.0f;\n      for (int h = 0; h < H; ++h)"),
     ("dense_drops_shared_expert", "if (Is > 0) {\n      expert_ffn", "if (Is < 0) {\n      expert_ffn"),
+    # NVFP4 expert weights
+    ("fp4_nibbles_swapped", "(codes[j / 2] >> (4 * (j % 2)))", "(codes[j / 2] >> (4 * (1 - j % 2)))"),
+    ("fp4_block_of_8", "e4m3_value(bscale[j / 16])", "e4m3_value(bscale[j / 8])"),
+    ("e2m1_bias_2", "std::ldexp(1.0 + 0.5 * man, (int)ex - 1)", "std::ldexp(1.0 + 0.5 * man, (int)ex - 2)"),
+    ("e2m1_subnormal_1", "ex == 0 ? 0.5 * man :", "ex == 0 ? 1.0 * man :"),
+    ("e2m1_sign_bit_2", "const unsigned sgn = (code >> 3) & 1u", "const unsigned sgn = (code >> 2) & 1u"),
+    ("e4m3_bias_8", "std::ldexp(1.0 + man / 8.0, (int)ex - 7)", "std::ldexp(1.0 + man / 8.0, (int)ex - 8)"),
+    ("e4m3_subnormal_exp", "std::ldexp(man / 8.0, -6)", "std::ldexp(man / 8.0, -7)"),
+    ("e4m3_implicit_one_dropped", "std::ldexp(1.0 + man / 8.0,", "std::ldexp(man / 8.0,"),
+    ("fp4_up_with_gate_scale", "L->g_gate[e], L->g_up[e]", "L->g_gate[e], L->g_gate[e]"),
+    ("fp4_shared_up_scale", "L->sh_g[0], L->sh_g[1], L->sh_g[2]", "L->sh_g[0], L->sh_g[0], L->sh_g[2]"),
+    ("fp4_down_scale_row", "Bd + (size_t)o * (I / 16)", "Bd + (size_t)(o / 2) * (I / 16)"),
+    ("fp4_nan_scale_accepted", "if (b[i] >= 0x7f) return false;", "if (b[i] > 0x7f) return false;"),
+    ("fp4_gate_without_token_scale", "const float g4 = (static_cast<float>(ag) * sx) * gg;",
+     "const float g4 = static_cast<float>(ag) * gg;"),
 ]
 
 

@@ -409,3 +409,185 @@ def test_residual_rounding_ties_go_to_even():
     y = np.array([[c[1] for c in cases]], np.float64)
     x2, _ = oracle.rmsnorm_residual(x, y)
     assert _bf16_to_f32(x2).numpy()[0].tolist() == [c[2] for c in cases]
+
+
+# ---------------------------------------------------------------- NVFP4 expert weights
+
+def _e2m1_table():
+    return np.array(json.load(open(os.path.join(GOLD, "e2m1_codes.json")))["values"], np.float64)
+
+
+def _e4m3_library(byte_array):
+    """E4M3 bytes decoded by torch's float8_e4m3fn (a library routine)."""
+    b = torch.from_numpy(np.ascontiguousarray(byte_array, np.uint8))
+    return b.view(torch.float8_e4m3fn).double().numpy()
+
+
+def test_e2m1_codes_golden_and_library():
+    tab = _e2m1_table()
+    got = np.array([oracle.e2m1_value(c) for c in range(16)])
+    assert (got == tab).all() and (np.signbit(got) == np.signbit(tab)).all()
+    # each E2M1 value re-encoded by bit placement as an E4M3 byte (exponent bias 1 -> 7,
+    # the mantissa bit on top) and decoded by torch's float8_e4m3fn
+    enc = []
+    for c in range(16):
+        s, e, m = c >> 3, (c >> 1) & 3, c & 1
+        enc.append((s << 7) | (((e + 6) << 3) | (m << 2) if e else (0x30 if m else 0)))
+    assert (_e4m3_library(enc) == got).all()
+
+
+def test_e4m3_every_byte_matches_library():
+    lib_vals = _e4m3_library(np.arange(256))
+    got = np.array([oracle.e4m3_value(b) for b in range(256)])
+    nan = np.isnan(lib_vals)
+    assert (np.isnan(got) == nan).all() and nan.sum() == 2       # 0x7F and 0xFF
+    assert (got[~nan] == lib_vals[~nan]).all()
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+
+
+def _dequant_nvfp4(codes, scales):
+    """w' = e2m1 * e4m3 of every element, decoded independently of the oracle: nibbles by
+    numpy (element 2j low), values from the golden E2M1 table, scales by torch."""
+    c = np.asarray(codes, np.uint8)
+    nib = np.stack([c & 15, c >> 4], axis=-1).reshape(*c.shape[:-1], c.shape[-1] * 2)
+    vals = _e2m1_table()[nib]
+    sc = np.repeat(_e4m3_library(scales), 16, axis=-1)
+    return vals * sc
+
+
+def _random_nvfp4_layer(rng, E, k, H, I, Is):
+    """Codes uniform over all bytes, block scales uniform over every finite non-negative
+    E4M3 byte (subnormals and 448 included), matrix scales in [0.5, 2)."""
+    W = dict(w_gate=rng.integers(0, 256, (E, I, H // 2)), w_up=rng.integers(0, 256, (E, I, H // 2)),
+             w_down=rng.integers(0, 256, (E, H, I // 2)),
+             b_gate=rng.integers(0, 127, (E, I, H // 16)), b_up=rng.integers(0, 127, (E, I, H // 16)),
+             b_down=rng.integers(0, 127, (E, H, I // 16)),
+             g_gate=rng.uniform(0.5, 2, E), g_up=rng.uniform(0.5, 2, E), g_down=rng.uniform(0.5, 2, E))
+    if Is:
+        W.update(sh_gate=rng.integers(0, 256, (Is, H // 2)), sh_up=rng.integers(0, 256, (Is, H // 2)),
+                 sh_down=rng.integers(0, 256, (H, Is // 2)), sh_b_gate=rng.integers(0, 127, (Is, H // 16)),
+                 sh_b_up=rng.integers(0, 127, (Is, H // 16)), sh_b_down=rng.integers(0, 127, (H, Is // 16)),
+                 sh_g=rng.uniform(0.5, 2, 3))
+    out = {}
+    for key, v in W.items():
+        out[key] = np.ascontiguousarray(v, np.float32 if key.startswith("g_") or key == "sh_g" else np.uint8)
+    return out
+
+
+@pytest.mark.parametrize("weights", ["random_bytes", "synth"])
+def test_nvfp4_accumulators_match_library_matmul(weights):
+    T, H, E, k, I, Is = 6, 64, 4, 2, 32, 48
+    d = synth.small_layer(T, H, E, k, I, Is, seed=21)
+    if weights == "synth":
+        W = {key: v.numpy() for key, v in synth.make_weights_nvfp4(d["shape"], 21).items()}
+    else:
+        W = _random_nvfp4_layer(np.random.default_rng(21), E, k, H, I, Is)
+    L = oracle.LayerNvfp4(W, E, k, H, I, Is)
+    idx, w = oracle.route(d["logits"], k)
+    y, tp = oracle.forward_nvfp4(L, d["x"], idx, w, taps=True)
+    q, _ = oracle.quant_rows(d["x"])
+    assert (tp["qx"] == q).all()
+    qx = tp["qx"].astype(np.float64)
+    for t in range(T):
+        for s in range(k + 1):
+            if s < k:
+                e = idx[t, s]
+                wg, wu = _dequant_nvfp4(W["w_gate"][e], W["b_gate"][e]), _dequant_nvfp4(W["w_up"][e], W["b_up"][e])
+                wd, n = _dequant_nvfp4(W["w_down"][e], W["b_down"][e]), I
+            else:
+                wg, wu = _dequant_nvfp4(W["sh_gate"], W["sh_b_gate"]), _dequant_nvfp4(W["sh_up"], W["sh_b_up"])
+                wd, n = _dequant_nvfp4(W["sh_down"], W["sh_b_down"]), Is
+            # every term is a multiple of 2^-10 and every partial sum is far below 2^43:
+            # the float64 matmul is exact in any summation order
+            assert (tp["acc_gu"][t, s, 0, :n] == wg @ qx[t]).all()
+            assert (tp["acc_gu"][t, s, 1, :n] == wu @ qx[t]).all()
+            assert (tp["acc_d"][t, s] == wd @ tp["hq"][t, s, :n].astype(np.float64)).all()
+
+
+def test_nvfp4_integer_weights_reduce_to_int8_layer():
+    # Block scales 1.0 and codes of integer values (0, +-1, +-2, +-3, +-4, +-6): the NVFP4
+    # layer is the int8 layer with those integers as weights and the matrix scale as every
+    # channel's scale, bit for bit.
+    T, H, E, k, I, Is = 7, 64, 5, 2, 32, 48
+    rng = np.random.default_rng(22)
+    d = synth.small_layer(T, H, E, k, I, Is, seed=22)
+    int_codes = np.array([0, 2, 4, 5, 6, 7, 8, 10, 12, 13, 14, 15], np.uint8)
+    tab = _e2m1_table()
+
+    def mat(shape):
+        c = rng.choice(int_codes, size=shape[:-1] + (shape[-1],))
+        packed = (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+        return packed, tab[c].astype(np.int8), np.full(shape[:-1] + (shape[-1] // 16,), 0x38, np.uint8)
+
+    g = rng.uniform(0.001, 0.01, (E, 3)).astype(np.float32)
+    shg = rng.uniform(0.001, 0.01, 3).astype(np.float32)
+    F, N = {}, {}
+    for name, shape, r in (("gate", (E, I, H), 0), ("up", (E, I, H), 1), ("down", (E, H, I), 2)):
+        F["w_" + name], N["w_" + name], F["b_" + name] = mat(shape)
+        F["g_" + name] = np.ascontiguousarray(g[:, r])
+        N["s_" + name] = np.ascontiguousarray(np.repeat(g[:, r:r + 1], shape[1], axis=1))
+    for name, shape, r in (("gate", (Is, H), 0), ("up", (Is, H), 1), ("down", (H, Is), 2)):
+        F["sh_" + name], N["sh_" + name], F["sh_b_" + name] = mat(shape)
+        N["sh_s_" + name] = np.full(shape[0], shg[r], np.float32)
+    F["sh_g"] = shg
+    idx, w = oracle.route(d["logits"], k)
+    y4, t4 = oracle.forward_nvfp4(oracle.LayerNvfp4(F, E, k, H, I, Is), d["x"], idx, w, taps=True)
+    y8, t8 = oracle.forward(oracle.Layer(N, E, k, H, I, Is), d["x"], idx, w, taps=True)
+    assert (t4["acc_gu"] == t8["acc_gu"]).all() and (t4["acc_d"] == t8["acc_d"]).all()
+    assert (t4["hq"] == t8["hq"]).all()
+    assert np.array_equal(y4, y8)
+
+
+def test_golden_hand_layer_nvfp4():
+    G = json.load(open(os.path.join(GOLD, "hand_layer_nvfp4.json")))
+    E, k, H, I = 2, 1, 16, 16
+    ex1 = G["expert1"]
+    W = {}
+    for name, rows, K in (("gate", I, H), ("up", I, H), ("down", H, I)):
+        codes = np.zeros((E, rows, K // 2), np.uint8)
+        sc = np.full((E, rows, K // 16), ex1["default_scale"], np.uint8)
+        for r, b in ex1[name + "_rows"].items():
+            codes[1, int(r)] = b
+        for r, b in ex1[name + "_scales"].items():
+            sc[1, int(r)] = b
+        W["w_" + name], W["b_" + name] = codes, sc
+        W["g_" + name] = np.array([1.0, ex1["g_" + name]], np.float32)
+    lay = oracle.LayerNvfp4(W, E, k, H, I, 0)
+    x = bf16_bits([G["x"]])
+    idx, w = oracle.route(np.array([G["logits"]], np.float32), G["top_k"])
+    ex = G["expect"]
+    assert idx[0].tolist() == ex["idx"]
+    y, tp = oracle.forward_nvfp4(lay, x, idx, w, taps=True)
+    assert tp["qx"][0].tolist() == ex["q_x"]
+    assert tp["acc_gu"][0, 0, 0].tolist() == ex["acc_gate"]
+    assert tp["acc_gu"][0, 0, 1].tolist() == ex["acc_up"]
+    assert tp["hq"][0, 0].tolist() == ex["q_h"]
+    assert tp["acc_d"][0, 0].tolist() == ex["acc_down"]
+    s_h = ex["h0"] / 127
+    yc = [a * s_h * ex1["g_down"] for a in ex["acc_down"]]
+    np.testing.assert_allclose(y[0], yc, rtol=2e-6, atol=0)
+
+
+@pytest.mark.parametrize("bad", [0x7F, 0x80, 0xB8, 0xFF])
+def test_nvfp4_rejects_negative_or_nan_block_scales(bad):
+    T, H, E, k, I = 2, 32, 2, 1, 16
+    W = _random_nvfp4_layer(np.random.default_rng(23), E, k, H, I, 0)
+    W["b_down"][1, 3, 0] = bad
+    d = synth.small_layer(T, H, E, k, I, 0, seed=23)
+    idx = np.array([[0], [0]], np.int32)
+    w = np.ones((T, 1), np.float32)
+    lay = oracle.LayerNvfp4(W, E, k, H, I, 0)
+    with pytest.raises(ValueError):
+        oracle.forward_nvfp4(lay, d["x"], idx, w)
+
+
+def test_nvfp4_synth_weights_close_to_their_fp32_draws():
+    # the generator's NVFP4 quantisation of N(0, 0.02) draws: relative RMS error of an E2M1
+    # element with an E4M3 block scale is about 10%; a wrong scale or nibble order is not
+    g = torch.Generator().manual_seed(5)
+    w = torch.randn((64, 256), generator=g) * 0.02
+    gs = w.abs().amax() / (6 * 448)
+    codes, bsc = synth.quantize_nvfp4_rows(w, gs)
+    deq = _dequant_nvfp4(codes.numpy(), bsc.numpy()) * float(gs)
+    rel = np.sqrt(((deq - w.double().numpy()) ** 2).mean() / (w.double().numpy() ** 2).mean())
+    assert rel < 0.15, rel
