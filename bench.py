@@ -183,12 +183,12 @@ def oracle_sample_rate(W_dev, wl, n_tokens, nthreads):
     return n_tokens / dt, dt
 
 
-def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
-    """Batched decode, C=8 rows, through the same layers' weights (CUDA graph of one
+def measure_decode(moe, plan, packed_list, peaks, H, E, k, bytes_per_expert, steps, stream,
+                   what="int8 weights of the stack's 40 layers"):
+    """Batched decode, C=8 rows, through one packed weight set per layer (CUDA graph of one
     moe_route_forward per layer: routing from the logits inside the forward); microseconds
-    per layer and the HBM roofline."""
+    per layer and the HBM roofline of the unique experts' bytes."""
     dev = torch.device("cuda")
-    n_layers = len(layers)
     dwl = synth.WORKLOADS["decode"]
     xd = synth.make_activations(dwl.shape.T, H, dwl.seed, dwl.outliers, dev)
     lgd = synth.make_logits(dwl.shape.T, E, dwl.seed, dwl.zipf_s, dev)
@@ -197,9 +197,10 @@ def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
     yd = torch.empty((dwl.shape.T, H), dtype=torch.float32, device=dev)
 
     def decode_stack():
-        for (W, wr, packed) in layers:
+        for packed in packed_list:
             moe.moe_route_forward(plan, packed, xd, lgd, idd, wd, yd)
 
+    n_layers = len(packed_list)
     decode_stack()
     torch.cuda.synchronize()
     counts = moe.moe_debug_tap(plan, moe.TAP_COUNTS)
@@ -232,19 +233,42 @@ def measure_decode(moe, plan, layers, peaks, H, E, k, I, steps, stream):
     st, calls = moe.moe_profile_read(plan, 1)
     moe.moe_profile_enable(plan, False)
     dstage_us = [v * 1e3 / max(calls, 1) for v in st][:3]
-    bpe = synth.weight_bytes_per_expert(H, I)
-    uniq_bytes = (U + 1) * bpe
+    uniq_bytes = (U + 1) * bytes_per_expert
     hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
     dec_gbs = uniq_bytes / (us_layer * 1e-6) / 1e9
     kern_us = dstage_us[1] + dstage_us[2]
 
-    return {"workload": "C=8 rows, T=8, Zipf(1.1) routing, outliers, through the stack's 40 layers' weights",
+    return {"workload": f"C=8 rows, T=8, Zipf(1.1) routing, outliers, through the {what}",
             "us_per_layer": us_layer, "unique_experts": U,
             "unique_bytes_per_layer": uniq_bytes, "achieved_gbs": dec_gbs,
             "hbm_peak_gbs": hbm, "frac": dec_gbs / hbm,
             "stage_us": {"route_dedup_quant": dstage_us[0], "gate_up_stream_requant": dstage_us[1],
                          "down_stream_into_y": dstage_us[2]},
             "kernel_gbs": uniq_bytes / (kern_us * 1e-6) / 1e9 if kern_us > 0 else None}
+
+
+def measure_decode_nvfp4(moe, plan, wl, n_layers, peaks, steps, stream):
+    """The C=8 decode measurement with NVFP4 expert weights (one NVFP4 weight set per layer,
+    the same shapes): microseconds per layer and the HBM roofline of the unique experts'
+    NVFP4 bytes (codes + block scales)."""
+    sh = wl.shape
+    dev = torch.device("cuda")
+    Ws, packed = [], []
+    for l in range(n_layers):
+        W4 = synth.make_weights_nvfp4(sh, synth.layer_seed(wl, l), device=dev)
+        Ws.append(W4)
+        packed.append(moe.moe_pack_weights_nvfp4(plan, W4))
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(plan) == 0
+    try:
+        return measure_decode(moe, plan, packed, peaks, sh.H, sh.E, sh.k,
+                              synth.weight_bytes_per_expert_nvfp4(sh.H, sh.I), steps, stream,
+                              what=f"NVFP4 weights of {n_layers} layers")
+    finally:
+        for pk in packed:
+            moe.moe_packed_destroy(pk)
+        del Ws
+        torch.cuda.empty_cache()
 
 
 def measure_crossover(moe, plan, layers, H, E, k, steps, stream,
@@ -488,7 +512,8 @@ def run_ours(args, world, rank):
                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2}
 
     decode = None if args.no_decode else measure_decode(
-        moe, plan, layers, peaks, H, E, k, sh.I, args.steps, stream)
+        moe, plan, [pk for (_, _, pk) in layers], peaks, H, E, k,
+        synth.weight_bytes_per_expert(H, sh.I), args.steps, stream)
 
     # ---- oracle CPU baseline (bounded sample, rank 0 only, N=1 only)
     cpu = None
@@ -505,6 +530,9 @@ def run_ours(args, world, rank):
         extra["prefill_chunk_T256"] = measure_layer(moe, "prefill", peaks, args.steps)
         extra["stress_T8192"] = measure_layer(moe, "stress", peaks, args.steps)
         extra["decode_crossover"] = measure_crossover(moe, plan, layers, H, E, k, args.steps, stream)
+        if not args.no_decode:
+            extra["decode_nvfp4"] = measure_decode_nvfp4(moe, plan, wl, n_layers, peaks, args.steps,
+                                                         stream)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         extra["cpu_baseline_1core"] = oracle_one_core(["tiny", "decode", "prefill"],
                                                       {"prefill": args.cpu_tokens_1core})

@@ -24,6 +24,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_OOM = 0, 1, 2, 3
 MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE, MOE_ERR_NO_DEVICE = 4, 5, 6, 7, 8
 
 TAP_COUNTS, TAP_OFFSETS, TAP_PERM, TAP_QX, TAP_SX, TAP_ACC_GU, TAP_HQ, TAP_SH, TAP_ACC_D = range(9)
+TAP_ACC_GU_F64, TAP_ACC_D_F64 = 9, 10  # NVFP4 weights: fp64 accumulators
 
 
 class MoeError(RuntimeError):
@@ -36,6 +37,12 @@ class Weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in (
         "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down",
         "sh_gate", "sh_up", "sh_down", "sh_s_gate", "sh_s_up", "sh_s_down")]
+
+
+class WeightsNvfp4(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in (
+        "w_gate", "w_up", "w_down", "b_gate", "b_up", "b_down", "g_gate", "g_up", "g_down",
+        "sh_gate", "sh_up", "sh_down", "sh_b_gate", "sh_b_up", "sh_b_down", "sh_g")]
 
 
 _lib = None
@@ -55,6 +62,7 @@ def lib() -> C.CDLL:
             "moe_plan_destroy": ([vp], i32),
             "moe_plan_set_decode_rows": ([vp, i32], i32),
             "moe_pack_weights": ([vp, C.POINTER(Weights), vp, C.POINTER(vp)], i32),
+            "moe_pack_weights_nvfp4": ([vp, C.POINTER(WeightsNvfp4), vp, C.POINTER(vp)], i32),
             "moe_packed_destroy": ([vp], i32),
             "moe_route": ([vp, vp, i32, vp, vp, vp], i32),
             "moe_forward": ([vp, vp, vp, i32, vp, vp, vp, vp], i32),
@@ -151,6 +159,16 @@ def moe_pack_weights(plan: int, W: dict, stream=None) -> int:
     return h.value
 
 
+def moe_pack_weights_nvfp4(plan: int, W: dict, stream=None) -> int:
+    """Register NVFP4 expert weights (uint8 codes and E4M3 block scales, fp32 matrix scales;
+    the keys of moe_weights_nvfp4). The tensors are read in place: keep them alive."""
+    h = C.c_void_p()
+    ws = WeightsNvfp4(*[_ptr(W.get(n)) for n, _ in WeightsNvfp4._fields_])
+    _check(lib().moe_pack_weights_nvfp4(plan, C.byref(ws), _stream(stream), C.byref(h)),
+           "moe_pack_weights_nvfp4")
+    return h.value
+
+
 def moe_packed_destroy(packed: int):
     _check(lib().moe_packed_destroy(packed), "moe_packed_destroy")
 
@@ -196,7 +214,8 @@ def moe_debug_tap(plan: int, which: int):
     """Host copy (numpy) of one intermediate of the last moe_forward."""
     import numpy as np
     n = lib().moe_debug_tap_bytes(plan, which)
-    dt = {TAP_QX: np.int8, TAP_HQ: np.int8, TAP_SX: np.float32, TAP_SH: np.float32}.get(which, np.int32)
+    dt = {TAP_QX: np.int8, TAP_HQ: np.int8, TAP_SX: np.float32, TAP_SH: np.float32,
+          TAP_ACC_GU_F64: np.float64, TAP_ACC_D_F64: np.float64}.get(which, np.int32)
     out = np.zeros(n // np.dtype(dt).itemsize, dt)
     _check(lib().moe_debug_tap(plan, which, out.ctypes.data, n), "moe_debug_tap")
     return out
@@ -255,13 +274,16 @@ def moe_rmsnorm_residual(x, y, x_in, stream=None):
 # ---- convenience wrapper ---------------------------------------------------------------
 
 class MoELayer:
-    """One plan plus one packed weight set; keeps the caller's weight tensors alive."""
+    """One plan plus one packed weight set; keeps the caller's weight tensors alive. The
+    weight format follows the dict's keys: NVFP4 when it holds block scales (b_gate)."""
 
     def __init__(self, E, top_k, H, I, I_shared, max_tokens, weights: dict, stream=None):
         self.E, self.k, self.H, self.I, self.Is = E, top_k, H, I, I_shared
         self.plan = moe_plan(E, top_k, H, I, I_shared, max_tokens)
         self.weights = weights
-        self.packed = moe_pack_weights(self.plan, weights, stream)
+        self.nvfp4 = "b_gate" in weights
+        pack = moe_pack_weights_nvfp4 if self.nvfp4 else moe_pack_weights
+        self.packed = pack(self.plan, weights, stream)
 
     def route(self, logits, stream=None):
         T = logits.shape[0]

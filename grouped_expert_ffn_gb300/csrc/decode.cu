@@ -20,6 +20,8 @@
 //  decode_down_kernel  (64 output channels of one unique expert) per block: stages up to 8 of
 //                      the expert's h code rows as int8 in shared memory per pass, streams 64
 //                      down rows, dp4a, and adds w * d into y.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,14 +43,15 @@ __device__ __forceinline__ int dot16(int4 a, int4 b, int c) {
 }
 
 // v[i] summed over the warp; afterwards lane L holds the total of index L in v[0].
-__device__ __forceinline__ void transpose_reduce32(int (&v)[32], int lane) {
+template <typename V>
+__device__ __forceinline__ void transpose_reduce32(V (&v)[32], int lane) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < o; ++i) {
-      const int send = up ? v[i] : v[i + o];
-      const int keep = up ? v[i + o] : v[i];
+      const V send = up ? v[i] : v[i + o];
+      const V keep = up ? v[i + o] : v[i];
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
@@ -339,6 +342,244 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
   }
 }
 
+// ---- NVFP4 experts ---------------------------------------------------------------------
+// The same two streaming kernels for weights stored as E2M1 codes (two per byte, element 2j
+// in the low nibble) with one E4M3 scale per 16-element block and a matrix scale. Each lane
+// takes one block per step: 8 code bytes and 1 scale byte per weight row. The codes are
+// expanded in registers to int8 values 2 * e2m1 (integers in [-12, 12]) and dotted with the
+// int8 activation codes by dp4a: the block sum A is an exact int32 (|A| <= 16 * 127 * 12).
+// The block scale is an integer S in units of 2^-9 (below 2^18), so A * S is the block's
+// exact contribution in units of 2^-10 and the row sum is an exact int64. float(acc) is then
+// the round-to-nearest-even of the exact sum, as the layer definition takes it.
+
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+  uint2 v;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u8(const void* p) {
+  uint16_t v;
+  asm("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// Four E2M1 codes (the low 16 bits of c, code i in bits 4i..4i+3) -> four int8 values
+// 2 * e2m1(code), value i in byte i. Magnitudes come from a byte lookup (prmt) into
+// {0, 1, 2, 3, 4, 6, 8, 12} and its negation; the sign bits, replicated over their bytes by
+// prmt's sign mode, pick between the two.
+__device__ __forceinline__ uint32_t e2m1x4_to_s8(uint32_t c) {
+  const uint32_t sel = c & 0x7777u;
+  uint32_t pos, neg, sgn;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(pos) : "r"(0x03020100u), "r"(0x0C080604u), "r"(sel));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(neg) : "r"(0xFDFEFF00u), "r"(0xF4F8FAFCu), "r"(sel));
+  // output byte i replicates the top bit of: byte 0 of c << 4 (code 0's sign), byte 0 of c
+  // (code 1), byte 1 of c << 4 (code 2), byte 1 of c (code 3)
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sgn) : "r"(c << 4), "r"(c), "r"(0xD9C8u));
+  return (pos & ~sgn) | (neg & sgn);
+}
+
+// 16 E2M1 codes (8 bytes) -> 16 int8 values 2 * e2m1, as the int4 dot16 takes.
+__device__ __forceinline__ int4 e2m1x16_to_s8(uint2 w) {
+  return make_int4((int)e2m1x4_to_s8(w.x), (int)e2m1x4_to_s8(w.x >> 16),
+                   (int)e2m1x4_to_s8(w.y), (int)e2m1x4_to_s8(w.y >> 16));
+}
+
+// A finite non-negative E4M3 byte -> its value in units of 2^-9: (8 + f) << (e - 1) for a
+// normal value (exponent field e > 0, mantissa f), f for a subnormal one.
+__device__ __forceinline__ int e4m3_units(uint32_t b) {
+  const int e = (int)((b >> 3) & 15u), f = (int)(b & 7u);
+  return e ? (8 | f) << (e - 1) : f;
+}
+
+// acc + a * b with a 64-bit accumulator, one instruction.
+__device__ __forceinline__ long long mad_wide(int a, int b, long long acc) {
+  long long d;
+  asm("mad.wide.s32 %0, %1, %2, %3;" : "=l"(d) : "r"(a), "r"(b), "l"(acc));
+  return d;
+}
+
+// float(exact sum) of an accumulator in units of 2^-10 (a power-of-two scaling: exact).
+__device__ __forceinline__ float fp4_acc_float(long long acc) {
+  return __fmul_rn(__ll2float_rn(acc), 0x1p-10f);
+}
+
+constexpr int kGuFp4ChannelsPerBlock = 16;  // 8 warps x 2 channels (4 weight rows)
+constexpr int kDownFp4RowsPerBlock = 32;    // 8 warps x 4 output rows
+
+__global__ void __launch_bounds__(256, 2) decode_gu_fp4_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) int8_t xs[];  // [kChunk][H] token codes of one pass
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
+  const int g = blockIdx.y;
+  if (g >= *a.n_groups) return;
+  const int4 grp = a.groups[g];
+  const bool shared = grp.x == a.E;
+  const int Ig = shared ? a.Is : a.I;
+  const int c0 = blockIdx.x * kGuFp4ChannelsPerBlock;
+  if (c0 >= Ig) return;
+  const int H = a.H, nr = grp.z, row0 = grp.y;
+  const size_t cb = H / 2, sb = H / 16;  // code and scale bytes per weight row
+  const uint8_t* Wg = shared ? a.f.sh_gate : a.f.w_gate + (size_t)grp.x * a.I * cb;
+  const uint8_t* Wu = shared ? a.f.sh_up : a.f.w_up + (size_t)grp.x * a.I * cb;
+  const uint8_t* Bg = shared ? a.f.sh_b_gate : a.f.b_gate + (size_t)grp.x * a.I * sb;
+  const uint8_t* Bu = shared ? a.f.sh_b_up : a.f.b_up + (size_t)grp.x * a.I * sb;
+  // matrix scales: sh_g exists only with a shared expert, so the pointer is chosen first
+  const float gg = *(shared ? a.f.sh_g : a.f.g_gate + grp.x);
+  const float gu = *(shared ? a.f.sh_g + 1 : a.f.g_up + grp.x);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int c = c0 + 2 * warp;
+  // rows {gate c, up c, gate c + 1, up c + 1}
+  const uint8_t* rows[4] = {Wg + c * cb, Wu + c * cb, Wg + (c + 1) * cb, Wu + (c + 1) * cb};
+  const uint8_t* srows[4] = {Bg + c * sb, Bu + c * sb, Bg + (c + 1) * sb, Bu + (c + 1) * sb};
+  for (int n0 = 0; n0 < nr; n0 += kChunk) {
+    const int nc = min(kChunk, nr - n0);
+    if (n0 > 0) __syncthreads();  // the previous pass no longer reads xs
+    for (int i = threadIdx.x; i < nc * H / 16; i += blockDim.x) {
+      const int n = i / (H / 16), u = i % (H / 16);
+      const int tok = a.row_token[row0 + n0 + n];
+      reinterpret_cast<int4*>(xs + (size_t)n * H)[u] =
+          reinterpret_cast<const int4*>(a.qtok + (size_t)tok * H)[u];
+    }
+    __syncthreads();
+    long long acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0;
+#pragma unroll 2
+    for (int u = lane; u < H / 16; u += 32) {  // block u of every row
+      uint2 wv[4];
+      uint32_t bv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        wv[r] = ld_stream8(rows[r] + (size_t)u * 8);
+        bv[r] = ld_stream_u8(srows[r] + u);
+      }
+      int4 wx[4];
+      int S[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        wx[r] = e2m1x16_to_s8(wv[r]);
+        S[r] = e4m3_units(bv[r]);
+      }
+#pragma unroll
+      for (int n = 0; n < kChunk; ++n) {
+        if (n < nc) {
+          const int4 xv = *reinterpret_cast<const int4*>(xs + (size_t)n * H + u * 16);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[r * 8 + n] = mad_wide(dot16(wx[r], xv, 0), S[r], acc[r * 8 + n]);
+        }
+      }
+    }
+    transpose_reduce32(acc, lane);
+    const long long mine = acc[0];
+    const long long other = __shfl_down_sync(0xffffffffu, mine, 8);
+    const int r = lane >> 3, n = lane & 7;
+    if ((r & 1) == 0 && n < nc) {
+      const int ch = c + (r >> 1);
+      const int row = row0 + n0 + n;
+      const float sx = a.stok[a.row_token[row]];
+      a.h32[(size_t)row * a.Imax + ch] =
+          silu_mul(dequant_f(fp4_acc_float(mine), sx, gg), dequant_f(fp4_acc_float(other), sx, gu));
+      if (a.tap_gu_f64) {
+        a.tap_gu_f64[(size_t)row * 2 * a.Imax + ch] = (double)mine * 0x1p-10;
+        a.tap_gu_f64[(size_t)row * 2 * a.Imax + a.Imax + ch] = (double)other * 0x1p-10;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256, 2) decode_down_fp4_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) int8_t hs[];  // [kChunk][Imax] h codes of one pass
+  __shared__ float shs[kChunk];
+  pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
+  pdl_trigger();
+  const int g = blockIdx.y;
+  if (g >= *a.n_groups) return;
+  const int4 grp = a.groups[g];
+  const bool shared = grp.x == a.E;
+  const int Ig = shared ? a.Is : a.I;
+  const int H = a.H, nr = grp.z, row0 = grp.y, Imax = a.Imax;
+  const int o0 = blockIdx.x * kDownFp4RowsPerBlock;
+  const size_t cb = Ig / 2, sb = Ig / 16;
+  const uint8_t* Wd = shared ? a.f.sh_down : a.f.w_down + (size_t)grp.x * H * cb;
+  const uint8_t* Bd = shared ? a.f.sh_b_down : a.f.b_down + (size_t)grp.x * H * sb;
+  const float gd = *(shared ? a.f.sh_g + 2 : a.f.g_down + grp.x);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int ob = o0 + warp * 4;
+  for (int n0 = 0; n0 < nr; n0 += kChunk) {
+    const int nc = min(kChunk, nr - n0);
+    if (n0 > 0) __syncthreads();  // the previous pass no longer reads hs and shs
+    // up to kChunk of this expert's h code rows (fp16 integers) -> int8
+    for (int i = threadIdx.x; i < nc * (Ig / 8); i += blockDim.x) {
+      const int n = i / (Ig / 8), u = i % (Ig / 8);
+      const uint4 v = reinterpret_cast<const uint4*>(a.hq + (size_t)(row0 + n0 + n) * Imax)[u];
+      const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+      uint32_t q[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float2 f0 = __half22float2(h2[2 * j]), f1 = __half22float2(h2[2 * j + 1]);
+        q[j] = (uint32_t)(uint8_t)(int8_t)(int)f0.x | (uint32_t)(uint8_t)(int8_t)(int)f0.y << 8 |
+               (uint32_t)(uint8_t)(int8_t)(int)f1.x << 16 | (uint32_t)(uint8_t)(int8_t)(int)f1.y << 24;
+      }
+      *reinterpret_cast<uint2*>(hs + (size_t)n * Imax + u * 8) = make_uint2(q[0], q[1]);
+    }
+    if ((int)threadIdx.x < nc) shs[threadIdx.x] = a.sh[row0 + n0 + threadIdx.x];
+    __syncthreads();
+    long long acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0;
+#pragma unroll 1
+    for (int u = lane; u < Ig / 16; u += 32) {
+      uint2 wv[4];
+      uint32_t bv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        wv[r] = ld_stream8(Wd + (size_t)(ob + r) * cb + (size_t)u * 8);
+        bv[r] = ld_stream_u8(Bd + (size_t)(ob + r) * sb + u);
+      }
+      int4 wx[4];
+      int S[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        wx[r] = e2m1x16_to_s8(wv[r]);
+        S[r] = e4m3_units(bv[r]);
+      }
+#pragma unroll
+      for (int n = 0; n < kChunk; ++n) {
+        if (n < nc) {
+          const int4 xv = *reinterpret_cast<const int4*>(hs + (size_t)n * Imax + u * 16);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[r * 8 + n] = mad_wide(dot16(wx[r], xv, 0), S[r], acc[r * 8 + n]);
+        }
+      }
+    }
+    transpose_reduce32(acc, lane);
+    const int r = lane >> 3, n = lane & 7;
+    if (n < nc) {
+      const int o = ob + r;
+      const int row = row0 + n0 + n;
+      const float d = dequant_f(fp4_acc_float(acc[0]), shs[n], gd);
+      atomicAdd(a.y + (size_t)a.row_token[row] * H + o, __fmul_rn(a.row_w[row], d));
+      if (a.tap_d_f64) a.tap_d_f64[(size_t)row * H + o] = (double)acc[0] * 0x1p-10;
+    }
+  }
+}
+
+__global__ void check_e4m3_kernel(const uint8_t* __restrict__ b, size_t n, int* err) {
+  bool bad = false;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    bad |= b[i] >= 0x7f;  // negative, or the NaN encoding
+  if (__syncthreads_or(bad) && threadIdx.x == 0) set_error(err, kErrDevice);
+}
+
+cudaError_t launch_check_e4m3(const uint8_t* b, size_t n, int* err, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
+  check_e4m3_kernel<<<blocks, 256, 0, s>>>(b, n, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) {
   if (a.T < 1 || a.T > kDecodeMaxRows || a.k > 8 || a.E > 256) return cudaErrorInvalidValue;
   const int R = a.T * a.k + (a.has_shared ? a.T : 0);
@@ -347,17 +588,25 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) 
   if (ev) cudaEventRecord(ev[1], s);
   if (e != cudaSuccess) return e;
   const int gmax = min(a.E, a.T * a.k) + (a.has_shared ? 1 : 0);
-  const dim3 ggu((a.Imax + kGuChannelsPerBlock - 1) / kGuChannelsPerBlock, gmax);
-  if ((e = launch_pdl(decode_gu_kernel, ggu, dim3(256), (size_t)kChunk * a.H, s, a)) !=
-      cudaSuccess)
-    return e;
+  if (a.fp4) {
+    const dim3 ggu((a.Imax + kGuFp4ChannelsPerBlock - 1) / kGuFp4ChannelsPerBlock, gmax);
+    e = launch_pdl(decode_gu_fp4_kernel, ggu, dim3(256), (size_t)kChunk * a.H, s, a);
+  } else {
+    const dim3 ggu((a.Imax + kGuChannelsPerBlock - 1) / kGuChannelsPerBlock, gmax);
+    e = launch_pdl(decode_gu_kernel, ggu, dim3(256), (size_t)kChunk * a.H, s, a);
+  }
+  if (e != cudaSuccess) return e;
   // one requantisation of every h row (warp per row), instead of one per down block
   e = launch_requant(a.h32, R, a.has_shared ? a.T : 0, a.I, a.Is, a.Imax, a.hq, a.sh,
                      a.sq_scratch, s);
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[2], s);
-  const dim3 gd(a.H / kDownRowsPerBlock, gmax);
-  e = launch_pdl(decode_down_kernel, gd, dim3(256), (size_t)kChunk * a.Imax, s, a);
+  if (a.fp4)
+    e = launch_pdl(decode_down_fp4_kernel, dim3(a.H / kDownFp4RowsPerBlock, gmax), dim3(256),
+                   (size_t)kChunk * a.Imax, s, a);
+  else
+    e = launch_pdl(decode_down_kernel, dim3(a.H / kDownRowsPerBlock, gmax), dim3(256),
+                   (size_t)kChunk * a.Imax, s, a);
   if (ev) cudaEventRecord(ev[3], s);
   return e;
 }
@@ -370,6 +619,12 @@ bool decode_shape_supported(int H, int Imax) { return H <= kDecodeMaxH && Imax <
 cudaError_t decode_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(decode_gu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kChunk * kDecodeMaxH);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_gu_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kChunk * kDecodeMaxH);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_down_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kChunk * kDecodeMaxI);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kChunk * kDecodeMaxI);

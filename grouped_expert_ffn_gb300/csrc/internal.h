@@ -117,6 +117,26 @@ struct PrepArgs {
 };
 cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s);
 
+// One layer's NVFP4 expert weights (the caller's arrays; see moe_weights_nvfp4).
+struct Fp4Weights {
+  const uint8_t* w_gate = nullptr;   // [E, I, H/2] E2M1 codes, element 2j in the low nibble
+  const uint8_t* w_up = nullptr;
+  const uint8_t* w_down = nullptr;   // [E, H, I/2]
+  const uint8_t* b_gate = nullptr;   // [E, I, H/16] E4M3 block scales
+  const uint8_t* b_up = nullptr;
+  const uint8_t* b_down = nullptr;   // [E, H, I/16]
+  const float* g_gate = nullptr;     // [E] matrix scales
+  const float* g_up = nullptr;
+  const float* g_down = nullptr;
+  const uint8_t* sh_gate = nullptr;  // [Is, H/2]
+  const uint8_t* sh_up = nullptr;
+  const uint8_t* sh_down = nullptr;  // [H, Is/2]
+  const uint8_t* sh_b_gate = nullptr;
+  const uint8_t* sh_b_up = nullptr;
+  const uint8_t* sh_b_down = nullptr;
+  const float* sh_g = nullptr;       // [3] gate, up, down
+};
+
 struct DecodeArgs {
   const int32_t* idx;
   const float* w;
@@ -154,10 +174,19 @@ struct DecodeArgs {
   int32_t* tap_gu;   // NULL = off
   int32_t* tap_d;
   int* err;
+  // NVFP4 experts (fp4 != 0): the weights above are unused, these are read instead, and the
+  // accumulator taps are fp64 (exact sums of q * e2m1 * e4m3)
+  int fp4 = 0;
+  Fp4Weights f;
+  double* tap_gu_f64 = nullptr;
+  double* tap_d_f64 = nullptr;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev);
 cudaError_t decode_set_attributes();
 bool decode_shape_supported(int H, int Imax);  // shapes the streaming kernels take
+
+// Sets *err to MOE_ERR_DEVICE when one of the n bytes is not a finite non-negative E4M3 value.
+cudaError_t launch_check_e4m3(const uint8_t* b, size_t n, int* err, cudaStream_t s);
 
 // weight packing and the stacked-prefill helpers
 cudaError_t launch_pack_gu8(const int8_t* gate, const int8_t* up, int n_mats, int I, int H,

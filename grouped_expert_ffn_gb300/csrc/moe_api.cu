@@ -64,6 +64,8 @@ struct moe_plan_s {
 
 struct moe_packed_s {
   moe_plan_s* plan = nullptr;
+  int fp4 = 0;     // NVFP4 weights (f) instead of int8 (w)
+  Fp4Weights f;
   moe_weights w;
   int8_t* gu8 = nullptr;    // [E, 2I, H] gate/up rows interleaved in pairs
   int8_t* shgu8 = nullptr;  // [2Is, H]
@@ -199,6 +201,8 @@ size_t tap_bytes(const moe_plan_s* p, int which, int T) {
     case MOE_TAP_HQ: return R * p->Imax;
     case MOE_TAP_SH: return R * 4;
     case MOE_TAP_ACC_D: return R * p->H * 4;
+    case MOE_TAP_ACC_GU_F64: return R * 2 * p->Imax * 8;
+    case MOE_TAP_ACC_D_F64: return R * p->H * 8;
     default: return 0;
   }
 }
@@ -418,6 +422,63 @@ moe_status moe_pack_weights(moe_plan_t p, const moe_weights* w, void* stream, mo
   return MOE_OK;
 }
 
+moe_status moe_pack_weights_nvfp4(moe_plan_t p, const moe_weights_nvfp4* w, void* stream,
+                                  moe_packed_t* out) {
+  if (!p || !w || !out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  const void* need[] = {w->w_gate, w->w_up, w->w_down, w->b_gate, w->b_up,
+                        w->b_down, w->g_gate, w->g_up, w->g_down};
+  for (const void* q : need)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (p->has_shared) {
+    const void* nsh[] = {w->sh_gate, w->sh_up, w->sh_down, w->sh_b_gate, w->sh_b_up, w->sh_b_down, w->sh_g};
+    for (const void* q : nsh)
+      if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  }
+  if (p->H % 16 || p->I % 16 || p->Is % 16) return MOE_ERR_UNSUPPORTED;
+  moe_packed_s* pk = new (std::nothrow) moe_packed_s();
+  if (!pk) return MOE_ERR_OOM;
+  pk->plan = p;
+  pk->fp4 = 1;
+  std::memset(&pk->w, 0, sizeof(pk->w));
+  Fp4Weights& f = pk->f;
+  f.w_gate = w->w_gate;
+  f.w_up = w->w_up;
+  f.w_down = w->w_down;
+  f.b_gate = w->b_gate;
+  f.b_up = w->b_up;
+  f.b_down = w->b_down;
+  f.g_gate = w->g_gate;
+  f.g_up = w->g_up;
+  f.g_down = w->g_down;
+  if (p->has_shared) {
+    f.sh_gate = w->sh_gate;
+    f.sh_up = w->sh_up;
+    f.sh_down = w->sh_down;
+    f.sh_b_gate = w->sh_b_gate;
+    f.sh_b_up = w->sh_b_up;
+    f.sh_b_down = w->sh_b_down;
+    f.sh_g = w->sh_g;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t E = p->E, H = p->H, I = p->I, Is = p->Is;
+  cudaError_t e = launch_check_e4m3(f.b_gate, E * I * (H / 16), p->err, s);
+  if (e == cudaSuccess) e = launch_check_e4m3(f.b_up, E * I * (H / 16), p->err, s);
+  if (e == cudaSuccess) e = launch_check_e4m3(f.b_down, E * H * (I / 16), p->err, s);
+  if (e == cudaSuccess && p->has_shared) {
+    e = launch_check_e4m3(f.sh_b_gate, Is * (H / 16), p->err, s);
+    if (e == cudaSuccess) e = launch_check_e4m3(f.sh_b_up, Is * (H / 16), p->err, s);
+    if (e == cudaSuccess) e = launch_check_e4m3(f.sh_b_down, H * (Is / 16), p->err, s);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete pk;
+    return MOE_ERR_CUDA;
+  }
+  *out = pk;
+  return MOE_OK;
+}
+
 moe_status moe_packed_destroy(moe_packed_t pk) {
   if (!pk) return MOE_ERR_INVALID_ARG;
   if (pk->gu8) cudaFree(pk->gu8);
@@ -450,9 +511,12 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int T_sh = p->has_shared ? T : 0;
   const int R = T * p->k + T_sh;
-  p->last_T = T;
   cudaError_t e;
-  if (T <= p->decode_rows && decode_shape_supported(p->H, p->Imax)) {
+  const bool stream_path = decode_shape_supported(p->H, p->Imax) &&
+                           T <= (pk->fp4 ? kDecodeMaxRows : p->decode_rows);
+  if (pk->fp4 && !stream_path) return MOE_ERR_UNSUPPORTED;  // NVFP4: streaming kernels only
+  p->last_T = T;
+  if (stream_path) {
     DecodeArgs a;
     a.idx = idx;
     a.w = w;
@@ -498,6 +562,14 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
     a.tap_gu = p->debug ? p->tap_gu : nullptr;
     a.tap_d = p->debug ? p->tap_d : nullptr;
     a.err = p->err;
+    if (pk->fp4) {
+      a.fp4 = 1;
+      a.f = pk->f;
+      a.tap_gu = nullptr;
+      a.tap_d = nullptr;
+      a.tap_gu_f64 = p->debug ? reinterpret_cast<double*>(p->tap_gu) : nullptr;
+      a.tap_d_f64 = p->debug ? reinterpret_cast<double*>(p->tap_d) : nullptr;
+    }
     e = launch_decode(a, s, prof_events(p, 1));
     return cuda_status(e);
   }
@@ -658,8 +730,9 @@ moe_status moe_selftest_wait_timeout(moe_plan_t p, void* stream) {
 moe_status moe_debug_enable(moe_plan_t p, int on) {
   if (!p) return MOE_ERR_INVALID_ARG;
   if (on && !p->tap_gu) {
-    if (cudaMalloc(&p->tap_gu, p->R_max * 2 * p->Imax * sizeof(int32_t)) != cudaSuccess ||
-        cudaMalloc(&p->tap_d, p->R_max * p->H * sizeof(int32_t)) != cudaSuccess) {
+    // 8 bytes per accumulator: int32 taps use the first half, fp64 (NVFP4) taps all of it
+    if (cudaMalloc(&p->tap_gu, p->R_max * 2 * p->Imax * sizeof(double)) != cudaSuccess ||
+        cudaMalloc(&p->tap_d, p->R_max * p->H * sizeof(double)) != cudaSuccess) {
       cudaGetLastError();
       if (p->tap_gu) cudaFree(p->tap_gu);
       p->tap_gu = nullptr;
@@ -679,7 +752,8 @@ moe_status moe_debug_tap(moe_plan_t p, int which, void* dst, size_t bytes) {
   if (!p || !dst || p->last_T < 1) return MOE_ERR_INVALID_ARG;
   const size_t need = tap_bytes(p, which, p->last_T);
   if (need == 0 || bytes != need) return MOE_ERR_INVALID_ARG;
-  if ((which == MOE_TAP_ACC_GU || which == MOE_TAP_ACC_D) && !p->tap_gu)
+  if ((which == MOE_TAP_ACC_GU || which == MOE_TAP_ACC_D || which == MOE_TAP_ACC_GU_F64 ||
+       which == MOE_TAP_ACC_D_F64) && !p->tap_gu)
     return MOE_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   const void* src = nullptr;
@@ -692,6 +766,8 @@ moe_status moe_debug_tap(moe_plan_t p, int which, void* dst, size_t bytes) {
     case MOE_TAP_ACC_GU: src = p->tap_gu; break;
     case MOE_TAP_SH: src = p->sh; break;
     case MOE_TAP_ACC_D: src = p->tap_d; break;
+    case MOE_TAP_ACC_GU_F64: src = p->tap_gu; break;
+    case MOE_TAP_ACC_D_F64: src = p->tap_d; break;
     case MOE_TAP_HQ: {
       const size_t n = need;
       std::vector<__half> tmp(n);

@@ -79,6 +79,41 @@ typedef struct {
   const float* sh_s_down;
 } moe_weights;
 
+/* One layer's NVFP4 expert weights (device pointers, caller-owned): the format the page
+ * "[job] Strix Halo: multi-session serving (parallel or sequential) and long context,
+ * Flash-Next and the 27B #145" keeps for the routed experts (comment of Oct 19, "FP4 dtype
+ * survey on the AMD track"). Every weight row (reduction dimension contiguous) is stored as
+ * 4-bit E2M1 codes (OCP Microscaling Formats v1.0, FP4: sign, 2 exponent bits with bias 1, 1
+ * mantissa bit), two per byte with element 2j in the low nibble, plus one E4M3 block scale
+ * byte (finite, non-negative) per 16 consecutive elements, plus one fp32 scale per matrix:
+ *   dequantised weight = e2m1(code) * e4m3(block scale) * matrix scale.
+ * Routed experts: w_gate, w_up uint8 [E, I, H/2]; w_down uint8 [E, H, I/2];
+ *                 b_gate, b_up uint8 [E, I, H/16]; b_down uint8 [E, H, I/16];
+ *                 g_gate, g_up, g_down fp32 [E].
+ * Shared expert (only when the plan has I_shared > 0, else all NULL): sh_gate, sh_up
+ *                 [I_shared, H/2]; sh_down [H, I_shared/2]; sh_b_gate, sh_b_up
+ *                 [I_shared, H/16]; sh_b_down [H, I_shared/16]; sh_g fp32 [3] (gate, up,
+ *                 down matrix scales).
+ * The activations stay int8 per token, as in the int8 layer. */
+typedef struct {
+  const uint8_t* w_gate;
+  const uint8_t* w_up;
+  const uint8_t* w_down;
+  const uint8_t* b_gate;
+  const uint8_t* b_up;
+  const uint8_t* b_down;
+  const float* g_gate;
+  const float* g_up;
+  const float* g_down;
+  const uint8_t* sh_gate;
+  const uint8_t* sh_up;
+  const uint8_t* sh_down;
+  const uint8_t* sh_b_gate;
+  const uint8_t* sh_b_up;
+  const uint8_t* sh_b_down;
+  const float* sh_g;
+} moe_weights_nvfp4;
+
 /* Create a plan for one layer shape and allocate its workspace for up to max_tokens
  * tokens per call (the only allocation on the forward path's behalf). The plan is the
  * persistent per-layer-shape state that the page "Qwen3.6-35B-A3B Linux v1.0.4: ~2.7s fixed
@@ -105,6 +140,21 @@ MOE_API moe_status moe_plan_destroy(moe_plan_t plan);
 MOE_API moe_status moe_pack_weights(moe_plan_t plan, const moe_weights* w, void* stream,
                             moe_packed_t* out);
 MOE_API moe_status moe_packed_destroy(moe_packed_t packed);
+
+/* Register one layer's NVFP4 expert weights (moe_weights_nvfp4). Reads the caller's arrays in
+ * place: they must stay alive and unchanged while the handle is in use. Queues on `stream` a
+ * check of every block scale byte; a negative or NaN one sets the plan's sticky error word
+ * to MOE_ERR_DEVICE (read by moe_get_error). With the returned handle, moe_forward and
+ * moe_route_forward compute the same layer with these weights:
+ *   per weight row, acc = sum over elements of q * e2m1(code) * e4m3(block scale), the
+ *   EXACT sum (q = the int8 activation or h code); then g = (float(acc) * s_x) * g_gate,
+ *   u likewise, h = SiLU(g) * u requantised per row as in the int8 layer, and
+ *   d = (float(acc_d) * s_h) * g_down, combined as in the int8 layer (float() rounds to
+ *   nearest even).
+ * T <= 64 rows run the deduplicated weight-streaming kernels (exact int64 accumulators);
+ * larger T returns MOE_ERR_UNSUPPORTED. Pointers must be 16-byte aligned. */
+MOE_API moe_status moe_pack_weights_nvfp4(moe_plan_t plan, const moe_weights_nvfp4* w, void* stream,
+                                  moe_packed_t* out);
 
 /* Top-k softmax routing (warp per token): the "top-8" selection of routed experts per token
  * that the page "Qwen3.6-35B-A3B Linux v1.0.4 ..." (section "The fix (concatenated-expert
@@ -171,7 +221,7 @@ MOE_API const char* moe_status_string(moe_status s);
 
 /* ---- test taps: copies of intermediate results of the last moe_forward ----------------
  * moe_debug_enable(plan, 1) allocates tap buffers and makes later forwards also write the
- * int32 accumulators (it is the one call besides moe_plan/moe_pack_weights that allocates).
+ * accumulators (int32 with int8 weights, fp64 with NVFP4 weights) (it is the one call besides moe_plan/moe_pack_weights that allocates).
  * Rows are in the plan's row order: rows [0, T) are the shared expert's (row t = token t),
  * when I_shared > 0; then the routed assignments, grouped by expert id and, inside an
  * expert, by (token, slot) ascending. moe_debug_tap copies one tap to HOST memory
@@ -186,7 +236,9 @@ typedef enum {
   MOE_TAP_ACC_GU = 5,   /* int32 [R, 2*Imax]      gate accumulators, then up accumulators */
   MOE_TAP_HQ = 6,       /* int8  [R, Imax]        requantised SiLU(gate)*up               */
   MOE_TAP_SH = 7,       /* fp32  [R]              scales of HQ                            */
-  MOE_TAP_ACC_D = 8     /* int32 [R, H]           down accumulators                       */
+  MOE_TAP_ACC_D = 8,    /* int32 [R, H]           down accumulators                       */
+  MOE_TAP_ACC_GU_F64 = 9,  /* fp64 [R, 2*Imax]    NVFP4 weights: gate, then up accumulators */
+  MOE_TAP_ACC_D_F64 = 10   /* fp64 [R, H]         NVFP4 weights: down accumulators          */
 } moe_tap;              /* R = T*top_k + (I_shared > 0 ? T : 0); Imax = max(I, I_shared)   */
 
 MOE_API moe_status moe_debug_enable(moe_plan_t plan, int on);

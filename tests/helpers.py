@@ -46,9 +46,18 @@ def row_map(perm: np.ndarray, T: int, k: int, has_shared: bool):
     return rows
 
 
-def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L: oracle.Layer,
+def oracle_layer_nvfp4(W: dict, sh: synth.LayerShape) -> oracle.LayerNvfp4:
+    return oracle.LayerNvfp4({k: v.cpu() for k, v in W.items()}, sh.E, sh.k, sh.H, sh.I, sh.Is)
+
+
+def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L,
                 sample=None, layer: moe.MoELayer | None = None, plan_tokens=None):
-    """Full parity of one layer call. Returns a dict of statistics."""
+    """Full parity of one layer call. Returns a dict of statistics. L is the oracle's layer:
+    oracle.Layer (int8 weights) or oracle.LayerNvfp4 (NVFP4 weights; the accumulators are
+    then the fp64 taps, compared bit-exactly with the oracle's exact sums)."""
+    fp4 = isinstance(L, oracle.LayerNvfp4)
+    tap_gu, tap_d = (moe.TAP_ACC_GU_F64, moe.TAP_ACC_D_F64) if fp4 else (moe.TAP_ACC_GU, moe.TAP_ACC_D)
+    forward = oracle.forward_nvfp4 if fp4 else oracle.forward
     dev = torch.device("cuda")
     T, k, E, H = sh.T, sh.k, sh.E, sh.H
     own = layer is None
@@ -68,8 +77,8 @@ def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L: oracle.
         assert moe.moe_get_error(layer.plan) == 0
         tap = {n: moe.moe_debug_tap(layer.plan, i) for n, i in (
             ("counts", moe.TAP_COUNTS), ("offsets", moe.TAP_OFFSETS), ("perm", moe.TAP_PERM),
-            ("qx", moe.TAP_QX), ("sx", moe.TAP_SX), ("acc_gu", moe.TAP_ACC_GU), ("hq", moe.TAP_HQ),
-            ("sh", moe.TAP_SH), ("acc_d", moe.TAP_ACC_D))}
+            ("qx", moe.TAP_QX), ("sx", moe.TAP_SX), ("acc_gu", tap_gu), ("hq", moe.TAP_HQ),
+            ("sh", moe.TAP_SH), ("acc_d", tap_d))}
         counts, offsets, perm = oracle.permute(idx_o, E)
         assert (tap["counts"] == counts).all()
         assert (tap["offsets"] == offsets).all()
@@ -79,7 +88,7 @@ def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L: oracle.
         assert (tap["sx"] == s_o).all()
 
         toks = np.arange(T) if sample is None else np.asarray(sample)
-        y_o, tp = oracle.forward(L, x_cpu[torch.from_numpy(toks)], idx_o[toks], w_o[toks], taps=True)
+        y_o, tp = forward(L, x_cpu[torch.from_numpy(toks)], idx_o[toks], w_o[toks], taps=True)
         has_sh = sh.Is > 0
         Imax = max(sh.I, sh.Is)
         R = T * k + (T if has_sh else 0)

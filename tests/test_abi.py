@@ -65,6 +65,7 @@ def test_null_handles_rejected(lib):
     assert lib.moe_plan_destroy(None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_plan_set_decode_rows(None, 8) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_packed_destroy(None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_weights_nvfp4(None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_get_error(None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_debug_tap_bytes(None, 0) == 0
     assert lib.moe_router_logits(None, None, 4, 64, 8, None, None) == moe.MOE_ERR_INVALID_ARG

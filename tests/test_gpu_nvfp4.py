@@ -1,0 +1,138 @@
+"""GPU parity of the layer with NVFP4 expert weights (E2M1 codes, E4M3 block scales per 16
+elements, fp32 matrix scales) against the CPU oracle's NVFP4 layer.
+
+The weight-streaming kernels accumulate every row exactly (int64 in units of 2^-10), so the
+fp64 accumulator taps must equal the oracle's exact sums bit for bit; the routing,
+permutation and activation codes are bit-identical; requantised h codes may differ by one
+at a rounding tie of exp (at most 1e-3 of them), and y is held to the int8 layer's
+tolerances (max|dy| <= 1e-2 max|y_ref|, rms(dy) <= 5e-3 rms(y_ref))."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import grouped_expert_ffn_gb300 as moe
+from helpers import check_layer, oracle_layer_nvfp4, weights_to
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    moe.lib()
+
+
+def _layer(T, H, E, k, I, Is, seed, zipf_s=1.1, outliers=8):
+    sh = synth.LayerShape(T=T, H=H, E=E, k=k, I=I, Is=Is)
+    d = synth.small_layer(T, H, E, k, I, Is, seed=seed, zipf_s=zipf_s, outliers=outliers)
+    W = synth.make_weights_nvfp4(sh, seed)
+    return sh, d, W
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 9, 24, 64])
+def test_nvfp4_decode_matches_the_oracle(T):
+    # the 35B-A3B-shaped layer (H=2048, E=128, k=8, I=512, shared expert 512) with NVFP4
+    # experts; above 8 rows an expert's rows take several passes
+    sh, d, W = _layer(T, 2048, 128, 8, 512, 512, seed=90 + T)
+    st = check_layer(sh, d["x"], d["logits"], weights_to(W, "cuda"), oracle_layer_nvfp4(W, sh))
+    if T > 8:
+        assert st["tap"]["counts"].max() > 8 or T < 24
+
+
+def _random_bytes_weights(rng, E, H, I, Is):
+    """Codes over every byte value, block scales over every finite non-negative E4M3 byte
+    (zero, subnormals, 448) with whole zero-scale rows, matrix scales around 1e-3."""
+    def codes(*s):
+        return torch.from_numpy(rng.integers(0, 256, s).astype(np.uint8))
+
+    def scales(*s):
+        b = rng.integers(0, 127, s).astype(np.uint8)
+        b.reshape(-1, s[-1])[::7] = 0  # every 7th row: all blocks zero
+        return torch.from_numpy(b)
+
+    def gs(*s):
+        return torch.from_numpy(rng.uniform(5e-4, 2e-3, s).astype(np.float32))
+
+    W = dict(w_gate=codes(E, I, H // 2), w_up=codes(E, I, H // 2), w_down=codes(E, H, I // 2),
+             b_gate=scales(E, I, H // 16), b_up=scales(E, I, H // 16), b_down=scales(E, H, I // 16),
+             g_gate=gs(E), g_up=gs(E), g_down=gs(E))
+    if Is:
+        W.update(sh_gate=codes(Is, H // 2), sh_up=codes(Is, H // 2), sh_down=codes(H, Is // 2),
+                 sh_b_gate=scales(Is, H // 16), sh_b_up=scales(Is, H // 16),
+                 sh_b_down=scales(H, Is // 16), sh_g=gs(3))
+    return W
+
+
+@pytest.mark.parametrize("T", [2, 8, 20])
+def test_nvfp4_every_code_and_scale_byte(T):
+    # full-range codes and block scales (subnormal and largest scales, zero blocks): the exact
+    # int64 accumulation has no headroom problem and every decode rule is exercised
+    H, E, k, I, Is = 512, 16, 4, 256, 128
+    sh = synth.LayerShape(T=T, H=H, E=E, k=k, I=I, Is=Is)
+    d = synth.small_layer(T, H, E, k, I, Is, seed=300 + T)
+    W = _random_bytes_weights(np.random.default_rng(T), E, H, I, Is)
+    check_layer(sh, d["x"], d["logits"], weights_to(W, "cuda"), oracle_layer_nvfp4(W, sh))
+
+
+def test_nvfp4_largest_supported_shape():
+    # H = 8192, I = I_shared = 4096: the largest exact sums the kernels form (a gate row sums
+    # 8192 products); compared on every slot of 3 tokens
+    T, H, E, k, I, Is = 3, 8192, 16, 4, 4096, 4096
+    sh, d, W = _layer(T, H, E, k, I, Is, seed=310)
+    check_layer(sh, d["x"], d["logits"], weights_to(W, "cuda"), oracle_layer_nvfp4(W, sh))
+
+
+def test_nvfp4_route_forward_matches_route_then_forward():
+    T, H, E, k, I, Is = 8, 2048, 128, 8, 512, 512
+    sh, d, W = _layer(T, H, E, k, I, Is, seed=320)
+    Wd = weights_to(W, "cuda")
+    lay = moe.MoELayer(E, k, H, I, Is, T, Wd)
+    try:
+        x, lg = d["x"].cuda(), d["logits"].cuda()
+        idx, w = lay.route(lg)
+        y1 = lay.forward(x, idx, w)
+        idx2 = torch.empty_like(idx)
+        w2 = torch.empty_like(w)
+        y2 = torch.empty_like(y1)
+        moe.moe_route_forward(lay.plan, lay.packed, x, lg, idx2, w2, y2)
+        torch.cuda.synchronize()
+        assert moe.moe_get_error(lay.plan) == 0
+        assert torch.equal(idx, idx2) and torch.equal(w, w2)
+        assert (y1 - y2).abs().max().item() <= 1e-5 * y1.abs().max().item()
+    finally:
+        lay.close()
+
+
+@pytest.mark.parametrize("bad", [0x7F, 0x80, 0xFE])
+def test_nvfp4_bad_block_scale_sets_device_error(bad):
+    # a NaN or negative block scale is found by the check moe_pack_weights_nvfp4 queues
+    T, H, E, k, I = 4, 256, 8, 2, 128
+    sh, d, W = _layer(T, H, E, k, I, 0, seed=330)
+    W["b_down"][5, 17, 3] = bad
+    lay = moe.MoELayer(E, k, H, I, 0, T, weights_to(W, "cuda"))
+    try:
+        assert moe.moe_get_error(lay.plan) == moe.MOE_ERR_DEVICE
+        moe.moe_clear_error(lay.plan)
+        assert moe.moe_get_error(lay.plan) == 0
+    finally:
+        lay.close()
+
+
+def test_nvfp4_capacity_and_unsupported_sizes():
+    T, H, E, k, I, Is = 65, 256, 8, 2, 128, 64
+    sh, d, W = _layer(T, H, E, k, I, Is, seed=340)
+    lay = moe.MoELayer(E, k, H, I, Is, T, weights_to(W, "cuda"))
+    try:
+        x = d["x"].cuda()
+        idx, w = lay.route(d["logits"].cuda())
+        with pytest.raises(moe.MoeError) as ei:
+            lay.forward(x, idx, w)  # 65 rows: beyond the streaming kernels
+        assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+        y = lay.forward(x[:64].contiguous(), idx[:64].contiguous(), w[:64].contiguous())
+        torch.cuda.synchronize()
+        assert moe.moe_get_error(lay.plan) == 0 and torch.isfinite(y).all()
+    finally:
+        lay.close()
