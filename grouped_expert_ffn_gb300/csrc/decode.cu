@@ -21,6 +21,7 @@
 //                      the expert's h code rows as int8 in shared memory per pass, streams 64
 //                      down rows, dp4a, and adds w * d into y.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -344,13 +345,42 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
 
 // ---- NVFP4 experts ---------------------------------------------------------------------
 // The same two streaming kernels for weights stored as E2M1 codes (two per byte, element 2j
-// in the low nibble) with one E4M3 scale per 16-element block and a matrix scale. Each lane
-// takes one block per step: 8 code bytes and 1 scale byte per weight row. The codes are
-// expanded in registers to int8 values 2 * e2m1 (integers in [-12, 12]) and dotted with the
-// int8 activation codes by dp4a: the block sum A is an exact int32 (|A| <= 16 * 127 * 12).
-// The block scale is an integer S in units of 2^-9 (below 2^18), so A * S is the block's
-// exact contribution in units of 2^-10 and the row sum is an exact int64. float(acc) is then
-// the round-to-nearest-even of the exact sum, as the layer definition takes it.
+// in the low nibble) with one E4M3 scale per 16-element block and a matrix scale. The codes
+// are expanded in registers to int8 values 2 * e2m1 (integers in [-12, 12]) and dotted with
+// the int8 activation (or h) codes by dp4a: a block's sum A is an exact int32
+// (|A| <= 16 * 127 * 12). The block scale is an integer S in units of 2^-9 (below 2^18), so
+// A * S is the block's exact contribution in units of 2^-10 and a row's sum is an exact int64
+// (below 2^42 for 8192 elements). float(acc) is then the round-to-nearest-even of the exact
+// sum, as the layer definition takes it.
+//
+// Shapes of the work (compile-time): a warp takes ROWS weight rows and up to NT token rows
+// per pass; each lane step reads BPL consecutive 16-element blocks of every row (8 * BPL
+// code bytes and BPL scale bytes per row). The accumulators are int64, two registers each,
+// so ROWS * NT is what bounds the registers.
+#ifndef MOE_FP4_GU_ROWS
+#define MOE_FP4_GU_ROWS 2
+#endif
+#ifndef MOE_FP4_GU_NT
+#define MOE_FP4_GU_NT 8
+#endif
+#ifndef MOE_FP4_GU_BPL
+#define MOE_FP4_GU_BPL 2
+#endif
+#ifndef MOE_FP4_GU_MINB
+#define MOE_FP4_GU_MINB 3
+#endif
+#ifndef MOE_FP4_DN_ROWS
+#define MOE_FP4_DN_ROWS 4
+#endif
+#ifndef MOE_FP4_DN_NT
+#define MOE_FP4_DN_NT 4
+#endif
+#ifndef MOE_FP4_DN_BPL
+#define MOE_FP4_DN_BPL 1
+#endif
+#ifndef MOE_FP4_DN_MINB
+#define MOE_FP4_DN_MINB 3
+#endif
 
 __device__ __forceinline__ uint2 ld_stream8(const void* p) {
   uint2 v;
@@ -361,6 +391,12 @@ __device__ __forceinline__ uint2 ld_stream8(const void* p) {
 __device__ __forceinline__ uint32_t ld_stream_u8(const void* p) {
   uint16_t v;
   asm("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u16(const void* p) {
+  uint16_t v;
+  asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
 }
 
@@ -380,13 +416,14 @@ __device__ __forceinline__ uint32_t e2m1x4_to_s8(uint32_t c) {
 }
 
 // 16 E2M1 codes (8 bytes) -> 16 int8 values 2 * e2m1, as the int4 dot16 takes.
-__device__ __forceinline__ int4 e2m1x16_to_s8(uint2 w) {
-  return make_int4((int)e2m1x4_to_s8(w.x), (int)e2m1x4_to_s8(w.x >> 16),
-                   (int)e2m1x4_to_s8(w.y), (int)e2m1x4_to_s8(w.y >> 16));
+__device__ __forceinline__ int4 e2m1x16_to_s8(uint32_t lo, uint32_t hi) {
+  return make_int4((int)e2m1x4_to_s8(lo), (int)e2m1x4_to_s8(lo >> 16), (int)e2m1x4_to_s8(hi),
+                   (int)e2m1x4_to_s8(hi >> 16));
 }
 
-// A finite non-negative E4M3 byte -> its value in units of 2^-9: (8 + f) << (e - 1) for a
-// normal value (exponent field e > 0, mantissa f), f for a subnormal one.
+// A finite non-negative E4M3 byte (bits 0-7 of b; higher bits ignored) -> its value in units
+// of 2^-9: (8 + f) << (e - 1) for a normal value (exponent field e > 0, mantissa f), f for a
+// subnormal one.
 __device__ __forceinline__ int e4m3_units(uint32_t b) {
   const int e = (int)((b >> 3) & 15u), f = (int)(b & 7u);
   return e ? (8 | f) << (e - 1) : f;
@@ -404,11 +441,107 @@ __device__ __forceinline__ float fp4_acc_float(long long acc) {
   return __fmul_rn(__ll2float_rn(acc), 0x1p-10f);
 }
 
-constexpr int kGuFp4ChannelsPerBlock = 16;  // 8 warps x 2 channels (4 weight rows)
-constexpr int kDownFp4RowsPerBlock = 32;    // 8 warps x 4 output rows
+// v[i] summed over the warp (N = 8, 16 or 32 values per lane); afterwards lane L holds the
+// total of index L % N in v[0].
+template <int N, typename V>
+__device__ __forceinline__ void transpose_reduce(V (&v)[N], int lane) {
+  static_assert(N == 8 || N == 16 || N == 32, "values per lane");
+#pragma unroll
+  for (int o = N / 2; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const V send = up ? v[i] : v[i + o];
+      const V keep = up ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (int o = N; o < 32; o <<= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+}
 
-__global__ void __launch_bounds__(256, 2) decode_gu_fp4_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) int8_t xs[];  // [kChunk][H] token codes of one pass
+// Calls f(std::integral_constant<int, n>()) for the runtime count n in [C, NT], so that a loop
+// over n tokens is unrolled for exactly n (no predicated iterations for absent tokens).
+template <int C, int NT, class F>
+__device__ __forceinline__ void with_count(int n, F&& f) {
+  if constexpr (C <= NT) {
+    if (n == C)
+      f(std::integral_constant<int, C>());
+    else
+      with_count<C + 1, NT>(n, f);
+  }
+}
+
+// acc[r * NT + n] = exact sum over the K elements of weight row r times token row n (int8
+// codes at xs + n * xstride), for n < NC, this lane's share: lane steps u = lane, lane + 32,
+// ... each covering BPL blocks. Weight row r is row r / NB of NB interleaved matrices: codes
+// at cb[r % NB] + (r / NB) * K / 2, block scales at sb[r % NB] + (r / NB) * K / 16 (gate/up:
+// NB = 2, rows gate c, up c, gate c + 1, ...; down: NB = 1, consecutive rows).
+template <int ROWS, int NT, int BPL, int NB, int NC>
+__device__ __forceinline__ void fp4_dot_rows(const uint8_t* const (&cb)[NB],
+                                             const uint8_t* const (&sb)[NB], int K,
+                                             const int8_t* xs, int xstride, int lane,
+                                             long long (&acc)[ROWS * NT]) {
+  static_assert(NC >= 1 && NC <= NT, "token count");
+  static_assert(BPL == 1 || BPL == 2, "blocks per lane step");
+  const int cstride = K / 2, sstride = K / 16;
+#pragma unroll
+  for (int i = 0; i < ROWS * NT; ++i) acc[i] = 0;
+#pragma unroll 2
+  for (int u = lane; u < K / (16 * BPL); u += 32) {
+    uint32_t cw[ROWS][2 * BPL];
+    uint32_t sw[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      const uint8_t* cp = cb[r % NB] + (r / NB) * cstride;
+      const uint8_t* sp = sb[r % NB] + (r / NB) * sstride;
+      if constexpr (BPL == 1) {
+        const uint2 v = ld_stream8(cp + u * 8);
+        cw[r][0] = v.x;
+        cw[r][1] = v.y;
+        sw[r] = ld_stream_u8(sp + u);
+      } else {
+        const int4 v = ld_stream(cp + u * 16);
+        cw[r][0] = (uint32_t)v.x;
+        cw[r][1] = (uint32_t)v.y;
+        cw[r][2] = (uint32_t)v.z;
+        cw[r][3] = (uint32_t)v.w;
+        sw[r] = ld_stream_u16(sp + 2 * u);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < BPL; ++b) {
+      int4 wx[ROWS];
+      int S[ROWS];
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) {
+        wx[r] = e2m1x16_to_s8(cw[r][2 * b], cw[r][2 * b + 1]);
+        S[r] = e4m3_units(sw[r] >> (8 * b));
+      }
+#pragma unroll
+      for (int n = 0; n < NC; ++n) {
+        const int4 xv =
+            *reinterpret_cast<const int4*>(xs + (size_t)n * xstride + (u * BPL + b) * 16);
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+          acc[r * NT + n] = mad_wide(dot16(wx[r], xv, 0), S[r], acc[r * NT + n]);
+      }
+    }
+  }
+}
+
+constexpr int kFp4GuRows = MOE_FP4_GU_ROWS;  // gate/up rows per warp: channel pairs
+constexpr int kFp4GuNt = MOE_FP4_GU_NT;
+constexpr int kFp4DnRows = MOE_FP4_DN_ROWS;
+constexpr int kFp4DnNt = MOE_FP4_DN_NT;
+constexpr int kGuFp4ChannelsPerBlock = 8 * kFp4GuRows / 2;
+constexpr int kDownFp4RowsPerBlock = 8 * kFp4DnRows;
+static_assert(kFp4GuRows % 2 == 0 && 64 % kGuFp4ChannelsPerBlock == 0, "gate/up channel blocks");
+static_assert(128 % kDownFp4RowsPerBlock == 0, "down row blocks");
+
+__global__ void __launch_bounds__(256, MOE_FP4_GU_MINB) decode_gu_fp4_kernel(DecodeArgs a) {
+  constexpr int ROWS = kFp4GuRows, NT = kFp4GuNt, N = ROWS * NT;
+  extern __shared__ __align__(16) int8_t xs[];  // [NT][H] token codes of one pass
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
   const int g = blockIdx.y;
@@ -419,21 +552,21 @@ __global__ void __launch_bounds__(256, 2) decode_gu_fp4_kernel(DecodeArgs a) {
   const int c0 = blockIdx.x * kGuFp4ChannelsPerBlock;
   if (c0 >= Ig) return;
   const int H = a.H, nr = grp.z, row0 = grp.y;
-  const size_t cb = H / 2, sb = H / 16;  // code and scale bytes per weight row
-  const uint8_t* Wg = shared ? a.f.sh_gate : a.f.w_gate + (size_t)grp.x * a.I * cb;
-  const uint8_t* Wu = shared ? a.f.sh_up : a.f.w_up + (size_t)grp.x * a.I * cb;
-  const uint8_t* Bg = shared ? a.f.sh_b_gate : a.f.b_gate + (size_t)grp.x * a.I * sb;
-  const uint8_t* Bu = shared ? a.f.sh_b_up : a.f.b_up + (size_t)grp.x * a.I * sb;
+  const size_t cs = H / 2, ss = H / 16;  // code and scale bytes per weight row
+  const uint8_t* Wg = shared ? a.f.sh_gate : a.f.w_gate + (size_t)grp.x * a.I * cs;
+  const uint8_t* Wu = shared ? a.f.sh_up : a.f.w_up + (size_t)grp.x * a.I * cs;
+  const uint8_t* Bg = shared ? a.f.sh_b_gate : a.f.b_gate + (size_t)grp.x * a.I * ss;
+  const uint8_t* Bu = shared ? a.f.sh_b_up : a.f.b_up + (size_t)grp.x * a.I * ss;
   // matrix scales: sh_g exists only with a shared expert, so the pointer is chosen first
   const float gg = *(shared ? a.f.sh_g : a.f.g_gate + grp.x);
   const float gu = *(shared ? a.f.sh_g + 1 : a.f.g_up + grp.x);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int c = c0 + 2 * warp;
-  // rows {gate c, up c, gate c + 1, up c + 1}
-  const uint8_t* rows[4] = {Wg + c * cb, Wu + c * cb, Wg + (c + 1) * cb, Wu + (c + 1) * cb};
-  const uint8_t* srows[4] = {Bg + c * sb, Bu + c * sb, Bg + (c + 1) * sb, Bu + (c + 1) * sb};
-  for (int n0 = 0; n0 < nr; n0 += kChunk) {
-    const int nc = min(kChunk, nr - n0);
+  const int c = c0 + warp * (ROWS / 2);
+  // rows {gate c, up c, gate c + 1, up c + 1, ...}
+  const uint8_t* const cb[2] = {Wg + c * cs, Wu + c * cs};
+  const uint8_t* const sb[2] = {Bg + c * ss, Bu + c * ss};
+  for (int n0 = 0; n0 < nr; n0 += NT) {
+    const int nc = min(NT, nr - n0);
     if (n0 > 0) __syncthreads();  // the previous pass no longer reads xs
     for (int i = threadIdx.x; i < nc * H / 16; i += blockDim.x) {
       const int n = i / (H / 16), u = i % (H / 16);
@@ -442,55 +575,33 @@ __global__ void __launch_bounds__(256, 2) decode_gu_fp4_kernel(DecodeArgs a) {
           reinterpret_cast<const int4*>(a.qtok + (size_t)tok * H)[u];
     }
     __syncthreads();
-    long long acc[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0;
-#pragma unroll 2
-    for (int u = lane; u < H / 16; u += 32) {  // block u of every row
-      uint2 wv[4];
-      uint32_t bv[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        wv[r] = ld_stream8(rows[r] + (size_t)u * 8);
-        bv[r] = ld_stream_u8(srows[r] + u);
-      }
-      int4 wx[4];
-      int S[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        wx[r] = e2m1x16_to_s8(wv[r]);
-        S[r] = e4m3_units(bv[r]);
-      }
-#pragma unroll
-      for (int n = 0; n < kChunk; ++n) {
-        if (n < nc) {
-          const int4 xv = *reinterpret_cast<const int4*>(xs + (size_t)n * H + u * 16);
-#pragma unroll
-          for (int r = 0; r < 4; ++r) acc[r * 8 + n] = mad_wide(dot16(wx[r], xv, 0), S[r], acc[r * 8 + n]);
+    // one specialisation per token count: the dot, the warp reduction and the epilogue
+    with_count<1, NT>(nc, [&](auto cnt) {
+      long long acc[N];
+      fp4_dot_rows<ROWS, NT, MOE_FP4_GU_BPL, 2, decltype(cnt)::value>(cb, sb, H, xs, H, lane, acc);
+      transpose_reduce<N>(acc, lane);
+      const long long mine = acc[0];
+      const long long other = __shfl_down_sync(0xffffffffu, mine, NT);  // the channel's up row
+      const int r = lane / NT, n = lane % NT;
+      if (lane < N && (r & 1) == 0 && n < nc) {
+        const int ch = c + (r >> 1);
+        const int row = row0 + n0 + n;
+        const float sx = a.stok[a.row_token[row]];
+        a.h32[(size_t)row * a.Imax + ch] = silu_mul(dequant_f(fp4_acc_float(mine), sx, gg),
+                                                    dequant_f(fp4_acc_float(other), sx, gu));
+        if (a.tap_gu_f64) {
+          a.tap_gu_f64[(size_t)row * 2 * a.Imax + ch] = (double)mine * 0x1p-10;
+          a.tap_gu_f64[(size_t)row * 2 * a.Imax + a.Imax + ch] = (double)other * 0x1p-10;
         }
       }
-    }
-    transpose_reduce32(acc, lane);
-    const long long mine = acc[0];
-    const long long other = __shfl_down_sync(0xffffffffu, mine, 8);
-    const int r = lane >> 3, n = lane & 7;
-    if ((r & 1) == 0 && n < nc) {
-      const int ch = c + (r >> 1);
-      const int row = row0 + n0 + n;
-      const float sx = a.stok[a.row_token[row]];
-      a.h32[(size_t)row * a.Imax + ch] =
-          silu_mul(dequant_f(fp4_acc_float(mine), sx, gg), dequant_f(fp4_acc_float(other), sx, gu));
-      if (a.tap_gu_f64) {
-        a.tap_gu_f64[(size_t)row * 2 * a.Imax + ch] = (double)mine * 0x1p-10;
-        a.tap_gu_f64[(size_t)row * 2 * a.Imax + a.Imax + ch] = (double)other * 0x1p-10;
-      }
-    }
+    });
   }
 }
 
-__global__ void __launch_bounds__(256, 2) decode_down_fp4_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) int8_t hs[];  // [kChunk][Imax] h codes of one pass
-  __shared__ float shs[kChunk];
+__global__ void __launch_bounds__(256, MOE_FP4_DN_MINB) decode_down_fp4_kernel(DecodeArgs a) {
+  constexpr int ROWS = kFp4DnRows, NT = kFp4DnNt, N = ROWS * NT;
+  extern __shared__ __align__(16) int8_t hs[];  // [NT][Imax] h codes of one pass
+  __shared__ float shs[NT];
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
   const int g = blockIdx.y;
@@ -500,16 +611,18 @@ __global__ void __launch_bounds__(256, 2) decode_down_fp4_kernel(DecodeArgs a) {
   const int Ig = shared ? a.Is : a.I;
   const int H = a.H, nr = grp.z, row0 = grp.y, Imax = a.Imax;
   const int o0 = blockIdx.x * kDownFp4RowsPerBlock;
-  const size_t cb = Ig / 2, sb = Ig / 16;
-  const uint8_t* Wd = shared ? a.f.sh_down : a.f.w_down + (size_t)grp.x * H * cb;
-  const uint8_t* Bd = shared ? a.f.sh_b_down : a.f.b_down + (size_t)grp.x * H * sb;
+  const size_t cs = Ig / 2, ss = Ig / 16;
+  const uint8_t* Wd = shared ? a.f.sh_down : a.f.w_down + (size_t)grp.x * H * cs;
+  const uint8_t* Bd = shared ? a.f.sh_b_down : a.f.b_down + (size_t)grp.x * H * ss;
   const float gd = *(shared ? a.f.sh_g + 2 : a.f.g_down + grp.x);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int ob = o0 + warp * 4;
-  for (int n0 = 0; n0 < nr; n0 += kChunk) {
-    const int nc = min(kChunk, nr - n0);
+  const int ob = o0 + warp * ROWS;
+  const uint8_t* const cb[1] = {Wd + (size_t)ob * cs};
+  const uint8_t* const sb[1] = {Bd + (size_t)ob * ss};
+  for (int n0 = 0; n0 < nr; n0 += NT) {
+    const int nc = min(NT, nr - n0);
     if (n0 > 0) __syncthreads();  // the previous pass no longer reads hs and shs
-    // up to kChunk of this expert's h code rows (fp16 integers) -> int8
+    // up to NT of this expert's h code rows (fp16 integers) -> int8
     for (int i = threadIdx.x; i < nc * (Ig / 8); i += blockDim.x) {
       const int n = i / (Ig / 8), u = i % (Ig / 8);
       const uint4 v = reinterpret_cast<const uint4*>(a.hq + (size_t)(row0 + n0 + n) * Imax)[u];
@@ -525,43 +638,19 @@ __global__ void __launch_bounds__(256, 2) decode_down_fp4_kernel(DecodeArgs a) {
     }
     if ((int)threadIdx.x < nc) shs[threadIdx.x] = a.sh[row0 + n0 + threadIdx.x];
     __syncthreads();
-    long long acc[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0;
-#pragma unroll 1
-    for (int u = lane; u < Ig / 16; u += 32) {
-      uint2 wv[4];
-      uint32_t bv[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        wv[r] = ld_stream8(Wd + (size_t)(ob + r) * cb + (size_t)u * 8);
-        bv[r] = ld_stream_u8(Bd + (size_t)(ob + r) * sb + u);
+    with_count<1, NT>(nc, [&](auto cnt) {
+      long long acc[N];
+      fp4_dot_rows<ROWS, NT, MOE_FP4_DN_BPL, 1, decltype(cnt)::value>(cb, sb, Ig, hs, Imax, lane, acc);
+      transpose_reduce<N>(acc, lane);
+      const int r = lane / NT, n = lane % NT;
+      if (lane < N && n < nc) {
+        const int o = ob + r;
+        const int row = row0 + n0 + n;
+        const float d = dequant_f(fp4_acc_float(acc[0]), shs[n], gd);
+        atomicAdd(a.y + (size_t)a.row_token[row] * H + o, __fmul_rn(a.row_w[row], d));
+        if (a.tap_d_f64) a.tap_d_f64[(size_t)row * H + o] = (double)acc[0] * 0x1p-10;
       }
-      int4 wx[4];
-      int S[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        wx[r] = e2m1x16_to_s8(wv[r]);
-        S[r] = e4m3_units(bv[r]);
-      }
-#pragma unroll
-      for (int n = 0; n < kChunk; ++n) {
-        if (n < nc) {
-          const int4 xv = *reinterpret_cast<const int4*>(hs + (size_t)n * Imax + u * 16);
-#pragma unroll
-          for (int r = 0; r < 4; ++r) acc[r * 8 + n] = mad_wide(dot16(wx[r], xv, 0), S[r], acc[r * 8 + n]);
-        }
-      }
-    }
-    transpose_reduce32(acc, lane);
-    const int r = lane >> 3, n = lane & 7;
-    if (n < nc) {
-      const int o = ob + r;
-      const int row = row0 + n0 + n;
-      const float d = dequant_f(fp4_acc_float(acc[0]), shs[n], gd);
-      atomicAdd(a.y + (size_t)a.row_token[row] * H + o, __fmul_rn(a.row_w[row], d));
-      if (a.tap_d_f64) a.tap_d_f64[(size_t)row * H + o] = (double)acc[0] * 0x1p-10;
-    }
+    });
   }
 }
 
@@ -590,7 +679,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) 
   const int gmax = min(a.E, a.T * a.k) + (a.has_shared ? 1 : 0);
   if (a.fp4) {
     const dim3 ggu((a.Imax + kGuFp4ChannelsPerBlock - 1) / kGuFp4ChannelsPerBlock, gmax);
-    e = launch_pdl(decode_gu_fp4_kernel, ggu, dim3(256), (size_t)kChunk * a.H, s, a);
+    e = launch_pdl(decode_gu_fp4_kernel, ggu, dim3(256), (size_t)kFp4GuNt * a.H, s, a);
   } else {
     const dim3 ggu((a.Imax + kGuChannelsPerBlock - 1) / kGuChannelsPerBlock, gmax);
     e = launch_pdl(decode_gu_kernel, ggu, dim3(256), (size_t)kChunk * a.H, s, a);
@@ -603,7 +692,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s, cudaEvent_t* ev) 
   if (ev) cudaEventRecord(ev[2], s);
   if (a.fp4)
     e = launch_pdl(decode_down_fp4_kernel, dim3(a.H / kDownFp4RowsPerBlock, gmax), dim3(256),
-                   (size_t)kChunk * a.Imax, s, a);
+                   (size_t)kFp4DnNt * a.Imax, s, a);
   else
     e = launch_pdl(decode_down_kernel, dim3(a.H / kDownRowsPerBlock, gmax), dim3(256),
                    (size_t)kChunk * a.Imax, s, a);
@@ -621,10 +710,10 @@ cudaError_t decode_set_attributes() {
                                        kChunk * kDecodeMaxH);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(decode_gu_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kChunk * kDecodeMaxH);
+                             kFp4GuNt * kDecodeMaxH);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(decode_down_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kChunk * kDecodeMaxI);
+                             kFp4DnNt * kDecodeMaxI);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kChunk * kDecodeMaxI);
