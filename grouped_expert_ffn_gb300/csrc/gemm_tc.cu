@@ -165,6 +165,46 @@ __device__ __forceinline__ void widen_half_row(const uint8_t* w8_tile, int r, in
   }
 }
 
+// NVFP4 converter thread of weight row r, half h of a 128-K stage (64 K): the row's 32 code
+// bytes of the half (chunks 2h and 2h + 1, stored at chunk positions c ^ ((r >> 1) & 3)) and its
+// 4 block scales, decoded exactly to fp16 pairs in the same 32-column layout as
+// widen_half_row: column c holds K elements 2c, 2c + 1 (code byte c: low nibble = element 2c,
+// the low half). e2m1(code) * e4m3(scale) is exact in fp16: at most 5 significant bits,
+// magnitude between 2^-10 and 2688 (or zero).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t b) {
+  uint32_t d;
+  asm("{.reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;}" : "=r"(d) : "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t b) {
+  uint32_t d;
+  const uint16_t two = (uint16_t)((b & 0xffu) | (b & 0xffu) << 8);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(two));
+  return d;
+}
+__device__ __forceinline__ void widen_half_row_fp4(const uint8_t* tile, int r, int h,
+                                                   uint32_t (&o)[32]) {
+  const uint8_t* src = tile + r * 64;
+  const int sw = (r >> 1) & 3;
+  const uint32_t sc = *reinterpret_cast<const uint32_t*>(tile + 8192 + r * 8 + 4 * h);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * ((2 * h + c) ^ sw));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {  // block 2c + b: 8 code bytes = words 2b, 2b + 1
+      const uint32_t s2 = e4m3_to_f16x2_bcast(sc >> (8 * (2 * c + b)));
+      const __half2 hs = *reinterpret_cast<const __half2*>(&s2);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t f = e2m1x2_to_f16x2(w[2 * b + q / 4] >> (8 * (q % 4)));
+        const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&f), hs);
+        o[16 * c + 8 * b + q] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+    }
+  }
+}
+
 // 16-column chunks one epilogue warp handles per tile (its column group takes every
 // kColGroups-th chunk of at most kMaxTokTile columns).
 template <int kColGroups>
@@ -276,6 +316,7 @@ __device__ __forceinline__ void load_meta_gate_up(const GemmArgs& a, int4 wi, in
     m.rv[j] = a.sx[min(wi.y + cg * 16 + j * 16 * kCG + (lane & 15), last)];
 }
 
+template <bool FP4>
 __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
                                                  uint32_t tbase, int cg, const EpiMeta<true>& m) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
@@ -303,7 +344,10 @@ __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int
           st_f32_hint(a.h32 + (size_t)row * a.Imax + ch, hv, m.pol);  // read again by requant
         else
           a.h32[(size_t)row * a.Imax + ch] = hv;
-        if (a.tap) {
+        if (FP4 && a.tap_f64) {
+          a.tap_f64[(size_t)row * 2 * a.Imax + ch] = (double)acc_f(g);
+          a.tap_f64[(size_t)row * 2 * a.Imax + a.Imax + ch] = (double)acc_f(u);
+        } else if (!FP4 && a.tap) {
           a.tap[(size_t)row * 2 * a.Imax + ch] = acc_i(g);
           a.tap[(size_t)row * 2 * a.Imax + a.Imax + ch] = acc_i(u);
         }
@@ -364,6 +408,7 @@ __device__ __forceinline__ void load_meta_down(const GemmArgs& a, int4 wi, int c
   }
 }
 
+template <bool FP4>
 __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase,
                                               int cg, const EpiMeta<false>& m) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
@@ -377,7 +422,11 @@ __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nc
   epilogue_columns<GemmRoles<false>::kColGroups>(a, nch, tbase, cg, ncols,
                                                  [&](const auto& v, int c0, int j) {
     using V = typename std::remove_cv<typename std::remove_reference<decltype(v[0])>::type>::type;
-    if (a.tap) {
+    if (FP4 && a.tap_f64) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (c0 + i < ncols) a.tap_f64[(size_t)(wi.y + c0 + i) * a.H + o] = (double)acc_f(v[i]);
+    } else if (!FP4 && a.tap) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         if (c0 + i < ncols) a.tap[(size_t)(wi.y + c0 + i) * a.H + o] = acc_i(v[i]);
@@ -400,7 +449,7 @@ __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nc
   });
 }
 
-template <bool GU>
+template <bool GU, bool FP4>
 __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ XMaps tmX,
                         const __grid_constant__ CUtensorMap tmW,
@@ -449,7 +498,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == R::kWProducerWarp && lane == 0) {
+  if (!FP4 && warp == R::kWProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmWs);
   }
@@ -465,7 +514,9 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
   // Accumulator layout for this launch: one accumulator over the whole K (two TMEM slots,
   // double-buffered) when the bound proves it exact, else 1024-K chunks (the host sizes the
   // token tile so that the chunks of one tile fit the accumulator columns).
-  const bool single = single_accumulator_exact(a);
+  // NVFP4 weights: one fp32 accumulator over the whole K (the products are not integers,
+  // the sum is rounded as the tensor core accumulates it)
+  const bool single = FP4 || single_accumulator_exact(a);
   const int kmax = a.K_r > a.K_s ? a.K_r : a.K_s;
   const int slot_cols = single ? a.TN : ((kmax + kChunkK - 1) / kChunkK) * a.TN;
   const int nslots = slot_cols <= kAccCols / 2 ? 2 : 1;
@@ -491,7 +542,14 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
         const bool shared = wi.x == a.E;
         const int nks = ((shared ? a.K_s : a.K_r) + kKS - 1) / kKS;
         const int rows = (wi.z + kXStep - 1) / kXStep * kXStep;  // box height
-        const uint32_t bytes = wprod ? (uint32_t)kW8Bytes : (uint32_t)(2 * rows * kBK * 2);
+        const uint32_t wbytes = FP4 ? (uint32_t)kFp4TileBytes : (uint32_t)kW8Bytes;
+        const uint32_t bytes = wprod ? wbytes : (uint32_t)(2 * rows * kBK * 2);
+        // NVFP4: this item's tiles, one block per 128-K stage
+        const uint8_t* w4 =
+            FP4 ? (shared ? a.w4s
+                          : a.w4 + (size_t)wi.x * (a.rows_r / kBM) * nks * kFp4TileBytes) +
+                      (size_t)(wi.w / kBM) * nks * kFp4TileBytes
+                : nullptr;
         const CUtensorMap* mx = &tmX.m[rows / kXStep - 1];
         for (int kb = 0; kb < nks; ++kb, ++ks) {
           if (wprod || (int)(ks & 1) == pidx) {
@@ -500,7 +558,10 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(&full[stage], bytes);
-            if (wprod) {
+            if (wprod && FP4) {
+              bulk_load_hint(smem + kOffW8 + stage * kW8Bytes, w4 + (size_t)kb * kFp4TileBytes,
+                             kFp4TileBytes, &full[stage], pol_first);
+            } else if (wprod) {
               uint8_t* sw = smem + kOffW8 + stage * kW8Bytes;
               if (MOE_L2_HINTS) {
                 if (shared)
@@ -558,7 +619,10 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       const int ws = (int)(k % kWStages);
       if (!__all_sync(0xffffffffu, mbar_wait(&wfull[ws], (k / kWStages) & 1u, abort_flag, a.err)))
         return false;
-      widen_half_row(smem + kOffW8 + ws * kW8Bytes, r, h, o);
+      if constexpr (FP4)
+        widen_half_row_fp4(smem + kOffW8 + ws * kW8Bytes, r, h, o);
+      else
+        widen_half_row(smem + kOffW8 + ws * kW8Bytes, r, h, o);
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty[ws]);  // values consumed: the int8 tile may be reused
       return true;
@@ -664,9 +728,9 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = lane_base + (uint32_t)(slot * slot_cols);
       if constexpr (GU)
-        epilogue_gate_up(a, wi, nch, tbase, cg, m);
+        epilogue_gate_up<FP4>(a, wi, nch, tbase, cg, m);
       else
-        epilogue_down(a, wi, nch, tbase, cg, m);
+        epilogue_down<FP4>(a, wi, nch, tbase, cg, m);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[slot]);
@@ -682,12 +746,16 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
 }
 
 cudaError_t gemm_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem::kBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem::kBytes);
-  return e;
+  const void* ks[] = {(const void*)grouped_gemm_kernel<true, false>,
+                      (const void*)grouped_gemm_kernel<false, false>,
+                      (const void*)grouped_gemm_kernel<true, true>,
+                      (const void*)grouped_gemm_kernel<false, true>};
+  for (const void* k : ks) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem::kBytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // CTAs of the GEMM that can run at once (one per SM).
@@ -695,7 +763,9 @@ cudaError_t gemm_max_ctas(bool gate_up, int* n) {
   *n = 0;
   int per_sm = 0, dev = 0, sms = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, gate_up ? (const void*)grouped_gemm_kernel<true> : (const void*)grouped_gemm_kernel<false>,
+      &per_sm,
+      gate_up ? (const void*)grouped_gemm_kernel<true, false>
+              : (const void*)grouped_gemm_kernel<false, false>,
       gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads, GemmSmem::kBytes);
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -703,15 +773,78 @@ cudaError_t gemm_max_ctas(bool gate_up, int* n) {
   return e;
 }
 
-cudaError_t launch_grouped_gemm(bool gate_up, const GemmArgs& a, const XMaps& tmX,
+cudaError_t launch_grouped_gemm(bool gate_up, bool fp4, const GemmArgs& a, const XMaps& tmX,
                                 const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
                                 cudaStream_t s) {
   if (grid < 1) return cudaErrorInvalidValue;
-  if (gate_up)
-    return launch_pdl(grouped_gemm_kernel<true>, dim3(grid), dim3(GemmRoles<true>::kThreads),
-                      GemmSmem::kBytes, s, a, tmX, tmW, tmWs);
-  return launch_pdl(grouped_gemm_kernel<false>, dim3(grid), dim3(GemmRoles<false>::kThreads),
-                    GemmSmem::kBytes, s, a, tmX, tmW, tmWs);
+  if (fp4 && (!a.w4 || a.rows_r % kBM || a.rows_s % kBM)) return cudaErrorInvalidValue;
+  const dim3 g(grid);
+  if (gate_up) {
+    const dim3 b(GemmRoles<true>::kThreads);
+    return fp4 ? launch_pdl(grouped_gemm_kernel<true, true>, g, b, GemmSmem::kBytes, s, a, tmX, tmW, tmWs)
+               : launch_pdl(grouped_gemm_kernel<true, false>, g, b, GemmSmem::kBytes, s, a, tmX, tmW, tmWs);
+  }
+  const dim3 b(GemmRoles<false>::kThreads);
+  return fp4 ? launch_pdl(grouped_gemm_kernel<false, true>, g, b, GemmSmem::kBytes, s, a, tmX, tmW, tmWs)
+             : launch_pdl(grouped_gemm_kernel<false, false>, g, b, GemmSmem::kBytes, s, a, tmX, tmW, tmWs);
+}
+
+// One thread per 16-byte piece of a packed tile: code chunk position p of tile row r (four per
+// row), or the row's 8 scale bytes (a fifth piece, half used).
+__global__ void pack_fp4_tiles_kernel(const uint8_t* __restrict__ c0, const uint8_t* __restrict__ c1,
+                                      const uint8_t* __restrict__ s0, const uint8_t* __restrict__ s1,
+                                      int n_mats, int rows, int K, uint8_t* __restrict__ out) {
+  const int nmat = c1 ? 2 : 1;
+  const int trows = nmat * rows;          // tile rows per matrix set
+  const int tiles = trows / kBM, stages = (K + kKS - 1) / kKS;
+  const size_t total = (size_t)n_mats * tiles * stages * kBM * 5;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int piece = (int)(i % 5);
+    const int r = (int)((i / 5) % kBM);
+    const size_t ts = i / 5 / kBM;  // (m * tiles + t) * stages + st
+    const int st = (int)(ts % stages);
+    const int t = (int)((ts / stages) % tiles);
+    const int m = (int)(ts / stages / tiles);
+    const int R = t * kBM + r;
+    const int mat = nmat == 2 ? R % 2 : 0;
+    const int srow = nmat == 2 ? R / 2 : R;
+    const uint8_t* cs = mat ? c1 : c0;
+    const uint8_t* ss = mat ? s1 : s0;
+    uint8_t* tile = out + ts * kFp4TileBytes;
+    if (piece < 4) {
+      const int c = piece ^ ((r >> 1) & 3);  // the chunk stored at position `piece`
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (st * kKS + c * 32 + 32 <= K)
+        v = *reinterpret_cast<const uint4*>(cs + ((size_t)m * rows + srow) * (K / 2) + st * 64 + c * 16);
+      *reinterpret_cast<uint4*>(tile + r * 64 + piece * 16) = v;
+    } else {
+      const uint8_t* sp = ss + ((size_t)m * rows + srow) * (K / 16);
+#pragma unroll
+      for (int b = 0; b < 8; ++b)
+        tile[8192 + r * 8 + b] = st * 8 + b < K / 16 ? sp[st * 8 + b] : (uint8_t)0;
+    }
+  }
+}
+
+cudaError_t launch_pack_fp4_tiles(const uint8_t* codes0, const uint8_t* codes1, const uint8_t* sc0,
+                                  const uint8_t* sc1, int n_mats, int rows, int K, uint8_t* out,
+                                  cudaStream_t s) {
+  if ((codes1 ? 2 : 1) * rows % kBM || K % 64) return cudaErrorInvalidValue;
+  pack_fp4_tiles_kernel<<<1024, 256, 0, s>>>(codes0, codes1, sc0, sc1, n_mats, rows, K, out);
+  return cudaGetLastError();
+}
+
+__global__ void fill_rows_kernel(const float* __restrict__ v, int n_mats, int n, float* __restrict__ out) {
+  const size_t total = (size_t)n_mats * n;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x)
+    out[i] = v[i / n];
+}
+
+cudaError_t launch_fill_rows(const float* v, int n_mats, int n, float* out, cudaStream_t s) {
+  fill_rows_kernel<<<256, 256, 0, s>>>(v, n_mats, n, out);
+  return cudaGetLastError();
 }
 
 // Per-row requantisation of h = SiLU(gate)*up: s = amax/127, q = rne(h/s) (|q| <= 127),

@@ -73,11 +73,32 @@ struct GemmArgs {
   // taps (NULL = off)
   int32_t* tap;
   int* err;
+  // NVFP4 weights (the fp4 kernels): tiles packed by launch_pack_fp4_tiles, one
+  // kFp4TileBytes block per (128-row tile, 128-K stage); rows_r / rows_s = weight rows of a
+  // routed / the shared group. Accumulator taps are then fp64.
+  const uint8_t* w4 = nullptr;
+  const uint8_t* w4s = nullptr;
+  int rows_r = 0, rows_s = 0;
+  double* tap_f64 = nullptr;
 };
 
-cudaError_t launch_grouped_gemm(bool gate_up, const GemmArgs& a, const XMaps& tmX,
+// One (128-row, 128-K) NVFP4 weight tile as the tensor-core kernels read it: 8192 code bytes
+// (row r's 64 bytes at r * 64, its 16-byte chunk c at chunk position c ^ ((r >> 1) & 3)), then
+// 1024 block-scale bytes (row r's 8 at 8192 + r * 8).
+constexpr int kFp4TileBytes = 9216;
+
+cudaError_t launch_grouped_gemm(bool gate_up, bool fp4, const GemmArgs& a, const XMaps& tmX,
                                 const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
                                 cudaStream_t s);
+// Repacks NVFP4 weight rows (codes [n_mats, rows, K/2], scales [n_mats, rows, K/16]; with
+// codes1 / sc1 given, two matrices interleaved row by row: tile row 2i = row i of matrix 0,
+// 2i + 1 = row i of matrix 1) into tiles [n_mats][tiles][ceil(K/128)][kFp4TileBytes], K past
+// the matrix zero.
+cudaError_t launch_pack_fp4_tiles(const uint8_t* codes0, const uint8_t* codes1, const uint8_t* sc0,
+                                  const uint8_t* sc1, int n_mats, int rows, int K, uint8_t* out,
+                                  cudaStream_t s);
+// out[m * n + i] = v[m] (m < n_mats, i < n): a matrix scale as per-row scales.
+cudaError_t launch_fill_rows(const float* v, int n_mats, int n, float* out, cudaStream_t s);
 cudaError_t gemm_set_attributes();
 cudaError_t gemm_max_ctas(bool gate_up, int* n);
 

@@ -66,6 +66,12 @@ struct moe_packed_s {
   moe_plan_s* plan = nullptr;
   int fp4 = 0;     // NVFP4 weights (f) instead of int8 (w)
   Fp4Weights f;
+  // NVFP4 tensor-core tiles (gate/up interleaved; down) and the matrix scales as per-row scales
+  uint8_t* gu4 = nullptr;
+  uint8_t* gu4s = nullptr;
+  uint8_t* d4 = nullptr;
+  uint8_t* d4s = nullptr;
+  float* rs4 = nullptr;  // [E*I gate | E*I up | E*H down | Is gate | Is up | H down]
   moe_weights w;
   int8_t* gu8 = nullptr;    // [E, 2I, H] gate/up rows interleaved in pairs
   int8_t* shgu8 = nullptr;  // [2Is, H]
@@ -462,7 +468,40 @@ moe_status moe_pack_weights_nvfp4(moe_plan_t p, const moe_weights_nvfp4* w, void
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t E = p->E, H = p->H, I = p->I, Is = p->Is;
-  cudaError_t e = launch_check_e4m3(f.b_gate, E * I * (H / 16), p->err, s);
+  auto fail = [&](moe_status st) {
+    moe_packed_destroy(pk);
+    cudaGetLastError();
+    return st;
+  };
+  // tensor-core tiles: one kFp4TileBytes block per (128-row tile, 128-K stage)
+  const size_t stH = (H + kKS - 1) / kKS, stI = (I + kKS - 1) / kKS, stIs = (Is + kKS - 1) / kKS;
+  const size_t n_rs = 2 * E * I + E * H + (p->has_shared ? 2 * Is + H : 0);
+  if (cudaMalloc(&pk->gu4, E * (2 * I / kBM) * stH * kFp4TileBytes) != cudaSuccess ||
+      cudaMalloc(&pk->d4, E * (H / kBM) * stI * kFp4TileBytes) != cudaSuccess ||
+      cudaMalloc(&pk->rs4, n_rs * sizeof(float)) != cudaSuccess)
+    return fail(MOE_ERR_OOM);
+  if (p->has_shared && (cudaMalloc(&pk->gu4s, (2 * Is / kBM) * stH * kFp4TileBytes) != cudaSuccess ||
+                        cudaMalloc(&pk->d4s, (H / kBM) * stIs * kFp4TileBytes) != cudaSuccess))
+    return fail(MOE_ERR_OOM);
+  float* rs = pk->rs4;
+  cudaError_t e = launch_pack_fp4_tiles(f.w_gate, f.w_up, f.b_gate, f.b_up, (int)E, (int)I, (int)H,
+                                        pk->gu4, s);
+  if (e == cudaSuccess)
+    e = launch_pack_fp4_tiles(f.w_down, nullptr, f.b_down, nullptr, (int)E, (int)H, (int)I, pk->d4, s);
+  if (e == cudaSuccess) e = launch_fill_rows(f.g_gate, (int)E, (int)I, rs, s);
+  if (e == cudaSuccess) e = launch_fill_rows(f.g_up, (int)E, (int)I, rs + E * I, s);
+  if (e == cudaSuccess) e = launch_fill_rows(f.g_down, (int)E, (int)H, rs + 2 * E * I, s);
+  if (e == cudaSuccess && p->has_shared) {
+    float* rsh = rs + 2 * E * I + E * H;
+    e = launch_pack_fp4_tiles(f.sh_gate, f.sh_up, f.sh_b_gate, f.sh_b_up, 1, (int)Is, (int)H, pk->gu4s, s);
+    if (e == cudaSuccess)
+      e = launch_pack_fp4_tiles(f.sh_down, nullptr, f.sh_b_down, nullptr, 1, (int)H, (int)Is, pk->d4s, s);
+    if (e == cudaSuccess) e = launch_fill_rows(f.sh_g, 1, (int)Is, rsh, s);
+    if (e == cudaSuccess) e = launch_fill_rows(f.sh_g + 1, 1, (int)Is, rsh + Is, s);
+    if (e == cudaSuccess) e = launch_fill_rows(f.sh_g + 2, 1, (int)H, rsh + 2 * Is, s);
+  }
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA);
+  e = launch_check_e4m3(f.b_gate, E * I * (H / 16), p->err, s);
   if (e == cudaSuccess) e = launch_check_e4m3(f.b_up, E * I * (H / 16), p->err, s);
   if (e == cudaSuccess) e = launch_check_e4m3(f.b_down, E * H * (I / 16), p->err, s);
   if (e == cudaSuccess && p->has_shared) {
@@ -470,17 +509,15 @@ moe_status moe_pack_weights_nvfp4(moe_plan_t p, const moe_weights_nvfp4* w, void
     if (e == cudaSuccess) e = launch_check_e4m3(f.sh_b_up, Is * (H / 16), p->err, s);
     if (e == cudaSuccess) e = launch_check_e4m3(f.sh_b_down, H * (Is / 16), p->err, s);
   }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    delete pk;
-    return MOE_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA);
   *out = pk;
   return MOE_OK;
 }
 
 moe_status moe_packed_destroy(moe_packed_t pk) {
   if (!pk) return MOE_ERR_INVALID_ARG;
+  for (void* q : {(void*)pk->gu4, (void*)pk->gu4s, (void*)pk->d4, (void*)pk->d4s, (void*)pk->rs4})
+    if (q) cudaFree(q);
   if (pk->gu8) cudaFree(pk->gu8);
   if (pk->shgu8) cudaFree(pk->shgu8);
   if (pk->w_sq) cudaFree(pk->w_sq);
@@ -512,9 +549,7 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   const int T_sh = p->has_shared ? T : 0;
   const int R = T * p->k + T_sh;
   cudaError_t e;
-  const bool stream_path = decode_shape_supported(p->H, p->Imax) &&
-                           T <= (pk->fp4 ? kDecodeMaxRows : p->decode_rows);
-  if (pk->fp4 && !stream_path) return MOE_ERR_UNSUPPORTED;  // NVFP4: streaming kernels only
+  const bool stream_path = decode_shape_supported(p->H, p->Imax) && T <= p->decode_rows;
   p->last_T = T;
   if (stream_path) {
     DecodeArgs a;
@@ -632,16 +667,32 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   g.row_w = p->row_w;
   g.y = y;
   g.err = p->err;
+  const bool fp4 = pk->fp4 != 0;
+  if (fp4) {  // matrix scales as per-row scales; taps fp64
+    const size_t E = p->E, I = p->I, H = p->H, Is = p->Is;
+    const float* rsh = pk->rs4 + 2 * E * I + E * H;
+    g.s_g = pk->rs4;
+    g.s_u = pk->rs4 + E * I;
+    g.s_d = pk->rs4 + 2 * E * I;
+    g.sh_s_g = p->has_shared ? rsh : nullptr;
+    g.sh_s_u = p->has_shared ? rsh + Is : nullptr;
+    g.sh_s_d = p->has_shared ? rsh + 2 * Is : nullptr;
+  }
   // gate/up: K = H for every group
   g.items = p->items_gu;
   g.n_items = p->n_items;
   g.K_r = p->H;
   g.K_s = p->H;
   g.TN = p->tn_gu;
-  g.tap = p->debug ? p->tap_gu : nullptr;
+  g.tap = p->debug && !fp4 ? p->tap_gu : nullptr;
+  g.tap_f64 = p->debug && fp4 ? reinterpret_cast<double*>(p->tap_gu) : nullptr;
   g.row_sq_max = p->sq_max;
   g.w_sq_max = pk->w_sq;
-  if ((e = launch_grouped_gemm(true, g, p->tmX_gu, pk->tmW_gu, pk->tmWs_gu, p->grid_gu, s)) !=
+  g.w4 = pk->gu4;
+  g.w4s = pk->gu4s;
+  g.rows_r = 2 * p->I;
+  g.rows_s = 2 * p->Is;
+  if ((e = launch_grouped_gemm(true, fp4, g, p->tmX_gu, pk->tmW_gu, pk->tmWs_gu, p->grid_gu, s)) !=
       cudaSuccess)
     return cuda_status(e);
   if (ev) cudaEventRecord(ev[2], s);
@@ -655,10 +706,15 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   g.K_r = p->I;
   g.K_s = p->has_shared ? p->Is : p->I;
   g.TN = p->tn_d;
-  g.tap = p->debug ? p->tap_d : nullptr;
+  g.tap = p->debug && !fp4 ? p->tap_d : nullptr;
+  g.tap_f64 = p->debug && fp4 ? reinterpret_cast<double*>(p->tap_d) : nullptr;
   g.row_sq_max = p->sq_max + 1;
-  g.w_sq_max = pk->w_sq + 1;
-  e = launch_grouped_gemm(false, g, p->tmX_d, pk->tmW_d, pk->tmWs_d, p->grid_d, s);
+  g.w_sq_max = fp4 ? nullptr : pk->w_sq + 1;
+  g.w4 = pk->d4;
+  g.w4s = pk->d4s;
+  g.rows_r = p->H;
+  g.rows_s = p->H;
+  e = launch_grouped_gemm(false, fp4, g, p->tmX_d, pk->tmW_d, pk->tmWs_d, p->grid_d, s);
   if (ev) cudaEventRecord(ev[4], s);
   return cuda_status(e);
 }

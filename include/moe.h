@@ -141,18 +141,23 @@ MOE_API moe_status moe_pack_weights(moe_plan_t plan, const moe_weights* w, void*
                             moe_packed_t* out);
 MOE_API moe_status moe_packed_destroy(moe_packed_t packed);
 
-/* Register one layer's NVFP4 expert weights (moe_weights_nvfp4). Reads the caller's arrays in
- * place: they must stay alive and unchanged while the handle is in use. Queues on `stream` a
- * check of every block scale byte; a negative or NaN one sets the plan's sticky error word
- * to MOE_ERR_DEVICE (read by moe_get_error). With the returned handle, moe_forward and
+/* Register one layer's NVFP4 expert weights (moe_weights_nvfp4). Allocates and fills (on
+ * `stream`) the tensor-core copy: every (128-row, 128-K) weight tile's codes and block scales
+ * in one contiguous 9216-byte block, gate and up rows interleaved in channel pairs, plus the
+ * matrix scales as per-row scales. The decode path reads the caller's arrays in place, so
+ * they must stay alive and unchanged while the handle is in use. Also queues a check of every
+ * block scale byte; a negative or NaN one sets the plan's sticky error word to
+ * MOE_ERR_DEVICE (read by moe_get_error). With the returned handle, moe_forward and
  * moe_route_forward compute the same layer with these weights:
- *   per weight row, acc = sum over elements of q * e2m1(code) * e4m3(block scale), the
- *   EXACT sum (q = the int8 activation or h code); then g = (float(acc) * s_x) * g_gate,
- *   u likewise, h = SiLU(g) * u requantised per row as in the int8 layer, and
- *   d = (float(acc_d) * s_h) * g_down, combined as in the int8 layer (float() rounds to
- *   nearest even).
- * T <= 64 rows run the deduplicated weight-streaming kernels (exact int64 accumulators);
- * larger T returns MOE_ERR_UNSUPPORTED. Pointers must be 16-byte aligned. */
+ *   per weight row, acc = sum over elements of q * e2m1(code) * e4m3(block scale)
+ *   (q = the int8 activation or h code); then g = (float(acc) * s_x) * g_gate, u likewise,
+ *   h = SiLU(g) * u requantised per row as in the int8 layer, and
+ *   d = (float(acc_d) * s_h) * g_down, combined as in the int8 layer.
+ * The dispatch is the int8 layer's: T <= the plan's decode threshold runs the deduplicated
+ * weight-streaming kernels, which form acc exactly (int64) and round it once to fp32; larger
+ * T runs the grouped tensor-core GEMMs, which decode each weight exactly to fp16 and
+ * accumulate the products in fp32 (rounded as the tensor core adds them). Pointers must be
+ * 16-byte aligned. */
 MOE_API moe_status moe_pack_weights_nvfp4(moe_plan_t plan, const moe_weights_nvfp4* w, void* stream,
                                   moe_packed_t* out);
 

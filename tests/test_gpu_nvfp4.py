@@ -2,7 +2,10 @@
 elements, fp32 matrix scales) against the CPU oracle's NVFP4 layer.
 
 The weight-streaming kernels accumulate every row exactly (int64 in units of 2^-10), so the
-fp64 accumulator taps must equal the oracle's exact sums bit for bit; the routing,
+fp64 accumulator taps must equal the oracle's exact sums bit for bit; the grouped tensor-core
+GEMMs decode the weights exactly to fp16 and accumulate in fp32, so their accumulators are
+held within 1e-4 * ||q|| * ||w'|| of the exact sums (q the activation or h codes, w' the
+dequantised weight row without its matrix scale); the routing,
 permutation and activation codes are bit-identical; requantised h codes may differ by one
 at a rounding tie of exp (at most 1e-3 of them), and y is held to the int8 layer's
 tolerances (max|dy| <= 1e-2 max|y_ref|, rms(dy) <= 5e-3 rms(y_ref))."""
@@ -37,9 +40,15 @@ def test_nvfp4_decode_matches_the_oracle(T):
     # the 35B-A3B-shaped layer (H=2048, E=128, k=8, I=512, shared expert 512) with NVFP4
     # experts; above 8 rows an expert's rows take several passes
     sh, d, W = _layer(T, 2048, 128, 8, 512, 512, seed=90 + T)
-    st = check_layer(sh, d["x"], d["logits"], weights_to(W, "cuda"), oracle_layer_nvfp4(W, sh))
-    if T > 8:
-        assert st["tap"]["counts"].max() > 8 or T < 24
+    Wd = weights_to(W, "cuda")
+    lay = moe.MoELayer(sh.E, sh.k, sh.H, sh.I, sh.Is, T, Wd)
+    try:
+        moe.moe_plan_set_decode_rows(lay.plan, 64)  # every T here on the streaming kernels
+        st = check_layer(sh, d["x"], d["logits"], Wd, oracle_layer_nvfp4(W, sh), layer=lay)
+        if T >= 24:
+            assert st["tap"]["counts"].max() > 8  # some routed expert took more than one pass
+    finally:
+        lay.close()
 
 
 def _random_bytes_weights(rng, E, H, I, Is):
@@ -121,18 +130,52 @@ def test_nvfp4_bad_block_scale_sets_device_error(bad):
         lay.close()
 
 
-def test_nvfp4_capacity_and_unsupported_sizes():
-    T, H, E, k, I, Is = 65, 256, 8, 2, 128, 64
-    sh, d, W = _layer(T, H, E, k, I, Is, seed=340)
+@pytest.mark.parametrize("T", [40, 256])
+def test_nvfp4_grouped_gemms_match_the_oracle(T):
+    # above the decode threshold: the grouped tensor-core GEMMs (weights decoded exactly to
+    # fp16, fp32 accumulation); T = 256 is the prefill chunk of the 35B-A3B-shaped layer
+    sh, d, W = _layer(T, 2048, 128, 8, 512, 512, seed=350 + T)
+    st = check_layer(sh, d["x"], d["logits"], weights_to(W, "cuda"), oracle_layer_nvfp4(W, sh),
+                     acc_exact=False)
+    assert st["tap"]["counts"].max() > 0
+
+
+@pytest.mark.parametrize("T", [65, 77, 200])
+def test_nvfp4_grouped_ragged_and_every_byte(T):
+    # ragged token counts, a K (= I_shared = 192) that ends half-way through a 128-K stage,
+    # and codes / block scales over every byte value
+    H, E, k, I, Is = 512, 16, 4, 256, 192
+    sh = synth.LayerShape(T=T, H=H, E=E, k=k, I=I, Is=Is)
+    d = synth.small_layer(T, H, E, k, I, Is, seed=360 + T)
+    W = _random_bytes_weights(np.random.default_rng(360 + T), E, H, I, Is)
+    check_layer(sh, d["x"], d["logits"], weights_to(W, "cuda"), oracle_layer_nvfp4(W, sh),
+                acc_exact=False)
+
+
+def test_nvfp4_stream_and_grouped_paths_agree():
+    # the same call through the exact streaming kernels and through the grouped GEMMs: the
+    # permutation and activation codes are identical, the accumulators agree within the fp32
+    # accumulation bound, y within the layer tolerance
+    T, H, E, k, I, Is = 24, 2048, 128, 8, 512, 512
+    sh, d, W = _layer(T, H, E, k, I, Is, seed=370)
     lay = moe.MoELayer(E, k, H, I, Is, T, weights_to(W, "cuda"))
     try:
+        moe.moe_debug_enable(lay.plan, True)
         x = d["x"].cuda()
         idx, w = lay.route(d["logits"].cuda())
-        with pytest.raises(moe.MoeError) as ei:
-            lay.forward(x, idx, w)  # 65 rows: beyond the streaming kernels
-        assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
-        y = lay.forward(x[:64].contiguous(), idx[:64].contiguous(), w[:64].contiguous())
-        torch.cuda.synchronize()
-        assert moe.moe_get_error(lay.plan) == 0 and torch.isfinite(y).all()
+        out = {}
+        for rows in (64, 0):
+            moe.moe_plan_set_decode_rows(lay.plan, rows)
+            y = lay.forward(x, idx, w)
+            torch.cuda.synchronize()
+            assert moe.moe_get_error(lay.plan) == 0
+            out[rows] = (y.clone(), moe.moe_debug_tap(lay.plan, moe.TAP_PERM),
+                         moe.moe_debug_tap(lay.plan, moe.TAP_QX),
+                         moe.moe_debug_tap(lay.plan, moe.TAP_ACC_GU_F64))
+        (ys, ps, qs, gs), (yg, pg, qg, gg) = out[64], out[0]
+        assert (ps == pg).all() and (qs == qg).all()
+        scale = np.abs(gs).max()
+        assert np.abs(gs - gg).max() <= 2e-4 * scale
+        assert (ys - yg).abs().max().item() <= 1e-2 * yg.abs().max().item()
     finally:
         lay.close()
