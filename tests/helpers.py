@@ -162,7 +162,8 @@ def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L,
                         wn = [w[e] for w in wn]
                     bgu = qn[i] * np.stack([wn[0][:Ig], wn[1][:Ig]])
                     hn = np.sqrt((tp["hq"][i, s, :Ig].astype(np.float64) ** 2).sum())
-                    bd = hn * wn[2]
+                    wdn = wn[2]  # norms of the down rows
+                    bd = hn * wdn
                 assert acc_ok(acc_gu[r, :, :Ig], tp["acc_gu"][i, s, :, :Ig], bgu), (t, s)
                 dq = np.abs(hq[r, :Ig].astype(np.int32) - tp["hq"][i, s, :Ig].astype(np.int32))
                 assert dq.max() <= 1, (t, s)
@@ -171,11 +172,21 @@ def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L,
                 # the row's scale comes from an amax over SiLU outputs whose exp may differ in
                 # the last ulp between the CUDA and host math libraries
                 s_o = np.float32(tp["sh"][i, s])
-                assert abs(float(shs[r]) - float(s_o)) <= SH_ULPS * float(np.spacing(s_o)), (t, s)
+                if acc_exact:
+                    assert abs(float(shs[r]) - float(s_o)) <= SH_ULPS * float(np.spacing(s_o)), (t, s)
+                else:  # the amax of h moves with the fp32 accumulation of g and u
+                    assert abs(float(shs[r]) - float(s_o)) <= 1e-3 * float(s_o), (t, s)
                 # the down accumulators depend only on the h codes (not on their scale): compared
-                # bit-exactly on every row whose codes agree
-                if dq.max() == 0:
+                # bit-exactly on every row whose codes agree; with fp32 accumulation on every
+                # row, the bound widened by what the differing codes can contribute
+                # (||dq|| * ||w'||, Cauchy-Schwarz)
+                if acc_exact and dq.max() == 0:
                     assert acc_ok(acc_d[r], tp["acc_d"][i, s], bd), (t, s)
+                    n_rows_d += 1
+                elif not acc_exact:
+                    dqn = np.sqrt((dq.astype(np.float64) ** 2).sum())
+                    assert (np.abs(acc_d[r] - tp["acc_d"][i, s]) <=
+                            ACC_F32_REL * bd + dqn * wdn).all(), (t, s)
                     n_rows_d += 1
         assert n_hq_diff <= HQ_MISMATCH_FRAC * n_hq, (n_hq_diff, n_hq)
         # the bit-exact down check must have covered nearly every compared row (a run in which
