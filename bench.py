@@ -384,6 +384,81 @@ def measure_layer(moe, name, peaks, steps):
             "stage_us": [v * 1e3 / max(calls, 1) for v in st]}
 
 
+def measure_prefill_formats(moe, peaks, steps, n_layers=8):
+    """The stacked-prefill layer shape (T=2600, H=2048, E=128, top_k=8, I=512, shared 512) with
+    int8 and with NVFP4 expert weights, in the same harness: n_layers layers of each (weights
+    above L2 in total), N(0,1) router logits per layer, moe_forward per layer timed with CUDA
+    events; microseconds per layer, the two GEMM stages and the gate/up GEMM's tensor
+    fraction."""
+    dev = torch.device("cuda")
+    wl = synth.WORKLOADS["stack"]
+    sh = wl.shape
+    T, H, E, k = sh.T, sh.H, sh.E, sh.k
+    x = synth.make_activations(T, H, wl.seed, wl.outliers, dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    R = T * k + T
+    gu_flops = 2.0 * R * 2 * sh.I * H
+    peak_tf = peaks.get("bf16_tflops", FALLBACK["bf16_tflops"])
+    out = {"workload": f"{n_layers} layers x T={T}, H={H}, E={E}, top_k={k}, I={sh.I}, shared I={sh.Is}, "
+                       "N(0,1) router logits"}
+    for fmt in ("int8", "nvfp4"):
+        plan = moe.moe_plan(E, k, H, sh.I, sh.Is, T)
+        Ws, packed, routes = [], [], []
+        try:
+            for l in range(n_layers):
+                seed = synth.layer_seed(wl, l)
+                if fmt == "int8":
+                    W = synth.make_weights(sh, seed, device=dev)
+                    packed.append(moe.moe_pack_weights(plan, W))
+                else:
+                    W = synth.make_weights_nvfp4(sh, seed, device=dev)
+                    packed.append(moe.moe_pack_weights_nvfp4(plan, W))
+                Ws.append(W)
+                lg = synth.make_logits(T, E, seed, 0.0, dev)
+                idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+                w = torch.empty((T, k), dtype=torch.float32, device=dev)
+                moe.moe_route(plan, lg, idx, w)
+                routes.append((idx, w))
+
+            def run():
+                for pk, (idx, w) in zip(packed, routes):
+                    moe.moe_forward(plan, pk, x, idx, w, y)
+
+            for _ in range(3):
+                run()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(steps, 5)
+            e0.record(stream)
+            for _ in range(reps):
+                run()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / reps / n_layers
+            moe.moe_profile_enable(plan, True)
+            for _ in range(2):
+                run()
+            torch.cuda.synchronize()
+            st, calls = moe.moe_profile_read(plan, 0)
+            moe.moe_profile_enable(plan, False)
+            if moe.moe_get_error(plan):
+                raise moe.MoeError(moe.moe_get_error(plan), f"prefill {fmt}")
+        finally:
+            for pk in packed:
+                moe.moe_packed_destroy(pk)
+            moe.moe_plan_destroy(plan)
+            del Ws
+            torch.cuda.empty_cache()
+        stage = [v * 1e3 / max(calls, 1) for v in st]
+        gu_tf = gu_flops / (stage[1] * 1e-6) / 1e12
+        out[fmt] = {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6),
+                    "stage_us": {"permute_quant": stage[0], "gate_up_gemm": stage[1],
+                                 "requant": stage[2], "down_gemm_into_y": stage[3]},
+                    "gate_up_tflops": gu_tf, "gate_up_frac": gu_tf / peak_tf}
+    return out
+
+
 def oracle_one_core(names, max_tokens):
     """The oracle (as it stands) on one host core: MoE-layer tokens/s per workload, on the
     first min(T, max_tokens[name]) tokens of the workload's layer."""
@@ -533,6 +608,7 @@ def run_ours(args, world, rank):
         if not args.no_decode:
             extra["decode_nvfp4"] = measure_decode_nvfp4(moe, plan, wl, n_layers, peaks, args.steps,
                                                          stream)
+        extra["prefill_int8_vs_nvfp4"] = measure_prefill_formats(moe, peaks, args.steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         extra["cpu_baseline_1core"] = oracle_one_core(["tiny", "decode", "prefill"],
                                                       {"prefill": args.cpu_tokens_1core})
