@@ -707,6 +707,36 @@ def run_reference(args, world, rank):
     print(json.dumps(line))
 
 
+def nvfp4_probe():
+    """A short fixed launch sequence for a profiler capture of the NVFP4 kernels (no timing,
+    no JSON line): one plan and one NVFP4 weight set of the stacked layer's shape, two
+    moe_route_forward calls at T=2600 (grouped GEMMs, N(0,1) router logits), then two at T=8
+    (streaming decode kernels, the decode workload's Zipf(1.1) logits)."""
+    import grouped_expert_ffn_gb300 as moe
+    dev = torch.device("cuda")
+    wl = synth.WORKLOADS["stack"]
+    sh = wl.shape
+    plan = moe.moe_plan(sh.E, sh.k, sh.H, sh.I, sh.Is, sh.T)
+    W = synth.make_weights_nvfp4(sh, synth.layer_seed(wl, 0), device=dev)
+    pk = moe.moe_pack_weights_nvfp4(plan, W)
+    dwl = synth.WORKLOADS["decode"]
+    for T, x, lg in ((sh.T, synth.make_activations(sh.T, sh.H, wl.seed, wl.outliers, dev),
+                      synth.make_logits(sh.T, sh.E, wl.seed, 0.0, dev)),
+                     (8, synth.make_activations(8, sh.H, dwl.seed, dwl.outliers, dev),
+                      synth.make_logits(8, sh.E, dwl.seed, dwl.zipf_s, dev))):
+        idx = torch.empty((T, sh.k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, sh.k), dtype=torch.float32, device=dev)
+        y = torch.empty((T, sh.H), dtype=torch.float32, device=dev)
+        for _ in range(2):
+            moe.moe_route_forward(plan, pk, x, lg, idx, w, y)
+    torch.cuda.synchronize()
+    if moe.moe_get_error(plan):
+        raise moe.MoeError(moe.moe_get_error(plan), "nvfp4 probe")
+    moe.moe_packed_destroy(pk)
+    moe.moe_plan_destroy(plan)
+    print("nvfp4 probe ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -725,7 +755,12 @@ def main():
                     help="skip the T=256 prefill-chunk and T=8192 stress layer lines")
     ap.add_argument("--cpu-tokens-1core", type=int, default=48,
                     help="tokens of the T=256 prefill layer the one-core oracle runs")
+    ap.add_argument("--nvfp4-probe", action="store_true",
+                    help="only run the short NVFP4 launch sequence a profiler capture uses")
     args = ap.parse_args()
+    if args.nvfp4_probe:
+        nvfp4_probe()
+        return
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         world = int(os.environ.get("WORLD_SIZE", "1"))
