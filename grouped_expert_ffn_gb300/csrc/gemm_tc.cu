@@ -109,10 +109,17 @@ struct GemmRoles {
 #ifndef MOE_W_STAGES
 #define MOE_W_STAGES 4
 #endif
-// Shared-memory layout: token stages, int8 weight stages, barriers.
+#ifndef MOE_D_X_STAGES
+#define MOE_D_X_STAGES MOE_X_STAGES
+#endif
+#ifndef MOE_D_W_STAGES
+#define MOE_D_W_STAGES 5  // the down GEMM's 4-stage items: one more weight stage in flight
+#endif
+// Shared-memory layout: token stages, int8 weight stages, barriers (stage counts per GEMM).
+template <bool GU>
 struct GemmSmem {
-  static constexpr int kXStages = MOE_X_STAGES;
-  static constexpr int kWStages = MOE_W_STAGES;
+  static constexpr int kXStages = GU ? MOE_X_STAGES : MOE_D_X_STAGES;
+  static constexpr int kWStages = GU ? MOE_W_STAGES : MOE_D_W_STAGES;
   static constexpr int kOffW8 = kXStages * kXStageBytes;
   static constexpr int kOffBar = kOffW8 + kWStages * kW8Bytes;
   static constexpr int kBarBytes = 256;
@@ -454,8 +461,8 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ XMaps tmX,
                         const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmWs) {
-  constexpr int kXStages = GemmSmem::kXStages, kWStages = GemmSmem::kWStages;
-  constexpr int kOffW8 = GemmSmem::kOffW8, kOffBar = GemmSmem::kOffBar;
+  constexpr int kXStages = GemmSmem<GU>::kXStages, kWStages = GemmSmem<GU>::kWStages;
+  constexpr int kOffW8 = GemmSmem<GU>::kOffW8, kOffBar = GemmSmem<GU>::kOffBar;
   using R = GemmRoles<GU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -747,12 +754,13 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
 
 cudaError_t gemm_set_attributes() {
   const void* ks[] = {(const void*)grouped_gemm_kernel<true, false>,
-                      (const void*)grouped_gemm_kernel<false, false>,
                       (const void*)grouped_gemm_kernel<true, true>,
+                      (const void*)grouped_gemm_kernel<false, false>,
                       (const void*)grouped_gemm_kernel<false, true>};
-  for (const void* k : ks) {
+  for (int i = 0; i < 4; ++i) {
+    const int bytes = i < 2 ? GemmSmem<true>::kBytes : GemmSmem<false>::kBytes;
     const cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem::kBytes);
+        cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -766,7 +774,8 @@ cudaError_t gemm_max_ctas(bool gate_up, int* n) {
       &per_sm,
       gate_up ? (const void*)grouped_gemm_kernel<true, false>
               : (const void*)grouped_gemm_kernel<false, false>,
-      gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads, GemmSmem::kBytes);
+      gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads,
+      gate_up ? GemmSmem<true>::kBytes : GemmSmem<false>::kBytes);
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   *n = per_sm * sms;
@@ -781,12 +790,14 @@ cudaError_t launch_grouped_gemm(bool gate_up, bool fp4, const GemmArgs& a, const
   const dim3 g(grid);
   if (gate_up) {
     const dim3 b(GemmRoles<true>::kThreads);
-    return fp4 ? launch_pdl(grouped_gemm_kernel<true, true>, g, b, GemmSmem::kBytes, s, a, tmX, tmW, tmWs)
-               : launch_pdl(grouped_gemm_kernel<true, false>, g, b, GemmSmem::kBytes, s, a, tmX, tmW, tmWs);
+    constexpr int sm = GemmSmem<true>::kBytes;
+    return fp4 ? launch_pdl(grouped_gemm_kernel<true, true>, g, b, sm, s, a, tmX, tmW, tmWs)
+               : launch_pdl(grouped_gemm_kernel<true, false>, g, b, sm, s, a, tmX, tmW, tmWs);
   }
   const dim3 b(GemmRoles<false>::kThreads);
-  return fp4 ? launch_pdl(grouped_gemm_kernel<false, true>, g, b, GemmSmem::kBytes, s, a, tmX, tmW, tmWs)
-             : launch_pdl(grouped_gemm_kernel<false, false>, g, b, GemmSmem::kBytes, s, a, tmX, tmW, tmWs);
+  constexpr int sm = GemmSmem<false>::kBytes;
+  return fp4 ? launch_pdl(grouped_gemm_kernel<false, true>, g, b, sm, s, a, tmX, tmW, tmWs)
+             : launch_pdl(grouped_gemm_kernel<false, false>, g, b, sm, s, a, tmX, tmW, tmWs);
 }
 
 // One thread per 16-byte piece of a packed tile: code chunk position p of tile row r (four per
