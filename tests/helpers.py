@@ -138,10 +138,19 @@ def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L,
         n_rows_d = 0
         if not acc_exact:
             A = L.arrs
-            ng = {n: nvfp4_row_norms(A["w_" + n], A["b_" + n]) for n in ("gate", "up", "down")}
-            if sh.Is:
-                ng.update({"sh_" + n: nvfp4_row_norms(A["sh_" + n], A["sh_b_" + n])
-                           for n in ("gate", "up", "down")})
+            norm_cache = {}
+
+            def wnorms(e):
+                """Row norms of (gate, up, down) of routed expert e, or of the shared expert
+                (e None), decoded once per expert the sample touches."""
+                if e not in norm_cache:
+                    if e is None:
+                        norm_cache[e] = [nvfp4_row_norms(A["sh_" + n], A["sh_b_" + n])
+                                         for n in ("gate", "up", "down")]
+                    else:
+                        norm_cache[e] = [nvfp4_row_norms(A["w_" + n][e], A["b_" + n][e])
+                                         for n in ("gate", "up", "down")]
+                return norm_cache[e]
             qn = np.sqrt((tp["qx"].astype(np.float64) ** 2).sum(1))
 
         def acc_ok(got, ref, bound):
@@ -155,11 +164,7 @@ def check_layer(sh: synth.LayerShape, x_cpu, logits_cpu, W_dev: dict, L,
                 if acc_exact:
                     bgu = bd = None
                 else:
-                    e = None if s == k else idx_o[t, s]
-                    pre = "sh_" if s == k else ""
-                    wn = [ng[pre + "gate"], ng[pre + "up"], ng[pre + "down"]]
-                    if e is not None:
-                        wn = [w[e] for w in wn]
+                    wn = wnorms(None if s == k else int(idx_o[t, s]))
                     bgu = qn[i] * np.stack([wn[0][:Ig], wn[1][:Ig]])
                     hn = np.sqrt((tp["hq"][i, s, :Ig].astype(np.float64) ** 2).sum())
                     wdn = wn[2]  # norms of the down rows

@@ -179,3 +179,17 @@ def test_nvfp4_stream_and_grouped_paths_agree():
         assert (ys - yg).abs().max().item() <= 1e-2 * yg.abs().max().item()
     finally:
         lay.close()
+
+
+def test_nvfp4_stress_dimensions_sampled():
+    # the stress layer's dimensions (H = 4096, I = 1024, shared 2048, top_k 8, Zipf 1.5) with
+    # 64 experts and 600 tokens on the grouped tensor-core GEMMs (several 128-row weight tiles
+    # per expert, 32 K stages); oracle parity on 12 sampled tokens
+    T, H, E, k, I, Is = 600, 4096, 64, 8, 1024, 2048
+    sh = synth.LayerShape(T=T, H=H, E=E, k=k, I=I, Is=Is)
+    d = synth.small_layer(T, H, E, k, I, Is, seed=380, zipf_s=1.5)
+    W_dev = synth.make_weights_nvfp4(sh, 380, device="cuda")
+    W = {n: v.cpu() for n, v in W_dev.items()}
+    sample = np.random.default_rng(380).choice(T, 12, replace=False)
+    check_layer(sh, d["x"], d["logits"], W_dev, oracle_layer_nvfp4(W, sh), sample=sample,
+                acc_exact=False)
