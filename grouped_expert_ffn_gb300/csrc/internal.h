@@ -135,7 +135,9 @@ struct PrepArgs {
   float* stok;                // [T]   or NULL
   int* sq_max;                // [2] row sum(q^2) maxima (gate/up rows, down rows), reset here
   int* err;
+  int* gbase = nullptr;       // [2][kMaxGroups + 1] item bases per group (gate/up, down)
 };
+constexpr int kMaxGroups = 257;  // routed experts (<= 256) + the shared expert
 cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s);
 
 // One layer's NVFP4 expert weights (the caller's arrays; see moe_weights_nvfp4).

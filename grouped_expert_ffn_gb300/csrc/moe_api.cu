@@ -42,6 +42,7 @@ struct moe_plan_s {
   int* n_groups = nullptr;
   int* sq_max = nullptr;  // [2] per-forward maxima of row sum(q^2): gate/up rows, down rows
   int* scan_ctr = nullptr;  // blocks of the routing/histogram kernel counted in (zero between calls)
+  int* gbase = nullptr;     // [2][kMaxGroups + 1] work-item bases of the groups
   int* err = nullptr;
   // taps
   int debug = 0;
@@ -315,6 +316,7 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   ALLOC(sq_max, 2);
   ALLOC(err, 1);
   ALLOC(scan_ctr, 1);
+  ALLOC(gbase, 2 * (kMaxGroups + 1));
 #undef ALLOC
   if (cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess ||
       cudaMemset(p->scan_ctr, 0, sizeof(int)) != cudaSuccess ||
@@ -627,6 +629,7 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   pa.tn_d = p->tn_d;
   pa.bmask = p->bmask;
   pa.bhist = p->bhist;
+  pa.gbase = p->gbase;
   pa.counts = p->counts;
   pa.offsets = p->offsets;
   pa.perm = p->perm;

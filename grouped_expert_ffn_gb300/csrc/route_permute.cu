@@ -3,15 +3,16 @@
 //  route_kernel      warp per token: top-k of the fp32 logits (ties to the lowest expert id),
 //                    softmax over the selected logits.
 //  route_hist_scan_kernel
-//                    per block of 64 tokens: the tokens' routing (when logits are given), one
+//                    per block of 32 tokens: the tokens' routing (when logits are given), one
 //                    64-bit token mask per expert (which of the block's tokens chose it; its
 //                    popcount is the block's histogram); the last block to finish runs the
 //                    scan: per-expert counts, exclusive prefixes over blocks and over experts,
-//                    and the grouped-GEMM work lists (expert-tile queue).
+//                    and each group's base in the grouped-GEMM work lists.
 //  scatter_kernel    block per token: per-token int8 quantisation of x, the codes written as
 //                    fp16 integers into every row the token occupies (one per routed slot plus
 //                    the shared expert's row) with 16-byte stores; row metadata; the token's
-//                    row of y zeroed (the down GEMM adds every row's output into it).
+//                    row of y zeroed (the down GEMM adds every row's output into it); and the
+//                    work items (expert-tile queue) of one group per block.
 // Row order: the shared expert's rows [0, T) first (row t = token t), then the routed
 // assignments grouped by expert id and, inside an expert, by token. This is the order a
 // stable sort of the flattened idx by expert id gives.
@@ -76,7 +77,6 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 // remainder.
 __device__ __forceinline__ void scan_block(const PrepArgs& a, int nblk) {
   __shared__ int s_cnt[257];
-  __shared__ int s_off[257];
   __shared__ int s_base_gu[258];
   __shared__ int s_base_d[258];
   __shared__ int s_warp[33];
@@ -130,13 +130,11 @@ __device__ __forceinline__ void scan_block(const PrepArgs& a, int nblk) {
   __syncthreads();
   // row offsets of the experts, and item bases of the groups (group g: shared when
   // g < has_shared, else expert g - has_shared)
-  const int T_sh = a.has_shared ? a.T : 0;
   const int ng = E + (a.has_shared ? 1 : 0);
   int total;
   const int ecnt = (int)threadIdx.x < E ? s_cnt[threadIdx.x] : 0;
   const int eoff = block_exclusive_scan(ecnt, s_warp, &total);
   if ((int)threadIdx.x < E) {
-    s_off[threadIdx.x] = eoff;
     a.offsets[threadIdx.x] = eoff;
   }
   if (threadIdx.x == 0) a.offsets[E] = total;
@@ -161,27 +159,37 @@ __device__ __forceinline__ void scan_block(const PrepArgs& a, int nblk) {
     a.n_items[1] = total;
   }
   __syncthreads();
-  // items, one per thread and pass: find the group by binary search over the bases
+  // the item bases of the groups; the scatter kernel writes the items from them
+  for (int i = threadIdx.x; i <= ng; i += blockDim.x) {
+    a.gbase[i] = s_base_gu[i];
+    a.gbase[kMaxGroups + 1 + i] = s_base_d[i];
+  }
+}
+
+// (t * cnt) / tt for 0 <= t <= tt, in 32-bit arithmetic when the product fits.
+__device__ __forceinline__ int tile_bound(int t, int cnt, int tt) {
+  return cnt <= 46340 ? (t * cnt) / tt : (int)(((long long)t * cnt) / tt);
+}
+
+// The gate/up and down work items of group g (shared when g < has_shared, else expert
+// g - has_shared), all threads of the block: per (128-row weight tile, token tile) pair,
+// ordered by weight tile, then token tile, so consecutive items of a large group reuse one
+// weight tile from L2. A group of cnt rows is split into ceil(cnt / TN) token tiles of equal
+// size (within one row), so no tile is a thin remainder.
+__device__ __forceinline__ void write_group_items(const PrepArgs& a, int g) {
+  const bool sh = a.has_shared && g == 0;
+  const int gid = sh ? a.E : g - a.has_shared;
+  const int cnt = sh ? a.T : a.counts[gid];
+  if (cnt == 0) return;
+  const int row0 = sh ? 0 : (a.has_shared ? a.T : 0) + a.offsets[gid];
   for (int list = 0; list < 2; ++list) {
-    const int* base = list == 0 ? s_base_gu : s_base_d;
-    const int n = base[ng];
     const int tn = list == 0 ? a.tn_gu : a.tn_d;
-    int4* items = list == 0 ? a.items_gu : a.items_d;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      int lo = 0, hi = ng - 1;  // last group with base <= i
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (base[mid] <= i) lo = mid; else hi = mid - 1;
-      }
-      const int gg = lo;
-      const bool sh = a.has_shared && gg == 0;
-      const int gid = sh ? E : gg - a.has_shared;
-      const int cnt = sh ? a.T : s_cnt[gid];
-      const int row0 = sh ? 0 : T_sh + s_off[gid];
-      const int tt = (cnt + tn - 1) / tn;
-      const int local = i - base[gg];
-      const int wt = local / tt, t = local % tt;
-      const int r0 = (int)((long long)t * cnt / tt), r1 = (int)((long long)(t + 1) * cnt / tt);
+    const int nwt = list == 0 ? 2 * (sh ? a.Is : a.I) / kBM : a.H / kBM;
+    int4* items = (list == 0 ? a.items_gu : a.items_d) + a.gbase[list * (kMaxGroups + 1) + g];
+    const int tt = (cnt + tn - 1) / tn;
+    for (int i = threadIdx.x; i < nwt * tt; i += blockDim.x) {
+      const int wt = i / tt, t = i - wt * tt;
+      const int r0 = tile_bound(t, cnt, tt), r1 = tile_bound(t + 1, cnt, tt);
       items[i] = make_int4(gid, row0 + r0, r1 - r0, wt * kBM);
     }
   }
@@ -238,9 +246,12 @@ __global__ void __launch_bounds__(1024) route_hist_scan_kernel(PrepArgs a, int n
 }
 
 // Block per token: quantise x[t] once, write its codes (fp16 integers) to each of its rows.
+// Block b also writes the work items of groups b, b + T, ... (the grouped GEMMs read them).
 __global__ void scatter_kernel(PrepArgs a) {
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
+  const int ng = a.E + (a.has_shared ? 1 : 0);
+  for (int g = blockIdx.x; g < ng; g += gridDim.x) write_group_items(a, g);
   const int t = blockIdx.x;
   const int H = a.H, k = a.k, E = a.E;
   const int T_sh = a.has_shared ? a.T : 0;
