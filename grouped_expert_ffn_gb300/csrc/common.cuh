@@ -381,7 +381,8 @@ constexpr int kMaxEPerLane = 8;  // E <= 256
 
 __device__ __forceinline__ void route_token_warp(const float* __restrict__ l, int E, int k,
                                                  int32_t* __restrict__ idx, float* __restrict__ w,
-                                                 int lane) {
+                                                 int lane, int* s_idx = nullptr,
+                                                 float* s_w = nullptr) {
   float v[kMaxEPerLane];
   bool taken[kMaxEPerLane];
 #pragma unroll
@@ -448,8 +449,11 @@ __device__ __forceinline__ void route_token_warp(const float* __restrict__ l, in
     if (j < k) z += ej;
   }
   if (lane < k) {
+    const float wl = ex / z;
     idx[lane] = my_e;
-    w[lane] = ex / z;
+    w[lane] = wl;
+    if (s_idx) s_idx[lane] = my_e;  // a shared-memory copy for the calling block
+    if (s_w) s_w[lane] = wl;
   }
 }
 

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(DecodeArgs a)
   __shared__ int s_cnt[256];
   __shared__ int s_off[257];
   __shared__ int s_idx[kDecodeMaxRows * 8];
+  __shared__ float s_wt[kDecodeMaxRows * 8];
   __shared__ int s_warp[kPrepThreads / 32];
   const int T = a.T, k = a.k, E = a.E;
   const int T_sh = a.has_shared ? T : 0;
@@ -131,12 +132,17 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(DecodeArgs a)
   if (a.logits) {  // the tokens' routing first (warp per token); idx, w = idx_out, w_out
     for (int t = warp; t < T; t += kPrepThreads / 32)
       route_token_warp(a.logits + (size_t)t * E, E, k, a.idx_out + (size_t)t * k,
-                       a.w_out + (size_t)t * k, lane);
-    __syncthreads();
+                       a.w_out + (size_t)t * k, lane, s_idx + t * k, s_wt + t * k);
+  } else {
+    for (int r = tid; r < T * k; r += blockDim.x) {
+      s_idx[r] = a.idx[r];
+      s_wt[r] = a.w[r];
+    }
   }
+  __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
   for (int r = tid; r < T * k; r += blockDim.x) {
-    int e = a.idx[r];
+    int e = s_idx[r];
     if (e < 0 || e >= E) {
       set_error(a.err, kErrDevice);
       e = 0;
@@ -196,7 +202,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(DecodeArgs a)
     a.perm[pos] = r;
     const int row = T_sh + pos;
     a.row_token[row] = t;
-    a.row_w[row] = a.w[r];
+    a.row_w[row] = s_wt[r];
   }
   if (a.has_shared && tid < T) {
     a.row_token[tid] = tid;

@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(1024) route_hist_scan_kernel(PrepArgs a, int n
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
   __shared__ unsigned long long s_mask[256];
+  __shared__ int s_idx[kTokPerBlk * 8];  // this block's routing (when computed here)
   __shared__ int s_last;
   const int T = a.T, k = a.k, E = a.E;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
@@ -213,13 +214,13 @@ __global__ void __launch_bounds__(1024) route_hist_scan_kernel(PrepArgs a, int n
   if (a.logits) {
     for (int tt = warp; tt < nt; tt += nwarps) {
       const size_t t = (size_t)(t0 + tt);
-      route_token_warp(a.logits + t * E, E, k, a.idx_out + t * k, a.w_out + t * k, lane);
+      route_token_warp(a.logits + t * E, E, k, a.idx_out + t * k, a.w_out + t * k, lane,
+                       s_idx + tt * k);
     }
   }
   __syncthreads();  // this block's routing and the cleared masks are visible to the block
-  const int32_t* idx = a.logits ? a.idx_out : a.idx;
   for (int r = threadIdx.x; r < nt * k; r += blockDim.x) {
-    const int e = idx[(size_t)t0 * k + r];
+    const int e = a.logits ? s_idx[r] : a.idx[(size_t)t0 * k + r];
     if (e < 0 || e >= E) {
       set_error(a.err, kErrDevice);
       continue;
