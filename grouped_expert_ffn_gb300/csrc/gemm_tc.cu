@@ -921,8 +921,14 @@ __device__ __forceinline__ float requant_row_loop(const float* __restrict__ h, i
 // Each warp takes kRequantRows consecutive rows and issues the loads of all of them before
 // reducing any; rows of up to 128 * kRegV values stay in registers. Small blocks of one row per
 // warp give many short waves, so that no second wave runs nearly alone.
-constexpr int kRequantRows = 1;
-constexpr int kRequantThreads = 256;
+#ifndef MOE_RQ_ROWS
+#define MOE_RQ_ROWS 1
+#endif
+#ifndef MOE_RQ_THREADS
+#define MOE_RQ_THREADS 256
+#endif
+constexpr int kRequantRows = MOE_RQ_ROWS;
+constexpr int kRequantThreads = MOE_RQ_THREADS;
 
 template <int kRegV>
 __global__ void __launch_bounds__(kRequantThreads) requant_kernel(
