@@ -36,12 +36,12 @@ METRIC = "MoE layer tokens/s (prefill) & µs/layer decode C=8; % int8/HBM roofli
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up GEMM launch on the
 # stacked-prefill layer (T=2600), from one ncu capture of the kernel as it is now. Set to None
 # whenever the kernel changes, until it is captured again.
-GU_TRAFFIC_BYTES = 400.4e6
+GU_TRAFFIC_BYTES = 400.9e6
 # Kernels one stacked-prefill layer launches: RMS pre-norm, router projection, and the
 # forward's routing + histogram + scan, scatter, gate/up GEMM, requantisation, down GEMM.
 LAUNCHES_PER_LAYER = 7
 # moe_forward's default dispatch threshold (T <= this runs the weight-streaming kernels).
-DEFAULT_DECODE_ROWS = 32
+DEFAULT_DECODE_ROWS = 24
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 

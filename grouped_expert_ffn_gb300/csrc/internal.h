@@ -33,11 +33,11 @@ constexpr int kAccCols = 384;
 constexpr int kTokPerBlk = 32;  // tokens per routing/histogram block (a 64-bit mask per expert holds them)
 // Largest T the deduplicated weight-streaming kernels take, and the default dispatch
 // threshold of a plan (T <= threshold runs them, larger T the grouped GEMMs). Measured on
-// GB300 for the 35B-A3B-shaped layer (H=2048, E=128, k=8, I=512, Zipf 1.1 routing, weights
-// streamed from HBM): streaming 66.8 us against grouped 76.0 us per layer at T=32, 97.7
-// against 81.2 at T=48.
+// GB300 for the 35B-A3B-shaped layer (H=2048, E=128, k=8, I=512, Zipf 1.1 routing, routing
+// inside the forward, weights streamed from HBM): streaming 67.7 us against grouped 73.6 us
+// per layer at T=24, 78.4 against 74.2 at T=32.
 constexpr int kDecodeMaxRows = 64;
-constexpr int kDecodeDefaultRows = 32;
+constexpr int kDecodeDefaultRows = 24;
 constexpr int kDecodeMaxH = 8192;  // largest H and intermediate size the decode kernels take
 constexpr int kDecodeMaxI = 4096;
 constexpr int kREB = 16;  // experts per router tensor-core tile (packed router weight block)

@@ -180,7 +180,7 @@ MOE_API moe_status moe_route(moe_plan_t plan, const float* logits, int T, int32_
  *   routing: idx[t,*] distinct, in [0, E)); y is overwritten. 1 <= T <= max_tokens: an
  *   empty batch (T = 0) is MOE_ERR_INVALID_ARG, a larger one MOE_ERR_CAPACITY, both
  *   returned before any work is queued.
- * T <= the plan's decode threshold (moe_plan_set_decode_rows; default 32) runs the
+ * T <= the plan's decode threshold (moe_plan_set_decode_rows; default 24) runs the
  * deduplicated weight-streaming decode kernels; larger T runs the grouped tensor-core GEMMs.
  * Both give identical integer accumulators. Allocates nothing, never
  * synchronises, and may be captured in a CUDA graph. The workspace is per plan: calls on
@@ -203,8 +203,9 @@ MOE_API moe_status moe_route_forward(moe_plan_t plan, moe_packed_t packed, const
 /* Dispatch threshold of moe_forward on this plan: T <= rows runs the weight-streaming decode
  * kernels (each unique expert's weights read once, rows applied 8 at a time), larger T the
  * grouped GEMMs. 0 <= rows <= 64 (else MOE_ERR_INVALID_ARG); 0 sends every call to the
- * grouped GEMMs. Default 32: measured on GB300 for a 35B-A3B-shaped layer, streaming is the
- * faster path up to T=32 and the grouped GEMMs from T=48. The crossover between the two paths is a measured property of the GPU and
+ * grouped GEMMs. Default 24: measured on GB300 for a 35B-A3B-shaped layer with the routing
+ * inside the forward, streaming is the faster path up to T=24 and the grouped GEMMs from
+ * T=32. The crossover between the two paths is a measured property of the GPU and
  * the layer shape (the page "[job] Strix Halo ... #145", "Done / measured", on the grouped
  * threshold), so it is a setting rather than a constant. Host-only; takes effect on the next
  * moe_forward. */
