@@ -377,9 +377,10 @@ __device__ __forceinline__ int warp_sum_i(int v) {
 // slots ordered by logit descending, then id ascending) and their softmax weights
 // exp(l_j - l_max) / sum_i exp(l_i - l_max), the sum taken in slot order. Lane j < k writes
 // slot j of idx[0..k) and w[0..k). Every lane of the warp must call it.
-constexpr int kMaxEPerLane = 8;  // E <= 256
+// Routing keeps E / 32 logits per lane in registers: 4 slots for E <= 128, 8 for E <= 256.
 
-__device__ __forceinline__ void route_token_warp(const float* __restrict__ l, int E, int k,
+template <int kMaxEPerLane>
+__device__ __forceinline__ void route_token_warp_n(const float* __restrict__ l, int E, int k,
                                                  int32_t* __restrict__ idx, float* __restrict__ w,
                                                  int lane, int* s_idx = nullptr,
                                                  float* s_w = nullptr) {
@@ -455,6 +456,18 @@ __device__ __forceinline__ void route_token_warp(const float* __restrict__ l, in
     if (s_idx) s_idx[lane] = my_e;  // a shared-memory copy for the calling block
     if (s_w) s_w[lane] = wl;
   }
+}
+
+// E <= 128 keeps 4 logits per lane (the top-k loop scans 4 register slots per round), larger
+// E (<= 256) 8.
+__device__ __forceinline__ void route_token_warp(const float* __restrict__ l, int E, int k,
+                                                 int32_t* __restrict__ idx, float* __restrict__ w,
+                                                 int lane, int* s_idx = nullptr,
+                                                 float* s_w = nullptr) {
+  if (E <= 128)
+    route_token_warp_n<4>(l, E, k, idx, w, lane, s_idx, s_w);
+  else
+    route_token_warp_n<8>(l, E, k, idx, w, lane, s_idx, s_w);
 }
 
 }  // namespace moe
