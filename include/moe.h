@@ -227,7 +227,8 @@ MOE_API const char* moe_status_string(moe_status s);
 
 /* ---- test taps: copies of intermediate results of the last moe_forward ----------------
  * moe_debug_enable(plan, 1) allocates tap buffers and makes later forwards also write the
- * accumulators (int32 with int8 weights, fp64 with NVFP4 weights) (it is the one call besides moe_plan/moe_pack_weights that allocates).
+ * accumulators: the int32 taps after a forward with int8 weights, the fp64 taps after one
+ * with NVFP4 weights (the other kind then holds no valid data) (it is the one call besides moe_plan/moe_pack_weights that allocates).
  * Rows are in the plan's row order: rows [0, T) are the shared expert's (row t = token t),
  * when I_shared > 0; then the routed assignments, grouped by expert id and, inside an
  * expert, by (token, slot) ascending. moe_debug_tap copies one tap to HOST memory

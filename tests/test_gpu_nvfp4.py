@@ -193,3 +193,30 @@ def test_nvfp4_stress_dimensions_sampled():
     sample = np.random.default_rng(380).choice(T, 12, replace=False)
     check_layer(sh, d["x"], d["logits"], W_dev, oracle_layer_nvfp4(W, sh), sample=sample,
                 acc_exact=False)
+
+
+def test_nvfp4_pack_argument_errors():
+    # host-side checks of moe_pack_weights_nvfp4: missing or misaligned arrays, and shared
+    # expert arrays missing on a plan with a shared expert
+    T, H, E, k, I, Is = 4, 256, 8, 2, 128, 64
+    sh, d, W = _layer(T, H, E, k, I, Is, seed=390)
+    Wd = weights_to(W, "cuda")
+    plan = moe.moe_plan(E, k, H, I, Is, T)
+    try:
+        bad = dict(Wd)
+        del bad["b_up"]
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_pack_weights_nvfp4(plan, bad)
+        assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+        bad = dict(Wd)
+        bad["w_down"] = Wd["w_down"].data_ptr() + 8  # not 16-byte aligned
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_pack_weights_nvfp4(plan, bad)
+        assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+        bad = {n: v for n, v in Wd.items() if not n.startswith("sh_")}
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_pack_weights_nvfp4(plan, bad)
+        assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+        assert moe.moe_get_error(plan) == 0
+    finally:
+        moe.moe_plan_destroy(plan)
