@@ -334,14 +334,15 @@ def layer_work(sh, counts=None):
     return ops, wbytes
 
 
-def measure_layer(moe, name, peaks, steps):
+def measure_layer(moe, name, peaks, steps, fmt="int8"):
     """One layer of a single-layer workload (the 256-token prefill chunk, the 8192-token
-    stress layer): routing once, then `steps` timed forwards (CUDA events on the stream);
-    tokens/s, microseconds per layer, and the layer's tensor and HBM roofline fractions."""
+    stress layer) with int8 or NVFP4 expert weights: routing once, then `steps` timed
+    forwards (CUDA events on the stream); tokens/s, microseconds per layer, and the layer's
+    tensor and HBM roofline fractions."""
     dev = torch.device("cuda")
     wl = synth.WORKLOADS[name]
     sh = wl.shape
-    W = synth.make_weights(sh, wl.seed, device=dev)
+    W = (synth.make_weights if fmt == "int8" else synth.make_weights_nvfp4)(sh, wl.seed, device=dev)
     x = synth.make_activations(sh.T, sh.H, wl.seed, wl.outliers, dev)
     lg = synth.make_logits(sh.T, sh.E, wl.seed, wl.zipf_s, dev)
     lay = moe.MoELayer(sh.E, sh.k, sh.H, sh.I, sh.Is, sh.T, W)
@@ -372,10 +373,15 @@ def measure_layer(moe, name, peaks, steps):
     finally:
         lay.close()
     ops, wbytes = layer_work(sh, counts)
+    if fmt == "nvfp4":  # the same experts at NVFP4 width
+        used = int((counts > 0).sum())
+        wbytes = used * synth.weight_bytes_per_expert_nvfp4(sh.H, sh.I) + \
+            (synth.weight_bytes_per_expert_nvfp4(sh.H, sh.Is) if sh.Is else 0)
     act_bytes = sh.T * sh.H * 2 + sh.T * sh.H * 4  # x in (bf16), y out (fp32)
     tf = ops / (us * 1e-6) / 1e12
     gbs = (wbytes + act_bytes) / (us * 1e-6) / 1e9
-    return {"workload": wl.note, "tokens_per_s": sh.T / (us * 1e-6), "us_per_layer": us,
+    return {"workload": wl.note + ("" if fmt == "int8" else ", NVFP4 expert weights"),
+            "tokens_per_s": sh.T / (us * 1e-6), "us_per_layer": us,
             "int_ops": ops, "achieved_tops": tf,
             "tensor_frac": tf / peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]),
             "hbm_bytes": wbytes + act_bytes, "achieved_gbs": gbs,
@@ -604,6 +610,7 @@ def run_ours(args, world, rank):
     if rank == 0 and not args.no_extra:
         extra["prefill_chunk_T256"] = measure_layer(moe, "prefill", peaks, args.steps)
         extra["stress_T8192"] = measure_layer(moe, "stress", peaks, args.steps)
+        extra["stress_T8192_nvfp4"] = measure_layer(moe, "stress", peaks, args.steps, fmt="nvfp4")
         extra["decode_crossover"] = measure_crossover(moe, plan, layers, H, E, k, args.steps, stream)
         if not args.no_decode:
             extra["decode_nvfp4"] = measure_decode_nvfp4(moe, plan, wl, n_layers, peaks, args.steps,
