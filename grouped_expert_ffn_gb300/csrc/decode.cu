@@ -20,6 +20,9 @@
 //  decode_down_kernel  (64 output channels of one unique expert) per block: stages up to 8 of
 //                      the expert's h code rows as int8 in shared memory per pass, streams 64
 //                      down rows, dp4a, and adds w * d into y.
+//  decode_gu_fp4_kernel, decode_down_fp4_kernel
+//                      the same two streams for NVFP4 expert weights (see "NVFP4 experts"
+//                      below): the codes expanded to int8 in registers, exact int64 sums.
 #include <algorithm>
 #include <type_traits>
 

@@ -11,7 +11,8 @@
  * N = TOP_K x 2 x IM_EXP). Batched decode and small batches (T <= 64 rows) deduplicate
  * experts across rows and stream each unique expert's int8 weights once with an int8 dot,
  * as the page "[job] Strix Halo: multi-session serving ... #145", section "Status", item
- * "Next" asks.
+ * "Next" asks. The expert weights may instead be NVFP4 (moe_pack_weights_nvfp4), the format
+ * the same page keeps for the routed experts; the activations stay int8.
  *
  * Conventions (every entry point):
  *  - Data pointers are DEVICE pointers unless a comment says host. Tensors are row-major
@@ -24,7 +25,7 @@
  *    range) set a sticky error word in the plan, read by moe_get_error. No entry point
  *    aborts, throws, or falls back to a CPU path.
  *  - Numerics: integer results (routing indices, permutation, int32 accumulators) are
- *    exact; floating point is fp32.
+ *    exact; floating point is fp32 (NVFP4 weights: see moe_pack_weights_nvfp4).
  */
 #ifndef MOE_H_
 #define MOE_H_
