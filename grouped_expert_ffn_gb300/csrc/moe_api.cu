@@ -610,6 +610,11 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
     e = launch_decode(a, s, prof_events(p, 1));
     return cuda_status(e);
   }
+  // token tiles: int8 weights take the plan's (sized so the exact 1024-K accumulator chunks
+  // fit TMEM); NVFP4 weights always use one accumulator, so the full tile
+  const bool fp4 = pk->fp4 != 0;
+  const int tn_gu = fp4 ? kMaxTokTile : p->tn_gu;
+  const int tn_d = fp4 ? kMaxTokTile : p->tn_d;
   PrepArgs pa;
   pa.idx = idx;
   pa.w = w;
@@ -625,8 +630,8 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   pa.I = p->I;
   pa.Is = p->Is;
   pa.has_shared = p->has_shared;
-  pa.tn_gu = p->tn_gu;
-  pa.tn_d = p->tn_d;
+  pa.tn_gu = tn_gu;
+  pa.tn_d = tn_d;
   pa.bmask = p->bmask;
   pa.bhist = p->bhist;
   pa.gbase = p->gbase;
@@ -670,7 +675,6 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   g.row_w = p->row_w;
   g.y = y;
   g.err = p->err;
-  const bool fp4 = pk->fp4 != 0;
   if (fp4) {  // matrix scales as per-row scales; taps fp64
     const size_t E = p->E, I = p->I, H = p->H, Is = p->Is;
     const float* rsh = pk->rs4 + 2 * E * I + E * H;
@@ -686,7 +690,7 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   g.n_items = p->n_items;
   g.K_r = p->H;
   g.K_s = p->H;
-  g.TN = p->tn_gu;
+  g.TN = tn_gu;
   g.tap = p->debug && !fp4 ? p->tap_gu : nullptr;
   g.tap_f64 = p->debug && fp4 ? reinterpret_cast<double*>(p->tap_gu) : nullptr;
   g.row_sq_max = p->sq_max;
@@ -708,7 +712,7 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   g.n_items = p->n_items + 1;
   g.K_r = p->I;
   g.K_s = p->has_shared ? p->Is : p->I;
-  g.TN = p->tn_d;
+  g.TN = tn_d;
   g.tap = p->debug && !fp4 ? p->tap_d : nullptr;
   g.tap_f64 = p->debug && fp4 ? reinterpret_cast<double*>(p->tap_d) : nullptr;
   g.row_sq_max = p->sq_max + 1;
