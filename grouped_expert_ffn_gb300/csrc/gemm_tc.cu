@@ -258,7 +258,7 @@ __device__ __forceinline__ int acc_i(int x) { return x; }
 // arithmetic (the total may exceed what fp32 holds exactly) and v is the int32 sums.
 template <int kColGroups, typename Store>
 __device__ __forceinline__ void epilogue_columns(const GemmArgs& a, int nch, uint32_t tbase,
-                                                 int cg, int ncols, Store&& store) {
+                                                 int cg, int ncols, int TN, Store&& store) {
   if (nch == 1) {
     uint32_t ra[16], rb[16];
     auto emit = [&](const uint32_t (&r)[16], int c, int j) {
@@ -295,7 +295,7 @@ __device__ __forceinline__ void epilogue_columns(const GemmArgs& a, int nch, uin
 #pragma unroll 1
     for (int kc = 0; kc < nch; ++kc) {
       uint32_t r[16];
-      tmem_ld16(tbase + kc * a.TN + c0, r);
+      tmem_ld16(tbase + kc * TN + c0, r);
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] += __float2int_rn(__uint_as_float(r[i]));
@@ -325,12 +325,13 @@ __device__ __forceinline__ void load_meta_gate_up(const GemmArgs& a, int4 wi, in
 
 template <bool FP4>
 __device__ __forceinline__ void epilogue_gate_up(const GemmArgs& a, int4 wi, int nch,
-                                                 uint32_t tbase, int cg, const EpiMeta<true>& m) {
+                                                 uint32_t tbase, int cg, int TN,
+                                                 const EpiMeta<true>& m) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const bool odd = lane & 1;
   const int ch = (wi.w >> 1) + q * 16 + (lane >> 1);
   const int ncols = wi.z;
-  epilogue_columns<GemmRoles<true>::kColGroups>(a, nch, tbase, cg, ncols,
+  epilogue_columns<GemmRoles<true>::kColGroups>(a, nch, tbase, cg, ncols, TN,
                                                 [&](const auto& v, int c0, int j) {
     using V = typename std::remove_cv<typename std::remove_reference<decltype(v[0])>::type>::type;
     V recv[8];
@@ -417,7 +418,7 @@ __device__ __forceinline__ void load_meta_down(const GemmArgs& a, int4 wi, int c
 
 template <bool FP4>
 __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nch, uint32_t tbase,
-                                              int cg, const EpiMeta<false>& m) {
+                                              int cg, int TN, const EpiMeta<false>& m) {
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
   const int o = wi.w + q * 32 + lane;
   const int ncols = wi.z;
@@ -426,7 +427,7 @@ __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nc
   float sw[4];                // weight-row scales of the quad's channels o - b + i
 #pragma unroll
   for (int i = 0; i < 4; ++i) sw[i] = __shfl_sync(0xffffffffu, m.s0, (lane & ~3) + i);
-  epilogue_columns<GemmRoles<false>::kColGroups>(a, nch, tbase, cg, ncols,
+  epilogue_columns<GemmRoles<false>::kColGroups>(a, nch, tbase, cg, ncols, TN,
                                                  [&](const auto& v, int c0, int j) {
     using V = typename std::remove_cv<typename std::remove_reference<decltype(v[0])>::type>::type;
     if (FP4 && a.tap_f64) {
@@ -517,15 +518,20 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
   pdl_wait();
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
-  const int n_items = *a.n_items;
   // Accumulator layout for this launch: one accumulator over the whole K (two TMEM slots,
   // double-buffered) when the bound proves it exact, else 1024-K chunks (the host sizes the
   // token tile so that the chunks of one tile fit the accumulator columns).
   // NVFP4 weights: one fp32 accumulator over the whole K (the products are not integers,
   // the sum is rounded as the tensor core accumulates it)
   const bool single = FP4 || single_accumulator_exact(a);
+  // the work list in the token tiles this accumulator layout fits (every CTA and role
+  // takes the same one)
+  const bool main_list = single || a.items_c == nullptr;
+  const int4* __restrict__ items = main_list ? a.items : a.items_c;
+  const int n_items = main_list ? *a.n_items : *a.n_items_c;
+  const int TN = main_list ? a.TN : a.TN_c;
   const int kmax = a.K_r > a.K_s ? a.K_r : a.K_s;
-  const int slot_cols = single ? a.TN : ((kmax + kChunkK - 1) / kChunkK) * a.TN;
+  const int slot_cols = single ? TN : ((kmax + kChunkK - 1) / kChunkK) * TN;
   const int nslots = slot_cols <= kAccCols / 2 ? 2 : 1;
   const int kpc = single ? (1 << 30) : kChunkK / kKS;  // stages per accumulator
 
@@ -545,7 +551,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       const uint64_t pol_first = l2_policy_evict_first();  // weights: read once
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const int4 wi = a.items[item];
+        const int4 wi = items[item];
         const bool shared = wi.x == a.E;
         const int nks = ((shared ? a.K_s : a.K_r) + kKS - 1) / kKS;
         const int rows = (wi.z + kXStep - 1) / kXStep * kXStep;  // box height
@@ -619,7 +625,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
                         (uint32_t)(kAccCols + 32 * h);
     uint32_t o[32];
     int item = blockIdx.x, kb = 0;
-    int nks = item < n_items ? ((a.items[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS : 0;
+    int nks = item < n_items ? ((items[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS : 0;
     uint32_t ks = 0;
     // widen stage k's half into o and release the int8 tile
     auto load = [&](uint32_t k) -> bool {
@@ -657,7 +663,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
         kb = 0;
         item += gridDim.x;
         if (item >= n_items) break;
-        nks = ((a.items[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
+        nks = ((items[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
       }
       ok = load(ks);
     }
@@ -677,7 +683,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++it) {
-        const int4 wi = a.items[item];
+        const int4 wi = items[item];
         const int nks = ((wi.x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
         const int n_mma = (wi.z + 15) & ~15;
         const uint32_t idesc = idesc_f16_f32(kBM, n_mma);
@@ -702,7 +708,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
                                smem_u32(&afull[kn & 1]), (kn >> 1) & 1u);
           if (++kin == kpc) {
             kin = 0;
-            dt += (uint32_t)a.TN;
+            dt += (uint32_t)TN;
           }
           if (++xs == kXStages) xs = 0;
         }
@@ -721,7 +727,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     int it = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
-      const int4 wi = a.items[item];
+      const int4 wi = items[item];
       const int K = wi.x == a.E ? a.K_s : a.K_r;
       const int nch = single ? 1 : (K + kChunkK - 1) / kChunkK;
       const int slot = it % nslots;
@@ -735,9 +741,9 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = lane_base + (uint32_t)(slot * slot_cols);
       if constexpr (GU)
-        epilogue_gate_up<FP4>(a, wi, nch, tbase, cg, m);
+        epilogue_gate_up<FP4>(a, wi, nch, tbase, cg, TN, m);
       else
-        epilogue_down<FP4>(a, wi, nch, tbase, cg, m);
+        epilogue_down<FP4>(a, wi, nch, tbase, cg, TN, m);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[slot]);

@@ -51,6 +51,12 @@ struct GemmArgs {
   const int* n_items;
   int E;
   int TN;                // token tile (items have rows <= TN)
+  // The same work in token tiles of TN_c rows, for a launch whose exactness bound fails and
+  // takes 1024-K accumulator chunks (which fit TMEM only with the smaller tile); NULL when
+  // TN_c == TN.
+  const int4* items_c = nullptr;
+  const int* n_items_c = nullptr;
+  int TN_c = 0;
   int K_r, K_s;          // reduction length of routed / shared groups
   int I, Is, Imax, H;
   // gate/up epilogue
@@ -117,15 +123,17 @@ struct PrepArgs {
   float* w_out = nullptr;
   int* scan_ctr = nullptr;        // one zero-initialised counter, left at zero
   const uint16_t* x;
-  int T, k, E, H, I, Is, has_shared, tn_gu, tn_d;
+  int T, k, E, H, I, Is, has_shared;
   unsigned long long* bmask;  // [nblk, E]
   int* bhist;                 // [nblk, E]
   int* counts;                // [E]
   int* offsets;               // [E + 1]
   int* perm;                  // [T*k]
-  int4* items_gu;
-  int4* items_d;
-  int* n_items;               // [2]
+  // work lists: 0 gate/up, 1 down (token tiles tn[0], tn[1]); 2, 3 the same in the smaller
+  // tiles of the exact chunked accumulation (items[l] NULL: list not built)
+  int tn[4];
+  int4* items[4];
+  int* n_items;               // [4]
   __half* xq;                 // [R, H] activation codes as fp16 integers, row order
   float* sx;                  // [R]
   int* row_token;             // [R]
@@ -135,7 +143,7 @@ struct PrepArgs {
   float* stok;                // [T]   or NULL
   int* sq_max;                // [2] row sum(q^2) maxima (gate/up rows, down rows), reset here
   int* err;
-  int* gbase = nullptr;       // [2][kMaxGroups + 1] item bases per group (gate/up, down)
+  int* gbase = nullptr;       // [4][kMaxGroups + 1] item bases per group and list
 };
 constexpr int kMaxGroups = 257;  // routed experts (<= 256) + the shared expert
 cudaError_t launch_prefill_prep(const PrepArgs& a, cudaStream_t s);

@@ -16,10 +16,12 @@ using namespace moe;
 struct moe_plan_s {
   int E = 0, k = 0, H = 0, I = 0, Is = 0, max_tokens = 0, Imax = 0, has_shared = 0;
   int device = 0, num_sms = 0;
-  int tn_gu = 0, tn_d = 0;  // token tiles of the two GEMMs
+  // token tiles of the two GEMMs with the exact chunked accumulation (fit TMEM with its 1024-K
+  // chunks); with one accumulator over the whole K both take kMaxTokTile rows
+  int tn_gu = 0, tn_d = 0;
   int grid_gu = 0, grid_d = 0;
   size_t R_max = 0;
-  int max_items_gu = 0, max_items_d = 0;
+  int max_items[4] = {0, 0, 0, 0};  // work lists: gate/up, down, and both in the chunked tiles
   // workspace (device)
   __half* xq = nullptr;  // [R, H] activation codes (fp16 integers) in row order
   float* sx = nullptr;
@@ -33,8 +35,7 @@ struct moe_plan_s {
   int* perm = nullptr;
   unsigned long long* bmask = nullptr;
   int* bhist = nullptr;
-  int4* items_gu = nullptr;
-  int4* items_d = nullptr;
+  int4* items[4] = {nullptr, nullptr, nullptr, nullptr};  // lists 2, 3 only when tn < kMaxTokTile
   int* n_items = nullptr;
   int8_t* qtok = nullptr;
   float* stok = nullptr;
@@ -286,8 +287,10 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   auto tiles = [&](int tn) {
     return (T * top_k + (size_t)(tn - 1) * E) / tn + (p->has_shared ? (T + tn - 1) / tn : 0) + 1;
   };
-  p->max_items_gu = (int)(tiles(p->tn_gu) * (2 * p->Imax / kBM));
-  p->max_items_d = (int)(tiles(p->tn_d) * (H / kBM));
+  p->max_items[0] = (int)(tiles(kMaxTokTile) * (2 * p->Imax / kBM));
+  p->max_items[1] = (int)(tiles(kMaxTokTile) * (H / kBM));
+  if (p->tn_gu < kMaxTokTile) p->max_items[2] = (int)(tiles(p->tn_gu) * (2 * p->Imax / kBM));
+  if (p->tn_d < kMaxTokTile) p->max_items[3] = (int)(tiles(p->tn_d) * (H / kBM));
   moe_status st = MOE_OK;
 #define ALLOC(ptr, n)                                  \
   if ((st = dalloc(p, &p->ptr, (n))) != MOE_OK) {      \
@@ -306,9 +309,9 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   ALLOC(perm, T * top_k);
   ALLOC(bmask, nblk * E);
   ALLOC(bhist, nblk * E);
-  ALLOC(items_gu, (size_t)p->max_items_gu);
-  ALLOC(items_d, (size_t)p->max_items_d);
-  ALLOC(n_items, 2);
+  for (int l = 0; l < 4; ++l)
+    if (p->max_items[l] > 0) ALLOC(items[l], (size_t)p->max_items[l]);
+  ALLOC(n_items, 4);
   ALLOC(qtok, T * H);
   ALLOC(stok, T);
   ALLOC(groups, (size_t)E + 1);
@@ -316,7 +319,7 @@ moe_status moe_plan(int E, int top_k, int H, int I, int I_shared, int max_tokens
   ALLOC(sq_max, 2);
   ALLOC(err, 1);
   ALLOC(scan_ctr, 1);
-  ALLOC(gbase, 2 * (kMaxGroups + 1));
+  ALLOC(gbase, 4 * (kMaxGroups + 1));
 #undef ALLOC
   if (cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess ||
       cudaMemset(p->scan_ctr, 0, sizeof(int)) != cudaSuccess ||
@@ -610,11 +613,11 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
     e = launch_decode(a, s, prof_events(p, 1));
     return cuda_status(e);
   }
-  // token tiles: int8 weights take the plan's (sized so the exact 1024-K accumulator chunks
-  // fit TMEM); NVFP4 weights always use one accumulator, so the full tile
+  // work lists: in full token tiles for one accumulator over the whole K; for int8 weights
+  // also in the plan's smaller tiles when the exact chunked accumulation needs them (the
+  // GEMMs pick one at launch from the exactness bound); NVFP4 weights always take one
+  // accumulator
   const bool fp4 = pk->fp4 != 0;
-  const int tn_gu = fp4 ? kMaxTokTile : p->tn_gu;
-  const int tn_d = fp4 ? kMaxTokTile : p->tn_d;
   PrepArgs pa;
   pa.idx = idx;
   pa.w = w;
@@ -630,16 +633,16 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
   pa.I = p->I;
   pa.Is = p->Is;
   pa.has_shared = p->has_shared;
-  pa.tn_gu = tn_gu;
-  pa.tn_d = tn_d;
+  pa.tn[0] = pa.tn[1] = kMaxTokTile;
+  pa.tn[2] = p->tn_gu;
+  pa.tn[3] = p->tn_d;
+  for (int l = 0; l < 4; ++l) pa.items[l] = (l >= 2 && fp4) ? nullptr : p->items[l];
   pa.bmask = p->bmask;
   pa.bhist = p->bhist;
   pa.gbase = p->gbase;
   pa.counts = p->counts;
   pa.offsets = p->offsets;
   pa.perm = p->perm;
-  pa.items_gu = p->items_gu;
-  pa.items_d = p->items_d;
   pa.n_items = p->n_items;
   pa.xq = p->xq;
   pa.sx = p->sx;
@@ -686,11 +689,14 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
     g.sh_s_d = p->has_shared ? rsh + 2 * Is : nullptr;
   }
   // gate/up: K = H for every group
-  g.items = p->items_gu;
+  g.items = p->items[0];
   g.n_items = p->n_items;
+  g.items_c = pa.items[2];
+  g.n_items_c = p->n_items + 2;
+  g.TN_c = p->tn_gu;
   g.K_r = p->H;
   g.K_s = p->H;
-  g.TN = tn_gu;
+  g.TN = kMaxTokTile;
   g.tap = p->debug && !fp4 ? p->tap_gu : nullptr;
   g.tap_f64 = p->debug && fp4 ? reinterpret_cast<double*>(p->tap_gu) : nullptr;
   g.row_sq_max = p->sq_max;
@@ -708,11 +714,14 @@ static moe_status forward_impl(moe_plan_t p, moe_packed_t pk, const uint16_t* x,
     return cuda_status(e);
   if (ev) cudaEventRecord(ev[3], s);
   // down: K = I (routed) or I_shared (shared)
-  g.items = p->items_d;
+  g.items = p->items[1];
   g.n_items = p->n_items + 1;
+  g.items_c = pa.items[3];
+  g.n_items_c = p->n_items + 3;
+  g.TN_c = p->tn_d;
   g.K_r = p->I;
   g.K_s = p->has_shared ? p->Is : p->I;
-  g.TN = tn_d;
+  g.TN = kMaxTokTile;
   g.tap = p->debug && !fp4 ? p->tap_d : nullptr;
   g.tap_f64 = p->debug && fp4 ? reinterpret_cast<double*>(p->tap_d) : nullptr;
   g.row_sq_max = p->sq_max + 1;

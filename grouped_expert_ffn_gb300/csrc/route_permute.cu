@@ -77,8 +77,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 // remainder.
 __device__ __forceinline__ void scan_block(const PrepArgs& a, int nblk) {
   __shared__ int s_cnt[257];
-  __shared__ int s_base_gu[258];
-  __shared__ int s_base_d[258];
+  __shared__ int s_base[4][258];
   __shared__ int s_warp[33];
   const int E = a.E;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
@@ -138,31 +137,30 @@ __device__ __forceinline__ void scan_block(const PrepArgs& a, int nblk) {
     a.offsets[threadIdx.x] = eoff;
   }
   if (threadIdx.x == 0) a.offsets[E] = total;
+  // item counts of every group in each work list (l = 0 gate/up, 1 down, 2 and 3 the same
+  // in the chunked accumulation's token tiles), their exclusive prefixes = the groups' bases
   const int g = threadIdx.x;
-  int ngu = 0, nd = 0;
-  if (g < ng) {
-    const bool sh = a.has_shared && g == 0;
-    const int cnt = sh ? a.T : s_cnt[g - a.has_shared];
-    ngu = (2 * (sh ? a.Is : a.I)) / kBM * ((cnt + a.tn_gu - 1) / a.tn_gu);
-    nd = a.H / kBM * ((cnt + a.tn_d - 1) / a.tn_d);
-  }
-  const int bgu = block_exclusive_scan(ngu, s_warp, &total);
-  if (g < ng) s_base_gu[g] = bgu;
-  if (threadIdx.x == 0) {
-    s_base_gu[ng] = total;
-    a.n_items[0] = total;
-  }
-  const int bd = block_exclusive_scan(nd, s_warp, &total);
-  if (g < ng) s_base_d[g] = bd;
-  if (threadIdx.x == 0) {
-    s_base_d[ng] = total;
-    a.n_items[1] = total;
+  for (int l = 0; l < 4; ++l) {
+    if (!a.items[l]) continue;  // uniform over the block
+    int n = 0;
+    if (g < ng) {
+      const bool sh = a.has_shared && g == 0;
+      const int cnt = sh ? a.T : s_cnt[g - a.has_shared];
+      const int nwt = l % 2 == 0 ? 2 * (sh ? a.Is : a.I) / kBM : a.H / kBM;
+      n = nwt * ((cnt + a.tn[l] - 1) / a.tn[l]);
+    }
+    const int base = block_exclusive_scan(n, s_warp, &total);
+    if (g < ng) s_base[l][g] = base;
+    if (threadIdx.x == 0) {
+      s_base[l][ng] = total;
+      a.n_items[l] = total;
+    }
   }
   __syncthreads();
   // the item bases of the groups; the scatter kernel writes the items from them
-  for (int i = threadIdx.x; i <= ng; i += blockDim.x) {
-    a.gbase[i] = s_base_gu[i];
-    a.gbase[kMaxGroups + 1 + i] = s_base_d[i];
+  for (int l = 0; l < 4; ++l) {
+    if (!a.items[l]) continue;
+    for (int i = threadIdx.x; i <= ng; i += blockDim.x) a.gbase[l * (kMaxGroups + 1) + i] = s_base[l][i];
   }
 }
 
@@ -171,8 +169,8 @@ __device__ __forceinline__ int tile_bound(int t, int cnt, int tt) {
   return cnt <= 46340 ? (t * cnt) / tt : (int)(((long long)t * cnt) / tt);
 }
 
-// The gate/up and down work items of group g (shared when g < has_shared, else expert
-// g - has_shared), all threads of the block: per (128-row weight tile, token tile) pair,
+// The work items of group g (shared when g < has_shared, else expert g - has_shared) in every
+// list that is built, all threads of the block: per (128-row weight tile, token tile) pair,
 // ordered by weight tile, then token tile, so consecutive items of a large group reuse one
 // weight tile from L2. A group of cnt rows is split into ceil(cnt / TN) token tiles of equal
 // size (within one row), so no tile is a thin remainder.
@@ -182,10 +180,11 @@ __device__ __forceinline__ void write_group_items(const PrepArgs& a, int g) {
   const int cnt = sh ? a.T : a.counts[gid];
   if (cnt == 0) return;
   const int row0 = sh ? 0 : (a.has_shared ? a.T : 0) + a.offsets[gid];
-  for (int list = 0; list < 2; ++list) {
-    const int tn = list == 0 ? a.tn_gu : a.tn_d;
-    const int nwt = list == 0 ? 2 * (sh ? a.Is : a.I) / kBM : a.H / kBM;
-    int4* items = (list == 0 ? a.items_gu : a.items_d) + a.gbase[list * (kMaxGroups + 1) + g];
+  for (int list = 0; list < 4; ++list) {
+    if (!a.items[list]) continue;
+    const int tn = a.tn[list];
+    const int nwt = list % 2 == 0 ? 2 * (sh ? a.Is : a.I) / kBM : a.H / kBM;
+    int4* items = a.items[list] + a.gbase[list * (kMaxGroups + 1) + g];
     const int tt = (cnt + tn - 1) / tn;
     for (int i = threadIdx.x; i < nwt * tt; i += blockDim.x) {
       const int wt = i / tt, t = i - wt * tt;

@@ -466,6 +466,38 @@ def test_adversarial_rows_take_the_exact_chunked_path():
     assert np.abs(gu).max() == 2048 * 127 * 127
 
 
+def test_adversarial_rows_take_the_chunked_lists_at_k_4096():
+    # H = I = 4096: with one accumulator the GEMMs take 192-row token tiles, but the exact
+    # 1024-K chunked accumulation fits TMEM only with 96-row tiles, so the routing step also
+    # builds both work lists in 96-row tiles and the GEMMs switch to them when the exactness
+    # bound fails. Constant token rows (codes +-127) and an expert whose gate, up and down rows
+    # are all 127 make the gate accumulators reach 4096 * 127^2 and the down accumulators pass
+    # 2^24, so both GEMMs must take the chunked lists; every int32 stays bit-exact.
+    sh = synth.LayerShape(T=40, H=4096, E=4, k=2, I=4096, Is=0)
+    d = synth.small_layer(sh.T, sh.H, sh.E, sh.k, sh.I, sh.Is, seed=33)
+    W = d["weights"]
+    W["w_gate"][0] = 127
+    W["w_up"][0] = 127
+    W["w_down"][0] = 127
+    x = d["x"].float()
+    x[:20] = 0.75
+    x[20:30] = -2.0
+    x = x.to(torch.bfloat16)
+    lg = d["logits"].clone()
+    lg[:, 0] += 10.0                  # every token routes to expert 0
+    Wd = weights_to(W, "cuda")
+    layer = moe.MoELayer(sh.E, sh.k, sh.H, sh.I, sh.Is, sh.T, Wd)
+    try:
+        moe.moe_plan_set_decode_rows(layer.plan, 0)  # the grouped GEMMs
+        st = check_layer(sh, x, lg, Wd, oracle_layer(W, sh), layer=layer,
+                         sample=np.arange(0, sh.T, 3))
+    finally:
+        layer.close()
+    assert np.abs(st["tap"]["acc_gu"]).max() == 4096 * 127 * 127
+    # the h codes vary with the channels' weight scales, but the down sums still pass 2^24
+    assert np.abs(st["tap"]["acc_d"]).max() > 1 << 24
+
+
 @pytest.mark.parametrize("T", [2600, 77])
 def test_router_tensor_core_projection(T):
     # bf16 x against the exact three-part bf16 split of the fp32 router weight: within the
