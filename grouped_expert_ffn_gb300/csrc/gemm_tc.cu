@@ -457,7 +457,9 @@ __device__ __forceinline__ void epilogue_down(const GemmArgs& a, int4 wi, int nc
   });
 }
 
-template <bool GU, bool FP4>
+// DUAL: the launch has a second work list in the chunked accumulation's smaller token tiles
+// (int8 weights with K > 2048); without one the list and tile are the parameters' own.
+template <bool GU, bool FP4, bool DUAL>
 __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     grouped_gemm_kernel(const GemmArgs a, const __grid_constant__ XMaps tmX,
                         const __grid_constant__ CUtensorMap tmW,
@@ -526,12 +528,14 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
   const bool single = FP4 || single_accumulator_exact(a);
   // the work list in the token tiles this accumulator layout fits (every CTA and role
   // takes the same one)
-  const bool main_list = single || a.items_c == nullptr;
-  const int4* __restrict__ items = main_list ? a.items : a.items_c;
+  // (selected from the parameters at each use rather than held in registers: the roles are
+  // at their register limits)
+  const bool main_list = !DUAL || single;
+#define KITEMS (main_list ? a.items : a.items_c)
   const int n_items = main_list ? *a.n_items : *a.n_items_c;
-  const int TN = main_list ? a.TN : a.TN_c;
+#define KTN (main_list ? a.TN : a.TN_c)
   const int kmax = a.K_r > a.K_s ? a.K_r : a.K_s;
-  const int slot_cols = single ? TN : ((kmax + kChunkK - 1) / kChunkK) * TN;
+  const int slot_cols = single ? KTN : ((kmax + kChunkK - 1) / kChunkK) * KTN;
   const int nslots = slot_cols <= kAccCols / 2 ? 2 : 1;
   const int kpc = single ? (1 << 30) : kChunkK / kKS;  // stages per accumulator
 
@@ -551,7 +555,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       const uint64_t pol_first = l2_policy_evict_first();  // weights: read once
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const int4 wi = items[item];
+        const int4 wi = KITEMS[item];
         const bool shared = wi.x == a.E;
         const int nks = ((shared ? a.K_s : a.K_r) + kKS - 1) / kKS;
         const int rows = (wi.z + kXStep - 1) / kXStep * kXStep;  // box height
@@ -625,7 +629,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
                         (uint32_t)(kAccCols + 32 * h);
     uint32_t o[32];
     int item = blockIdx.x, kb = 0;
-    int nks = item < n_items ? ((items[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS : 0;
+    int nks = item < n_items ? ((KITEMS[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS : 0;
     uint32_t ks = 0;
     // widen stage k's half into o and release the int8 tile
     auto load = [&](uint32_t k) -> bool {
@@ -663,7 +667,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
         kb = 0;
         item += gridDim.x;
         if (item >= n_items) break;
-        nks = ((items[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
+        nks = ((KITEMS[item].x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
       }
       ok = load(ks);
     }
@@ -683,7 +687,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++it) {
-        const int4 wi = items[item];
+        const int4 wi = KITEMS[item];
         const int nks = ((wi.x == a.E ? a.K_s : a.K_r) + kKS - 1) / kKS;
         const int n_mma = (wi.z + 15) & ~15;
         const uint32_t idesc = idesc_f16_f32(kBM, n_mma);
@@ -708,7 +712,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
                                smem_u32(&afull[kn & 1]), (kn >> 1) & 1u);
           if (++kin == kpc) {
             kin = 0;
-            dt += (uint32_t)TN;
+            dt += (uint32_t)KTN;
           }
           if (++xs == kXStages) xs = 0;
         }
@@ -727,7 +731,7 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
     int it = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
-      const int4 wi = items[item];
+      const int4 wi = KITEMS[item];
       const int K = wi.x == a.E ? a.K_s : a.K_r;
       const int nch = single ? 1 : (K + kChunkK - 1) / kChunkK;
       const int slot = it % nslots;
@@ -741,9 +745,9 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = lane_base + (uint32_t)(slot * slot_cols);
       if constexpr (GU)
-        epilogue_gate_up<FP4>(a, wi, nch, tbase, cg, TN, m);
+        epilogue_gate_up<FP4>(a, wi, nch, tbase, cg, KTN, m);
       else
-        epilogue_down<FP4>(a, wi, nch, tbase, cg, TN, m);
+        epilogue_down<FP4>(a, wi, nch, tbase, cg, KTN, m);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[slot]);
@@ -756,15 +760,19 @@ __global__ void __launch_bounds__(GemmRoles<GU>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+#undef KITEMS
+#undef KTN
 }
 
 cudaError_t gemm_set_attributes() {
-  const void* ks[] = {(const void*)grouped_gemm_kernel<true, false>,
-                      (const void*)grouped_gemm_kernel<true, true>,
-                      (const void*)grouped_gemm_kernel<false, false>,
-                      (const void*)grouped_gemm_kernel<false, true>};
-  for (int i = 0; i < 4; ++i) {
-    const int bytes = i < 2 ? GemmSmem<true>::kBytes : GemmSmem<false>::kBytes;
+  const void* ks[] = {(const void*)grouped_gemm_kernel<true, false, false>,
+                      (const void*)grouped_gemm_kernel<true, false, true>,
+                      (const void*)grouped_gemm_kernel<true, true, false>,
+                      (const void*)grouped_gemm_kernel<false, false, false>,
+                      (const void*)grouped_gemm_kernel<false, false, true>,
+                      (const void*)grouped_gemm_kernel<false, true, false>};
+  for (int i = 0; i < 6; ++i) {
+    const int bytes = i < 3 ? GemmSmem<true>::kBytes : GemmSmem<false>::kBytes;
     const cudaError_t e =
         cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
@@ -778,8 +786,8 @@ cudaError_t gemm_max_ctas(bool gate_up, int* n) {
   int per_sm = 0, dev = 0, sms = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &per_sm,
-      gate_up ? (const void*)grouped_gemm_kernel<true, false>
-              : (const void*)grouped_gemm_kernel<false, false>,
+      gate_up ? (const void*)grouped_gemm_kernel<true, false, false>
+              : (const void*)grouped_gemm_kernel<false, false, false>,
       gate_up ? GemmRoles<true>::kThreads : GemmRoles<false>::kThreads,
       gate_up ? GemmSmem<true>::kBytes : GemmSmem<false>::kBytes);
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
@@ -792,18 +800,21 @@ cudaError_t launch_grouped_gemm(bool gate_up, bool fp4, const GemmArgs& a, const
                                 const CUtensorMap& tmW, const CUtensorMap& tmWs, int grid,
                                 cudaStream_t s) {
   if (grid < 1) return cudaErrorInvalidValue;
-  if (fp4 && (!a.w4 || a.rows_r % kBM || a.rows_s % kBM)) return cudaErrorInvalidValue;
+  if (fp4 && (!a.w4 || a.rows_r % kBM || a.rows_s % kBM || a.items_c)) return cudaErrorInvalidValue;
+  const bool dual = a.items_c != nullptr;
   const dim3 g(grid);
   if (gate_up) {
     const dim3 b(GemmRoles<true>::kThreads);
     constexpr int sm = GemmSmem<true>::kBytes;
-    return fp4 ? launch_pdl(grouped_gemm_kernel<true, true>, g, b, sm, s, a, tmX, tmW, tmWs)
-               : launch_pdl(grouped_gemm_kernel<true, false>, g, b, sm, s, a, tmX, tmW, tmWs);
+    if (fp4) return launch_pdl(grouped_gemm_kernel<true, true, false>, g, b, sm, s, a, tmX, tmW, tmWs);
+    return dual ? launch_pdl(grouped_gemm_kernel<true, false, true>, g, b, sm, s, a, tmX, tmW, tmWs)
+                : launch_pdl(grouped_gemm_kernel<true, false, false>, g, b, sm, s, a, tmX, tmW, tmWs);
   }
   const dim3 b(GemmRoles<false>::kThreads);
   constexpr int sm = GemmSmem<false>::kBytes;
-  return fp4 ? launch_pdl(grouped_gemm_kernel<false, true>, g, b, sm, s, a, tmX, tmW, tmWs)
-             : launch_pdl(grouped_gemm_kernel<false, false>, g, b, sm, s, a, tmX, tmW, tmWs);
+  if (fp4) return launch_pdl(grouped_gemm_kernel<false, true, false>, g, b, sm, s, a, tmX, tmW, tmWs);
+  return dual ? launch_pdl(grouped_gemm_kernel<false, false, true>, g, b, sm, s, a, tmX, tmW, tmWs)
+              : launch_pdl(grouped_gemm_kernel<false, false, false>, g, b, sm, s, a, tmX, tmW, tmWs);
 }
 
 // One thread per 16-byte piece of a packed tile: code chunk position p of tile row r (four per

@@ -140,7 +140,8 @@ __device__ __forceinline__ void scan_block(const PrepArgs& a, int nblk) {
   // item counts of every group in each work list (l = 0 gate/up, 1 down, 2 and 3 the same
   // in the chunked accumulation's token tiles), their exclusive prefixes = the groups' bases
   const int g = threadIdx.x;
-  for (int l = 0; l < 4; ++l) {
+#pragma unroll
+  for (int l = 0; l < 4; ++l) {  // unrolled: the parameter arrays are indexed by constants
     if (!a.items[l]) continue;  // uniform over the block
     int n = 0;
     if (g < ng) {
@@ -158,6 +159,7 @@ __device__ __forceinline__ void scan_block(const PrepArgs& a, int nblk) {
   }
   __syncthreads();
   // the item bases of the groups; the scatter kernel writes the items from them
+#pragma unroll
   for (int l = 0; l < 4; ++l) {
     if (!a.items[l]) continue;
     for (int i = threadIdx.x; i <= ng; i += blockDim.x) a.gbase[l * (kMaxGroups + 1) + i] = s_base[l][i];
@@ -180,11 +182,13 @@ __device__ __forceinline__ void write_group_items(const PrepArgs& a, int g) {
   const int cnt = sh ? a.T : a.counts[gid];
   if (cnt == 0) return;
   const int row0 = sh ? 0 : (a.has_shared ? a.T : 0) + a.offsets[gid];
+#pragma unroll 1
   for (int list = 0; list < 4; ++list) {
-    if (!a.items[list]) continue;
-    const int tn = a.tn[list];
+    int4* const base = list == 0 ? a.items[0] : list == 1 ? a.items[1] : list == 2 ? a.items[2] : a.items[3];
+    if (!base) continue;
+    const int tn = list == 0 ? a.tn[0] : list == 1 ? a.tn[1] : list == 2 ? a.tn[2] : a.tn[3];
     const int nwt = list % 2 == 0 ? 2 * (sh ? a.Is : a.I) / kBM : a.H / kBM;
-    int4* items = a.items[list] + a.gbase[list * (kMaxGroups + 1) + g];
+    int4* items = base + a.gbase[list * (kMaxGroups + 1) + g];
     const int tt = (cnt + tn - 1) / tn;
     for (int i = threadIdx.x; i < nwt * tt; i += blockDim.x) {
       const int wt = i / tt, t = i - wt * tt;
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(1024) route_hist_scan_kernel(PrepArgs a, int n
 
 // Block per token: quantise x[t] once, write its codes (fp16 integers) to each of its rows.
 // Block b also writes the work items of groups b, b + T, ... (the grouped GEMMs read them).
-__global__ void scatter_kernel(PrepArgs a) {
+__global__ void __launch_bounds__(256, 6) scatter_kernel(PrepArgs a) {
   pdl_wait();  // the predecessor on the stream (launched with launch_pdl)
   pdl_trigger();
   const int ng = a.E + (a.has_shared ? 1 : 0);
