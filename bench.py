@@ -36,7 +36,7 @@ METRIC = "MoE layer tokens/s (prefill) & µs/layer decode C=8; % int8/HBM roofli
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up GEMM launch on the
 # stacked-prefill layer (T=2600), from one ncu capture of the kernel as it is now. Set to None
 # whenever the kernel changes, until it is captured again.
-GU_TRAFFIC_BYTES = 400.9e6
+GU_TRAFFIC_BYTES = 399.5e6
 # Kernels one stacked-prefill layer launches: RMS pre-norm, router projection, and the
 # forward's routing + histogram + scan, scatter, gate/up GEMM, requantisation, down GEMM.
 LAUNCHES_PER_LAYER = 7
