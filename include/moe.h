@@ -82,8 +82,8 @@ typedef struct {
 
 /* One layer's NVFP4 expert weights (device pointers, caller-owned): the format the page
  * "[job] Strix Halo: multi-session serving (parallel or sequential) and long context,
- * Flash-Next and the 27B #145" keeps for the routed experts (comment of Oct 19, "FP4 dtype
- * survey on the AMD track"). Every weight row (reduction dimension contiguous) is stored as
+ * Flash-Next and the 27B #145" keeps for the routed experts (its comment of Oct 19, which
+ * compares the FP4 formats). Every weight row (reduction dimension contiguous) is stored as
  * 4-bit E2M1 codes (OCP Microscaling Formats v1.0, FP4: sign, 2 exponent bits with bias 1, 1
  * mantissa bit), two per byte with element 2j in the low nibble, plus one E4M3 block scale
  * byte (finite, non-negative) per 16 consecutive elements, plus one fp32 scale per matrix:

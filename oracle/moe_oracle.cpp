@@ -30,8 +30,8 @@
 //
 // NVFP4 experts. The same layer with its expert weights (routed and shared) in NVFP4 instead
 // of int8: the format the page "[job] Strix Halo: multi-session serving ... #145" keeps for
-// the routed experts (comment of Oct 19, "FP4 dtype survey on the AMD track ... decided: stay
-// on NVFP4"). A weight row is a sequence of 4-bit E2M1 codes, two per byte (element 2j in the
+// the routed experts (its comment of Oct 19, which compares the FP4 formats and keeps NVFP4).
+// A weight row is a sequence of 4-bit E2M1 codes, two per byte (element 2j in the
 // low nibble), with one E4M3 block scale per 16 consecutive elements and one fp32 scale per
 // weight matrix. Dequantised weight = e2m1(code) * e4m3(block scale) * matrix scale. The
 // activations stay int8 as above. With w' = e2m1 * e4m3 (the weight without the matrix
